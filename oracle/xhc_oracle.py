@@ -1,0 +1,267 @@
+"""Plain fp64 CPU oracle of the xHC per-sublayer residual-stream update.
+
+TEST INFRASTRUCTURE ONLY.  Nothing on the product path may import this module:
+it is used by ``tests/``, by ``__graft_entry__.smoke()`` (to check one small GPU
+run) and by ``bench.py``'s ``cpu_baseline`` / ``--impl reference`` legs.  It
+shares no code with the CUDA library under ``residual_stream_expansion_xhc_b300``.
+
+Sources (page, section), from "xHC: Expanded Hyper-Connections" (qingkeai.online
+research retrospective, cited below as [xHC]):
+
+* [xHC] "Scaling N": the state of a sublayer is N residual streams of width C;
+  H^pre reads the sublayer input from the streams, H^post writes the output
+  back, H^res mixes the streams and is made doubly stochastic by Sinkhorn.
+* [xHC] "Write-back bottleneck": the mHC write of stream i is h^post_i * out.
+* [xHC] "Temporal Feature Augmentation": out in R^{S x C}; three causal
+  depthwise convolutions with kernel sizes 4, 8, 12 along the sequence, each
+  channel on its own, stacked with the raw output into 4 components.
+* [xHC] "Conv / Gram-Schmidt": the components u_c in R^C, c = 0..3.
+* [xHC] "Dense read, sparse write": the sublayer input is read from all N
+  streams; only the k active streams (set A_l, |A_l| = k) are written, by a
+  combination sum_c h^post_{l,i,c} u_c; inactive streams are left unchanged
+  and only the active streams take part in the H^res mixing.
+
+The formulas themselves did not survive on the pages; the formulation below is
+the one fixed by the project specification, with these readings where the
+pages are silent (each is listed in the design notes):
+
+* rmsnorm over the whole flattened state vec X (length N*C), eps = 1e-6, no
+  gain; projection W of shape [P, N*C], P = N + 4k + k^2, no bias.
+* rows of W: [0, N) -> H^pre; N + 4i + c -> H^post[i, c];
+  N + 4k + k*i + j -> H^res logit [i, j]; W's columns follow vec X's order
+  n*C + c.
+* H^pre, H^post: plain sigmoid.  H^res: exp(Z - max Z), then ``iters`` times
+  (normalise rows, then normalise columns).
+* X'[a_i] = sum_j H^res[i, j] X[a_j] + sum_c H^post[i, c] u_c for slot i of
+  the ordered index list a; other streams unchanged.
+* conv tap tau multiplies out[t - tau] (tau = 0 is the current token), zero
+  padding before the start of each sequence, no bias.  No Gram-Schmidt, router
+  score s = 1 (the active indices are given).
+
+All arrays are float64 numpy arrays.  The backward is the exact reverse mode of
+the forward, hand-derived step by step (the Sinkhorn reverse recomputes and
+keeps the forward iterates).  Sequences are processed one at a time to bound
+memory; nothing couples two sequences except the weight-gradient sums.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+CONV_KS = (4, 8, 12)
+
+
+def n_logits(N: int, k: int) -> int:
+    """P = N (H^pre) + 4k (H^post) + k^2 (H^res logits)."""
+    return N + 4 * k + k * k
+
+
+def sigmoid(x):
+    return 1.0 / (1.0 + np.exp(-x))
+
+
+def sinkhorn(Z, iters):
+    """exp(Z - max Z) followed by ``iters`` rounds of (row-normalise,
+    column-normalise), batched over leading axes.  Z: [..., k, k].
+
+    Returns (H, trace) where trace keeps every intermediate matrix for the
+    reverse pass: trace[0] = M0 = exp(Z - max Z); then for each iteration the
+    matrix before the row step and before the column step.
+    """
+    zmax = Z.max(axis=(-2, -1), keepdims=True)
+    M = np.exp(Z - zmax)
+    trace = [M]
+    for _ in range(iters):
+        before_row = M
+        M = M / M.sum(axis=-1, keepdims=True)      # row i: sum over j
+        before_col = M
+        M = M / M.sum(axis=-2, keepdims=True)      # column j: sum over i
+        trace.append((before_row, before_col))
+    return M, trace
+
+
+def sinkhorn_reverse(dH, trace):
+    """Reverse mode of ``sinkhorn``: given dL/dH, return dL/dZ.
+
+    A normalisation y = x / s with s = sum over the normalised axis of x has
+    dL/dx = dL/dy / s - sum_axis(dL/dy * x) / s^2 (broadcast along the axis).
+    The max subtracted before exp is treated as a constant: a shift of one
+    row's logits is removed exactly by the next row normalisation, so its
+    gradient contribution is zero.
+    """
+    g = dH
+    for before_row, before_col in reversed(trace[1:]):
+        s = before_col.sum(axis=-2, keepdims=True)
+        g = g / s - (g * before_col).sum(axis=-2, keepdims=True) / (s * s)
+        s = before_row.sum(axis=-1, keepdims=True)
+        g = g / s - (g * before_row).sum(axis=-1, keepdims=True) / (s * s)
+    M0 = trace[0]
+    return g * M0
+
+
+def tfa_components(out_seq, conv):
+    """Temporal Feature Augmentation of one sequence.
+
+    out_seq: [S, C].  conv: (w4 [C,4], w8 [C,8], w12 [C,12]) or None.
+    Returns u: [4, S, C] with u[0] = out and u[j][t, c] =
+    sum_{tau < K_j} w_j[c, tau] * out[t - tau, c] (zero for t - tau < 0).
+    With conv = None the three convolution components are zero.
+    """
+    S, C = out_seq.shape
+    u = np.zeros((4, S, C))
+    u[0] = out_seq
+    if conv is None:
+        return u
+    for j, w in enumerate(conv, start=1):
+        K = w.shape[1]
+        for tau in range(K):
+            if tau >= S:
+                break
+            # u_j[t] += w[:, tau] * out[t - tau] for t >= tau
+            u[j, tau:, :] += w[None, :, tau] * out_seq[: S - tau, :]
+    return u
+
+
+def _check(X, out, conv, W, idx):
+    B, S, N, C = X.shape
+    k = len(idx)
+    assert out.shape == (B, S, C)
+    assert W.shape == (n_logits(N, k), N * C)
+    assert len(set(int(a) for a in idx)) == k and all(0 <= int(a) < N for a in idx)
+    if conv is not None:
+        assert tuple(w.shape for w in conv) == tuple((C, K) for K in CONV_KS)
+    return B, S, N, C, k
+
+
+def _coeffs_seq(Xs, W, N, C, k, iters, eps):
+    """Coefficients for one sequence.  Xs: [S, N, C]."""
+    S = Xs.shape[0]
+    v = Xs.reshape(S, N * C)
+    rstd = 1.0 / np.sqrt((v * v).mean(axis=1) + eps)           # rmsnorm scale
+    p = v @ W.T                                                  # [S, P]
+    z = rstd[:, None] * p
+    hpre = sigmoid(z[:, :N])
+    hpost = sigmoid(z[:, N:N + 4 * k]).reshape(S, k, 4)
+    Z = z[:, N + 4 * k:].reshape(S, k, k)
+    hres, trace = sinkhorn(Z, iters)
+    return dict(v=v, rstd=rstd, p=p, z=z, hpre=hpre, hpost=hpost, hres=hres, trace=trace)
+
+
+def forward(X, out, conv, W, idx, iters=20, eps=1e-6):
+    """One xHC sublayer update (forward).
+
+    X: [B, S, N, C]; out: [B, S, C]; conv: (w4, w8, w12) or None;
+    W: [P, N*C]; idx: the k active stream indices (ordered, slot i <-> idx[i]).
+
+    Returns a dict with Xp (updated state [B,S,N,C]), x_in (dense read
+    [B,S,C]), z (logits [B,S,P]), rstd [B,S], hpre [B,S,N], hpost [B,S,k,4],
+    hres [B,S,k,k], u (components [B,4,S,C]).
+    """
+    B, S, N, C, k = _check(X, out, conv, W, idx)
+    idx = [int(a) for a in idx]
+    P = n_logits(N, k)
+    res = dict(Xp=X.copy(), x_in=np.zeros((B, S, C)), z=np.zeros((B, S, P)),
+               rstd=np.zeros((B, S)), hpre=np.zeros((B, S, N)),
+               hpost=np.zeros((B, S, k, 4)), hres=np.zeros((B, S, k, k)),
+               u=np.zeros((B, 4, S, C)))
+    for b in range(B):
+        cf = _coeffs_seq(X[b], W, N, C, k, iters, eps)
+        # dense read over all N streams
+        x_in = np.einsum("sn,snc->sc", cf["hpre"], X[b])
+        u = tfa_components(out[b], conv)
+        Xa = X[b][:, idx, :]                                     # [S, k, C]
+        mix = np.einsum("sij,sjc->sic", cf["hres"], Xa)
+        write = np.einsum("sic,csx->six", cf["hpost"], u)       # sum over components
+        res["Xp"][b][:, idx, :] = mix + write
+        res["x_in"][b] = x_in
+        res["u"][b] = u
+        for key in ("z", "rstd", "hpre", "hpost", "hres"):
+            res[key][b] = cf[key]
+    return res
+
+
+def backward(X, out, conv, W, idx, dXp, dx_in=None, iters=20, eps=1e-6, keep=False):
+    """Exact reverse mode of ``forward``.
+
+    X is the state BEFORE the update.  dXp = dL/dX' [B,S,N,C]; dx_in = dL/dx_in
+    [B,S,C] or None (no gradient through the dense read).
+
+    Returns dict with dX [B,S,N,C], dout [B,S,C], dconv (three arrays, or None
+    when conv is None), dW [P, N*C]; with keep=True also dz [B,S,P] (gradient
+    at the logits) and the per-token dp [B,S,P] and drstd [B,S].
+    """
+    B, S, N, C, k = _check(X, out, conv, W, idx)
+    idx = [int(a) for a in idx]
+    inactive = [n for n in range(N) if n not in idx]
+    P = n_logits(N, k)
+    dX = np.zeros_like(X)
+    dout = np.zeros_like(out)
+    dW = np.zeros_like(W)
+    dconv = None if conv is None else [np.zeros_like(w) for w in conv]
+    extra = dict(dz=np.zeros((B, S, P)), dp=np.zeros((B, S, P)), drstd=np.zeros((B, S)))
+    for b in range(B):
+        Xs = X[b]
+        cf = _coeffs_seq(Xs, W, N, C, k, iters, eps)
+        u = tfa_components(out[b], conv)                        # [4, S, C]
+        G = dXp[b][:, idx, :]                                   # [S, k, C]
+        Xa = Xs[:, idx, :]                                      # [S, k, C]
+        # gradients at the coefficients
+        d_hres = np.einsum("sic,sjc->sij", G, Xa)
+        d_hpost = np.einsum("sic,xsc->six", G, u)
+        if dx_in is not None:
+            d_hpre = np.einsum("sc,snc->sn", dx_in[b], Xs)
+        else:
+            d_hpre = np.zeros((S, N))
+        # through the nonlinearities to the logits
+        dZ = sinkhorn_reverse(d_hres, cf["trace"])             # [S, k, k]
+        hpre, hpost = cf["hpre"], cf["hpost"]
+        dz = np.concatenate([
+            d_hpre * hpre * (1.0 - hpre),
+            (d_hpost * hpost * (1.0 - hpost)).reshape(S, 4 * k),
+            dZ.reshape(S, k * k)], axis=1)
+        # z = rstd * p
+        rstd, p, v = cf["rstd"], cf["p"], cf["v"]
+        dp = rstd[:, None] * dz
+        drstd = (dz * p).sum(axis=1)
+        # p = W v ;  rstd = (mean(v^2) + eps)^(-1/2)  => d rstd / dv = -rstd^3 v / (N C)
+        dv = dp @ W + (drstd * (-(rstd ** 3) / (N * C)))[:, None] * v
+        dW += dp.T @ v
+        dXs = dv.reshape(S, N, C).copy()
+        # dense read x_in = sum_n hpre[n] X[n]
+        if dx_in is not None:
+            dXs += hpre[:, :, None] * dx_in[b][:, None, :]
+        # sparse write: inactive streams pass through, active ones are mixed
+        dXs[:, inactive, :] += dXp[b][:, inactive, :]
+        dXs[:, idx, :] += np.einsum("sij,sic->sjc", cf["hres"], G)
+        dX[b] = dXs
+        # components: du_c = sum_i hpost[i, c] G_i
+        du = np.einsum("six,sic->xsc", hpost, G)                # [4, S, C]
+        dout_b = du[0].copy()
+        if conv is not None:
+            for j, w in enumerate(conv, start=1):
+                K = w.shape[1]
+                for tau in range(min(K, S)):
+                    # u_j[t] += w[:, tau] * out[t - tau]  (t >= tau)
+                    dout_b[: S - tau, :] += w[None, :, tau] * du[j, tau:, :]
+                    dconv[j - 1][:, tau] += (du[j, tau:, :] * out[b][: S - tau, :]).sum(axis=0)
+        dout[b] = dout_b
+        extra["dz"][b] = dz
+        extra["dp"][b] = dp
+        extra["drstd"][b] = drstd
+    res = dict(dX=dX, dout=dout, dconv=dconv, dW=dW)
+    if keep:
+        res.update(extra)
+    return res
+
+
+def max_rel_err(got, ref):
+    """Error measure used by every parity check: max_i |g_i - r_i| /
+    max(|r_i|, rms(r)) -- elementwise relative, floored at the tensor's RMS so
+    that entries near zero do not dominate."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    if ref.size == 0:
+        return 0.0
+    rms = float(np.sqrt(np.mean(ref * ref)))
+    floor = np.maximum(np.abs(ref), rms)
+    floor = np.where(floor == 0.0, 1.0, floor)
+    return float(np.max(np.abs(got - ref) / floor))
