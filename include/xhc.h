@@ -1,0 +1,210 @@
+/*
+ * xhc.h -- C ABI of the xHC per-sublayer residual-stream update on one GPU
+ * (NVIDIA B300, sm_103a).
+ *
+ * Method: "xHC: Expanded Hyper-Connections" (qingkeai.online research
+ * retrospective).  Per token the residual state is N streams of width C
+ * (section "Scaling N"); the sublayer input is a dense read over all N
+ * streams weighted by H^pre (section "Dense read, sparse write"); the
+ * sublayer output `out` is expanded along the sequence by three causal
+ * depthwise convolutions of kernel size 4, 8 and 12 stacked with the raw
+ * output (section "Temporal Feature Augmentation"); only k active streams are
+ * rewritten, by a Sinkhorn-normalised k x k mix H^res of the active streams
+ * plus an H^post combination of the four components; the other streams pass
+ * through unchanged (sections "Scaling N", "Dense read, sparse write").
+ *
+ * Formulation used (the pages' formulas were lost; these choices are fixed by
+ * the project specification), per token with v = vec X (length N*C, index
+ * n*C + c), P = N + 4k + k*k:
+ *   rstd = 1 / sqrt(mean(v^2) + eps)         z = rstd * (W v),  W: [P, N*C]
+ *   hpre = sigmoid(z[0:N])                    hpost[i][c] = sigmoid(z[N + 4i + c])
+ *   Hres = Sinkhorn(exp(Z - max Z)), Z[i][j] = z[N + 4k + k*i + j];
+ *          each Sinkhorn iteration normalises rows, then columns
+ *   x_in = sum_n hpre[n] X[n]
+ *   u0 = out[t];  u_j[t][c] = sum_{tau < K_j} w_j[c][tau] out[t - tau][c]
+ *          (K = 4, 8, 12; zero before the start of each sequence)
+ *   X'[a_i] = sum_j Hres[i][j] X[a_j] + sum_c hpost[i][c] u_c   (i < k)
+ *   X'[n]   = X[n] for streams n not in the active list a.
+ *
+ * Conventions shared by every entry point
+ *   - All tensor pointers are DEVICE pointers owned by the caller, except the
+ *     active-index list `idx`, which is a HOST array of k int32.
+ *   - Layouts are dense row-major: X, X', dX' and dX are [B, S, N, C];
+ *     out, x_in, dx_in, dout are [B, S, C]; conv weights w4, w8, w12 are
+ *     [C, 4], [C, 8], [C, 12] (tap tau multiplies out[t - tau]); W and dW are
+ *     [P, N*C]; hpre [B, S, N]; hpost [B, S, k, 4]; hres [B, S, k, k];
+ *     saved [B, S, P + 1] holds the logits z followed by rstd.
+ *   - Activations (X, out, x_in, dX', dx_in, dX, dout, u, saved_active) use
+ *     the shape's dtype (fp32 or bf16); W, conv weights, coefficients and
+ *     weight gradients are always fp32.  Arithmetic accumulates in fp32;
+ *     bf16 results are rounded to nearest even.
+ *   - Every pointer must be 16-byte aligned; C * sizeof(dtype) must be a
+ *     multiple of 16.
+ *   - Work is enqueued asynchronously on `stream`; nothing synchronises the
+ *     host.  Gradients are written, not accumulated.
+ *   - On any error status nothing has been launched, except XHC_ERR_CUDA,
+ *     which reports a launch failure (see xhc_last_cuda_error).
+ *   - The library allocates no device memory.  Entry points that need
+ *     scratch take a caller workspace and report its size.
+ *   - Limits: 1 <= N <= 16, 1 <= k <= min(N, 4), 0 <= sinkhorn_iters <= 64.
+ *     B * S == 0 is a valid empty call that launches nothing.
+ */
+#ifndef XHC_H_
+#define XHC_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* xhc_stream_t; /* same type as cudaStream_t */
+
+enum {
+  XHC_F32 = 0,
+  XHC_BF16 = 1
+};
+
+enum {
+  XHC_OK = 0,
+  XHC_ERR_SHAPE = 1,     /* bad B, S, N, C, k, iteration count or eps */
+  XHC_ERR_INDEX = 2,     /* idx missing, repeated or outside [0, N) */
+  XHC_ERR_ALIGN = 3,     /* a pointer is not 16-byte aligned */
+  XHC_ERR_DTYPE = 4,     /* unsupported dtype */
+  XHC_ERR_WORKSPACE = 5, /* workspace missing or too small */
+  XHC_ERR_CUDA = 6,      /* a kernel launch failed */
+  XHC_ERR_TIMEOUT = 7,   /* a bounded device-side wait gave up */
+  XHC_ERR_ARG = 8        /* a required pointer is NULL */
+};
+
+typedef struct xhc_shape {
+  int B, S, N, C, k;
+  int dtype;          /* XHC_F32 or XHC_BF16 */
+  int sinkhorn_iters; /* 20 in the method's setting */
+  float eps;          /* rmsnorm epsilon, 1e-6 in the method's setting */
+} xhc_shape_t;
+
+/* Human-readable name of a status code.  Never NULL. */
+const char* xhc_status_string(int status);
+
+/* cudaError_t of the most recent XHC_ERR_CUDA in this process (0 if none). */
+int xhc_last_cuda_error(void);
+
+/* Number of projection rows P = N + 4k + k^2 for a shape. */
+int xhc_num_logits(const xhc_shape_t* sh);
+
+/*
+ * xhc_coeffs -- coefficient generation and dense read.
+ * Section "Scaling N" (H^pre, H^post, H^res from the state; Sinkhorn) and
+ * section "Dense read, sparse write" (the input is read from all N streams).
+ *   X      [B,S,N,C] dtype, read.
+ *   W      [P, N*C] fp32, read.
+ *   hpre   [B,S,N], hpost [B,S,k,4], hres [B,S,k,k] fp32, written.
+ *   saved  [B,S,P+1] fp32 (z then rstd), written; may be NULL.
+ *   x_in   [B,S,C] dtype, written; may be NULL (no dense read).
+ */
+int xhc_coeffs(const xhc_shape_t* sh, const void* X, const float* W,
+               float* hpre, float* hpost, float* hres, float* saved,
+               void* x_in, xhc_stream_t stream);
+
+/*
+ * xhc_tfa -- Temporal Feature Augmentation components u_1, u_2, u_3.
+ * Section "Temporal Feature Augmentation": three causal depthwise
+ * convolutions, kernel sizes 4, 8, 12, each channel independent along the
+ * sequence; u_0 is `out` itself and is not written.
+ *   out          [B,S,C] dtype, read.
+ *   w4, w8, w12  [C,4], [C,8], [C,12] fp32, read; all three required.
+ *   u            [3,B,S,C] dtype, written (u_1, u_2, u_3).
+ */
+int xhc_tfa(const xhc_shape_t* sh, const void* out, const float* w4,
+            const float* w8, const float* w12, void* u, xhc_stream_t stream);
+
+/*
+ * xhc_sparse_update -- the sparse write given coefficients.
+ * Section "Dense read, sparse write": only the k streams in idx are
+ * rewritten; section "Temporal Feature Augmentation" for the components.
+ *   X_in   [B,S,N,C] dtype, read.
+ *   X_out  [B,S,N,C] dtype, written.  X_out == X_in updates in place and
+ *          writes only the k active rows; otherwise the N-k inactive rows are
+ *          copied as well.  Partial overlap is not allowed.
+ *   out    [B,S,C] dtype, read.
+ *   w4, w8, w12  fp32 conv weights, or all three NULL for no convolution
+ *          branches (u_1 = u_2 = u_3 = 0).
+ *   hpost  [B,S,k,4] fp32, hres [B,S,k,k] fp32, read.
+ *   idx    host int32[k]: slot i rewrites stream idx[i].
+ */
+int xhc_sparse_update(const xhc_shape_t* sh, const void* X_in, void* X_out,
+                      const void* out, const float* w4, const float* w8,
+                      const float* w12, const float* hpost, const float* hres,
+                      const int32_t* idx, xhc_stream_t stream);
+
+/*
+ * Workspace the fused forward needs when `saved` is NULL (bytes; 0 when none
+ * is needed).
+ */
+size_t xhc_fwd_workspace_bytes(const xhc_shape_t* sh);
+
+/*
+ * xhc_sublayer_fwd -- the whole per-sublayer update: coefficients, dense
+ * read, TFA and sparse write (all sections cited above).
+ *   X_in, X_out  as in xhc_sparse_update (X_out == X_in: in place).
+ *   out, w4, w8, w12, idx  as in xhc_sparse_update.
+ *   W      [P, N*C] fp32.
+ *   x_in   [B,S,C] dtype, written; may be NULL.
+ *   saved  [B,S,P+1] fp32 (z, rstd), written; may be NULL.
+ *   saved_active  [B,S,k,C] dtype: the k active rows of X_in before the
+ *          update (slot order), written; may be NULL.  Needed by the backward
+ *          when the state is updated in place.
+ *   workspace, ws_bytes  at least xhc_fwd_workspace_bytes() bytes when saved
+ *          is NULL, else may be NULL/0.
+ */
+int xhc_sublayer_fwd(const xhc_shape_t* sh, const void* X_in, void* X_out,
+                     const void* out, const float* w4, const float* w8,
+                     const float* w12, const float* W, const int32_t* idx,
+                     void* x_in, float* saved, void* saved_active,
+                     void* workspace, size_t ws_bytes, xhc_stream_t stream);
+
+/* Workspace the backward needs (bytes). */
+size_t xhc_bwd_workspace_bytes(const xhc_shape_t* sh);
+
+/*
+ * xhc_sublayer_bwd -- exact reverse mode of xhc_sublayer_fwd, including the
+ * pass back through every Sinkhorn iteration.
+ *   X_state  [B,S,N,C] dtype.  If saved_active is NULL it is the state BEFORE
+ *            the update; otherwise it is the state AFTER the in-place update
+ *            and the k old active rows are read from saved_active.
+ *   saved_active  [B,S,k,C] dtype or NULL (see X_state).
+ *   out, w4, w8, w12, W, idx  the forward's inputs (conv weights all NULL for
+ *            no convolution branches).
+ *   saved    [B,S,P+1] fp32 from the forward, or NULL to recompute it.
+ *   dXp      [B,S,N,C] dtype: dL/dX', read.
+ *   dx_in    [B,S,C] dtype: dL/dx_in, or NULL when x_in carries no gradient.
+ *   dX       [B,S,N,C] dtype: dL/dX, written.  dX may equal dXp.
+ *   dout     [B,S,C] dtype: dL/dout, written.
+ *   dw4, dw8, dw12  [C,4], [C,8], [C,12] fp32, written (NULL when the conv
+ *            weights are NULL).
+ *   dW       [P, N*C] fp32, written.
+ *   workspace, ws_bytes  at least xhc_bwd_workspace_bytes() bytes.
+ */
+int xhc_sublayer_bwd(const xhc_shape_t* sh, const void* X_state,
+                     const void* saved_active, const void* out,
+                     const float* w4, const float* w8, const float* w12,
+                     const float* W, const int32_t* idx, const float* saved,
+                     const void* dXp, const void* dx_in, void* dX, void* dout,
+                     float* dw4, float* dw8, float* dw12, float* dW,
+                     void* workspace, size_t ws_bytes, xhc_stream_t stream);
+
+/*
+ * xhc_copy -- device-to-device copy of `bytes` bytes with 16-byte vector
+ * loads and stores.  Used to measure the HBM copy bandwidth in the same
+ * process as the update kernels.  Both pointers 16-byte aligned, bytes a
+ * multiple of 16; the ranges must not overlap.
+ */
+int xhc_copy(const void* src, void* dst, size_t bytes, xhc_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* XHC_H_ */

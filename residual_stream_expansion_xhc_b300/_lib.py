@@ -1,0 +1,72 @@
+"""ctypes binding of libxhc.so (include/xhc.h): argument marshalling only.
+
+Tensors are passed as raw device pointers (``tensor.data_ptr()``) together
+with the current CUDA stream; every step of the update runs in the library's
+kernels.  Importing this module fails loudly when the library is missing.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libxhc.so")
+
+XHC_F32, XHC_BF16 = 0, 1
+STATUS = {0: "XHC_OK", 1: "XHC_ERR_SHAPE", 2: "XHC_ERR_INDEX", 3: "XHC_ERR_ALIGN", 4: "XHC_ERR_DTYPE",
+          5: "XHC_ERR_WORKSPACE", 6: "XHC_ERR_CUDA", 7: "XHC_ERR_TIMEOUT", 8: "XHC_ERR_ARG"}
+
+EXPORTS = ("xhc_status_string", "xhc_last_cuda_error", "xhc_num_logits", "xhc_coeffs", "xhc_tfa",
+           "xhc_sparse_update", "xhc_fwd_workspace_bytes", "xhc_sublayer_fwd", "xhc_bwd_workspace_bytes",
+           "xhc_sublayer_bwd", "xhc_copy")
+
+
+class XhcShape(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int), ("S", ctypes.c_int), ("N", ctypes.c_int), ("C", ctypes.c_int),
+                ("k", ctypes.c_int), ("dtype", ctypes.c_int), ("sinkhorn_iters", ctypes.c_int),
+                ("eps", ctypes.c_float)]
+
+
+class XhcError(RuntimeError):
+    def __init__(self, fn, status, lib):
+        msg = lib.xhc_status_string(status).decode()
+        detail = ""
+        if status == 6:
+            detail = f" (cudaError {lib.xhc_last_cuda_error()})"
+        super().__init__(f"{fn}: {STATUS.get(status, status)}: {msg}{detail}")
+        self.status = status
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"libxhc.so not built at {LIB_PATH}; run "
+                          "`python -m residual_stream_expansion_xhc_b300.build`")
+    lib = ctypes.CDLL(LIB_PATH)
+    P, I, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+    sh = ctypes.POINTER(XhcShape)
+    lib.xhc_status_string.restype = ctypes.c_char_p
+    lib.xhc_status_string.argtypes = [I]
+    lib.xhc_last_cuda_error.restype = I
+    lib.xhc_last_cuda_error.argtypes = []
+    lib.xhc_num_logits.restype = I
+    lib.xhc_num_logits.argtypes = [sh]
+    lib.xhc_coeffs.restype = I
+    lib.xhc_coeffs.argtypes = [sh, P, P, P, P, P, P, P, P]
+    lib.xhc_tfa.restype = I
+    lib.xhc_tfa.argtypes = [sh, P, P, P, P, P, P]
+    lib.xhc_sparse_update.restype = I
+    lib.xhc_sparse_update.argtypes = [sh, P, P, P, P, P, P, P, P, P, P]
+    lib.xhc_fwd_workspace_bytes.restype = Z
+    lib.xhc_fwd_workspace_bytes.argtypes = [sh]
+    lib.xhc_sublayer_fwd.restype = I
+    lib.xhc_sublayer_fwd.argtypes = [sh, P, P, P, P, P, P, P, P, P, P, P, P, Z, P]
+    lib.xhc_bwd_workspace_bytes.restype = Z
+    lib.xhc_bwd_workspace_bytes.argtypes = [sh]
+    lib.xhc_sublayer_bwd.restype = I
+    lib.xhc_sublayer_bwd.argtypes = [sh, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, Z, P]
+    lib.xhc_copy.restype = I
+    lib.xhc_copy.argtypes = [P, P, Z, P]
+    return lib
+
+
+LIB = _load()

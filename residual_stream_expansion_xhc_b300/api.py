@@ -1,0 +1,111 @@
+"""Python binding of the xHC C ABI (include/xhc.h), same entry-point names.
+
+Argument marshalling only: torch tensors are passed as device pointers with
+the current CUDA stream (or an explicit one); the library's kernels do all of
+the work.  Conventions (layouts, dtypes, ownership, errors) are those of the
+C header; a non-zero status raises ``XhcError``.
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional, Sequence
+
+import torch
+
+from ._lib import LIB, XHC_BF16, XHC_F32, XhcError, XhcShape
+
+Tensor = torch.Tensor
+_DT = {torch.float32: XHC_F32, torch.bfloat16: XHC_BF16}
+
+
+def make_shape(B: int, S: int, N: int, C: int, k: int, dtype, iters: int = 20, eps: float = 1e-6) -> XhcShape:
+    """Build an ``xhc_shape_t``; ``dtype`` is a torch dtype or "f32"/"bf16"."""
+    if isinstance(dtype, str):
+        dt = {"f32": XHC_F32, "bf16": XHC_BF16}[dtype]
+    else:
+        dt = _DT[dtype]
+    return XhcShape(B, S, N, C, k, dt, iters, eps)
+
+
+def num_logits(sh: XhcShape) -> int:
+    return LIB.xhc_num_logits(ctypes.byref(sh))
+
+
+def _p(t: Optional[Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _s(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _idx(idx: Sequence[int]):
+    arr = (ctypes.c_int32 * len(idx))(*[int(i) for i in idx])
+    return arr
+
+
+def _conv(conv):
+    if conv is None:
+        return None, None, None
+    return tuple(_p(w) for w in conv)
+
+
+def _check(name: str, status: int):
+    if status != 0:
+        raise XhcError(name, status, LIB)
+
+
+def xhc_coeffs(sh, X, W, hpre, hpost, hres, saved=None, x_in=None, stream=None):
+    _check("xhc_coeffs", LIB.xhc_coeffs(ctypes.byref(sh), _p(X), _p(W), _p(hpre), _p(hpost), _p(hres),
+                                        _p(saved), _p(x_in), _s(stream)))
+
+
+def xhc_tfa(sh, out, conv, u, stream=None):
+    w4, w8, w12 = _conv(conv)
+    _check("xhc_tfa", LIB.xhc_tfa(ctypes.byref(sh), _p(out), w4, w8, w12, _p(u), _s(stream)))
+
+
+def xhc_sparse_update(sh, X_in, X_out, out, conv, hpost, hres, idx, stream=None):
+    w4, w8, w12 = _conv(conv)
+    _check("xhc_sparse_update", LIB.xhc_sparse_update(ctypes.byref(sh), _p(X_in), _p(X_out), _p(out), w4, w8,
+                                                      w12, _p(hpost), _p(hres), _idx(idx), _s(stream)))
+
+
+def xhc_fwd_workspace_bytes(sh) -> int:
+    return int(LIB.xhc_fwd_workspace_bytes(ctypes.byref(sh)))
+
+
+def xhc_bwd_workspace_bytes(sh) -> int:
+    return int(LIB.xhc_bwd_workspace_bytes(ctypes.byref(sh)))
+
+
+def xhc_sublayer_fwd(sh, X_in, X_out, out, conv, W, idx, x_in=None, saved=None, saved_active=None,
+                     workspace=None, stream=None):
+    w4, w8, w12 = _conv(conv)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("xhc_sublayer_fwd", LIB.xhc_sublayer_fwd(ctypes.byref(sh), _p(X_in), _p(X_out), _p(out), w4, w8, w12,
+                                                    _p(W), _idx(idx), _p(x_in), _p(saved), _p(saved_active),
+                                                    _p(workspace), ws_bytes, _s(stream)))
+
+
+def xhc_sublayer_bwd(sh, X_state, saved_active, out, conv, W, idx, saved, dXp, dx_in, dX, dout, dconv, dW,
+                     workspace, stream=None):
+    w4, w8, w12 = _conv(conv)
+    d4, d8, d12 = _conv(dconv)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check("xhc_sublayer_bwd", LIB.xhc_sublayer_bwd(ctypes.byref(sh), _p(X_state), _p(saved_active), _p(out), w4,
+                                                    w8, w12, _p(W), _idx(idx), _p(saved), _p(dXp), _p(dx_in),
+                                                    _p(dX), _p(dout), d4, d8, d12, _p(dW), _p(workspace),
+                                                    ws_bytes, _s(stream)))
+
+
+def xhc_copy(src: Tensor, dst: Tensor, nbytes: Optional[int] = None, stream=None):
+    n = src.numel() * src.element_size() if nbytes is None else nbytes
+    _check("xhc_copy", LIB.xhc_copy(_p(src), _p(dst), n, _s(stream)))
+
+
+def workspace(nbytes: int, device="cuda") -> Tensor:
+    """A caller-owned workspace buffer (uint8) of at least ``nbytes`` bytes."""
+    return torch.empty(max(int(nbytes), 16), dtype=torch.uint8, device=device)

@@ -1,0 +1,309 @@
+// C ABI of the xHC sublayer update: host-side validation and kernel dispatch.
+// Declarations and argument conventions: include/xhc.h.
+#include <algorithm>
+#include <cstring>
+
+#include "../../include/xhc.h"
+#include "xhc_kernels.cuh"
+#include "xhc_tc.cuh"
+
+using namespace xhc;
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+int cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return XHC_OK;
+  g_last_cuda_error = (int)e;
+  return XHC_ERR_CUDA;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t esize(const xhc_shape_t* sh) { return sh->dtype == XHC_BF16 ? 2 : 4; }
+
+int check_shape(const xhc_shape_t* sh) {
+  if (!sh) return XHC_ERR_ARG;
+  if (sh->dtype != XHC_F32 && sh->dtype != XHC_BF16) return XHC_ERR_DTYPE;
+  if (sh->B < 0 || sh->S < 0 || sh->N < 1 || sh->N > NMAX || sh->C < 1) return XHC_ERR_SHAPE;
+  if (sh->k < 1 || sh->k > KMAX || sh->k > sh->N) return XHC_ERR_SHAPE;
+  if (sh->sinkhorn_iters < 0 || sh->sinkhorn_iters > ITERS_MAX) return XHC_ERR_SHAPE;
+  if (!(sh->eps > 0.0f)) return XHC_ERR_SHAPE;
+  if (((size_t)sh->C * esize(sh)) % 16 != 0) return XHC_ERR_ALIGN;
+  if ((size_t)sh->B * (size_t)sh->S > (size_t)INT32_MAX) return XHC_ERR_SHAPE;
+  return XHC_OK;
+}
+
+int check_idx(const xhc_shape_t* sh, const int32_t* idx) {
+  if (!idx) return XHC_ERR_INDEX;
+  for (int i = 0; i < sh->k; ++i) {
+    if (idx[i] < 0 || idx[i] >= sh->N) return XHC_ERR_INDEX;
+    for (int j = 0; j < i; ++j)
+      if (idx[j] == idx[i]) return XHC_ERR_INDEX;
+  }
+  return XHC_OK;
+}
+
+// Every listed pointer must be non-NULL (when required) and 16-byte aligned.
+int check_ptrs(std::initializer_list<const void*> required, std::initializer_list<const void*> optional) {
+  for (const void* p : required) {
+    if (!p) return XHC_ERR_ARG;
+    if (!aligned16(p)) return XHC_ERR_ALIGN;
+  }
+  for (const void* p : optional)
+    if (p && !aligned16(p)) return XHC_ERR_ALIGN;
+  return XHC_OK;
+}
+
+// conv weights: all three or none
+int check_conv(const float* a, const float* b, const float* c, bool* has) {
+  const int n = (a != nullptr) + (b != nullptr) + (c != nullptr);
+  if (n != 0 && n != 3) return XHC_ERR_ARG;
+  *has = n == 3;
+  return XHC_OK;
+}
+
+Params make_params(const xhc_shape_t* sh, const int32_t* idx) {
+  Params p;
+  std::memset(&p, 0, sizeof(p));
+  p.B = sh->B; p.S = sh->S; p.N = sh->N; p.C = sh->C; p.k = sh->k;
+  p.P = sh->N + 4 * sh->k + sh->k * sh->k;
+  p.iters = sh->sinkhorn_iters;
+  p.eps = sh->eps;
+  if (idx) {
+    for (int i = 0; i < sh->k; ++i) {
+      p.idx[i] = idx[i];
+      p.is_active[idx[i]] = i + 1;
+    }
+  }
+  return p;
+}
+
+size_t round_up(size_t x) { return (x + 255) & ~(size_t)255; }
+size_t tokens(const xhc_shape_t* sh) { return (size_t)sh->B * (size_t)sh->S; }
+
+int num_sms() {
+  static int sms = 0;
+  if (!sms) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (sms <= 0) sms = 148;
+  }
+  return sms;
+}
+
+// Coefficient pass: tensor-core kernel where the shape tiles, else CUDA cores.
+int run_coeffs(const xhc_shape_t* sh, const Params& p, const void* X, const float* W, float* hpre, float* hpost,
+               float* hres, float* saved, void* x_in, cudaStream_t st) {
+  if (sh->dtype == XHC_BF16) {
+    if (tc_coeffs_supported(p))
+      return cuda_status(launch_coeffs_tc(p, X, W, hpre, hpost, hres, saved, x_in, st));
+    return cuda_status(launch_coeffs_simt<__nv_bfloat16>(p, X, W, hpre, hpost, hres, saved, x_in, st));
+  }
+  return cuda_status(launch_coeffs_simt<float>(p, X, W, hpre, hpost, hres, saved, x_in, st));
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* xhc_status_string(int status) {
+  switch (status) {
+    case XHC_OK: return "ok";
+    case XHC_ERR_SHAPE: return "bad shape";
+    case XHC_ERR_INDEX: return "bad active-index list";
+    case XHC_ERR_ALIGN: return "pointer or row not 16-byte aligned";
+    case XHC_ERR_DTYPE: return "unsupported dtype";
+    case XHC_ERR_WORKSPACE: return "workspace missing or too small";
+    case XHC_ERR_CUDA: return "CUDA launch failed";
+    case XHC_ERR_TIMEOUT: return "bounded device wait timed out";
+    case XHC_ERR_ARG: return "required pointer is NULL";
+    default: return "unknown status";
+  }
+}
+
+int xhc_last_cuda_error(void) { return g_last_cuda_error; }
+
+int xhc_num_logits(const xhc_shape_t* sh) {
+  if (!sh) return 0;
+  return sh->N + 4 * sh->k + sh->k * sh->k;
+}
+
+int xhc_coeffs(const xhc_shape_t* sh, const void* X, const float* W, float* hpre, float* hpost, float* hres,
+               float* saved, void* x_in, xhc_stream_t stream) {
+  int s = check_shape(sh);
+  if (s) return s;
+  if (tokens(sh) == 0) return XHC_OK;
+  if ((s = check_ptrs({X, W, hpre, hpost, hres}, {saved, x_in}))) return s;
+  const Params p = make_params(sh, nullptr);
+  return run_coeffs(sh, p, X, W, hpre, hpost, hres, saved, x_in, (cudaStream_t)stream);
+}
+
+int xhc_tfa(const xhc_shape_t* sh, const void* out, const float* w4, const float* w8, const float* w12, void* u,
+            xhc_stream_t stream) {
+  int s = check_shape(sh);
+  if (s) return s;
+  if (tokens(sh) == 0) return XHC_OK;
+  if ((s = check_ptrs({out, w4, w8, w12, u}, {}))) return s;
+  const Params p = make_params(sh, nullptr);
+  cudaStream_t st = (cudaStream_t)stream;
+  if (sh->dtype == XHC_BF16) return cuda_status(launch_tfa<__nv_bfloat16>(p, out, w4, w8, w12, u, st));
+  return cuda_status(launch_tfa<float>(p, out, w4, w8, w12, u, st));
+}
+
+int xhc_sparse_update(const xhc_shape_t* sh, const void* X_in, void* X_out, const void* out, const float* w4,
+                      const float* w8, const float* w12, const float* hpost, const float* hres, const int32_t* idx,
+                      xhc_stream_t stream) {
+  int s = check_shape(sh);
+  if (s) return s;
+  if ((s = check_idx(sh, idx))) return s;
+  bool has_conv = false;
+  if ((s = check_conv(w4, w8, w12, &has_conv))) return s;
+  if (tokens(sh) == 0) return XHC_OK;
+  if ((s = check_ptrs({X_in, X_out, out, hpost, hres}, {w4, w8, w12}))) return s;
+  const Params p = make_params(sh, idx);
+  cudaStream_t st = (cudaStream_t)stream;
+  if (sh->dtype == XHC_BF16) {
+    using T = __nv_bfloat16;
+    UpdArgs<T> a{(const T*)X_in, (T*)X_out, (const T*)out, {w4, w8, w12}, nullptr, hpost, hres, nullptr,
+                 nullptr, nullptr, X_out != X_in};
+    if (tc_update_supported(p)) return cuda_status(launch_update_tc(p, a, has_conv, st));
+    return cuda_status(launch_update_simt<T>(p, a, has_conv, st));
+  }
+  UpdArgs<float> a{(const float*)X_in, (float*)X_out, (const float*)out, {w4, w8, w12}, nullptr, hpost, hres,
+                   nullptr, nullptr, nullptr, X_out != X_in};
+  return cuda_status(launch_update_simt<float>(p, a, has_conv, st));
+}
+
+size_t xhc_fwd_workspace_bytes(const xhc_shape_t* sh) {
+  if (check_shape(sh)) return 0;
+  const Params p = make_params(sh, nullptr);
+  return round_up(tokens(sh) * (size_t)(p.P + 1) * sizeof(float));
+}
+
+int xhc_sublayer_fwd(const xhc_shape_t* sh, const void* X_in, void* X_out, const void* out, const float* w4,
+                     const float* w8, const float* w12, const float* W, const int32_t* idx, void* x_in, float* saved,
+                     void* saved_active, void* workspace, size_t ws_bytes, xhc_stream_t stream) {
+  int s = check_shape(sh);
+  if (s) return s;
+  if ((s = check_idx(sh, idx))) return s;
+  bool has_conv = false;
+  if ((s = check_conv(w4, w8, w12, &has_conv))) return s;
+  if (tokens(sh) == 0) return XHC_OK;
+  if ((s = check_ptrs({X_in, X_out, out, W}, {w4, w8, w12, x_in, saved, saved_active, workspace}))) return s;
+  float* z = saved;
+  if (!z) {
+    if (!workspace || ws_bytes < xhc_fwd_workspace_bytes(sh)) return XHC_ERR_WORKSPACE;
+    z = (float*)workspace;
+  }
+  const Params p = make_params(sh, idx);
+  cudaStream_t st = (cudaStream_t)stream;
+  if ((s = run_coeffs(sh, p, X_in, W, nullptr, nullptr, nullptr, z, x_in, st))) return s;
+  if (sh->dtype == XHC_BF16) {
+    using T = __nv_bfloat16;
+    UpdArgs<T> a{(const T*)X_in, (T*)X_out, (const T*)out, {w4, w8, w12}, nullptr, nullptr, nullptr, z,
+                 nullptr, (T*)saved_active, X_out != X_in};
+    if (tc_update_supported(p)) return cuda_status(launch_update_tc(p, a, has_conv, st));
+    return cuda_status(launch_update_simt<T>(p, a, has_conv, st));
+  }
+  UpdArgs<float> a{(const float*)X_in, (float*)X_out, (const float*)out, {w4, w8, w12}, nullptr, nullptr, nullptr,
+                   z, nullptr, (float*)saved_active, X_out != X_in};
+  return cuda_status(launch_update_simt<float>(p, a, has_conv, st));
+}
+
+namespace {
+struct BwdLayout {
+  size_t rec, saved, partial, gbuf, total;
+};
+BwdLayout bwd_layout(const xhc_shape_t* sh) {
+  const Params p = make_params(sh, nullptr);
+  BwdLayout L;
+  const size_t T = tokens(sh);
+  L.rec = 0;
+  L.saved = round_up(T * (size_t)(2 * p.P + 1) * sizeof(float));
+  L.partial = L.saved + round_up(T * (size_t)(p.P + 1) * sizeof(float));
+  size_t part = bwd_tfa_partial_floats(p) * sizeof(float);
+  if (sh->dtype == XHC_BF16 && tc_bwd_supported(p)) part = std::max(part, tc_bwd_partial_bytes(p));
+  L.gbuf = L.partial + round_up(part);
+  // copy of the active rows of dX' for the CUDA-core path when dX aliases dX'
+  const bool tc = sh->dtype == XHC_BF16 && tc_bwd_supported(p);
+  L.total = L.gbuf + (tc ? 0 : round_up(T * (size_t)p.k * (size_t)p.C * esize(sh)));
+  return L;
+}
+}  // namespace
+
+size_t xhc_bwd_workspace_bytes(const xhc_shape_t* sh) {
+  if (check_shape(sh)) return 0;
+  return bwd_layout(sh).total;
+}
+
+int xhc_sublayer_bwd(const xhc_shape_t* sh, const void* X_state, const void* saved_active, const void* out,
+                     const float* w4, const float* w8, const float* w12, const float* W, const int32_t* idx,
+                     const float* saved, const void* dXp, const void* dx_in, void* dX, void* dout, float* dw4,
+                     float* dw8, float* dw12, float* dW, void* workspace, size_t ws_bytes, xhc_stream_t stream) {
+  int s = check_shape(sh);
+  if (s) return s;
+  if ((s = check_idx(sh, idx))) return s;
+  bool has_conv = false;
+  if ((s = check_conv(w4, w8, w12, &has_conv))) return s;
+  bool has_dconv = false;
+  if ((s = check_conv(dw4, dw8, dw12, &has_dconv))) return s;
+  if (has_conv != has_dconv) return XHC_ERR_ARG;
+  if (saved_active && !saved) return XHC_ERR_ARG;   // recomputation needs the pre-update state
+  if ((s = check_ptrs({X_state, out, W, dXp, dX, dout, dW}, {saved_active, w4, w8, w12, saved, dx_in, dw4, dw8,
+                                                              dw12, workspace})))
+    return s;
+  const BwdLayout L = bwd_layout(sh);
+  if (tokens(sh) == 0) {
+    // empty batch: weight gradients are sums over no tokens
+    cudaStream_t st = (cudaStream_t)stream;
+    const Params p = make_params(sh, idx);
+    cudaError_t e = cudaMemsetAsync(dW, 0, (size_t)p.P * p.N * p.C * sizeof(float), st);
+    if (has_conv && e == cudaSuccess) e = cudaMemsetAsync(dw4, 0, (size_t)p.C * 4 * sizeof(float), st);
+    if (has_conv && e == cudaSuccess) e = cudaMemsetAsync(dw8, 0, (size_t)p.C * 8 * sizeof(float), st);
+    if (has_conv && e == cudaSuccess) e = cudaMemsetAsync(dw12, 0, (size_t)p.C * 12 * sizeof(float), st);
+    return cuda_status(e);
+  }
+  if (!workspace || ws_bytes < L.total) return XHC_ERR_WORKSPACE;
+  char* ws = (char*)workspace;
+  const Params p = make_params(sh, idx);
+  cudaStream_t st = (cudaStream_t)stream;
+  float* rec = (float*)(ws + L.rec);
+  const float* z = saved;
+  if (!z) {
+    float* zw = (float*)(ws + L.saved);
+    if ((s = run_coeffs(sh, p, X_state, W, nullptr, nullptr, nullptr, zw, nullptr, st))) return s;
+    z = zw;
+  }
+  float* partial = (float*)(ws + L.partial);
+  if (sh->dtype == XHC_BF16) {
+    using T = __nv_bfloat16;
+    BwdArgs<T> a{(const T*)X_state, (const T*)saved_active, (const T*)out, {w4, w8, w12}, W, z, (const T*)dXp,
+                 (const T*)dx_in, (T*)dX, (T*)dout, {dw4, dw8, dw12}, dW, rec, nullptr};
+    if (tc_bwd_supported(p)) return cuda_status(launch_bwd_tc(p, a, has_conv, partial, st));
+    if (dX == dXp) {
+      a.Gbuf = (const T*)(ws + L.gbuf);
+      if ((s = cuda_status(launch_gather_active<T>(p, (const T*)dXp, (T*)(ws + L.gbuf), st)))) return s;
+    }
+    return cuda_status(launch_bwd_simt<T>(p, a, has_conv, partial, true, st));
+  }
+  BwdArgs<float> a{(const float*)X_state, (const float*)saved_active, (const float*)out, {w4, w8, w12}, W, z,
+                   (const float*)dXp, (const float*)dx_in, (float*)dX, (float*)dout, {dw4, dw8, dw12}, dW, rec,
+                   nullptr};
+  if (dX == dXp) {
+    a.Gbuf = (const float*)(ws + L.gbuf);
+    if ((s = cuda_status(launch_gather_active<float>(p, (const float*)dXp, (float*)(ws + L.gbuf), st)))) return s;
+  }
+  return cuda_status(launch_bwd_simt<float>(p, a, has_conv, partial, true, st));
+}
+
+int xhc_copy(const void* src, void* dst, size_t bytes, xhc_stream_t stream) {
+  if (!src || !dst) return XHC_ERR_ARG;
+  if (!aligned16(src) || !aligned16(dst) || bytes % 16) return XHC_ERR_ALIGN;
+  if (bytes == 0) return XHC_OK;
+  return cuda_status(launch_copy16(src, dst, bytes, num_sms(), (cudaStream_t)stream));
+}
+
+}  // extern "C"

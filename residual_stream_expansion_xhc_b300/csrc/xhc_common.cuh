@@ -1,0 +1,134 @@
+// Shared device helpers of the xHC update kernels (sm_103a).
+//
+// Method: "xHC: Expanded Hyper-Connections" (qingkeai.online), sections
+// "Scaling N", "Temporal Feature Augmentation", "Dense read, sparse write".
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+namespace xhc {
+
+constexpr int NMAX = 16;             // streams
+constexpr int KMAX = 4;              // active streams
+constexpr int PMAX = NMAX + 4 * KMAX + KMAX * KMAX;   // 48 logits
+constexpr int ITERS_MAX = 64;        // Sinkhorn iterations
+constexpr int HALO = 11;             // longest conv (K = 12) reaches 11 tokens back
+constexpr int NTAPS = 4 + 8 + 12;    // taps of the three convolutions
+constexpr unsigned FULL = 0xffffffffu;
+
+// Kernel-side copy of the problem description.
+struct Params {
+  int B, S, N, C, k, P, iters;
+  float eps;
+  int idx[KMAX];
+  int is_active[NMAX];    // slot+1 of stream n if active, else 0
+};
+
+// ---------------------------------------------------------------- element access
+
+template <typename T> struct Vec;
+template <> struct Vec<float> {
+  static constexpr int W = 4;     // elements per 16-byte vector
+};
+template <> struct Vec<__nv_bfloat16> {
+  static constexpr int W = 8;
+};
+
+__device__ __forceinline__ void load_vec(const float* p, float (&v)[4]) {
+  float4 a = *reinterpret_cast<const float4*>(p);
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+}
+__device__ __forceinline__ void store_vec(float* p, const float (&v)[4]) {
+  *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+}
+__device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+__device__ __forceinline__ uint32_t pack_bf2(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);   // round to nearest even
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+__device__ __forceinline__ void load_vec(const __nv_bfloat16* p, float (&v)[8]) {
+  uint4 a = *reinterpret_cast<const uint4*>(p);
+  v[0] = bf_lo(a.x); v[1] = bf_hi(a.x); v[2] = bf_lo(a.y); v[3] = bf_hi(a.y);
+  v[4] = bf_lo(a.z); v[5] = bf_hi(a.z); v[6] = bf_lo(a.w); v[7] = bf_hi(a.w);
+}
+__device__ __forceinline__ void store_vec(__nv_bfloat16* p, const float (&v)[8]) {
+  uint4 a;
+  a.x = pack_bf2(v[0], v[1]); a.y = pack_bf2(v[2], v[3]);
+  a.z = pack_bf2(v[4], v[5]); a.w = pack_bf2(v[6], v[7]);
+  *reinterpret_cast<uint4*>(p) = a;
+}
+__device__ __forceinline__ float to_f(float x) { return x; }
+__device__ __forceinline__ float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+__device__ __forceinline__ void from_f(float& d, float x) { d = x; }
+__device__ __forceinline__ void from_f(__nv_bfloat16& d, float x) { d = __float2bfloat16_rn(x); }
+
+__device__ __forceinline__ float sigmoidf_(float z) { return 1.0f / (1.0f + expf(-z)); }
+
+// ---------------------------------------------------------------- Sinkhorn on 16 lanes
+//
+// One token's k x k H^res is held by a half-warp: lane e = 4 i + j holds entry
+// (i, j); entries with i >= k or j >= k are padding and stay 0.  Both halves
+// of the warp run the same code (two tokens per warp).  Row sums combine lanes
+// differing in bits 0-1, column sums lanes differing in bits 2-3; because IEEE
+// addition is commutative every lane of a row (column) obtains the same sum.
+// Section "Scaling N": H^res is made doubly stochastic by Sinkhorn
+// normalisation; each iteration normalises rows, then columns.
+
+__device__ __forceinline__ float rowsum16(float x) {
+  x += __shfl_xor_sync(FULL, x, 1);
+  x += __shfl_xor_sync(FULL, x, 2);
+  return x;
+}
+__device__ __forceinline__ float colsum16(float x) {
+  x += __shfl_xor_sync(FULL, x, 4);
+  x += __shfl_xor_sync(FULL, x, 8);
+  return x;
+}
+__device__ __forceinline__ float max16(float x) {
+  x = fmaxf(x, __shfl_xor_sync(FULL, x, 1));
+  x = fmaxf(x, __shfl_xor_sync(FULL, x, 2));
+  x = fmaxf(x, __shfl_xor_sync(FULL, x, 4));
+  x = fmaxf(x, __shfl_xor_sync(FULL, x, 8));
+  return x;
+}
+
+// M0 = exp(z - max z) over the valid entries.
+__device__ __forceinline__ float sinkhorn_init(float z, bool valid) {
+  float m = max16(valid ? z : -INFINITY);
+  return valid ? expf(z - m) : 0.0f;
+}
+
+// One iteration; optionally records the matrices entering each step.
+__device__ __forceinline__ float sinkhorn_step(float M, bool valid, float* before_row, float* before_col) {
+  if (before_row) *before_row = M;
+  float s = rowsum16(M);
+  M = valid ? M / s : 0.0f;
+  if (before_col) *before_col = M;
+  s = colsum16(M);
+  M = valid ? M / s : 0.0f;
+  return M;
+}
+
+__device__ __forceinline__ float sinkhorn16(float z, bool valid, int iters) {
+  float M = sinkhorn_init(z, valid);
+  for (int it = 0; it < iters; ++it) M = sinkhorn_step(M, valid, nullptr, nullptr);
+  return M;
+}
+
+// Reverse of one normalisation y = x / s (s = sum of x along the axis):
+// dx = dy / s - sum(dy * x) / s^2.
+__device__ __forceinline__ float norm_reverse_row(float g, float x, bool valid) {
+  float s = rowsum16(x);
+  float gx = rowsum16(g * x);
+  return valid ? (g / s - gx / (s * s)) : 0.0f;
+}
+__device__ __forceinline__ float norm_reverse_col(float g, float x, bool valid) {
+  float s = colsum16(x);
+  float gx = colsum16(g * x);
+  return valid ? (g / s - gx / (s * s)) : 0.0f;
+}
+
+}  // namespace xhc

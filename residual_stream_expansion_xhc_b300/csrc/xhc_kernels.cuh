@@ -1,0 +1,64 @@
+// Launcher interface between the C ABI (xhc_api.cu) and the kernel files.
+#pragma once
+
+#include "xhc_common.cuh"
+
+namespace xhc {
+
+template <typename T>
+struct UpdArgs {
+  const T* X_in;
+  T* X_out;
+  const T* out;
+  const float* w[3];
+  const float* hpre;     // [T, N] or nullptr
+  const float* hpost;    // [T, k, 4]; nullptr: coefficients come from `saved`
+  const float* hres;     // [T, k, k]
+  const float* saved;    // [T, P+1] (z, rstd)
+  T* x_in;               // nullptr: no dense read
+  T* saved_active;       // [T, k, C] or nullptr
+  int copy_inactive;     // X_out != X_in
+};
+
+template <typename T>
+struct BwdArgs {
+  const T* X;             // state before the update, or after it when saved_active != nullptr
+  const T* saved_active;  // [T, k, C] or nullptr
+  const T* out;
+  const float* w[3];
+  const float* W;
+  const float* saved;     // [T, P+1]
+  const T* dXp;
+  const T* dx_in;         // nullptr: no gradient through the dense read
+  T* dX;
+  T* dout;
+  float* dw[3];
+  float* dW;
+  float* rec;             // [T, 2P+1] per-token records (workspace)
+  const T* Gbuf;          // [T, k, C] copy of the active rows of dX' (used when dX aliases dX'), or nullptr
+};
+
+// Active row i of dX' for token t (G_i = dX'[a_i]), from dX' itself or from its copy.
+template <typename T>
+__device__ __forceinline__ const T* grad_row(const Params& p, const BwdArgs<T>& a, size_t t, int i) {
+  if (a.Gbuf) return a.Gbuf + (t * p.k + i) * (size_t)p.C;
+  return a.dXp + (t * p.N + p.idx[i]) * (size_t)p.C;
+}
+
+template <typename T>
+cudaError_t launch_coeffs_simt(const Params& p, const void* X, const float* W, float* hpre, float* hpost,
+                               float* hres, float* saved, void* x_in, cudaStream_t st);
+template <typename T>
+cudaError_t launch_update_simt(const Params& p, const UpdArgs<T>& a, bool has_conv, cudaStream_t st);
+template <typename T>
+cudaError_t launch_tfa(const Params& p, const void* out, const float* w4, const float* w8, const float* w12,
+                       void* u, cudaStream_t st);
+template <typename T>
+cudaError_t launch_bwd_simt(const Params& p, const BwdArgs<T>& a, bool has_conv, float* partial, bool do_token,
+                            cudaStream_t st);
+size_t bwd_tfa_partial_floats(const Params& p);
+template <typename T>
+cudaError_t launch_gather_active(const Params& p, const T* src, T* dst, cudaStream_t st);
+cudaError_t launch_copy16(const void* src, void* dst, size_t bytes, int sms, cudaStream_t st);
+
+}  // namespace xhc

@@ -1,0 +1,20 @@
+// Tensor-core (tcgen05 / TMEM / TMA) kernels of the xHC update for bf16 state.
+#pragma once
+
+#include "xhc_kernels.cuh"
+
+namespace xhc {
+
+bool tc_coeffs_supported(const Params& p);
+cudaError_t launch_coeffs_tc(const Params& p, const void* X, const float* W, float* hpre, float* hpost, float* hres,
+                             float* saved, void* x_in, cudaStream_t st);
+
+bool tc_update_supported(const Params& p);
+cudaError_t launch_update_tc(const Params& p, const UpdArgs<__nv_bfloat16>& a, bool has_conv, cudaStream_t st);
+
+bool tc_bwd_supported(const Params& p);
+size_t tc_bwd_partial_bytes(const Params& p);
+cudaError_t launch_bwd_tc(const Params& p, const BwdArgs<__nv_bfloat16>& a, bool has_conv, float* partial,
+                          cudaStream_t st);
+
+}  // namespace xhc

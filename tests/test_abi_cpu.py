@@ -1,0 +1,123 @@
+"""The C-ABI library loads, exports every symbol include/xhc.h declares, and
+rejects bad arguments on the host before any launch (no GPU needed: every
+call below returns from host-side validation)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "xhc.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(xhc_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from residual_stream_expansion_xhc_b300 import _lib
+    return _lib
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(lib.LIB, n), n
+    assert set(names) == set(lib.EXPORTS)
+    out = subprocess.run(["nm", "-D", "--defined-only", lib.LIB_PATH], capture_output=True, text=True).stdout
+    for n in names:
+        assert re.search(rf"\bT {n}$", out, flags=re.M), n
+
+
+def shape(lib, B=2, S=8, N=16, C=256, k=4, dtype=1, iters=20, eps=1e-6):
+    return lib.XhcShape(B, S, N, C, k, dtype, iters, eps)
+
+
+FAKE = ctypes.c_void_p(1 << 20)        # 16-byte aligned, never dereferenced on the host
+MIS = ctypes.c_void_p((1 << 20) + 8)   # misaligned
+
+
+def idx(*v):
+    return (ctypes.c_int32 * len(v))(*v)
+
+
+def fwd(lib, sh, ix, X=FAKE, W=FAKE, conv=(None, None, None), ws=None, ws_bytes=0, saved=None):
+    return lib.LIB.xhc_sublayer_fwd(ctypes.byref(sh), X, X, FAKE, conv[0], conv[1], conv[2], W, ix, None, saved,
+                                    None, ws, ws_bytes, None)
+
+
+def test_status_strings(lib):
+    for s in range(9):
+        assert lib.LIB.xhc_status_string(s)
+    assert lib.LIB.xhc_status_string(99) == b"unknown status"
+
+
+def test_num_logits(lib):
+    assert lib.LIB.xhc_num_logits(ctypes.byref(shape(lib))) == 48
+    assert lib.LIB.xhc_num_logits(ctypes.byref(shape(lib, N=4, k=4))) == 36
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(N=17), 1), (dict(N=0), 1), (dict(k=5), 1), (dict(k=0), 1), (dict(N=3, k=4), 1),
+    (dict(iters=65), 1), (dict(iters=-1), 1), (dict(eps=0.0), 1), (dict(B=-1), 1),
+    (dict(dtype=7), 4), (dict(C=100), 3), (dict(C=6, dtype=0), 3)])
+def test_shape_rejected(lib, kw, status):
+    sh = shape(lib, **kw)
+    assert fwd(lib, sh, idx(0, 1, 2, 3)) == status
+
+
+@pytest.mark.parametrize("ix", [(0, 1, 2, 2), (0, 1, 2, 16), (-1, 1, 2, 3)])
+def test_index_rejected(lib, ix):
+    assert fwd(lib, shape(lib), idx(*ix)) == 2
+
+
+def test_null_and_alignment_rejected(lib):
+    sh = shape(lib)
+    assert fwd(lib, sh, idx(0, 1, 2, 3), X=None) == 8
+    assert fwd(lib, sh, idx(0, 1, 2, 3), X=MIS) == 3
+    assert fwd(lib, sh, None) == 2
+    # conv weights: all three or none
+    assert fwd(lib, sh, idx(0, 1, 2, 3), conv=(FAKE, None, FAKE)) == 8
+    # no saved coefficients and no workspace
+    assert fwd(lib, sh, idx(0, 1, 2, 3)) == 5
+    need = lib.LIB.xhc_fwd_workspace_bytes(ctypes.byref(sh))
+    assert need >= 2 * 8 * 49 * 4
+    assert fwd(lib, sh, idx(0, 1, 2, 3), ws=FAKE, ws_bytes=need - 1) == 5
+
+
+def test_empty_forward_launches_nothing(lib):
+    sh = shape(lib, B=0)
+    assert fwd(lib, sh, idx(0, 1, 2, 3)) == 0
+
+
+def test_backward_rejections(lib):
+    sh = shape(lib)
+    L = lib.LIB
+    need = L.xhc_bwd_workspace_bytes(ctypes.byref(sh))
+    assert need > 0
+    args = dict(X=FAKE, act=None, out=FAKE, w=(None, None, None), W=FAKE, saved=FAKE, dXp=FAKE, dxi=None, dX=FAKE,
+                dout=FAKE, dw=(None, None, None), dW=FAKE, ws=FAKE, wsb=need)
+
+    def call(**kw):
+        a = dict(args)
+        a.update(kw)
+        return L.xhc_sublayer_bwd(ctypes.byref(sh), a["X"], a["act"], a["out"], *a["w"], a["W"], idx(0, 1, 2, 3),
+                                  a["saved"], a["dXp"], a["dxi"], a["dX"], a["dout"], *a["dw"], a["dW"], a["ws"],
+                                  a["wsb"], None)
+    assert call(wsb=need - 1) == 5
+    assert call(ws=None) == 5
+    assert call(w=(FAKE, FAKE, FAKE)) == 8               # conv weights without their gradients
+    assert call(act=FAKE, saved=None) == 8               # recomputation needs the pre-update state
+    assert call(dW=MIS) == 3
+
+
+def test_copy_rejections(lib):
+    assert lib.LIB.xhc_copy(FAKE, FAKE, 24, None) == 3
+    assert lib.LIB.xhc_copy(None, FAKE, 32, None) == 8
+    assert lib.LIB.xhc_copy(FAKE, FAKE, 0, None) == 0
