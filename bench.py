@@ -1,0 +1,434 @@
+#!/usr/bin/env python3
+"""Benchmark of the xHC per-sublayer residual-stream update on B300.
+
+One step = the whole per-sublayer hot path on one batch: the fused forward in
+training mode (in-place state update, dense read x_in, saved logits and the
+saved active rows) followed by the fused backward (dL/dX', no gradient through
+x_in), on the bf16 workload B=4, S=4096, N=16, C=2048, k=4 with seeded
+synthetic inputs (X, out ~ N(0,1); conv weights and W ~ N(0, 0.02)).
+
+Prints one JSON line (rank 0).  `--impl reference` times the fp64 CPU oracle
+(on host cores) on a bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from residual_stream_expansion_xhc_b300 import inputs as xin  # noqa: E402
+
+METRIC = "tokens/s per xHC sublayer (fwd, fwd+bwd) and achieved HBM GB/s vs peak"
+
+# Algorithmic bytes per token of each kernel, in C-units (one row of C
+# elements of the state dtype) plus fixed per-token fp32 side data.
+#   forward, fused:   16 (read X) + 1 (read out) + 4 (write active rows)
+#                     + 1 (write x_in) + 4 (write saved active rows) = 26
+#   backward, token:  4 (dX' active) + 4 (old active rows) + 1 (out) = 9
+#   backward, stream: 16 (X) + 16 (dX') + 1 (out) + 16 (dX) + 1 (dout) = 50
+ALG_C = {
+    "fwd_fused_tc": 26, "coeffs_tc": 17, "coeffs_simt": 17, "update_tc": 9, "update_simt": 13,
+    "bwd_token_tc": 9, "bwd_token_simt": 9, "bwd_stream_tc": 50, "bwd_dx_simt": 48, "bwd_dw_simt": 16,
+    "bwd_tfa_simt": 6, "gather_active": 8,
+}
+ALG_SIDE = {  # fp32 bytes per token
+    "fwd_fused_tc": 0, "coeffs_tc": 0, "coeffs_simt": 0, "bwd_token_tc": 0, "bwd_token_simt": 0,
+}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6400.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup():
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- oracle timing
+
+def oracle_sample(wl, tensors, ntok: int):
+    """The first ``ntok`` tokens of sequence 0 of the workload (exact for those
+    tokens: nothing before a sequence start enters the update)."""
+    X = xin.to_f64(wl, tensors.X[:1, :ntok])
+    out = xin.to_f64(wl, tensors.out[:1, :ntok])
+    dXp = xin.to_f64(wl, tensors.dXp[:1, :ntok])
+    conv = None if tensors.conv is None else tuple(np.asarray(w, np.float64) for w in tensors.conv)
+    return X, out, conv, np.asarray(tensors.W, np.float64), tensors.idx, dXp
+
+
+def time_oracle(sample, wl):
+    from oracle import xhc_oracle as xo
+    X, out, conv, W, idx, dXp = sample
+    t0 = time.perf_counter()
+    xo.forward(X, out, conv, W, idx, iters=wl.iters, eps=wl.eps)
+    xo.backward(X, out, conv, W, idx, dXp, None, iters=wl.iters, eps=wl.eps)
+    return time.perf_counter() - t0
+
+
+def blas_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [d.get("num_threads", 1) for d in threadpool_info()]
+        return max(n) if n else 1
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(wl, tensors, ntok=1024):
+    sample = oracle_sample(wl, tensors, ntok)
+    dt = time_oracle(sample, wl)
+    return {"value": ntok / dt, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
+            "sample": f"fp64 numpy oracle, forward+backward of the first {ntok} tokens of sequence 0 "
+                      f"({dt:.1f} s)"}
+
+
+def run_reference(args, wl):
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return
+    tensors = xin.make(wl, grads=True)
+    ntok = args.ref_tokens
+    sample = oracle_sample(wl, tensors, ntok)
+    for _ in range(args.warmup):
+        time_oracle(sample, wl)
+    t = sum(time_oracle(sample, wl) for _ in range(args.steps))
+    value = ntok * args.steps / t
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl_desc(wl), "sample_tokens_per_step": ntok},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
+                             "sample": f"fp64 numpy oracle, forward+backward of the first {ntok} tokens of "
+                                       f"sequence 0 per step"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def wl_desc(wl):
+    return (f"{wl.name}: B={wl.B} S={wl.S} N={wl.N} C={wl.C} k={wl.k} {wl.dtype}; forward (training mode: in "
+            f"place, x_in, saved logits, saved active rows) + backward (dX', no dx_in)")
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+class Step:
+    """Device buffers of one sublayer and the fused forward + backward calls."""
+
+    def __init__(self, wl, tensors, dev):
+        import torch
+        from residual_stream_expansion_xhc_b300 import api
+        self.api, self.wl, self.torch = api, wl, torch
+        dt = torch.bfloat16 if wl.dtype == "bf16" else torch.float32
+
+        def act(a):
+            if wl.dtype == "f32":
+                return torch.from_numpy(a).to(dev)
+            return torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+
+        self.sh = api.make_shape(wl.B, wl.S, wl.N, wl.C, wl.k, dt, wl.iters, wl.eps)
+        self.X = act(tensors.X)
+        self.out = act(tensors.out)
+        self.dXp = act(tensors.dXp)
+        self.conv = None if tensors.conv is None else tuple(torch.from_numpy(w).to(dev) for w in tensors.conv)
+        self.W = torch.from_numpy(tensors.W).to(dev)
+        self.idx = [int(i) for i in tensors.idx]
+        B, S, N, C, k, P = wl.B, wl.S, wl.N, wl.C, wl.k, wl.P
+        self.x_in = torch.empty(B, S, C, dtype=dt, device=dev)
+        self.saved = torch.empty(B, S, P + 1, dtype=torch.float32, device=dev)
+        self.act = torch.empty(B, S, k, C, dtype=dt, device=dev)
+        self.dX = torch.empty_like(self.X)
+        self.dout = torch.empty_like(self.out)
+        self.dconv = None if self.conv is None else tuple(torch.empty_like(w) for w in self.conv)
+        self.dW = torch.empty_like(self.W)
+        self.ws = api.workspace(api.xhc_bwd_workspace_bytes(self.sh), dev)
+
+    def fwd(self):
+        self.api.xhc_sublayer_fwd(self.sh, self.X, self.X, self.out, self.conv, self.W, self.idx, x_in=self.x_in,
+                                  saved=self.saved, saved_active=self.act)
+
+    def bwd(self):
+        self.api.xhc_sublayer_bwd(self.sh, self.X, self.act, self.out, self.conv, self.W, self.idx, self.saved,
+                                  self.dXp, None, self.dX, self.dout, self.dconv, self.dW, self.ws)
+
+    def __call__(self):
+        self.fwd()
+        self.bwd()
+
+
+def timed(fn, steps):
+    import torch
+    s = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(s)
+    for _ in range(steps):
+        fn()
+    e1.record(s)
+    e1.synchronize()
+    return e0.elapsed_time(e1)
+
+
+def copy_peak(dev):
+    import torch
+    from residual_stream_expansion_xhc_b300 import api
+    n = 1 << 30
+    a = torch.empty(n, dtype=torch.uint8, device=dev)
+    a.fill_(1)
+    b = torch.empty_like(a)
+    api.xhc_copy(a, b)
+    ms = timed(lambda: api.xhc_copy(a, b), 10)
+    del a, b
+    return 2 * n * 10 / (ms * 1e-3) / 1e9
+
+
+def e2e_run(step, tensors, steps):
+    """Host buffers through the public API: pinned host -> device copies of the
+    step's inputs (X, out, dX'), forward + backward, device -> host reads of
+    its results (X', dX, dout, dW, conv-weight gradients)."""
+    torch = step.torch
+    wl = step.wl
+
+    def pinned(a):
+        t = torch.from_numpy(a if wl.dtype == "f32" else a.view(np.int16))
+        return t.pin_memory()
+
+    hX, hout, hdXp = pinned(tensors.X), pinned(tensors.out), pinned(tensors.dXp)
+    rX, rdX = torch.empty_like(hX).pin_memory(), torch.empty_like(hdXp).pin_memory()
+    rdout = torch.empty_like(hout).pin_memory()
+    rdW = torch.empty(step.W.shape, dtype=torch.float32).pin_memory()
+    rdc = None if step.dconv is None else [torch.empty(w.shape, dtype=torch.float32).pin_memory() for w in step.dconv]
+    as_raw = (lambda t: t) if wl.dtype == "f32" else (lambda t: t.view(torch.int16))
+
+    def one():
+        as_raw(step.X).copy_(hX, non_blocking=True)
+        as_raw(step.out).copy_(hout, non_blocking=True)
+        as_raw(step.dXp).copy_(hdXp, non_blocking=True)
+        step()
+        rX.copy_(as_raw(step.X), non_blocking=True)
+        rdX.copy_(as_raw(step.dX), non_blocking=True)
+        rdout.copy_(as_raw(step.dout), non_blocking=True)
+        rdW.copy_(step.dW, non_blocking=True)
+        if rdc is not None:
+            for h, d in zip(rdc, step.dconv):
+                h.copy_(d, non_blocking=True)
+
+    one()
+    ms = timed(one, steps)
+    h2d = sum(t.numel() * t.element_size() for t in (hX, hout, hdXp))
+    d2h = sum(t.numel() * t.element_size() for t in (rX, rdX, rdout, rdW)) + (
+        0 if rdc is None else sum(t.numel() * 4 for t in rdc))
+    return {"value": wl.tokens * steps / (ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
+            "d2h_bytes_per_step": int(d2h), "ms_per_step": ms / steps}
+
+
+def run_gpu(args, wl):
+    import torch
+    world, rank, local = dist_setup()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    from residual_stream_expansion_xhc_b300 import api
+
+    tensors = xin.make(wl, grads=True)
+    step = Step(wl, tensors, dev)
+    same_run_copy = copy_peak(dev)
+    esz = wl.esize
+    cunit = wl.C * esz
+
+    for _ in range(args.warmup):
+        step()
+    # forward alone and backward alone (for the per-pass numbers)
+    torch.cuda.synchronize()
+    fwd_ms = timed(step.fwd, args.steps) / args.steps
+    bwd_ms = timed(step.bwd, args.steps) / args.steps
+
+    api.xhc_timing_collect()
+    torch.cuda.synchronize()
+    barrier(world)
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    api.xhc_timing_enable(True)
+    ms = timed(step, args.steps)
+    api.xhc_timing_enable(False)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop() if sampler else None
+    kern = api.xhc_timing_collect()
+    ms = max_over_ranks(ms, world)
+    ms_step = ms / args.steps
+    tokens = wl.tokens * world
+    value = tokens * args.steps / (ms * 1e-3)
+
+    peak, peak_kind = load_peaks()
+    dom = max(kern.items(), key=lambda kv: kv[1][1])
+    dname, (dcount, dtotal) = dom
+    per_launch_ms = dtotal / dcount
+    alg = (ALG_C.get(dname, 0) * cunit + ALG_SIDE.get(dname, 0)) * wl.tokens
+    achieved = alg / (per_launch_ms * 1e-3) / 1e9
+    traffic = load_traffic(dname)
+    e2e = None
+    if not args.no_e2e:
+        e2e = e2e_run(step, tensors, args.e2e_steps)
+        e2e["value"] *= world
+    cpu = None
+    if rank == 0 and not args.no_cpu:
+        cpu = cpu_baseline(wl, tensors, args.cpu_tokens)
+    if rank != 0:
+        return
+    fwd_alg = 26 * cunit * wl.tokens
+    bwd_alg = 59 * cunit * wl.tokens
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
+        "config": {"workload": wl_desc(wl), "tokens_per_step_per_gpu": wl.tokens,
+                   "l2": "inputs larger than L2 (state X is %.2f GB per GPU)" % (wl.tokens * wl.N * cunit / 1e9),
+                   "parallelism": f"replicas x{world} (independent batches, no collective)"},
+        "roofline": {"kernel": dname, "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_kind})",
+                     "alg_bytes_per_launch": alg, "launch_ms": per_launch_ms},
+        "fwd": {"tokens_per_s": wl.tokens / (fwd_ms * 1e-3), "ms": fwd_ms,
+                "alg_GBps": fwd_alg / (fwd_ms * 1e-3) / 1e9, "alg_bytes": fwd_alg},
+        "bwd": {"tokens_per_s": wl.tokens / (bwd_ms * 1e-3), "ms": bwd_ms,
+                "alg_GBps": bwd_alg / (bwd_ms * 1e-3) / 1e9, "alg_bytes": bwd_alg},
+        "kernels": {k: {"launches": c, "avg_ms": t / c, "share": t / sum(v[1] for v in kern.values())}
+                    for k, (c, t) in kern.items()},
+        "gpu_launches": int(sum(c for c, _ in kern.values())),
+        "same_run_copy_GBps": same_run_copy,
+        "clocks": clocks,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def load_traffic(kernel: str):
+    """DRAM bytes per launch of the kernel from a committed ncu summary, or None."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    v = d.get(kernel)
+    return None if v is None else v.get("bytes_per_launch")
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["xhc", "reference"], default="xhc")
+    ap.add_argument("--workload", default="fwdbwd_bf16", choices=sorted(xin.WORKLOADS))
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--cpu-tokens", type=int, default=8192)
+    ap.add_argument("--ref-tokens", type=int, default=256)
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    wl = xin.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, wl)
+    else:
+        run_gpu(args, wl)
+
+
+if __name__ == "__main__":
+    main()

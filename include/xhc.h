@@ -203,6 +203,19 @@ int xhc_sublayer_bwd(const xhc_shape_t* sh, const void* X_state,
  */
 int xhc_copy(const void* src, void* dst, size_t bytes, xhc_stream_t stream);
 
+/*
+ * Optional per-kernel timing.  While enabled (on != 0), every kernel the
+ * library launches is bracketed by two CUDA events recorded on the stream it
+ * runs on.  xhc_timing_collect waits for the recorded events, writes for each
+ * distinct kernel name its launch count and total milliseconds (names: up to
+ * max_kernels entries of 48 bytes each, NUL-terminated), clears the record
+ * and returns the number of entries written (a negative status on a CUDA
+ * error).  Any of names / counts / total_ms may be NULL.  Not thread-safe:
+ * enable it only around single-threaded use of the library.
+ */
+int xhc_timing_enable(int on);
+int xhc_timing_collect(char* names, int* counts, float* total_ms, int max_kernels);
+
 #ifdef __cplusplus
 }
 #endif

@@ -18,7 +18,7 @@ STATUS = {0: "XHC_OK", 1: "XHC_ERR_SHAPE", 2: "XHC_ERR_INDEX", 3: "XHC_ERR_ALIGN
 
 EXPORTS = ("xhc_status_string", "xhc_last_cuda_error", "xhc_num_logits", "xhc_coeffs", "xhc_tfa",
            "xhc_sparse_update", "xhc_fwd_workspace_bytes", "xhc_sublayer_fwd", "xhc_bwd_workspace_bytes",
-           "xhc_sublayer_bwd", "xhc_copy")
+           "xhc_sublayer_bwd", "xhc_copy", "xhc_timing_enable", "xhc_timing_collect")
 
 
 class XhcShape(ctypes.Structure):
@@ -66,6 +66,10 @@ def _load() -> ctypes.CDLL:
     lib.xhc_sublayer_bwd.argtypes = [sh, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, Z, P]
     lib.xhc_copy.restype = I
     lib.xhc_copy.argtypes = [P, P, Z, P]
+    lib.xhc_timing_enable.restype = I
+    lib.xhc_timing_enable.argtypes = [I]
+    lib.xhc_timing_collect.restype = I
+    lib.xhc_timing_collect.argtypes = [ctypes.c_char_p, ctypes.POINTER(I), ctypes.POINTER(ctypes.c_float), I]
     return lib
 
 

@@ -109,3 +109,23 @@ def xhc_copy(src: Tensor, dst: Tensor, nbytes: Optional[int] = None, stream=None
 def workspace(nbytes: int, device="cuda") -> Tensor:
     """A caller-owned workspace buffer (uint8) of at least ``nbytes`` bytes."""
     return torch.empty(max(int(nbytes), 16), dtype=torch.uint8, device=device)
+
+
+def xhc_timing_enable(on: bool = True):
+    LIB.xhc_timing_enable(1 if on else 0)
+
+
+def xhc_timing_collect(max_kernels: int = 64) -> dict:
+    """{kernel name: (launches, total ms)} since the last collect."""
+    names = ctypes.create_string_buffer(48 * max_kernels)
+    counts = (ctypes.c_int * max_kernels)()
+    ms = (ctypes.c_float * max_kernels)()
+    n = LIB.xhc_timing_collect(names, counts, ms, max_kernels)
+    if n < 0:
+        raise XhcError("xhc_timing_collect", -n, LIB)
+    raw = names.raw
+    out = {}
+    for i in range(n):
+        nm = raw[48 * i: 48 * i + 48].split(b"\0", 1)[0].decode()
+        out[nm] = (int(counts[i]), float(ms[i]))
+    return out

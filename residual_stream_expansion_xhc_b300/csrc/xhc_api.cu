@@ -2,6 +2,8 @@
 // Declarations and argument conventions: include/xhc.h.
 #include <algorithm>
 #include <cstring>
+#include <string>
+#include <vector>
 
 #include "../../include/xhc.h"
 #include "xhc_kernels.cuh"
@@ -105,9 +107,89 @@ int run_coeffs(const xhc_shape_t* sh, const Params& p, const void* X, const floa
   return cuda_status(launch_coeffs_simt<float>(p, X, W, hpre, hpost, hres, saved, x_in, st));
 }
 
+// ---------------------------------------------------------------- timing records
+
+struct TimingRec {
+  const char* name;
+  cudaEvent_t a, b;
+};
+bool g_timing = false;
+std::vector<TimingRec> g_recs;
+std::vector<cudaEvent_t> g_pool;
+int g_open = -1;
+constexpr size_t kMaxRecs = 1 << 16;
+
+cudaEvent_t pooled_event() {
+  if (!g_pool.empty()) {
+    cudaEvent_t e = g_pool.back();
+    g_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
 }  // namespace
 
+namespace xhc {
+void timing_begin(const char* name, cudaStream_t st) {
+  g_open = -1;
+  if (!g_timing || g_recs.size() >= kMaxRecs) return;
+  TimingRec r{name, pooled_event(), pooled_event()};
+  if (!r.a || !r.b) return;
+  cudaEventRecord(r.a, st);
+  g_recs.push_back(r);
+  g_open = (int)g_recs.size() - 1;
+}
+void timing_end(cudaStream_t st) {
+  if (!g_timing || g_open < 0) return;
+  cudaEventRecord(g_recs[g_open].b, st);
+  g_open = -1;
+}
+}  // namespace xhc
+
 extern "C" {
+
+int xhc_timing_enable(int on) {
+  g_timing = on != 0;
+  return XHC_OK;
+}
+
+int xhc_timing_collect(char* names, int* counts, float* total_ms, int max_kernels) {
+  std::vector<std::string> keys;
+  std::vector<int> cnt;
+  std::vector<double> tot;
+  int status = XHC_OK;
+  for (const TimingRec& r : g_recs) {
+    float ms = 0.0f;
+    cudaError_t e = cudaEventSynchronize(r.b);
+    if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, r.a, r.b);
+    if (e != cudaSuccess) status = cuda_status(e);
+    size_t i = 0;
+    while (i < keys.size() && keys[i] != r.name) ++i;
+    if (i == keys.size()) {
+      keys.push_back(r.name);
+      cnt.push_back(0);
+      tot.push_back(0.0);
+    }
+    cnt[i] += 1;
+    tot[i] += ms;
+    g_pool.push_back(r.a);
+    g_pool.push_back(r.b);
+  }
+  g_recs.clear();
+  const int n = (int)std::min(keys.size(), (size_t)std::max(max_kernels, 0));
+  for (int i = 0; i < n; ++i) {
+    if (names) {
+      std::strncpy(names + 48 * i, keys[i].c_str(), 47);
+      names[48 * i + 47] = 0;
+    }
+    if (counts) counts[i] = cnt[i];
+    if (total_ms) total_ms[i] = (float)tot[i];
+  }
+  return status == XHC_OK ? n : -status;
+}
 
 const char* xhc_status_string(int status) {
   switch (status) {

@@ -5,6 +5,11 @@
 
 namespace xhc {
 
+// Optional per-kernel timing (see xhc_timing_enable in the C header): when
+// enabled, every launch is bracketed by CUDA events on its stream.
+void timing_begin(const char* name, cudaStream_t st);
+void timing_end(cudaStream_t st);
+
 template <typename T>
 struct UpdArgs {
   const T* X_in;

@@ -715,7 +715,9 @@ __global__ void gather_active_kernel(Params p, const T* __restrict__ src, T* __r
 
 template <typename T>
 cudaError_t launch_gather_active(const Params& p, const T* src, T* dst, cudaStream_t st) {
+  timing_begin("gather_active", st);
   gather_active_kernel<T><<<(unsigned)((size_t)p.B * p.S), 256, 0, st>>>(p, src, dst);
+  timing_end(st);
   return cudaGetLastError();
 }
 template cudaError_t launch_gather_active<float>(const Params&, const float*, float*, cudaStream_t);
@@ -733,7 +735,9 @@ template <typename T>
 cudaError_t launch_coeffs_simt(const Params& p, const void* X, const float* W, float* hpre, float* hpost,
                                float* hres, float* saved, void* x_in, cudaStream_t st) {
   const size_t T_all = (size_t)p.B * p.S;
+  timing_begin("coeffs_simt", st);
   coeffs_simt_kernel<T><<<(unsigned)T_all, 256, 0, st>>>(p, (const T*)X, W, hpre, hpost, hres, saved, (T*)x_in);
+  timing_end(st);
   return cudaGetLastError();
 }
 
@@ -742,6 +746,7 @@ cudaError_t launch_update_simt(const Params& p, const UpdArgs<T>& a, bool has_co
   constexpr int CC = 32 * Vec<T>::W;
   dim3 grid((p.C + CC - 1) / CC, (p.S + UPD_TT - 1) / UPD_TT, p.B);
   size_t smem = ((UPD_TT + HALO) * CC + (has_conv ? NTAPS * CC : 0) + UPD_TT * PMAX) * sizeof(float);
+  timing_begin("update_simt", st);
   if (has_conv) {
     cudaFuncSetAttribute(update_simt_kernel<T, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     update_simt_kernel<T, true><<<grid, 256, smem, st>>>(p, a);
@@ -749,6 +754,7 @@ cudaError_t launch_update_simt(const Params& p, const UpdArgs<T>& a, bool has_co
     cudaFuncSetAttribute(update_simt_kernel<T, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     update_simt_kernel<T, false><<<grid, 256, smem, st>>>(p, a);
   }
+  timing_end(st);
   return cudaGetLastError();
 }
 
@@ -759,7 +765,9 @@ cudaError_t launch_tfa(const Params& p, const void* out, const float* w4, const 
   dim3 grid((p.C + CC - 1) / CC, (p.S + UPD_TT - 1) / UPD_TT, p.B);
   size_t smem = ((UPD_TT + HALO) * CC + NTAPS * CC) * sizeof(float);
   cudaFuncSetAttribute(tfa_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  timing_begin("tfa", st);
   tfa_kernel<T><<<grid, 256, smem, st>>>(p, (const T*)out, w4, w8, w12, (T*)u);
+  timing_end(st);
   return cudaGetLastError();
 }
 
@@ -774,40 +782,54 @@ cudaError_t launch_bwd_simt(const Params& p, const BwdArgs<T>& a, bool has_conv,
   const size_t T_all = (size_t)p.B * p.S;
   constexpr int V = Vec<T>::W;
   if (do_token) {
+    timing_begin("bwd_token_simt", st);
     if (has_conv) bwd_token_simt_kernel<T, true><<<(unsigned)T_all, 256, 0, st>>>(p, a);
     else bwd_token_simt_kernel<T, false><<<(unsigned)T_all, 256, 0, st>>>(p, a);
+    timing_end(st);
   }
   {
     dim3 grid((p.C + TFA_CC - 1) / TFA_CC, (p.S + TFA_TT - 1) / TFA_TT, p.B);
     size_t smem = ((TFA_TT + HALO) * 4 * TFA_CC + (TFA_TT + HALO) * TFA_CC + 8 * NTAPS * TFA_CC) * sizeof(float);
     if (has_conv) {
       cudaFuncSetAttribute(bwd_tfa_simt_kernel<T, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      timing_begin("bwd_tfa_simt", st);
       bwd_tfa_simt_kernel<T, true><<<grid, 256, smem, st>>>(p, a, partial);
+      timing_end(st);
       const int ntiles = (int)(grid.y * grid.z);
       const int n = NTAPS * p.C;
+      timing_begin("bwd_tfa_reduce", st);
       bwd_tfa_reduce_kernel<<<(n + 255) / 256, 256, 0, st>>>(ntiles, p.C, partial, a.dw[0], a.dw[1], a.dw[2]);
+      timing_end(st);
     } else {
       cudaFuncSetAttribute(bwd_tfa_simt_kernel<T, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      timing_begin("bwd_tfa_simt", st);
       bwd_tfa_simt_kernel<T, false><<<grid, 256, smem, st>>>(p, a, partial);
+      timing_end(st);
     }
   }
   {
     const size_t NC = (size_t)p.N * p.C;
+    timing_begin("bwd_dw_simt", st);
     bwd_dw_simt_kernel<T><<<(unsigned)((NC + 63) / 64), 256, 0, st>>>(p, a);
+    timing_end(st);
   }
   {
     constexpr int CC = 32 * V;
     dim3 grid((p.C + CC - 1) / CC, p.N, (unsigned)((T_all + 31) / 32));
     size_t smem = (PMAX * CC + 32 * (2 * p.P + 1)) * sizeof(float);
     cudaFuncSetAttribute(bwd_dx_simt_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    timing_begin("bwd_dx_simt", st);
     bwd_dx_simt_kernel<T><<<grid, 256, smem, st>>>(p, a);
+    timing_end(st);
   }
   return cudaGetLastError();
 }
 
 cudaError_t launch_copy16(const void* src, void* dst, size_t bytes, int sms, cudaStream_t st) {
   const size_t n = bytes / 16;
+  timing_begin("copy16", st);
   copy16_kernel<<<sms * 4, 512, 0, st>>>((const uint4*)src, (uint4*)dst, n);
+  timing_end(st);
   return cudaGetLastError();
 }
 
