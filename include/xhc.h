@@ -91,6 +91,14 @@ const char* xhc_status_string(int status);
 /* cudaError_t of the most recent XHC_ERR_CUDA in this process (0 if none). */
 int xhc_last_cuda_error(void);
 
+/*
+ * Status of the library's bounded device-side waits.  Synchronises `stream`,
+ * returns XHC_ERR_TIMEOUT if a kernel gave up waiting since the last call (the
+ * affected outputs are then undefined) and clears the record; XHC_OK
+ * otherwise.
+ */
+int xhc_device_status(xhc_stream_t stream);
+
 /* Number of projection rows P = N + 4k + k^2 for a shape. */
 int xhc_num_logits(const xhc_shape_t* sh);
 

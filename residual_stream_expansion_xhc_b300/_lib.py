@@ -16,7 +16,7 @@ XHC_F32, XHC_BF16 = 0, 1
 STATUS = {0: "XHC_OK", 1: "XHC_ERR_SHAPE", 2: "XHC_ERR_INDEX", 3: "XHC_ERR_ALIGN", 4: "XHC_ERR_DTYPE",
           5: "XHC_ERR_WORKSPACE", 6: "XHC_ERR_CUDA", 7: "XHC_ERR_TIMEOUT", 8: "XHC_ERR_ARG"}
 
-EXPORTS = ("xhc_status_string", "xhc_last_cuda_error", "xhc_num_logits", "xhc_coeffs", "xhc_tfa",
+EXPORTS = ("xhc_status_string", "xhc_last_cuda_error", "xhc_device_status", "xhc_num_logits", "xhc_coeffs", "xhc_tfa",
            "xhc_sparse_update", "xhc_fwd_workspace_bytes", "xhc_sublayer_fwd", "xhc_bwd_workspace_bytes",
            "xhc_sublayer_bwd", "xhc_copy", "xhc_timing_enable", "xhc_timing_collect")
 
@@ -48,6 +48,8 @@ def _load() -> ctypes.CDLL:
     lib.xhc_status_string.argtypes = [I]
     lib.xhc_last_cuda_error.restype = I
     lib.xhc_last_cuda_error.argtypes = []
+    lib.xhc_device_status.restype = I
+    lib.xhc_device_status.argtypes = [P]
     lib.xhc_num_logits.restype = I
     lib.xhc_num_logits.argtypes = [sh]
     lib.xhc_coeffs.restype = I

@@ -73,6 +73,11 @@ def xhc_sparse_update(sh, X_in, X_out, out, conv, hpost, hres, idx, stream=None)
                                                       w12, _p(hpost), _p(hres), _idx(idx), _s(stream)))
 
 
+def xhc_device_status(stream=None):
+    """Raise if a bounded device-side wait gave up since the last check."""
+    _check("xhc_device_status", LIB.xhc_device_status(_s(stream)))
+
+
 def xhc_fwd_workspace_bytes(sh) -> int:
     return int(LIB.xhc_fwd_workspace_bytes(ctypes.byref(sh)))
 

@@ -97,12 +97,20 @@ int num_sms() {
 }
 
 // Coefficient pass: tensor-core kernel where the shape tiles, else CUDA cores.
+// On the tensor-core path the dense read x_in (if requested) is a second,
+// bandwidth-bound kernel that takes H^pre from `hpre` or from `saved`.
 int run_coeffs(const xhc_shape_t* sh, const Params& p, const void* X, const float* W, float* hpre, float* hpost,
                float* hres, float* saved, void* x_in, cudaStream_t st) {
   if (sh->dtype == XHC_BF16) {
-    if (tc_coeffs_supported(p))
-      return cuda_status(launch_coeffs_tc(p, X, W, hpre, hpost, hres, saved, x_in, st));
-    return cuda_status(launch_coeffs_simt<__nv_bfloat16>(p, X, W, hpre, hpost, hres, saved, x_in, st));
+    using T = __nv_bfloat16;
+    if (tc_coeffs_supported(p)) {
+      int s = cuda_status(launch_coeffs_tc(p, X, W, hpre, hpost, hres, saved, st));
+      if (s || !x_in) return s;
+      UpdArgs<T> a{(const T*)X, nullptr, nullptr, {nullptr, nullptr, nullptr}, hpre, nullptr, nullptr,
+                   hpre ? nullptr : saved, (T*)x_in, nullptr, 0};
+      return cuda_status(launch_update_simt<T>(p, a, false, st));
+    }
+    return cuda_status(launch_coeffs_simt<T>(p, X, W, hpre, hpost, hres, saved, x_in, st));
   }
   return cuda_status(launch_coeffs_simt<float>(p, X, W, hpre, hpost, hres, saved, x_in, st));
 }
@@ -208,6 +216,12 @@ const char* xhc_status_string(int status) {
 
 int xhc_last_cuda_error(void) { return g_last_cuda_error; }
 
+int xhc_device_status(xhc_stream_t stream) {
+  const int v = read_device_error((cudaStream_t)stream);
+  if (v < 0) return cuda_status(cudaGetLastError());
+  return v ? XHC_ERR_TIMEOUT : XHC_OK;
+}
+
 int xhc_num_logits(const xhc_shape_t* sh) {
   if (!sh) return 0;
   return sh->N + 4 * sh->k + sh->k * sh->k;
@@ -282,6 +296,15 @@ int xhc_sublayer_fwd(const xhc_shape_t* sh, const void* X_in, void* X_out, const
   }
   const Params p = make_params(sh, idx);
   cudaStream_t st = (cudaStream_t)stream;
+  if (sh->dtype == XHC_BF16 && tc_coeffs_supported(p)) {
+    // coefficients on the tensor cores; the dense read runs with the update
+    using T = __nv_bfloat16;
+    if ((s = cuda_status(launch_coeffs_tc(p, X_in, W, nullptr, nullptr, nullptr, z, st)))) return s;
+    UpdArgs<T> a{(const T*)X_in, (T*)X_out, (const T*)out, {w4, w8, w12}, nullptr, nullptr, nullptr, z,
+                 (T*)x_in, (T*)saved_active, X_out != X_in};
+    if (tc_update_supported(p)) return cuda_status(launch_update_tc(p, a, has_conv, st));
+    return cuda_status(launch_update_simt<T>(p, a, has_conv, st));
+  }
   if ((s = run_coeffs(sh, p, X_in, W, nullptr, nullptr, nullptr, z, x_in, st))) return s;
   if (sh->dtype == XHC_BF16) {
     using T = __nv_bfloat16;

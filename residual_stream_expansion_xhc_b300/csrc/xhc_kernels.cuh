@@ -13,13 +13,13 @@ void timing_end(cudaStream_t st);
 template <typename T>
 struct UpdArgs {
   const T* X_in;
-  T* X_out;
+  T* X_out;              // nullptr: dense read only (x_in), no update
   const T* out;
   const float* w[3];
-  const float* hpre;     // [T, N] or nullptr
-  const float* hpost;    // [T, k, 4]; nullptr: coefficients come from `saved`
-  const float* hres;     // [T, k, k]
-  const float* saved;    // [T, P+1] (z, rstd)
+  const float* hpre;     // [T, N] or nullptr      (used when saved == nullptr)
+  const float* hpost;    // [T, k, 4]               (used when saved == nullptr)
+  const float* hres;     // [T, k, k]               (used when saved == nullptr)
+  const float* saved;    // [T, P+1] (z, rstd): coefficients derived per tile
   T* x_in;               // nullptr: no dense read
   T* saved_active;       // [T, k, C] or nullptr
   int copy_inactive;     // X_out != X_in

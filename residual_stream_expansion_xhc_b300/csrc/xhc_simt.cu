@@ -136,11 +136,12 @@ __global__ void __launch_bounds__(256) update_simt_kernel(Params p, UpdArgs<T> a
   const int ntok = min(UPD_TT, S - s0);
   const size_t tok0 = (size_t)b * S + s0;
 
-  // stage out rows [s0 - HALO, s0 + ntok) (zero before the sequence start)
+  // stage out rows [s0 - HALO, s0 + ntok) (zero before the sequence start;
+  // absent in the dense-read-only mode)
   for (int r = threadIdx.x / 32; r < UPD_TT + HALO; r += 8) {
     const int s = s0 - HALO + r;
     float v[V];
-    if (s >= 0 && s < S && c0 + (threadIdx.x & 31) * V < C) {
+    if (a.out != nullptr && s >= 0 && s < S && c0 + (threadIdx.x & 31) * V < C) {
       load_vec(a.out + ((size_t)b * S + s) * C + c0 + (threadIdx.x & 31) * V, v);
     } else {
 #pragma unroll
@@ -158,14 +159,16 @@ __global__ void __launch_bounds__(256) update_simt_kernel(Params p, UpdArgs<T> a
       w_s[i] = c < C ? a.w[j][(size_t)c * K + tau] : 0.0f;
     }
   }
-  // coefficients of the tile's tokens
-  if (a.hpost != nullptr) {
+  // coefficients of the tile's tokens: from the saved logits (sigmoid,
+  // Sinkhorn) or from coefficient arrays
+  const bool update = a.X_out != nullptr;
+  if (a.saved == nullptr) {
     for (int i = threadIdx.x; i < ntok * CS; i += blockDim.x) {
       const int tt = i / CS, q = i % CS;
       float v = 0.0f;
       if (q < N) v = a.hpre ? a.hpre[(tok0 + tt) * N + q] : 0.0f;
-      else if (q < N + 4 * k) v = a.hpost[(tok0 + tt) * 4 * k + (q - N)];
-      else if (q < N + 4 * k + k * k) v = a.hres[(tok0 + tt) * k * k + (q - N - 4 * k)];
+      else if (q < N + 4 * k) v = a.hpost ? a.hpost[(tok0 + tt) * 4 * k + (q - N)] : 0.0f;
+      else if (q < N + 4 * k + k * k) v = a.hres ? a.hres[(tok0 + tt) * k * k + (q - N - 4 * k)] : 0.0f;
       coef_s[i] = v;
     }
   } else {
@@ -174,15 +177,17 @@ __global__ void __launch_bounds__(256) update_simt_kernel(Params p, UpdArgs<T> a
       const int tt = i / CS, q = i % CS;
       if (q < N + 4 * k) coef_s[i] = sigmoidf_(a.saved[(tok0 + tt) * (P + 1) + q]);
     }
-    // Sinkhorn: two tokens per warp, one per half-warp
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int e = lane & 15, i = e >> 2, j = e & 3;
-    const bool valid = (i < k) && (j < k);
-    for (int tt = warp * 2 + (lane >> 4); tt - (lane >> 4) < ntok; tt += 16) {
-      const bool live = tt < ntok;
-      const float z = (live && valid) ? a.saved[(tok0 + tt) * (P + 1) + N + 4 * k + k * i + j] : 0.0f;
-      const float H = sinkhorn16(z, valid && live, p.iters);
-      if (live && valid) coef_s[tt * CS + N + 4 * k + k * i + j] = H;
+    if (update) {
+      // Sinkhorn: two tokens per warp, one per half-warp
+      const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+      const int e = lane & 15, i = e >> 2, j = e & 3;
+      const bool valid = (i < k) && (j < k);
+      for (int tt = warp * 2 + (lane >> 4); tt - (lane >> 4) < ntok; tt += 16) {
+        const bool live = tt < ntok;
+        const float z = (live && valid) ? a.saved[(tok0 + tt) * (P + 1) + N + 4 * k + k * i + j] : 0.0f;
+        const float H = sinkhorn16(z, valid && live, p.iters);
+        if (live && valid) coef_s[tt * CS + N + 4 * k + k * i + j] = H;
+      }
     }
   }
   __syncthreads();
@@ -237,6 +242,7 @@ __global__ void __launch_bounds__(256) update_simt_kernel(Params p, UpdArgs<T> a
       }
       store_vec(a.x_in + tok * C + c0 + cl, acc);
     }
+    if (!update) continue;
     if (a.saved_active) {
 #pragma unroll
       for (int j = 0; j < KMAX; ++j)
