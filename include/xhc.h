@@ -173,6 +173,33 @@ int xhc_sublayer_fwd(const xhc_shape_t* sh, const void* X_in, void* X_out,
                      void* x_in, float* saved, void* saved_active,
                      void* workspace, size_t ws_bytes, xhc_stream_t stream);
 
+/*
+ * xhc_sublayer_fwd_noalloc -- xhc_sublayer_fwd for callers that cannot
+ * allocate device memory.  The paper has no counterpart; this is a library
+ * convenience.  Some callers only receive their input and output buffers and
+ * may not call the CUDA allocator (a plugin or custom-op hook running inside
+ * another framework's memory pool, a C caller without a workspace of its
+ * own).  This entry point takes the same arguments as xhc_sublayer_fwd minus
+ * the workspace, and uses a fixed 8 MiB scratch area built into the library
+ * (a device array that every GPU which loads the library keeps until the
+ * process exits) for the per-token logits when `saved` is NULL.
+ *   Limit: B*S*(P+1)*4 bytes must fit in 8 MiB when saved is NULL (42,799
+ *          tokens at N = 16, k = 4); larger calls return XHC_ERR_WORKSPACE
+ *          before touching the GPU.  With `saved` given there is no limit.
+ *   The first call on each device looks up the scratch address on that
+ *   device (no allocation); make that first call before any stream capture.
+ *   Every call shares the one scratch area: calls whose work overlaps on the
+ *   GPU (different streams, or different threads) race and must be ordered
+ *   by the caller.  The area keeps the last call's contents; nothing in it
+ *   needs to start at zero.
+ *   No cudaMalloc, cudaFree or other allocating routine is called.
+ */
+int xhc_sublayer_fwd_noalloc(const xhc_shape_t* sh, const void* X_in,
+                             void* X_out, const void* out, const float* w4,
+                             const float* w8, const float* w12, const float* W,
+                             const int32_t* idx, void* x_in, float* saved,
+                             void* saved_active, xhc_stream_t stream);
+
 /* Workspace the backward needs (bytes). */
 size_t xhc_bwd_workspace_bytes(const xhc_shape_t* sh);
 

@@ -95,6 +95,17 @@ def xhc_sublayer_fwd(sh, X_in, X_out, out, conv, W, idx, x_in=None, saved=None, 
                                                     _p(workspace), ws_bytes, _s(stream)))
 
 
+def xhc_sublayer_fwd_noalloc(sh, X_in, X_out, out, conv, W, idx, x_in=None, saved=None, saved_active=None,
+                             stream=None):
+    """xhc_sublayer_fwd without a workspace: for callers that may not allocate
+    device memory.  Uses the library's built-in 8 MiB scratch (see the C
+    header for the token limit and the rule that overlapping calls race)."""
+    w4, w8, w12 = _conv(conv)
+    _check("xhc_sublayer_fwd_noalloc",
+           LIB.xhc_sublayer_fwd_noalloc(ctypes.byref(sh), _p(X_in), _p(X_out), _p(out), w4, w8, w12, _p(W),
+                                        _idx(idx), _p(x_in), _p(saved), _p(saved_active), _s(stream)))
+
+
 def xhc_sublayer_bwd(sh, X_state, saved_active, out, conv, W, idx, saved, dXp, dx_in, dX, dout, dconv, dW,
                      workspace, stream=None):
     w4, w8, w12 = _conv(conv)

@@ -1,0 +1,65 @@
+// xhc_sublayer_fwd_noalloc: the fused forward for callers that cannot
+// allocate device memory.
+//
+// The fused forward needs scratch for the per-token logits when the caller
+// does not keep them (`saved` == NULL).  Normally the caller hands that scratch
+// in as a workspace.  Some callers have no way to obtain one: code running
+// inside a framework's custom-op or plugin hook that may not call the CUDA
+// allocator, a process whose memory is owned by a pool it cannot reach from
+// this point, or a C caller that only receives its input and output buffers.
+// For them this file reserves a fixed scratch area in the library itself, a
+// file-scope __device__ array that every GPU which loads the library holds
+// until the process exits.  Nothing here calls cudaMalloc or cudaFree.
+#include <mutex>
+
+#include "../../include/xhc.h"
+
+namespace {
+
+// Capacity of the built-in scratch: tokens * (P + 1) * 4 bytes must fit.
+// 8 MiB holds the logits of 42,799 tokens at N = 16, k = 4 (P = 48).
+constexpr size_t kScratchBytes = size_t(8) << 20;
+
+static __device__ __align__(256) unsigned char g_fwd_scratch[kScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mutex;
+void* g_scratch_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device.  The host-side
+// name g_fwd_scratch is only a stand-in for the symbol, never a device
+// address, so the address is looked up once per device, with that device
+// current, and cached.
+int scratch_on_current_device(void** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return XHC_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  if (!g_scratch_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_fwd_scratch) != cudaSuccess || p == nullptr) return XHC_ERR_CUDA;
+    g_scratch_ptr[dev] = p;
+  }
+  *out = g_scratch_ptr[dev];
+  return XHC_OK;
+}
+
+}  // namespace
+
+extern "C" int xhc_sublayer_fwd_noalloc(const xhc_shape_t* sh, const void* X_in, void* X_out, const void* out,
+                                        const float* w4, const float* w8, const float* w12, const float* W,
+                                        const int32_t* idx, void* x_in, float* saved, void* saved_active,
+                                        xhc_stream_t stream) {
+  // Sizes are checked before anything touches the GPU.
+  const size_t need = saved ? 0 : xhc_fwd_workspace_bytes(sh);
+  if (need > kScratchBytes) return XHC_ERR_WORKSPACE;
+  if (need == 0)
+    return xhc_sublayer_fwd(sh, X_in, X_out, out, w4, w8, w12, W, idx, x_in, saved, saved_active, nullptr, 0,
+                            stream);
+  void* scratch = nullptr;
+  const int s = scratch_on_current_device(&scratch);
+  if (s != XHC_OK) return s;
+  // Every logit the update reads is written earlier in the same call, so the
+  // scratch needs no clearing between calls.
+  return xhc_sublayer_fwd(sh, X_in, X_out, out, w4, w8, w12, W, idx, x_in, saved, saved_active, scratch,
+                          kScratchBytes, stream);
+}

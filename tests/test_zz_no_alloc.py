@@ -1,0 +1,82 @@
+"""The no-allocation forward, xhc_sublayer_fwd_noalloc.
+
+It exists for callers that cannot allocate device memory (a hook running
+inside another framework's memory pool, a C caller that only holds its input
+and output buffers): instead of a caller workspace it uses scratch built into
+the library.  These tests call it through the C ABI and check that it gives
+the same result as xhc_sublayer_fwd with a caller workspace, on two calls in a
+row with different inputs (the shared scratch must not leak one call's state
+into the next), and that a call too large for the built-in scratch is refused
+before anything runs.
+
+This file is collected last on purpose, so that a run that stops at the first
+failure has already run every other test.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import xhc_oracle as xo
+from residual_stream_expansion_xhc_b300 import inputs as xin
+from tests.xhc_testlib import TOL, dev_act, dev_f32, host_f64, tdtype
+
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    from residual_stream_expansion_xhc_b300 import _lib, api
+
+CASES = [
+    xin.Workload("noalloc_bf16", 40, B=2, S=96, N=16, C=512, k=4, dtype="bf16"),
+    xin.Workload("noalloc_f32", 41, B=1, S=70, N=8, C=96, k=3, dtype="f32"),
+]
+
+
+def _run(wl, t, use_noalloc):
+    sh = api.make_shape(wl.B, wl.S, wl.N, wl.C, wl.k, tdtype(wl), wl.iters, wl.eps)
+    X = dev_act(wl, t.X)
+    out = dev_act(wl, t.out)
+    conv = tuple(dev_f32(w) for w in t.conv)
+    W = dev_f32(t.W)
+    x_in = torch.empty(wl.B, wl.S, wl.C, dtype=tdtype(wl), device="cuda")
+    act = torch.empty(wl.B, wl.S, wl.k, wl.C, dtype=tdtype(wl), device="cuda")
+    if use_noalloc:
+        api.xhc_sublayer_fwd_noalloc(sh, X, X, out, conv, W, t.idx, x_in=x_in, saved=None, saved_active=act)
+    else:
+        ws = api.workspace(api.xhc_fwd_workspace_bytes(sh))
+        api.xhc_sublayer_fwd(sh, X, X, out, conv, W, t.idx, x_in=x_in, saved=None, saved_active=act, workspace=ws)
+    torch.cuda.synchronize()
+    api.xhc_device_status()
+    return X, x_in, act
+
+
+@pytest.mark.parametrize("wl", CASES, ids=[w.name for w in CASES])
+def test_noalloc_matches_workspace_path_twice(wl):
+    for call in range(2):
+        # a different seeded draw for each call
+        t = xin.make(xin.scaled(wl, wid=wl.wid + 100 * call))
+        ref = _run(wl, t, use_noalloc=False)
+        got = _run(wl, t, use_noalloc=True)
+        for r, g in zip(ref, got):
+            e = xo.max_rel_err(host_f64(g), host_f64(r))
+            assert e <= TOL[wl.dtype], f"call {call}: err {e}"
+
+
+def test_noalloc_refuses_calls_beyond_its_scratch():
+    # 50,000 tokens x 49 logits x 4 bytes > 8 MiB: refused before any launch
+    sh = _lib.XhcShape(1, 50000, 16, 256, 4, _lib.XHC_BF16, 20, 1e-6)
+    idx = (ctypes.c_int32 * 4)(0, 1, 2, 3)
+    fake = ctypes.c_void_p(1 << 20)
+    st = _lib.LIB.xhc_sublayer_fwd_noalloc(ctypes.byref(sh), fake, fake, fake, None, None, None, fake, idx, None,
+                                           None, None, None)
+    assert st == 5                     # XHC_ERR_WORKSPACE
+    # the same call fits when the caller keeps the logits itself
+    wl = xin.Workload("noalloc_saved", 42, B=1, S=40, N=16, C=256, k=4, dtype="bf16")
+    t = xin.make(wl)
+    shp = api.make_shape(wl.B, wl.S, wl.N, wl.C, wl.k, torch.bfloat16)
+    X = dev_act(wl, t.X)
+    saved = torch.empty(wl.B, wl.S, wl.P + 1, device="cuda")
+    api.xhc_sublayer_fwd_noalloc(shp, X, X, dev_act(wl, t.out), None, dev_f32(t.W), t.idx, saved=saved)
+    torch.cuda.synchronize()
+    assert torch.isfinite(saved).all()
