@@ -7,6 +7,7 @@
 
 #include "../../include/xhc.h"
 #include "xhc_kernels.cuh"
+#include "xhc_bwd.cuh"
 #include "xhc_tc.cuh"
 
 using namespace xhc;
@@ -319,22 +320,34 @@ int xhc_sublayer_fwd(const xhc_shape_t* sh, const void* X_in, void* X_out, const
 }
 
 namespace {
+// Workspace of the backward.  CUDA-core path: per-token records (2P+1 floats),
+// recomputed logits, conv partials.  bf16 tensor-core path: records
+// (1+N+4k floats), recomputed logits, dp (bf16, 64 per token), W^T (bf16, 64
+// per column), conv partials, dW partials (one per token range).
 struct BwdLayout {
-  size_t rec, saved, partial, gbuf, total;
+  size_t rec, saved, dP, Wt, cpart, wpart, total;
+  int ranges;
 };
 BwdLayout bwd_layout(const xhc_shape_t* sh) {
   const Params p = make_params(sh, nullptr);
-  BwdLayout L;
   const size_t T = tokens(sh);
-  L.rec = 0;
-  L.saved = round_up(T * (size_t)(2 * p.P + 1) * sizeof(float));
-  L.partial = L.saved + round_up(T * (size_t)(p.P + 1) * sizeof(float));
-  size_t part = bwd_tfa_partial_floats(p) * sizeof(float);
-  if (sh->dtype == XHC_BF16 && tc_bwd_supported(p)) part = std::max(part, tc_bwd_partial_bytes(p));
-  L.gbuf = L.partial + round_up(part);
-  // copy of the active rows of dX' for the CUDA-core path when dX aliases dX'
-  const bool tc = sh->dtype == XHC_BF16 && tc_bwd_supported(p);
-  L.total = L.gbuf + (tc ? 0 : round_up(T * (size_t)p.k * (size_t)p.C * esize(sh)));
+  const size_t NC = (size_t)p.N * p.C;
+  BwdLayout L{};
+  if (sh->dtype == XHC_BF16 && tc_bwd_supported(p)) {
+    L.ranges = bwd_stream_ranges(p);
+    L.rec = 0;
+    L.saved = L.rec + round_up(T * (size_t)(1 + p.N + 4 * p.k) * sizeof(float));
+    L.dP = L.saved + round_up(T * (size_t)(p.P + 1) * sizeof(float));
+    L.Wt = L.dP + round_up(T * 64 * sizeof(uint16_t));
+    L.cpart = L.Wt + round_up(NC * 64 * sizeof(uint16_t));
+    L.wpart = L.cpart + round_up(bwd_conv_partial_rows(p) * NTAPS * (size_t)p.C * sizeof(float));
+    L.total = L.wpart + round_up((size_t)L.ranges * p.P * NC * sizeof(float));
+  } else {
+    L.rec = 0;
+    L.saved = round_up(T * (size_t)(2 * p.P + 1) * sizeof(float));
+    L.cpart = L.saved + round_up(T * (size_t)(p.P + 1) * sizeof(float));
+    L.total = L.cpart + round_up(bwd_tfa_partial_floats(p) * sizeof(float));
+  }
   return L;
 }
 }  // namespace
@@ -357,6 +370,7 @@ int xhc_sublayer_bwd(const xhc_shape_t* sh, const void* X_state, const void* sav
   if ((s = check_conv(dw4, dw8, dw12, &has_dconv))) return s;
   if (has_conv != has_dconv) return XHC_ERR_ARG;
   if (saved_active && !saved) return XHC_ERR_ARG;   // recomputation needs the pre-update state
+  if (dX == dXp) return XHC_ERR_ARG;                // dX must not alias dX'
   if ((s = check_ptrs({X_state, out, W, dXp, dX, dout, dW}, {saved_active, w4, w8, w12, saved, dx_in, dw4, dw8,
                                                               dw12, workspace})))
     return s;
@@ -382,26 +396,26 @@ int xhc_sublayer_bwd(const xhc_shape_t* sh, const void* X_state, const void* sav
     if ((s = run_coeffs(sh, p, X_state, W, nullptr, nullptr, nullptr, zw, nullptr, st))) return s;
     z = zw;
   }
-  float* partial = (float*)(ws + L.partial);
   if (sh->dtype == XHC_BF16) {
     using T = __nv_bfloat16;
     BwdArgs<T> a{(const T*)X_state, (const T*)saved_active, (const T*)out, {w4, w8, w12}, W, z, (const T*)dXp,
-                 (const T*)dx_in, (T*)dX, (T*)dout, {dw4, dw8, dw12}, dW, rec, nullptr};
-    if (tc_bwd_supported(p)) return cuda_status(launch_bwd_tc(p, a, has_conv, partial, st));
-    if (dX == dXp) {
-      a.Gbuf = (const T*)(ws + L.gbuf);
-      if ((s = cuda_status(launch_gather_active<T>(p, (const T*)dXp, (T*)(ws + L.gbuf), st)))) return s;
+                 (const T*)dx_in, (T*)dX, (T*)dout, {dw4, dw8, dw12}, dW, rec};
+    if (tc_bwd_supported(p)) {
+      T* dP = (T*)(ws + L.dP);
+      T* Wt = (T*)(ws + L.Wt);
+      float* cpart = (float*)(ws + L.cpart);
+      float* wpart = (float*)(ws + L.wpart);
+      if ((s = cuda_status(launch_wt_prep(p, W, Wt, st)))) return s;
+      if ((s = cuda_status(launch_bwd_token(p, a, has_conv, dP, st)))) return s;
+      if ((s = cuda_status(launch_bwd_tfa(p, a, has_conv, cpart, st)))) return s;
+      if ((s = cuda_status(launch_bwd_stream_tc(p, a, Wt, dP, L.ranges, wpart, st)))) return s;
+      return cuda_status(launch_bwd_reduce(p, a, has_conv, cpart, L.ranges, wpart, st));
     }
-    return cuda_status(launch_bwd_simt<T>(p, a, has_conv, partial, true, st));
+    return cuda_status(launch_bwd_simt<T>(p, a, has_conv, (float*)(ws + L.cpart), true, st));
   }
   BwdArgs<float> a{(const float*)X_state, (const float*)saved_active, (const float*)out, {w4, w8, w12}, W, z,
-                   (const float*)dXp, (const float*)dx_in, (float*)dX, (float*)dout, {dw4, dw8, dw12}, dW, rec,
-                   nullptr};
-  if (dX == dXp) {
-    a.Gbuf = (const float*)(ws + L.gbuf);
-    if ((s = cuda_status(launch_gather_active<float>(p, (const float*)dXp, (float*)(ws + L.gbuf), st)))) return s;
-  }
-  return cuda_status(launch_bwd_simt<float>(p, a, has_conv, partial, true, st));
+                   (const float*)dXp, (const float*)dx_in, (float*)dX, (float*)dout, {dw4, dw8, dw12}, dW, rec};
+  return cuda_status(launch_bwd_simt<float>(p, a, has_conv, (float*)(ws + L.cpart), true, st));
 }
 
 int xhc_copy(const void* src, void* dst, size_t bytes, xhc_stream_t stream) {

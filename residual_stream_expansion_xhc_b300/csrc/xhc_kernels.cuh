@@ -39,14 +39,12 @@ struct BwdArgs {
   T* dout;
   float* dw[3];
   float* dW;
-  float* rec;             // [T, 2P+1] per-token records (workspace)
-  const T* Gbuf;          // [T, k, C] copy of the active rows of dX' (used when dX aliases dX'), or nullptr
+  float* rec;             // per-token records (workspace)
 };
 
-// Active row i of dX' for token t (G_i = dX'[a_i]), from dX' itself or from its copy.
+// Active row i of dX' for token t: G_i = dX'[a_i].
 template <typename T>
 __device__ __forceinline__ const T* grad_row(const Params& p, const BwdArgs<T>& a, size_t t, int i) {
-  if (a.Gbuf) return a.Gbuf + (t * p.k + i) * (size_t)p.C;
   return a.dXp + (t * p.N + p.idx[i]) * (size_t)p.C;
 }
 
@@ -62,8 +60,6 @@ template <typename T>
 cudaError_t launch_bwd_simt(const Params& p, const BwdArgs<T>& a, bool has_conv, float* partial, bool do_token,
                             cudaStream_t st);
 size_t bwd_tfa_partial_floats(const Params& p);
-template <typename T>
-cudaError_t launch_gather_active(const Params& p, const T* src, T* dst, cudaStream_t st);
 cudaError_t launch_copy16(const void* src, void* dst, size_t bytes, int sms, cudaStream_t st);
 
 }  // namespace xhc

@@ -707,29 +707,6 @@ __global__ void bwd_tfa_reduce_kernel(int ntiles, int C, const float* __restrict
   else dw12[(size_t)c * 12 + (g - 12)] = s;
 }
 
-// Copy the k active rows of a [T, N, C] tensor into a [T, k, C] buffer.
-template <typename T>
-__global__ void gather_active_kernel(Params p, const T* __restrict__ src, T* __restrict__ dst) {
-  constexpr int V = Vec<T>::W;
-  const size_t t = blockIdx.x;
-  for (int i = 0; i < p.k; ++i)
-    for (int c0 = threadIdx.x * V; c0 < p.C; c0 += blockDim.x * V) {
-      const uint4 v = *reinterpret_cast<const uint4*>(src + (t * p.N + p.idx[i]) * (size_t)p.C + c0);
-      *reinterpret_cast<uint4*>(dst + (t * p.k + i) * (size_t)p.C + c0) = v;
-    }
-}
-
-template <typename T>
-cudaError_t launch_gather_active(const Params& p, const T* src, T* dst, cudaStream_t st) {
-  timing_begin("gather_active", st);
-  gather_active_kernel<T><<<(unsigned)((size_t)p.B * p.S), 256, 0, st>>>(p, src, dst);
-  timing_end(st);
-  return cudaGetLastError();
-}
-template cudaError_t launch_gather_active<float>(const Params&, const float*, float*, cudaStream_t);
-template cudaError_t launch_gather_active<__nv_bfloat16>(const Params&, const __nv_bfloat16*, __nv_bfloat16*,
-                                                         cudaStream_t);
-
 __global__ void copy16_kernel(const uint4* __restrict__ src, uint4* __restrict__ dst, size_t n) {
   const size_t stride = (size_t)gridDim.x * blockDim.x;
   for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) dst[i] = __ldcs(src + i);

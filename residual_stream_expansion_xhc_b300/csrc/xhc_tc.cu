@@ -11,6 +11,7 @@
 #include <mutex>
 
 #include "xhc_sm100.cuh"
+#include "xhc_bwd.cuh"
 #include "xhc_tc.cuh"
 
 namespace xhc {
@@ -372,14 +373,340 @@ int read_device_error(cudaStream_t st) {
   return v;
 }
 
+// ---------------------------------------------------------------- backward stream pass
+//
+// dX and dW of every stream on the tensor cores.  Work item = (column block:
+// stream n, channels c0 .. c0+127) x (token range); tiles of 128 tokens.
+// Per tile, TMA brings
+//   Xt   [128 tokens x 128 columns]  the state before the update (two 64-column
+//                                     boxes, 128-byte swizzle)
+//   Bt   [128 x 128]                 dX' (inactive n) or the active-stream mix
+//                                     written to dX by the token pass
+//   Pt   [128 tokens x 64]           dp (bf16, P <= 48 entries, zero padded)
+// and the tensor cores compute
+//   dV [128 tokens x 128 cols] = Pt . Wt_blk^T   (A K-major, B K-major; K = 48)
+//   dW [128 cols x 48]        += Xt^T . Pt       (A and B MN-major: the same
+//                                                 tiles, read along tokens)
+// dV goes to a double-buffered TMEM accumulator that the epilogue turns into
+// dX = dV + alpha X + base (+ hpre[n] dx_in); dW accumulates in TMEM over the
+// whole token range and is written as one partial per range.
+// Section "Scaling N" (coefficients come from the whole state, so every
+// stream receives the projection gradient); section "Dense read, sparse
+// write" (inactive streams pass dX' through, active ones receive the mix).
+
+namespace bwdtc {
+constexpr int TT = 128;
+constexpr int CB = 128;
+constexpr int STAGES = 2;
+constexpr int HALF = TT * 64 * 2;                 // one 64-column box: 16 KB
+constexpr int OFF_X = 0;
+constexpr int OFF_B = 2 * HALF;
+constexpr int OFF_P = 4 * HALF;
+constexpr int STAGE_BYTES = 5 * HALF;             // 80 KB
+constexpr int WT_BYTES = CB * 64 * 2;             // 16 KB
+constexpr int SMEM = STAGES * STAGE_BYTES + WT_BYTES + 1024;
+constexpr int THREADS = 192;
+constexpr int TMEM_COLS = 512;                    // dV: 2 x 128, dW: 48 at column 256
+constexpr int D2_COL = 256;
+}  // namespace bwdtc
+
+struct StreamMaps {
+  CUtensorMap X, Xa, dXp, dX, dP, Wt;
+};
+
+__global__ void __launch_bounds__(bwdtc::THREADS, 1)
+    bwd_stream_tc_kernel(const __grid_constant__ StreamMaps m, Params p, BwdArgs<__nv_bfloat16> a, int ranges,
+                         int range_len, float* __restrict__ wpart) {
+  using namespace bwdtc;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  uint8_t* wt_s = smem + STAGES * STAGE_BYTES;
+  __shared__ uint64_t full[STAGES], empty[STAGES], tfull[2], tempty[2], wt_full, wt_empty, d2full, d2empty;
+  __shared__ uint32_t tmem_slot;
+  int* err = &g_device_error;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int N = p.N, k = p.k, C = p.C, P = p.P;
+  const size_t T_all = (size_t)p.B * p.S;
+  const size_t NC = (size_t)N * C;
+  const int cblocks = C / CB;
+  const int nblocks = N * cblocks;
+  const int nitems = nblocks * ranges;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1 + 4);              // MMA commit + 4 epilogue warps
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 4);
+    }
+    mbar_init(&wt_full, 1);
+    mbar_init(&wt_empty, 1);
+    mbar_init(&d2full, 1);
+    mbar_init(&d2empty, 4);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_slot, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const uint64_t pol_stream = policy_evict_first(), pol_keep = policy_evict_last();
+      int it = 0, ii = 0;
+      for (int item = blockIdx.x; item < nitems; item += gridDim.x, ++ii) {
+        const int blk = item / ranges, r = item % ranges;
+        const int n = blk / cblocks, c0 = (blk % cblocks) * CB;
+        const int slot = p.is_active[n];
+        const size_t t_beg = (size_t)r * range_len;
+        const size_t t_end = (t_beg + range_len < T_all) ? t_beg + range_len : T_all;
+        if (ii > 0 && !mbar_wait(&wt_empty, (ii - 1) & 1, err, 21)) break;
+        mbar_expect_tx(&wt_full, WT_BYTES);
+        tma_load_2d(wt_s, &m.Wt, &wt_full, 0, (int)((size_t)n * C + c0), pol_keep);
+        bool ok = true;
+        for (size_t t0 = t_beg; t0 < t_end; t0 += TT, ++it) {
+          const int s = it % STAGES;
+          if (it >= STAGES && !mbar_wait(&empty[s], ((it / STAGES) & 1) ^ 1, err, 22)) { ok = false; break; }
+          uint8_t* st = smem + s * STAGE_BYTES;
+          mbar_expect_tx(&full[s], STAGE_BYTES);
+          const int tt = (int)t0;
+          for (int h = 0; h < 2; ++h) {
+            if (slot && a.saved_active)
+              tma_load_3d(st + OFF_X + h * HALF, &m.Xa, &full[s], c0 + 64 * h, slot - 1, tt, pol_stream);
+            else
+              tma_load_3d(st + OFF_X + h * HALF, &m.X, &full[s], c0 + 64 * h, n, tt, pol_stream);
+            if (slot) tma_load_3d(st + OFF_B + h * HALF, &m.dX, &full[s], c0 + 64 * h, n, tt, pol_stream);
+            else tma_load_3d(st + OFF_B + h * HALF, &m.dXp, &full[s], c0 + 64 * h, n, tt, pol_stream);
+          }
+          tma_load_2d(st + OFF_P, &m.dP, &full[s], 0, tt, pol_keep);
+        }
+        if (!ok) break;
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc_v = idesc_bf16(TT, CB, 0, 0);
+      const uint32_t idesc_w = idesc_bf16(CB, 48, 1, 1);
+      const uint32_t wt_addr = smem_u32(wt_s);
+      int it = 0, tl = 0, ii = 0;
+      for (int item = blockIdx.x; item < nitems; item += gridDim.x, ++ii) {
+        const int r = item % ranges;
+        const size_t t_beg = (size_t)r * range_len;
+        const size_t t_end = (t_beg + range_len < T_all) ? t_beg + range_len : T_all;
+        if (!mbar_wait(&wt_full, ii & 1, err, 23)) break;
+        if (ii > 0 && !mbar_wait(&d2empty, (ii - 1) & 1, err, 24)) break;
+        tc_fence_after();
+        bool ok = true, first = true;
+        for (size_t t0 = t_beg; t0 < t_end; t0 += TT, ++it, ++tl) {
+          const int s = it % STAGES, buf = tl & 1;
+          if (!mbar_wait(&full[s], (it / STAGES) & 1, err, 25)) { ok = false; break; }
+          if (tl >= 2 && !mbar_wait(&tempty[buf], ((tl >> 1) & 1) ^ 1, err, 26)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t st = smem_u32(smem + s * STAGE_BYTES);
+          // dV = dP . Wt^T  (K = 48: three K16 steps inside the 128-byte rows)
+#pragma unroll
+          for (int ks = 0; ks < 3; ++ks) {
+            const uint64_t da = sdesc_sw128(st + OFF_P + ks * 32, 16, 1024);
+            const uint64_t db = sdesc_sw128(wt_addr + ks * 32, 16, 1024);
+            umma_bf16(tmem + buf * 128, da, db, idesc_v, ks > 0);
+          }
+          umma_commit(&tfull[buf]);
+          // dW += X^T . dP  (K = 128 tokens: eight K16 steps of 16 rows)
+#pragma unroll
+          for (int ks = 0; ks < TT / 16; ++ks) {
+            const uint64_t da = sdesc_sw128(st + OFF_X + ks * 2048, HALF, 1024);
+            const uint64_t db = sdesc_sw128(st + OFF_P + ks * 2048, HALF, 1024);
+            umma_bf16(tmem + D2_COL, da, db, idesc_w, (first && ks == 0) ? 0u : 1u);
+          }
+          umma_commit(&empty[s]);
+          first = false;
+        }
+        if (!ok) break;
+        umma_commit(&d2full);
+        umma_commit(&wt_empty);
+      }
+    }
+  } else {
+    // ------------------------------------------------ epilogue: one thread per token / per column
+    const int q4 = warp & 3;
+    const int row = 32 * q4 + lane;
+    const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
+    const int rl = 1 + N + 4 * k;
+    int it = 0, tl = 0, ii = 0;
+    for (int item = blockIdx.x; item < nitems; item += gridDim.x, ++ii) {
+      const int blk = item / ranges, r = item % ranges;
+      const int n = blk / cblocks, c0 = (blk % cblocks) * CB;
+      const size_t t_beg = (size_t)r * range_len;
+      const size_t t_end = (t_beg + range_len < T_all) ? t_beg + range_len : T_all;
+      bool ok = true;
+      for (size_t t0 = t_beg; t0 < t_end; t0 += TT, ++it, ++tl) {
+        const int s = it % STAGES, buf = tl & 1;
+        if (!mbar_wait(&full[s], (it / STAGES) & 1, err, 27)) { ok = false; break; }
+        if (!mbar_wait(&tfull[buf], (tl >> 1) & 1, err, 28)) { ok = false; break; }
+        tc_fence_after();
+        const uint8_t* st = smem + s * STAGE_BYTES;
+        const size_t t = t0 + row;
+        const bool live = t < T_all;
+        float alpha = 0.0f, hp = 0.0f;
+        if (live) {
+          alpha = a.rec[t * rl];
+          if (a.dx_in) hp = a.rec[t * rl + 1 + n];
+        }
+#pragma unroll 1
+        for (int cc = 0; cc < CB / 16; ++cc) {
+          uint32_t d[16];
+          tmem_ld16(tmem + lane_base + buf * 128 + cc * 16, d);
+          tmem_wait_ld();
+          const int h = cc >> 2;                        // which 64-column box
+          const int byte0 = (cc & 3) * 32;              // 16 columns = 32 bytes
+          const uint8_t* xr = st + OFF_X + h * HALF;
+          const uint8_t* br = st + OFF_B + h * HALF;
+          const uint4 x0 = *reinterpret_cast<const uint4*>(xr + sw128_offset(row, byte0));
+          const uint4 x1 = *reinterpret_cast<const uint4*>(xr + sw128_offset(row, byte0 + 16));
+          const uint4 b0 = *reinterpret_cast<const uint4*>(br + sw128_offset(row, byte0));
+          const uint4 b1 = *reinterpret_cast<const uint4*>(br + sw128_offset(row, byte0 + 16));
+          const uint32_t xw[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+          const uint32_t bw[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+          float g[16];
+          if (a.dx_in && live) {
+            float v0[8], v1[8];
+            load_vec(a.dx_in + t * C + c0 + cc * 16, v0);
+            load_vec(a.dx_in + t * C + c0 + cc * 16 + 8, v1);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              g[e] = v0[e];
+              g[8 + e] = v1[e];
+            }
+          } else {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) g[e] = 0.0f;
+          }
+          uint32_t o[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            float ya = __uint_as_float(d[2 * e]) + bf_lo(bw[e]);
+            float yb = __uint_as_float(d[2 * e + 1]) + bf_hi(bw[e]);
+            ya = fmaf(alpha, bf_lo(xw[e]), ya);
+            yb = fmaf(alpha, bf_hi(xw[e]), yb);
+            ya = fmaf(hp, g[2 * e], ya);
+            yb = fmaf(hp, g[2 * e + 1], yb);
+            o[e] = pack_bf2(ya, yb);
+          }
+          if (live) {
+            uint4* dst = reinterpret_cast<uint4*>(a.dX + (t * N + n) * (size_t)C + c0 + cc * 16);
+            dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+            dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&tempty[buf]);
+          mbar_arrive(&empty[s]);
+        }
+      }
+      if (!ok) break;
+      // dW partial of this item: TMEM lane = column of the block, 48 columns = q
+      if (!mbar_wait(&d2full, ii & 1, err, 29)) break;
+      tc_fence_after();
+      float* dst = wpart + (size_t)r * P * NC + (size_t)n * C + c0 + row;
+#pragma unroll
+      for (int qc = 0; qc < 48; qc += 16) {
+        uint32_t d[16];
+        tmem_ld16(tmem + lane_base + D2_COL + qc, d);
+        tmem_wait_ld();
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          if (qc + e < P) dst[(size_t)(qc + e) * NC] = __uint_as_float(d[e]);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&d2empty);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tmem, TMEM_COLS);
+}
+
+int bwd_stream_ranges(const Params& p) {
+  const int blocks = p.N * (p.C / bwdtc::CB);
+  const size_t tiles = ((size_t)p.B * p.S + bwdtc::TT - 1) / bwdtc::TT;
+  if (tiles == 0) return 1;
+  const int sms = sm_count();
+  int best = 1;
+  double best_eff = 0.0;
+  for (int r = 1; r <= 16 && (size_t)r <= tiles; ++r) {
+    const long items = (long)blocks * r;
+    const long waves = (items + sms - 1) / sms;
+    const double eff = (double)items / (double)(waves * sms);
+    if (eff > best_eff + 1e-3) {
+      best_eff = eff;
+      best = r;
+    }
+  }
+  // no empty range: every range must own at least one tile
+  const size_t per = (tiles + best - 1) / best;
+  return (int)((tiles + per - 1) / per);
+}
+
+cudaError_t launch_bwd_stream_tc(const Params& p, const BwdArgs<__nv_bfloat16>& a, const __nv_bfloat16* Wt,
+                                 const __nv_bfloat16* dP, int ranges, float* wpart, cudaStream_t st) {
+  using namespace bwdtc;
+  const size_t T_all = (size_t)p.B * p.S;
+  const size_t NC = (size_t)p.N * p.C;
+  StreamMaps m;
+  const uint32_t box3[3] = {64, 1, TT};
+  {
+    const uint64_t dims[3] = {(uint64_t)p.C, (uint64_t)p.N, T_all};
+    const uint64_t strides[2] = {(uint64_t)p.C * 2, NC * 2};
+    if (!make_map(&m.X, a.X, 3, dims, strides, box3)) return cudaErrorInvalidValue;
+    if (!make_map(&m.dXp, a.dXp, 3, dims, strides, box3)) return cudaErrorInvalidValue;
+    if (!make_map(&m.dX, a.dX, 3, dims, strides, box3)) return cudaErrorInvalidValue;
+  }
+  if (a.saved_active) {
+    const uint64_t dims[3] = {(uint64_t)p.C, (uint64_t)p.k, T_all};
+    const uint64_t strides[2] = {(uint64_t)p.C * 2, (uint64_t)p.k * p.C * 2};
+    if (!make_map(&m.Xa, a.saved_active, 3, dims, strides, box3)) return cudaErrorInvalidValue;
+  } else {
+    m.Xa = m.X;
+  }
+  {
+    const uint64_t dims[2] = {64, T_all};
+    const uint64_t strides[1] = {128};
+    const uint32_t box[2] = {64, TT};
+    if (!make_map(&m.dP, dP, 2, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  {
+    const uint64_t dims[2] = {64, NC};
+    const uint64_t strides[1] = {128};
+    const uint32_t box[2] = {64, CB};
+    if (!make_map(&m.Wt, Wt, 2, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  const size_t tiles = (T_all + TT - 1) / TT;
+  const int range_len = (int)(((tiles + ranges - 1) / ranges) * TT);
+  const int nitems = p.N * (p.C / CB) * ranges;
+  const int grid = std::min(nitems, sm_count());
+  cudaFuncSetAttribute(bwd_stream_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+  timing_begin("bwd_stream_tc", st);
+  bwd_stream_tc_kernel<<<grid, THREADS, SMEM, st>>>(m, p, a, ranges, range_len, wpart);
+  timing_end(st);
+  return cudaGetLastError();
+}
+
 bool tc_update_supported(const Params&) { return false; }
 cudaError_t launch_update_tc(const Params&, const UpdArgs<__nv_bfloat16>&, bool, cudaStream_t) {
   return cudaErrorNotSupported;
 }
-bool tc_bwd_supported(const Params&) { return false; }
-size_t tc_bwd_partial_bytes(const Params&) { return 0; }
-cudaError_t launch_bwd_tc(const Params&, const BwdArgs<__nv_bfloat16>&, bool, float*, cudaStream_t) {
-  return cudaErrorNotSupported;
-}
+
+bool tc_bwd_supported(const Params& p) { return p.C % bwdtc::CB == 0 && p.P <= 48; }
 
 }  // namespace xhc

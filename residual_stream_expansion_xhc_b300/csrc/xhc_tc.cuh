@@ -17,9 +17,8 @@ int read_device_error(cudaStream_t st);
 bool tc_update_supported(const Params& p);
 cudaError_t launch_update_tc(const Params& p, const UpdArgs<__nv_bfloat16>& a, bool has_conv, cudaStream_t st);
 
+// The bf16 backward built from the token pass, the TFA pass, the tensor-core
+// stream pass and the reduction (see xhc_bwd.cuh) serves these shapes.
 bool tc_bwd_supported(const Params& p);
-size_t tc_bwd_partial_bytes(const Params& p);
-cudaError_t launch_bwd_tc(const Params& p, const BwdArgs<__nv_bfloat16>& a, bool has_conv, float* partial,
-                          cudaStream_t st);
 
 }  // namespace xhc

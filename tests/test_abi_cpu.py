@@ -101,7 +101,7 @@ def test_backward_rejections(lib):
     L = lib.LIB
     need = L.xhc_bwd_workspace_bytes(ctypes.byref(sh))
     assert need > 0
-    args = dict(X=FAKE, act=None, out=FAKE, w=(None, None, None), W=FAKE, saved=FAKE, dXp=FAKE, dxi=None, dX=FAKE,
+    args = dict(X=FAKE, act=None, out=FAKE, w=(None, None, None), W=FAKE, saved=FAKE, dXp=ctypes.c_void_p(1 << 22), dxi=None, dX=FAKE,
                 dout=FAKE, dw=(None, None, None), dW=FAKE, ws=FAKE, wsb=need)
 
     def call(**kw):
@@ -115,6 +115,7 @@ def test_backward_rejections(lib):
     assert call(w=(FAKE, FAKE, FAKE)) == 8               # conv weights without their gradients
     assert call(act=FAKE, saved=None) == 8               # recomputation needs the pre-update state
     assert call(dW=MIS) == 3
+    assert call(dX=ctypes.c_void_p(1 << 21), dXp=ctypes.c_void_p(1 << 21)) == 8   # dX may not alias dX'
 
 
 def test_copy_rejections(lib):
