@@ -37,12 +37,12 @@ METRIC = "tokens/s per xHC sublayer (fwd, fwd+bwd) and achieved HBM GB/s vs peak
 #   backward, token:  4 (dX' active) + 4 (old active rows) + 1 (out) = 9
 #   backward, stream: 16 (X) + 16 (dX') + 1 (out) + 16 (dX) + 1 (dout) = 50
 ALG_C = {
-    "fwd_fused_tc": 26, "coeffs_tc": 17, "coeffs_simt": 17, "update_tc": 9, "update_simt": 13,
-    "bwd_token_tc": 9, "bwd_token_simt": 9, "bwd_stream_tc": 50, "bwd_dx_simt": 48, "bwd_dw_simt": 16,
-    "bwd_tfa_simt": 6, "gather_active": 8,
+    "coeffs_tc": 16, "coeffs_simt": 17, "update_simt": 26,
+    "bwd_token": 13, "bwd_tfa": 6, "bwd_stream_tc": 48,
+    "bwd_token_simt": 9, "bwd_dx_simt": 48, "bwd_dw_simt": 16, "bwd_tfa_simt": 6,
 }
 ALG_SIDE = {  # fp32 bytes per token
-    "fwd_fused_tc": 0, "coeffs_tc": 0, "coeffs_simt": 0, "bwd_token_tc": 0, "bwd_token_simt": 0,
+    "coeffs_tc": 196, "coeffs_simt": 196,
 }
 
 
