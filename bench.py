@@ -235,10 +235,11 @@ class Step:
         self.dconv = None if self.conv is None else tuple(torch.empty_like(w) for w in self.conv)
         self.dW = torch.empty_like(self.W)
         self.ws = api.workspace(api.xhc_bwd_workspace_bytes(self.sh), dev)
+        self.fws = api.workspace(api.xhc_fwd_workspace_need(self.sh, True), dev)
 
     def fwd(self):
         self.api.xhc_sublayer_fwd(self.sh, self.X, self.X, self.out, self.conv, self.W, self.idx, x_in=self.x_in,
-                                  saved=self.saved, saved_active=self.act)
+                                  saved=self.saved, saved_active=self.act, workspace=self.fws)
 
     def bwd(self):
         self.api.xhc_sublayer_bwd(self.sh, self.X, self.act, self.out, self.conv, self.W, self.idx, self.saved,

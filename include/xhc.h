@@ -148,10 +148,14 @@ int xhc_sparse_update(const xhc_shape_t* sh, const void* X_in, void* X_out,
                       const int32_t* idx, xhc_stream_t stream);
 
 /*
- * Workspace the fused forward needs when `saved` is NULL (bytes; 0 when none
- * is needed).
+ * Workspace of the fused forward (bytes).  xhc_fwd_workspace_bytes() is enough
+ * for every call of the shape; xhc_fwd_workspace_need() is what a call needs
+ * when the caller keeps the logits (keeps_saved != 0: `saved` is non-NULL) or
+ * not.  The bf16 path uses it for a per-token coefficient block (48 fp32 per
+ * token) and, when `saved` is NULL, for the logits (P + 1 fp32 per token).
  */
 size_t xhc_fwd_workspace_bytes(const xhc_shape_t* sh);
+size_t xhc_fwd_workspace_need(const xhc_shape_t* sh, int keeps_saved);
 
 /*
  * xhc_sublayer_fwd -- the whole per-sublayer update: coefficients, dense
@@ -164,8 +168,9 @@ size_t xhc_fwd_workspace_bytes(const xhc_shape_t* sh);
  *   saved_active  [B,S,k,C] dtype: the k active rows of X_in before the
  *          update (slot order), written; may be NULL.  Needed by the backward
  *          when the state is updated in place.
- *   workspace, ws_bytes  at least xhc_fwd_workspace_bytes() bytes when saved
- *          is NULL, else may be NULL/0.
+ *   workspace, ws_bytes  at least xhc_fwd_workspace_need(sh, saved != NULL)
+ *          bytes (NULL/0 when that is 0); xhc_fwd_workspace_bytes() always
+ *          suffices.
  */
 int xhc_sublayer_fwd(const xhc_shape_t* sh, const void* X_in, void* X_out,
                      const void* out, const float* w4, const float* w8,
@@ -182,10 +187,11 @@ int xhc_sublayer_fwd(const xhc_shape_t* sh, const void* X_in, void* X_out,
  * own).  This entry point takes the same arguments as xhc_sublayer_fwd minus
  * the workspace, and uses a fixed 8 MiB scratch area built into the library
  * (a device array that every GPU which loads the library keeps until the
- * process exits) for the per-token logits when `saved` is NULL.
- *   Limit: B*S*(P+1)*4 bytes must fit in 8 MiB when saved is NULL (42,799
- *          tokens at N = 16, k = 4); larger calls return XHC_ERR_WORKSPACE
- *          before touching the GPU.  With `saved` given there is no limit.
+ * process exits) in place of the workspace.
+ *   Limit: xhc_fwd_workspace_need(sh, saved != NULL) must be at most 8 MiB:
+ *          43,690 tokens at N = 16, k = 4 with `saved` given, 21,620 without
+ *          (bf16; the fp32 path needs no scratch when `saved` is given).
+ *          Larger calls return XHC_ERR_WORKSPACE before touching the GPU.
  *   The first call on each device looks up the scratch address on that
  *   device (no allocation); make that first call before any stream capture.
  *   Every call shares the one scratch area: calls whose work overlaps on the

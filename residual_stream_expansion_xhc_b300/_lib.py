@@ -17,7 +17,7 @@ STATUS = {0: "XHC_OK", 1: "XHC_ERR_SHAPE", 2: "XHC_ERR_INDEX", 3: "XHC_ERR_ALIGN
           5: "XHC_ERR_WORKSPACE", 6: "XHC_ERR_CUDA", 7: "XHC_ERR_TIMEOUT", 8: "XHC_ERR_ARG"}
 
 EXPORTS = ("xhc_status_string", "xhc_last_cuda_error", "xhc_device_status", "xhc_num_logits", "xhc_coeffs", "xhc_tfa",
-           "xhc_sparse_update", "xhc_fwd_workspace_bytes", "xhc_sublayer_fwd", "xhc_sublayer_fwd_noalloc", "xhc_bwd_workspace_bytes",
+           "xhc_sparse_update", "xhc_fwd_workspace_bytes", "xhc_fwd_workspace_need", "xhc_sublayer_fwd", "xhc_sublayer_fwd_noalloc", "xhc_bwd_workspace_bytes",
            "xhc_sublayer_bwd", "xhc_copy", "xhc_timing_enable", "xhc_timing_collect")
 
 
@@ -60,6 +60,8 @@ def _load() -> ctypes.CDLL:
     lib.xhc_sparse_update.argtypes = [sh, P, P, P, P, P, P, P, P, P, P]
     lib.xhc_fwd_workspace_bytes.restype = Z
     lib.xhc_fwd_workspace_bytes.argtypes = [sh]
+    lib.xhc_fwd_workspace_need.restype = Z
+    lib.xhc_fwd_workspace_need.argtypes = [sh, I]
     lib.xhc_sublayer_fwd.restype = I
     lib.xhc_sublayer_fwd.argtypes = [sh, P, P, P, P, P, P, P, P, P, P, P, P, Z, P]
     lib.xhc_sublayer_fwd_noalloc.restype = I

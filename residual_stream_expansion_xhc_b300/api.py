@@ -82,6 +82,10 @@ def xhc_fwd_workspace_bytes(sh) -> int:
     return int(LIB.xhc_fwd_workspace_bytes(ctypes.byref(sh)))
 
 
+def xhc_fwd_workspace_need(sh, keeps_saved: bool) -> int:
+    return int(LIB.xhc_fwd_workspace_need(ctypes.byref(sh), 1 if keeps_saved else 0))
+
+
 def xhc_bwd_workspace_bytes(sh) -> int:
     return int(LIB.xhc_bwd_workspace_bytes(ctypes.byref(sh)))
 

@@ -9,6 +9,7 @@
 #include "xhc_kernels.cuh"
 #include "xhc_bwd.cuh"
 #include "xhc_tc.cuh"
+#include "xhc_stream.cuh"
 
 using namespace xhc;
 
@@ -105,7 +106,7 @@ int run_coeffs(const xhc_shape_t* sh, const Params& p, const void* X, const floa
   if (sh->dtype == XHC_BF16) {
     using T = __nv_bfloat16;
     if (tc_coeffs_supported(p)) {
-      int s = cuda_status(launch_coeffs_tc(p, X, W, hpre, hpost, hres, saved, st));
+      int s = cuda_status(launch_coeffs_tc(p, X, W, hpre, hpost, hres, saved, nullptr, st));
       if (s || !x_in) return s;
       UpdArgs<T> a{(const T*)X, nullptr, nullptr, {nullptr, nullptr, nullptr}, hpre, nullptr, nullptr,
                    hpre ? nullptr : saved, (T*)x_in, nullptr, 0};
@@ -266,7 +267,6 @@ int xhc_sparse_update(const xhc_shape_t* sh, const void* X_in, void* X_out, cons
     using T = __nv_bfloat16;
     UpdArgs<T> a{(const T*)X_in, (T*)X_out, (const T*)out, {w4, w8, w12}, nullptr, hpost, hres, nullptr,
                  nullptr, nullptr, X_out != X_in};
-    if (tc_update_supported(p)) return cuda_status(launch_update_tc(p, a, has_conv, st));
     return cuda_status(launch_update_simt<T>(p, a, has_conv, st));
   }
   UpdArgs<float> a{(const float*)X_in, (float*)X_out, (const float*)out, {w4, w8, w12}, nullptr, hpost, hres,
@@ -274,10 +274,27 @@ int xhc_sparse_update(const xhc_shape_t* sh, const void* X_in, void* X_out, cons
   return cuda_status(launch_update_simt<float>(p, a, has_conv, st));
 }
 
+namespace {
+// Forward workspace: the coefficient block [T, COEF_STRIDE] (bf16 tensor-core
+// path) followed by the logits [T, P + 1] when the caller keeps none.
+size_t fwd_coef_bytes(const xhc_shape_t* sh) { return round_up(tokens(sh) * COEF_STRIDE * sizeof(float)); }
+size_t fwd_z_bytes(const xhc_shape_t* sh) {
+  return round_up(tokens(sh) * (size_t)(sh->N + 4 * sh->k + sh->k * sh->k + 1) * sizeof(float));
+}
+bool fwd_uses_coef(const xhc_shape_t* sh, const Params& p) {
+  return sh->dtype == XHC_BF16 && tc_coeffs_supported(p) && stream_update_supported(p);
+}
+}  // namespace
+
 size_t xhc_fwd_workspace_bytes(const xhc_shape_t* sh) {
   if (check_shape(sh)) return 0;
+  return fwd_coef_bytes(sh) + fwd_z_bytes(sh);
+}
+
+size_t xhc_fwd_workspace_need(const xhc_shape_t* sh, int keeps_saved) {
+  if (check_shape(sh)) return 0;
   const Params p = make_params(sh, nullptr);
-  return round_up(tokens(sh) * (size_t)(p.P + 1) * sizeof(float));
+  return (fwd_uses_coef(sh, p) ? fwd_coef_bytes(sh) : 0) + (keeps_saved ? 0 : fwd_z_bytes(sh));
 }
 
 int xhc_sublayer_fwd(const xhc_shape_t* sh, const void* X_in, void* X_out, const void* out, const float* w4,
@@ -290,28 +307,28 @@ int xhc_sublayer_fwd(const xhc_shape_t* sh, const void* X_in, void* X_out, const
   if ((s = check_conv(w4, w8, w12, &has_conv))) return s;
   if (tokens(sh) == 0) return XHC_OK;
   if ((s = check_ptrs({X_in, X_out, out, W}, {w4, w8, w12, x_in, saved, saved_active, workspace}))) return s;
-  float* z = saved;
-  if (!z) {
-    if (!workspace || ws_bytes < xhc_fwd_workspace_bytes(sh)) return XHC_ERR_WORKSPACE;
-    z = (float*)workspace;
-  }
   const Params p = make_params(sh, idx);
+  const bool use_coef = fwd_uses_coef(sh, p);
+  const size_t need = xhc_fwd_workspace_need(sh, saved != nullptr);
+  if (need > 0 && (!workspace || ws_bytes < need)) return XHC_ERR_WORKSPACE;
+  char* ws = (char*)workspace;
+  float* coef = use_coef ? (float*)ws : nullptr;
+  float* z = saved ? saved : (float*)(ws + (use_coef ? fwd_coef_bytes(sh) : 0));
   cudaStream_t st = (cudaStream_t)stream;
-  if (sh->dtype == XHC_BF16 && tc_coeffs_supported(p)) {
-    // coefficients on the tensor cores; the dense read runs with the update
+  if (use_coef) {
+    // coefficients on the tensor cores, then one streaming pass: dense read,
+    // TFA and sparse write
     using T = __nv_bfloat16;
-    if ((s = cuda_status(launch_coeffs_tc(p, X_in, W, nullptr, nullptr, nullptr, z, st)))) return s;
+    if ((s = cuda_status(launch_coeffs_tc(p, X_in, W, nullptr, nullptr, nullptr, z, coef, st)))) return s;
     UpdArgs<T> a{(const T*)X_in, (T*)X_out, (const T*)out, {w4, w8, w12}, nullptr, nullptr, nullptr, z,
                  (T*)x_in, (T*)saved_active, X_out != X_in};
-    if (tc_update_supported(p)) return cuda_status(launch_update_tc(p, a, has_conv, st));
-    return cuda_status(launch_update_simt<T>(p, a, has_conv, st));
+    return cuda_status(launch_fwd_update(p, a, coef, has_conv, num_sms(), st));
   }
   if ((s = run_coeffs(sh, p, X_in, W, nullptr, nullptr, nullptr, z, x_in, st))) return s;
   if (sh->dtype == XHC_BF16) {
     using T = __nv_bfloat16;
     UpdArgs<T> a{(const T*)X_in, (T*)X_out, (const T*)out, {w4, w8, w12}, nullptr, nullptr, nullptr, z,
                  nullptr, (T*)saved_active, X_out != X_in};
-    if (tc_update_supported(p)) return cuda_status(launch_update_tc(p, a, has_conv, st));
     return cuda_status(launch_update_simt<T>(p, a, has_conv, st));
   }
   UpdArgs<float> a{(const float*)X_in, (float*)X_out, (const float*)out, {w4, w8, w12}, nullptr, nullptr, nullptr,
@@ -323,10 +340,11 @@ namespace {
 // Workspace of the backward.  CUDA-core path: per-token records (2P+1 floats),
 // recomputed logits, conv partials.  bf16 tensor-core path: records
 // (1+N+4k floats), recomputed logits, dp (bf16, 64 per token), W^T (bf16, 64
-// per column), conv partials, dW partials (one per token range).
+// per column), the coefficient block, the column pass's coefficient dots and
+// conv partials, dW partials (one per token range).
 struct BwdLayout {
-  size_t rec, saved, dP, Wt, cpart, wpart, total;
-  int ranges;
+  size_t rec, saved, dP, Wt, coef, pdot, cpart, wpart, total;
+  int ranges, cpart_rows;
 };
 BwdLayout bwd_layout(const xhc_shape_t* sh) {
   const Params p = make_params(sh, nullptr);
@@ -334,13 +352,17 @@ BwdLayout bwd_layout(const xhc_shape_t* sh) {
   const size_t NC = (size_t)p.N * p.C;
   BwdLayout L{};
   if (sh->dtype == XHC_BF16 && tc_bwd_supported(p)) {
+    const int sms = num_sms();
     L.ranges = bwd_stream_ranges(p);
+    L.cpart_rows = bwd_col_cpart_rows(p, sms);
     L.rec = 0;
     L.saved = L.rec + round_up(T * (size_t)(1 + p.N + 4 * p.k) * sizeof(float));
     L.dP = L.saved + round_up(T * (size_t)(p.P + 1) * sizeof(float));
     L.Wt = L.dP + round_up(T * 64 * sizeof(uint16_t));
-    L.cpart = L.Wt + round_up(NC * 64 * sizeof(uint16_t));
-    L.wpart = L.cpart + round_up(bwd_conv_partial_rows(p) * NTAPS * (size_t)p.C * sizeof(float));
+    L.coef = L.Wt + round_up(NC * 64 * sizeof(uint16_t));
+    L.pdot = L.coef + round_up(T * COEF_STRIDE * sizeof(float));
+    L.cpart = L.pdot + round_up(bwd_col_pdot_floats(p) * sizeof(float));
+    L.wpart = L.cpart + round_up(bwd_col_cpart_floats(p, sms) * sizeof(float));
     L.total = L.wpart + round_up((size_t)L.ranges * p.P * NC * sizeof(float));
   } else {
     L.rec = 0;
@@ -390,26 +412,37 @@ int xhc_sublayer_bwd(const xhc_shape_t* sh, const void* X_state, const void* sav
   const Params p = make_params(sh, idx);
   cudaStream_t st = (cudaStream_t)stream;
   float* rec = (float*)(ws + L.rec);
+  const bool tc_path = sh->dtype == XHC_BF16 && tc_bwd_supported(p);
+  float* coef = tc_path ? (float*)(ws + L.coef) : nullptr;
+  bool have_coef = false;
   const float* z = saved;
   if (!z) {
     float* zw = (float*)(ws + L.saved);
-    if ((s = run_coeffs(sh, p, X_state, W, nullptr, nullptr, nullptr, zw, nullptr, st))) return s;
+    if (tc_path && tc_coeffs_supported(p)) {
+      if ((s = cuda_status(launch_coeffs_tc(p, X_state, W, nullptr, nullptr, nullptr, zw, coef, st)))) return s;
+      have_coef = true;
+    } else if ((s = run_coeffs(sh, p, X_state, W, nullptr, nullptr, nullptr, zw, nullptr, st))) {
+      return s;
+    }
     z = zw;
   }
   if (sh->dtype == XHC_BF16) {
     using T = __nv_bfloat16;
     BwdArgs<T> a{(const T*)X_state, (const T*)saved_active, (const T*)out, {w4, w8, w12}, W, z, (const T*)dXp,
                  (const T*)dx_in, (T*)dX, (T*)dout, {dw4, dw8, dw12}, dW, rec};
-    if (tc_bwd_supported(p)) {
+    if (tc_path) {
       T* dP = (T*)(ws + L.dP);
       T* Wt = (T*)(ws + L.Wt);
+      float* pdot = (float*)(ws + L.pdot);
       float* cpart = (float*)(ws + L.cpart);
       float* wpart = (float*)(ws + L.wpart);
+      const int sms = num_sms();
       if ((s = cuda_status(launch_wt_prep(p, W, Wt, st)))) return s;
-      if ((s = cuda_status(launch_bwd_token(p, a, has_conv, dP, st)))) return s;
-      if ((s = cuda_status(launch_bwd_tfa(p, a, has_conv, cpart, st)))) return s;
+      if (!have_coef && (s = cuda_status(launch_coef(p, z, coef, st)))) return s;
+      if ((s = cuda_status(launch_bwd_col(p, a, coef, has_conv, pdot, cpart, sms, st)))) return s;
+      if ((s = cuda_status(launch_bwd_dz(p, z, pdot, dx_in != nullptr, dP, rec, st)))) return s;
       if ((s = cuda_status(launch_bwd_stream_tc(p, a, Wt, dP, L.ranges, wpart, st)))) return s;
-      return cuda_status(launch_bwd_reduce(p, a, has_conv, cpart, L.ranges, wpart, st));
+      return cuda_status(launch_bwd_reduce(p, a, has_conv, cpart, L.cpart_rows, L.ranges, wpart, st));
     }
     return cuda_status(launch_bwd_simt<T>(p, a, has_conv, (float*)(ws + L.cpart), true, st));
   }

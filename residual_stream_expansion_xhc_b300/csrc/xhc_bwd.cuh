@@ -5,16 +5,11 @@
 
 namespace xhc {
 
-// Rows of conv-weight partial sums written by the TFA pass.
-size_t bwd_conv_partial_rows(const Params& p);
-
 cudaError_t launch_wt_prep(const Params& p, const float* W, __nv_bfloat16* Wt, cudaStream_t st);
-cudaError_t launch_bwd_token(const Params& p, const BwdArgs<__nv_bfloat16>& a, bool has_conv, __nv_bfloat16* dP,
-                             cudaStream_t st);
-cudaError_t launch_bwd_tfa(const Params& p, const BwdArgs<__nv_bfloat16>& a, bool has_conv, float* cpart,
-                           cudaStream_t st);
+// Fixed-order sums of the conv-weight partials [conv_rows][24][C] and the dW
+// partials [w_ranges][P][N C].
 cudaError_t launch_bwd_reduce(const Params& p, const BwdArgs<__nv_bfloat16>& a, bool has_conv, const float* cpart,
-                              int w_ranges, const float* wpart, cudaStream_t st);
+                              int conv_rows, int w_ranges, const float* wpart, cudaStream_t st);
 
 // Token ranges the tensor-core stream pass splits the batch into (each range
 // writes one dW partial).

@@ -118,6 +118,48 @@ __device__ __forceinline__ float sinkhorn16(float z, bool valid, int iters) {
   return M;
 }
 
+// The same Sinkhorn normalisation with one token's k x k matrix in one
+// thread's registers (4 x 4, entries with i >= k or j >= k are padding and
+// stay 0).  Sums pair entries as the half-warp version does, ((e0 + e1) +
+// (e2 + e3)) along rows and ((r0 + r1) + (r2 + r3)) along columns, so both
+// versions produce identical values.  `z` holds the logits row-major (k per
+// row, entry (i, j) at z[k i + j]).
+__device__ __forceinline__ void sinkhorn_thread(const float* z, int k, int iters, float (&M)[KMAX][KMAX]) {
+  float zmax = -INFINITY;
+#pragma unroll
+  for (int i = 0; i < KMAX; ++i)
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j)
+      if (i < k && j < k) zmax = fmaxf(zmax, z[k * i + j]);
+#pragma unroll
+  for (int i = 0; i < KMAX; ++i)
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) M[i][j] = (i < k && j < k) ? expf(z[k * i + j] - zmax) : 0.0f;
+  for (int it = 0; it < iters; ++it) {
+#pragma unroll
+    for (int i = 0; i < KMAX; ++i) {
+      const float s = (M[i][0] + M[i][1]) + (M[i][2] + M[i][3]);
+#pragma unroll
+      for (int j = 0; j < KMAX; ++j) M[i][j] = (i < k && j < k) ? M[i][j] / s : 0.0f;
+    }
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+      const float s = (M[0][j] + M[1][j]) + (M[2][j] + M[3][j]);
+#pragma unroll
+      for (int i = 0; i < KMAX; ++i) M[i][j] = (i < k && j < k) ? M[i][j] / s : 0.0f;
+    }
+  }
+}
+
+// Per-token coefficient block written by the coefficient passes and read by
+// the update and backward passes: 48 fp32 per token,
+//   [ 0, 16) hpre[n]                (n < N, rest 0)
+//   [16, 32) hpost[4 i + c]         (i < k, rest 0)
+//   [32, 48) Hres[4 i + j]          (i, j < k, rest 0)
+constexpr int COEF_STRIDE = 48;
+constexpr int COEF_POST = 16;
+constexpr int COEF_RES = 32;
+
 // Reverse of one normalisation y = x / s (s = sum of x along the axis):
 // dx = dy / s - sum(dy * x) / s^2.
 __device__ __forceinline__ float norm_reverse_row(float g, float x, bool valid) {

@@ -1,9 +1,9 @@
 // xhc_sublayer_fwd_noalloc: the fused forward for callers that cannot
 // allocate device memory.
 //
-// The fused forward needs scratch for the per-token logits when the caller
-// does not keep them (`saved` == NULL).  Normally the caller hands that scratch
-// in as a workspace.  Some callers have no way to obtain one: code running
+// The fused forward needs scratch: a per-token coefficient block, and the
+// per-token logits when the caller does not keep them (`saved` == NULL).
+// Normally the caller hands that scratch in as a workspace.  Some callers have no way to obtain one: code running
 // inside a framework's custom-op or plugin hook that may not call the CUDA
 // allocator, a process whose memory is owned by a pool it cannot reach from
 // this point, or a C caller that only receives its input and output buffers.
@@ -16,8 +16,9 @@
 
 namespace {
 
-// Capacity of the built-in scratch: tokens * (P + 1) * 4 bytes must fit.
-// 8 MiB holds the logits of 42,799 tokens at N = 16, k = 4 (P = 48).
+// Capacity of the built-in scratch.  At N = 16, k = 4 (P = 48) a bf16 call
+// needs 192 bytes per token with `saved` given (43,690 tokens fit) and 388
+// bytes per token without (21,620 tokens fit).
 constexpr size_t kScratchBytes = size_t(8) << 20;
 
 static __device__ __align__(256) unsigned char g_fwd_scratch[kScratchBytes];
@@ -50,7 +51,7 @@ extern "C" int xhc_sublayer_fwd_noalloc(const xhc_shape_t* sh, const void* X_in,
                                         const int32_t* idx, void* x_in, float* saved, void* saved_active,
                                         xhc_stream_t stream) {
   // Sizes are checked before anything touches the GPU.
-  const size_t need = saved ? 0 : xhc_fwd_workspace_bytes(sh);
+  const size_t need = xhc_fwd_workspace_need(sh, saved != nullptr);
   if (need > kScratchBytes) return XHC_ERR_WORKSPACE;
   if (need == 0)
     return xhc_sublayer_fwd(sh, X_in, X_out, out, w4, w8, w12, W, idx, x_in, saved, saved_active, nullptr, 0,
@@ -58,8 +59,8 @@ extern "C" int xhc_sublayer_fwd_noalloc(const xhc_shape_t* sh, const void* X_in,
   void* scratch = nullptr;
   const int s = scratch_on_current_device(&scratch);
   if (s != XHC_OK) return s;
-  // Every logit the update reads is written earlier in the same call, so the
-  // scratch needs no clearing between calls.
+  // Every coefficient and logit the update reads is written earlier in the
+  // same call, so the scratch needs no clearing between calls.
   return xhc_sublayer_fwd(sh, X_in, X_out, out, w4, w8, w12, W, idx, x_in, saved, saved_active, scratch,
                           kScratchBytes, stream);
 }

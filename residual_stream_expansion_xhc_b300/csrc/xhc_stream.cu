@@ -1,0 +1,816 @@
+// Bandwidth-bound CUDA-core passes of the xHC update for bf16 state (sm_103a):
+//   coef_kernel       per-token coefficients (sigmoid H^pre / H^post, Sinkhorn
+//                     H^res) from saved logits
+//   fwd_update_kernel dense read x_in, TFA components and the sparse write
+//   bwd_col_kernel    backward: active-stream mix, du = H^post^T G, dout
+//                     (transpose of the causal convolutions), conv-weight
+//                     partial sums and the per-token coefficient dots
+//   bwd_dz_kernel     backward: per-token reverse through sigmoid and every
+//                     Sinkhorn iteration; dp and the rmsnorm term
+//
+// Method: "xHC: Expanded Hyper-Connections" (qingkeai.online research
+// retrospective).  Section "Scaling N": the state is N streams of width C;
+// H^pre reads the sublayer input from them, H^res (Sinkhorn-normalised) mixes
+// them.  Section "Temporal Feature Augmentation": three causal depthwise
+// convolutions of kernel size 4, 8, 12 along the sequence, stacked with the
+// raw output.  Section "Dense read, sparse write": the input is read from all
+// N streams, only the k active streams are rewritten.
+//
+// Layout of the work.  A CTA owns CB = 256 channels of the state (one channel
+// per thread in the channel phases) and walks token segments of one sequence
+// in chunks of TT = 8 tokens (one token per warp in the token phases, eight
+// channels = one 16-byte vector per lane).  The causal halo of `out` lives in
+// a ring of rows in shared memory, so every row of `out` is read from HBM
+// once per segment; the conv taps of the CTA's channels are read once per CTA.
+#include <algorithm>
+
+#include "xhc_stream.cuh"
+
+namespace xhc {
+
+namespace stream {
+constexpr int CB = 256;        // channels per CTA
+constexpr int TT = 8;          // tokens per chunk
+constexpr int THREADS = 256;
+constexpr int ORING = 32;      // rows in the `out` ring (power of two)
+constexpr int SEG = 64;        // tokens per segment (one job)
+constexpr int PDOT = 48;       // floats per token and channel block of dots
+}  // namespace stream
+
+using namespace stream;
+
+// ---------------------------------------------------------------- helpers
+
+__device__ __forceinline__ void unpack8(const uint4& a, float (&v)[8]) {
+  v[0] = bf_lo(a.x); v[1] = bf_hi(a.x); v[2] = bf_lo(a.y); v[3] = bf_hi(a.y);
+  v[4] = bf_lo(a.z); v[5] = bf_hi(a.z); v[6] = bf_lo(a.w); v[7] = bf_hi(a.w);
+}
+__device__ __forceinline__ uint4 pack8(const float (&v)[8]) {
+  return make_uint4(pack_bf2(v[0], v[1]), pack_bf2(v[2], v[3]), pack_bf2(v[4], v[5]), pack_bf2(v[6], v[7]));
+}
+__device__ __forceinline__ uint4 ld_stream(const __nv_bfloat16* p) {
+  return __ldcs(reinterpret_cast<const uint4*>(p));
+}
+__device__ __forceinline__ void st_stream(__nv_bfloat16* p, const uint4& v) {
+  __stcs(reinterpret_cast<uint4*>(p), v);
+}
+__device__ __forceinline__ float bf16_bits(uint16_t h) { return __uint_as_float((uint32_t)h << 16); }
+
+// Conv taps of channel c: w[g], g = 0..3 (K = 4), 4..11 (K = 8), 12..23 (K = 12);
+// tap tau multiplies out[t - tau].
+__device__ __forceinline__ void load_taps(const float* const (&w)[3], int c, int C, float (&tap)[NTAPS]) {
+#pragma unroll
+  for (int g = 0; g < NTAPS; ++g) tap[g] = 0.0f;
+  if (c >= C) return;
+  const float4 a = *reinterpret_cast<const float4*>(w[0] + (size_t)c * 4);
+  const float4 b0 = *reinterpret_cast<const float4*>(w[1] + (size_t)c * 8);
+  const float4 b1 = *reinterpret_cast<const float4*>(w[1] + (size_t)c * 8 + 4);
+  const float4 d0 = *reinterpret_cast<const float4*>(w[2] + (size_t)c * 12);
+  const float4 d1 = *reinterpret_cast<const float4*>(w[2] + (size_t)c * 12 + 4);
+  const float4 d2 = *reinterpret_cast<const float4*>(w[2] + (size_t)c * 12 + 8);
+  const float v[NTAPS] = {a.x,  a.y,  a.z,  a.w,  b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w,
+                          d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w, d2.x, d2.y, d2.z, d2.w};
+#pragma unroll
+  for (int g = 0; g < NTAPS; ++g) tap[g] = v[g];
+}
+
+// Warp `warp` loads rows r_beg + warp, r_beg + warp + TT, ... < r_end of the
+// sequence's `out` (channels of this CTA) into the ring; rows outside [0, S)
+// are zero (the causal padding before the sequence start).
+__device__ __forceinline__ void load_out_rows(uint16_t (*ring)[CB], const __nv_bfloat16* __restrict__ out,
+                                              size_t seq_base, int S, int C, int c_lane, int r_beg, int r_end,
+                                              int warp, int lane) {
+  for (int r = r_beg + warp; r < r_end; r += TT) {
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (r >= 0 && r < S && c_lane < C) v = *reinterpret_cast<const uint4*>(out + (seq_base + r) * C + c_lane);
+    *reinterpret_cast<uint4*>(&ring[r & (ORING - 1)][8 * lane]) = v;
+  }
+}
+
+// Reduce 32 per-lane values across the warp so that lane l ends with the sum
+// over all lanes of value l (31 shuffles: each level halves the values held).
+__device__ __forceinline__ float warp_transpose_sum32(float (&v)[32], int lane) {
+#pragma unroll
+  for (int o = 16; o >= 1; o >>= 1) {
+    const bool upper = (lane & o) != 0;
+#pragma unroll
+    for (int i = 0; i < o; ++i) {
+      const float send = upper ? v[i] : v[i + o];
+      const float keep = upper ? v[i + o] : v[i];
+      v[i] = keep + __shfl_xor_sync(FULL, send, o);
+    }
+  }
+  return v[0];
+}
+
+struct Walk {
+  int nseg;       // segments per sequence
+  int R;          // CTAs per channel block (grid.x)
+  int ncb;        // channel blocks (grid.y)
+};
+
+Walk make_walk(const Params& p, int sms) {
+  Walk w;
+  w.nseg = (p.S + SEG - 1) / SEG;
+  w.ncb = (p.C + CB - 1) / CB;
+  const long jobs = (long)p.B * w.nseg;
+  const long slots = std::max(1L, (long)(2 * sms) / w.ncb);
+  w.R = (int)std::max(1L, std::min(jobs, slots));
+  return w;
+}
+
+// ---------------------------------------------------------------- coefficients from saved logits
+//
+// One thread per token: hpre = sigmoid(z[0:N]), hpost = sigmoid(z[N:N+4k]),
+// Hres = Sinkhorn(exp(Z - max Z)) -> coefficient block.
+
+__global__ void __launch_bounds__(128) coef_kernel(Params p, const float* __restrict__ saved, float* __restrict__ coef,
+                                                   size_t T_all) {
+  const size_t t = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= T_all) return;
+  const int N = p.N, k = p.k, P = p.P;
+  const float* z = saved + t * (P + 1);
+  float4* cf = reinterpret_cast<float4*>(coef + t * COEF_STRIDE);
+#pragma unroll
+  for (int v = 0; v < 4; ++v) {
+    float h[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) h[e] = (4 * v + e < N) ? sigmoidf_(z[4 * v + e]) : 0.0f;
+    cf[v] = make_float4(h[0], h[1], h[2], h[3]);
+  }
+#pragma unroll
+  for (int v = 0; v < 4; ++v) {
+    float h[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) h[e] = (4 * v + e < 4 * k) ? sigmoidf_(z[N + 4 * v + e]) : 0.0f;
+    cf[4 + v] = make_float4(h[0], h[1], h[2], h[3]);
+  }
+  float zr[KMAX * KMAX];
+#pragma unroll
+  for (int q = 0; q < KMAX * KMAX; ++q) zr[q] = q < k * k ? z[N + 4 * k + q] : 0.0f;
+  float M[KMAX][KMAX];
+  sinkhorn_thread(zr, k, p.iters, M);
+#pragma unroll
+  for (int i = 0; i < KMAX; ++i) cf[8 + i] = make_float4(M[i][0], M[i][1], M[i][2], M[i][3]);
+}
+
+// ---------------------------------------------------------------- forward update
+//
+// Per chunk: the channel phase computes u_1..u_3 of the chunk (taps and
+// `out` from shared memory); the token phase reads the token's N state rows
+// once and writes x_in = sum_n hpre[n] X[n], the saved active rows, and
+// X'[a_i] = sum_j Hres[i][j] X[a_j] + sum_c hpost[i][c] u_c.
+
+struct FwdSmem {
+  uint16_t ring[ORING][CB];          // out rows (bf16 bits)
+  float u[3][TT][CB];                // u_1..u_3 of the chunk
+  float tap[NTAPS][CB];              // conv taps of the CTA's channels
+};
+
+__device__ __forceinline__ void stage_taps(float (*tap_s)[CB], const float* const (&w)[3], int c, int C, int ch) {
+  float t[NTAPS];
+  load_taps(w, c, C, t);
+#pragma unroll
+  for (int g = 0; g < NTAPS; ++g) tap_s[g][ch] = t[g];
+}
+
+// u_1..u_3 of one channel for the chunk tokens t0 .. t0+7 (< s_end) from the
+// ring rows t0 - 11 .. t0 + 7; U is float (forward) or bf16 bits (backward).
+template <typename U>
+__device__ __forceinline__ void tfa_chunk_s(const uint16_t (*ring)[CB], U (*u_s)[TT][CB], const float (&tap)[NTAPS],
+                                            int t0, int s_end, int ch) {
+  float ow[TT + HALO];
+#pragma unroll
+  for (int i = 0; i < TT + HALO; ++i) ow[i] = bf16_bits(ring[(t0 - HALO + i) & (ORING - 1)][ch]);
+#pragma unroll
+  for (int tt = 0; tt < TT; ++tt) {
+    if (t0 + tt >= s_end) break;
+    float u1 = 0.0f, u2 = 0.0f, u3 = 0.0f;
+#pragma unroll
+    for (int tau = 0; tau < 4; ++tau) u1 = fmaf(tap[tau], ow[tt + HALO - tau], u1);
+#pragma unroll
+    for (int tau = 0; tau < 8; ++tau) u2 = fmaf(tap[4 + tau], ow[tt + HALO - tau], u2);
+#pragma unroll
+    for (int tau = 0; tau < 12; ++tau) u3 = fmaf(tap[12 + tau], ow[tt + HALO - tau], u3);
+    if constexpr (sizeof(U) == 4) {
+      u_s[0][tt][ch] = u1;
+      u_s[1][tt][ch] = u2;
+      u_s[2][tt][ch] = u3;
+    } else {
+      u_s[0][tt][ch] = __bfloat16_as_ushort(__float2bfloat16_rn(u1));
+      u_s[1][tt][ch] = __bfloat16_as_ushort(__float2bfloat16_rn(u2));
+      u_s[2][tt][ch] = __bfloat16_as_ushort(__float2bfloat16_rn(u3));
+    }
+  }
+}
+
+template <bool HAS_CONV>
+__global__ void __launch_bounds__(THREADS, 2) fwd_update_kernel(Params p, UpdArgs<__nv_bfloat16> a,
+                                                                const float* __restrict__ coef, Walk wk) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  FwdSmem& sm = *reinterpret_cast<FwdSmem*>(smem_raw);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, ch = threadIdx.x;
+  const int N = p.N, k = p.k, C = p.C, S = p.S;
+  const int cb0 = blockIdx.y * CB;
+  const int c_lane = cb0 + 8 * lane;          // token phases: this lane's 8 channels
+  const bool lane_ok = c_lane < C;
+  if (HAS_CONV) stage_taps(sm.tap, a.w, cb0 + ch, C, ch);
+  const bool need_all = a.x_in != nullptr || a.copy_inactive;
+  const int jobs = p.B * wk.nseg;
+
+  auto channel_phase = [&](int t0, int s_end) {
+    float tap[NTAPS];
+#pragma unroll
+    for (int g = 0; g < NTAPS; ++g) tap[g] = sm.tap[g][ch];
+    tfa_chunk_s<float>(sm.ring, sm.u, tap, t0, s_end, ch);
+  };
+
+  for (int job = blockIdx.x; job < jobs; job += gridDim.x) {
+    const int b = job / wk.nseg;
+    const int s_beg = (job % wk.nseg) * SEG;
+    const int s_end = min(s_beg + SEG, S);
+    const size_t seq_base = (size_t)b * S;
+    const int nchunks = (s_end - s_beg + TT - 1) / TT;
+    __syncthreads();                           // previous job is done with the ring; taps staged
+    if (HAS_CONV) {
+      load_out_rows(sm.ring, a.out, seq_base, S, C, c_lane, s_beg - HALO, s_beg + TT, warp, lane);
+      __syncthreads();
+      channel_phase(s_beg, s_end);
+      __syncthreads();
+    }
+    for (int m = 0; m < nchunks; ++m) {
+      const int t0 = s_beg + m * TT;
+      if (HAS_CONV && m + 1 < nchunks)
+        load_out_rows(sm.ring, a.out, seq_base, S, C, c_lane, t0 + TT, t0 + 2 * TT, warp, lane);
+      const int t = t0 + warp;
+      if (t < s_end && lane_ok) {
+        const size_t tok = seq_base + t;
+        const float* cf = coef + tok * COEF_STRIDE;
+        const __nv_bfloat16* xrow = a.X_in + tok * (size_t)N * C + c_lane;
+        __nv_bfloat16* yrow = a.X_out + tok * (size_t)N * C + c_lane;
+        uint4 xa[KMAX];
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j)
+          if (j < k) xa[j] = ld_stream(xrow + (size_t)p.idx[j] * C);
+        float acc[8];
+#pragma unroll
+        for (int x = 0; x < 8; ++x) acc[x] = 0.0f;
+        if (need_all) {
+          // the inactive streams, eight rows at a time
+#pragma unroll
+          for (int nb = 0; nb < NMAX; nb += 8) {
+            uint4 xr[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              if (nb + q < N && !p.is_active[nb + q]) xr[q] = ld_stream(xrow + (size_t)(nb + q) * C);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              if (nb + q < N && !p.is_active[nb + q]) {
+                if (a.x_in) {
+                  const float h = cf[nb + q];
+                  float v[8];
+                  unpack8(xr[q], v);
+#pragma unroll
+                  for (int x = 0; x < 8; ++x) acc[x] = fmaf(h, v[x], acc[x]);
+                }
+                if (a.copy_inactive) st_stream(yrow + (size_t)(nb + q) * C, xr[q]);
+              }
+            }
+          }
+        }
+        if (a.x_in) {
+#pragma unroll
+          for (int j = 0; j < KMAX; ++j) {
+            if (j < k) {
+              const float h = cf[p.idx[j]];
+              float v[8];
+              unpack8(xa[j], v);
+#pragma unroll
+              for (int x = 0; x < 8; ++x) acc[x] = fmaf(h, v[x], acc[x]);
+            }
+          }
+          st_stream(a.x_in + tok * C + c_lane, pack8(acc));
+        }
+        if (a.saved_active) {
+#pragma unroll
+          for (int j = 0; j < KMAX; ++j)
+            if (j < k) st_stream(a.saved_active + (tok * k + j) * C + c_lane, xa[j]);
+        }
+        float u[4][8];
+        if (HAS_CONV) {
+          unpack8(*reinterpret_cast<const uint4*>(&sm.ring[t & (ORING - 1)][8 * lane]), u[0]);
+#pragma unroll
+          for (int j = 0; j < 3; ++j) {
+            const float4 q0 = *reinterpret_cast<const float4*>(&sm.u[j][warp][8 * lane]);
+            const float4 q1 = *reinterpret_cast<const float4*>(&sm.u[j][warp][8 * lane + 4]);
+            u[j + 1][0] = q0.x; u[j + 1][1] = q0.y; u[j + 1][2] = q0.z; u[j + 1][3] = q0.w;
+            u[j + 1][4] = q1.x; u[j + 1][5] = q1.y; u[j + 1][6] = q1.z; u[j + 1][7] = q1.w;
+          }
+        } else {
+          unpack8(*reinterpret_cast<const uint4*>(a.out + tok * C + c_lane), u[0]);
+#pragma unroll
+          for (int j = 1; j < 4; ++j)
+#pragma unroll
+            for (int x = 0; x < 8; ++x) u[j][x] = 0.0f;
+        }
+#pragma unroll
+        for (int i = 0; i < KMAX; ++i) {
+          if (i >= k) break;
+          const float4 hp = *reinterpret_cast<const float4*>(cf + COEF_POST + 4 * i);
+          const float4 hr = *reinterpret_cast<const float4*>(cf + COEF_RES + 4 * i);
+          const float hrv[4] = {hr.x, hr.y, hr.z, hr.w};
+          float y[8];
+#pragma unroll
+          for (int x = 0; x < 8; ++x) y[x] = 0.0f;
+#pragma unroll
+          for (int j = 0; j < KMAX; ++j) {
+            if (j < k) {
+              float v[8];
+              unpack8(xa[j], v);
+#pragma unroll
+              for (int x = 0; x < 8; ++x) y[x] = fmaf(hrv[j], v[x], y[x]);
+            }
+          }
+#pragma unroll
+          for (int x = 0; x < 8; ++x) {
+            y[x] = fmaf(hp.x, u[0][x], y[x]);
+            y[x] = fmaf(hp.y, u[1][x], y[x]);
+            y[x] = fmaf(hp.z, u[2][x], y[x]);
+            y[x] = fmaf(hp.w, u[3][x], y[x]);
+          }
+          st_stream(yrow + (size_t)p.idx[i] * C, pack8(y));
+        }
+      }
+      if (HAS_CONV) {
+        __syncthreads();                       // u of this chunk consumed; next rows in the ring
+        if (m + 1 < nchunks) channel_phase(t0 + TT, s_end);
+        __syncthreads();
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------- backward column pass
+//
+// Walks each segment from its last chunk to its first.  Per chunk:
+//   token phase (warp = token, lane = 8 channels)
+//     G_i = dX'[a_i], Xa_j (old active rows), u_c of the token
+//     mix   dX[a_j] = sum_i Hres[i][j] G_i
+//     du_c  = sum_i hpost[i][c] G_i  -> du rings (c >= 1), du0 (c = 0)
+//     dots  <G_i, Xa_j>, <G_i, u_c> (and <dx_in, X_n> with dx_in), reduced over
+//           the CTA's channels -> pdot[t][channel block]
+//     (and loads the `out` rows the next chunk's channel phase needs)
+//   channel phase (thread = channel)
+//     dout[t] = du_0[t] + sum_j sum_tau w_j[tau] du_j[t + tau]   (inside the sequence)
+//     dw_j[tau] += du_j[t] out[t - tau]
+//     u_1..u_3 of the next (earlier) chunk
+// The du rows of the tokens after a segment that its convolutions reach (3, 7
+// and 11 for K = 4, 8, 12) are computed first: the anti-causal halo.  Each
+// du_j ring holds K_j - 1 + TT rows or more.  Conv-weight partials: one row
+// per CTA, [R][24][C].
+
+constexpr int DR1 = 12, DR2 = 16, DR3 = 20;
+
+struct ColSmem {
+  uint16_t ring[ORING][CB];          // out rows (bf16 bits)
+  uint16_t u[3][TT][CB];             // u_1..u_3 of the chunk (bf16: they only enter dots)
+  float du1[DR1][CB];
+  float du2[DR2][CB];
+  float du3[DR3][CB];
+  float du0[TT][CB];                 // du_0 of the chunk
+  float dw[NTAPS][CB];               // conv-weight gradient of the CTA's channels
+};
+
+__device__ __forceinline__ void store8f(float* d, const float (&v)[8]) {
+  *reinterpret_cast<float4*>(d) = make_float4(v[0], v[1], v[2], v[3]);
+  *reinterpret_cast<float4*>(d + 4) = make_float4(v[4], v[5], v[6], v[7]);
+}
+
+template <bool HAS_CONV>
+__global__ void __launch_bounds__(THREADS, 2) bwd_col_kernel(Params p, BwdArgs<__nv_bfloat16> a,
+                                                             const float* __restrict__ coef, float* __restrict__ pdot,
+                                                             float* __restrict__ cpart, Walk wk) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  ColSmem& sm = *reinterpret_cast<ColSmem*>(smem_raw);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, ch = threadIdx.x;
+  const int N = p.N, k = p.k, C = p.C, S = p.S;
+  const size_t NC = (size_t)N * C;
+  const int cb = blockIdx.y, cb0 = cb * CB;
+  const int c_lane = cb0 + 8 * lane;
+  const bool lane_ok = c_lane < C;
+  const int c_ch = cb0 + ch;
+  if (HAS_CONV) {
+#pragma unroll
+    for (int g = 0; g < NTAPS; ++g) sm.dw[g][ch] = 0.0f;
+  }
+  const int jobs = p.B * wk.nseg;
+  const int ncb = wk.ncb;
+
+  auto taps = [&](float (&tap)[NTAPS]) { load_taps(a.w, c_ch, C, tap); };
+
+  // du_1..du_3 of a halo token t (lane's channels): rows the convolutions reach
+  auto du_halo = [&](size_t seq_base, int t, int s_end) {
+    const size_t tok = seq_base + t;
+    const float* cf = coef + tok * COEF_STRIDE;
+    float du[3][8];
+#pragma unroll
+    for (int c = 0; c < 3; ++c)
+#pragma unroll
+      for (int x = 0; x < 8; ++x) du[c][x] = 0.0f;
+#pragma unroll
+    for (int i = 0; i < KMAX; ++i) {
+      if (i < k) {
+        float g[8];
+        unpack8(ld_stream(a.dXp + tok * NC + (size_t)p.idx[i] * C + c_lane), g);
+        const float4 hp = *reinterpret_cast<const float4*>(cf + COEF_POST + 4 * i);
+#pragma unroll
+        for (int x = 0; x < 8; ++x) {
+          du[0][x] = fmaf(hp.y, g[x], du[0][x]);
+          du[1][x] = fmaf(hp.z, g[x], du[1][x]);
+          du[2][x] = fmaf(hp.w, g[x], du[2][x]);
+        }
+      }
+    }
+    const int d = t - s_end;                   // 0 .. 10
+    if (d < 3) store8f(&sm.du1[t % DR1][8 * lane], du[0]);
+    if (d < 7) store8f(&sm.du2[t % DR2][8 * lane], du[1]);
+    store8f(&sm.du3[t % DR3][8 * lane], du[2]);
+  };
+
+  for (int job = blockIdx.x; job < jobs; job += gridDim.x) {
+    const int b = job / wk.nseg;
+    const int s_beg = (job % wk.nseg) * SEG;
+    const int s_end = min(s_beg + SEG, S);
+    const size_t seq_base = (size_t)b * S;
+    const int nchunks = (s_end - s_beg + TT - 1) / TT;
+    const int t_top = s_beg + (nchunks - 1) * TT;
+    __syncthreads();                           // previous job is done with shared memory
+    if (HAS_CONV) {
+      // out rows of the top chunk and the du rows of the halo after the segment
+      load_out_rows(sm.ring, a.out, seq_base, S, C, c_lane, t_top - HALO, t_top + TT, warp, lane);
+      if (lane_ok) {
+        for (int t = s_end + warp; t < min(s_end + HALO, S); t += TT) du_halo(seq_base, t, s_end);
+      }
+      __syncthreads();
+      if (c_ch < C) {
+        float tap[NTAPS];
+        taps(tap);
+        tfa_chunk_s<uint16_t>(sm.ring, sm.u, tap, t_top, s_end, ch);
+      }
+      __syncthreads();
+    }
+    for (int m = nchunks - 1; m >= 0; --m) {
+      const int t0 = s_beg + m * TT;
+      // ------------------------------------------------ token phase
+      if (HAS_CONV && m > 0)
+        load_out_rows(sm.ring, a.out, seq_base, S, C, c_lane, t0 - TT - HALO, t0 - HALO, warp, lane);
+      const int t = t0 + warp;
+      if (t < s_end) {                         // warp-uniform
+        const size_t tok = seq_base + t;
+        const float* cf = coef + tok * COEF_STRIDE;
+        uint4 gr[KMAX], xr[KMAX];
+#pragma unroll
+        for (int i = 0; i < KMAX; ++i) gr[i] = xr[i] = make_uint4(0, 0, 0, 0);
+        if (lane_ok) {
+#pragma unroll
+          for (int i = 0; i < KMAX; ++i) {
+            if (i < k) {
+              gr[i] = ld_stream(a.dXp + tok * NC + (size_t)p.idx[i] * C + c_lane);
+              xr[i] = a.saved_active ? ld_stream(a.saved_active + (tok * k + i) * C + c_lane)
+                                     : ld_stream(a.X + tok * NC + (size_t)p.idx[i] * C + c_lane);
+            }
+          }
+          // active-stream mix: dX[a_j] = sum_i Hres[i][j] G_i
+#pragma unroll
+          for (int j = 0; j < KMAX; ++j) {
+            if (j < k) {
+              float mx[8];
+#pragma unroll
+              for (int x = 0; x < 8; ++x) mx[x] = 0.0f;
+#pragma unroll
+              for (int i = 0; i < KMAX; ++i) {
+                if (i < k) {
+                  const float h = cf[COEF_RES + 4 * i + j];
+                  float g[8];
+                  unpack8(gr[i], g);
+#pragma unroll
+                  for (int x = 0; x < 8; ++x) mx[x] = fmaf(h, g[x], mx[x]);
+                }
+              }
+              st_stream(a.dX + tok * NC + (size_t)p.idx[j] * C + c_lane, pack8(mx));
+            }
+          }
+          // du_c = sum_i hpost[i][c] G_i
+          {
+            float du[4][8];
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+#pragma unroll
+              for (int x = 0; x < 8; ++x) du[c][x] = 0.0f;
+#pragma unroll
+            for (int i = 0; i < KMAX; ++i) {
+              if (i < k) {
+                const float4 hp = *reinterpret_cast<const float4*>(cf + COEF_POST + 4 * i);
+                float g[8];
+                unpack8(gr[i], g);
+#pragma unroll
+                for (int x = 0; x < 8; ++x) {
+                  du[0][x] = fmaf(hp.x, g[x], du[0][x]);
+                  du[1][x] = fmaf(hp.y, g[x], du[1][x]);
+                  du[2][x] = fmaf(hp.z, g[x], du[2][x]);
+                  du[3][x] = fmaf(hp.w, g[x], du[3][x]);
+                }
+              }
+            }
+            if (HAS_CONV) {
+              store8f(&sm.du0[warp][8 * lane], du[0]);
+              store8f(&sm.du1[t % DR1][8 * lane], du[1]);
+              store8f(&sm.du2[t % DR2][8 * lane], du[2]);
+              store8f(&sm.du3[t % DR3][8 * lane], du[3]);
+            } else {
+              st_stream(a.dout + tok * C + c_lane, pack8(du[0]));
+            }
+          }
+        }
+        // dots over this lane's channels: [0,16) <G_i, Xa_j> at 4i+j, [16,32) <G_i, u_c> at 16+4i+c
+        float v[32];
+#pragma unroll
+        for (int q = 0; q < 32; ++q) v[q] = 0.0f;
+        if (lane_ok) {
+#pragma unroll
+          for (int j = 0; j < KMAX; ++j) {
+            if (j < k) {
+              float xv[8];
+              unpack8(xr[j], xv);
+#pragma unroll
+              for (int i = 0; i < KMAX; ++i) {
+                if (i < k) {
+                  float g[8];
+                  unpack8(gr[i], g);
+                  float d = 0.0f;
+#pragma unroll
+                  for (int x = 0; x < 8; ++x) d = fmaf(g[x], xv[x], d);
+                  v[4 * i + j] = d;
+                }
+              }
+            }
+          }
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            float uv[8];
+            if (c == 0) {
+              if (HAS_CONV) unpack8(*reinterpret_cast<const uint4*>(&sm.ring[t & (ORING - 1)][8 * lane]), uv);
+              else unpack8(*reinterpret_cast<const uint4*>(a.out + tok * C + c_lane), uv);
+            } else if (HAS_CONV) {
+              unpack8(*reinterpret_cast<const uint4*>(&sm.u[c - 1][warp][8 * lane]), uv);
+            } else {
+              break;
+            }
+#pragma unroll
+            for (int i = 0; i < KMAX; ++i) {
+              if (i < k) {
+                float g[8];
+                unpack8(gr[i], g);
+                float d = 0.0f;
+#pragma unroll
+                for (int x = 0; x < 8; ++x) d = fmaf(g[x], uv[x], d);
+                v[16 + 4 * i + c] = d;
+              }
+            }
+          }
+        }
+        // sum over the CTA's channels (all lanes take part)
+        float* pd = pdot + (tok * ncb + cb) * PDOT;
+        pd[lane] = warp_transpose_sum32(v, lane);
+        if (a.dx_in) {
+          // <dx_in, X_n> for every stream n
+#pragma unroll
+          for (int q = 0; q < 32; ++q) v[q] = 0.0f;
+          if (lane_ok) {
+            float g[8];
+            unpack8(ld_stream(a.dx_in + tok * C + c_lane), g);
+#pragma unroll
+            for (int n = 0; n < NMAX; ++n) {
+              if (n < N) {
+                const int slot = p.is_active[n];
+                float xv[8];
+                if (slot) {
+                  const __nv_bfloat16* src = a.saved_active ? a.saved_active + (tok * k + slot - 1) * C + c_lane
+                                                            : a.X + tok * NC + (size_t)n * C + c_lane;
+                  unpack8(*reinterpret_cast<const uint4*>(src), xv);
+                } else {
+                  unpack8(ld_stream(a.X + tok * NC + (size_t)n * C + c_lane), xv);
+                }
+                float d = 0.0f;
+#pragma unroll
+                for (int x = 0; x < 8; ++x) d = fmaf(g[x], xv[x], d);
+                v[n] = d;
+              }
+            }
+          }
+          const float r = warp_transpose_sum32(v, lane);
+          if (lane < 16) pd[32 + lane] = r;
+        }
+      }
+      if (!HAS_CONV) continue;
+      __syncthreads();
+      // ------------------------------------------------ channel phase
+      if (c_ch < C) {
+        float tap[NTAPS];
+        taps(tap);
+        // dout of the chunk tokens: du rows t0 .. t0 + 18 (zero past the sequence end)
+        float d1[TT + 3], d2[TT + 7], d3[TT + 11];
+#pragma unroll
+        for (int i = 0; i < TT + 11; ++i) {
+          const int tr = t0 + i;
+          const bool in = tr < S;
+          if (i < TT + 3) d1[i] = in ? sm.du1[tr % DR1][ch] : 0.0f;
+          if (i < TT + 7) d2[i] = in ? sm.du2[tr % DR2][ch] : 0.0f;
+          d3[i] = in ? sm.du3[tr % DR3][ch] : 0.0f;
+        }
+#pragma unroll
+        for (int tt = 0; tt < TT; ++tt) {
+          if (t0 + tt >= s_end) break;
+          float d = sm.du0[tt][ch];
+#pragma unroll
+          for (int tau = 0; tau < 4; ++tau) d = fmaf(tap[tau], d1[tt + tau], d);
+#pragma unroll
+          for (int tau = 0; tau < 8; ++tau) d = fmaf(tap[4 + tau], d2[tt + tau], d);
+#pragma unroll
+          for (int tau = 0; tau < 12; ++tau) d = fmaf(tap[12 + tau], d3[tt + tau], d);
+          a.dout[(seq_base + t0 + tt) * C + c_ch] = __float2bfloat16_rn(d);
+        }
+        // dw_j[tau] += du_j[t] out[t - tau] over the chunk tokens
+        float ow[TT + HALO];
+#pragma unroll
+        for (int i = 0; i < TT + HALO; ++i) ow[i] = bf16_bits(sm.ring[(t0 - HALO + i) & (ORING - 1)][ch]);
+        float dwl[NTAPS];
+#pragma unroll
+        for (int g = 0; g < NTAPS; ++g) dwl[g] = 0.0f;
+#pragma unroll
+        for (int tt = 0; tt < TT; ++tt) {
+          if (t0 + tt >= s_end) break;
+#pragma unroll
+          for (int tau = 0; tau < 4; ++tau) dwl[tau] = fmaf(d1[tt], ow[tt + HALO - tau], dwl[tau]);
+#pragma unroll
+          for (int tau = 0; tau < 8; ++tau) dwl[4 + tau] = fmaf(d2[tt], ow[tt + HALO - tau], dwl[4 + tau]);
+#pragma unroll
+          for (int tau = 0; tau < 12; ++tau) dwl[12 + tau] = fmaf(d3[tt], ow[tt + HALO - tau], dwl[12 + tau]);
+        }
+#pragma unroll
+        for (int g = 0; g < NTAPS; ++g) sm.dw[g][ch] += dwl[g];
+        if (m > 0) tfa_chunk_s<uint16_t>(sm.ring, sm.u, tap, t0 - TT, s_end, ch);
+      }
+      __syncthreads();
+    }
+  }
+  if (HAS_CONV && c_ch < C) {
+    __syncthreads();
+    float* dst = cpart + (size_t)blockIdx.x * NTAPS * C + c_ch;
+#pragma unroll
+    for (int g = 0; g < NTAPS; ++g) dst[(size_t)g * C] = sm.dw[g][ch];
+  }
+}
+
+// ---------------------------------------------------------------- backward per-token reverse
+//
+// Half-warp per token (lane e = 4 i + j for H^res entry (i, j)): sums the dot
+// partials of every channel block, reruns the Sinkhorn iterations keeping the
+// iterates, reverses them, and forms
+//   dz  (sigmoid' for H^pre / H^post, Sinkhorn reverse for H^res)
+//   dp  = rstd * dz                       -> dP[t][0..63] bf16 (zero padded)
+//   alpha = <dz, z / rstd> * (-rstd^3 / (N C))   -> rec[t][0]
+//   hpre[n]                               -> rec[t][1 + n]
+
+__global__ void __launch_bounds__(256) bwd_dz_kernel(Params p, const float* __restrict__ saved,
+                                                     const float* __restrict__ pdot, int ncb, int has_dxin,
+                                                     __nv_bfloat16* __restrict__ dP, float* __restrict__ rec,
+                                                     size_t T_all) {
+  extern __shared__ float trace_s[];           // [16 tokens][iters][32]
+  const int lane = threadIdx.x & 31, e = lane & 15;
+  const int slot = (threadIdx.x >> 5) * 2 + (lane >> 4);
+  const size_t t = (size_t)blockIdx.x * 16 + slot;
+  const bool live = t < T_all;
+  const size_t tc = live ? t : 0;
+  const int N = p.N, k = p.k, P = p.P;
+  const float* zt = saved + tc * (P + 1);
+  const float rstd = zt[P];
+  float dres = 0.0f, dpost = 0.0f, dpre = 0.0f;
+  for (int c = 0; c < ncb; ++c) {
+    const float* pd = pdot + (tc * ncb + c) * PDOT;
+    dres += pd[e];
+    dpost += pd[16 + e];
+    if (has_dxin) dpre += pd[32 + e];
+  }
+  const int i = e >> 2, j = e & 3;
+  const bool valid = i < k && j < k;
+  const float z = valid ? zt[N + 4 * k + k * i + j] : 0.0f;
+  float* tr = trace_s + (size_t)slot * p.iters * 32;
+  const float M0 = sinkhorn_init(z, valid);
+  float M = M0;
+  for (int it = 0; it < p.iters; ++it) M = sinkhorn_step(M, valid, &tr[it * 32 + e], &tr[it * 32 + 16 + e]);
+  float g = valid ? dres : 0.0f;
+  for (int it = p.iters - 1; it >= 0; --it) {
+    g = norm_reverse_col(g, tr[it * 32 + 16 + e], valid);
+    g = norm_reverse_row(g, tr[it * 32 + e], valid);
+  }
+  const float dz_res = valid ? g * M0 : 0.0f;
+  float dz_post = 0.0f, dz_pre = 0.0f, hpre = 0.0f;
+  if (e < 4 * k) {
+    const float h = sigmoidf_(zt[N + e]);
+    dz_post = dpost * h * (1.0f - h);
+  }
+  if (e < N) {
+    hpre = sigmoidf_(zt[e]);
+    dz_pre = has_dxin ? dpre * hpre * (1.0f - hpre) : 0.0f;
+  }
+  float part = 0.0f;
+  if (e < N) part = fmaf(dz_pre, zt[e], part);
+  if (e < 4 * k) part = fmaf(dz_post, zt[N + e], part);
+  if (valid) part = fmaf(dz_res, z, part);
+  part += __shfl_xor_sync(FULL, part, 1);
+  part += __shfl_xor_sync(FULL, part, 2);
+  part += __shfl_xor_sync(FULL, part, 4);
+  part += __shfl_xor_sync(FULL, part, 8);
+  if (!live) return;
+  __nv_bfloat16* dprow = dP + t * 64;
+  if (e < N) dprow[e] = __float2bfloat16_rn(rstd * dz_pre);
+  if (e < 4 * k) dprow[N + e] = __float2bfloat16_rn(rstd * dz_post);
+  if (valid) dprow[N + 4 * k + k * i + j] = __float2bfloat16_rn(rstd * dz_res);
+  for (int q = P + e; q < 64; q += 16) dprow[q] = __float2bfloat16_rn(0.0f);
+  const int rl = 1 + N + 4 * k;
+  float* rc = rec + t * rl;
+  if (e == 0) rc[0] = -part * rstd * rstd / (float)((size_t)N * p.C);
+  if (e < N) rc[1 + e] = hpre;
+}
+
+// ---------------------------------------------------------------- launchers
+
+cudaError_t launch_coef(const Params& p, const float* saved, float* coef, cudaStream_t st) {
+  const size_t T_all = (size_t)p.B * p.S;
+  timing_begin("coef", st);
+  coef_kernel<<<(unsigned)((T_all + 127) / 128), 128, 0, st>>>(p, saved, coef, T_all);
+  timing_end(st);
+  return cudaGetLastError();
+}
+
+bool stream_update_supported(const Params& p) { return p.C % 8 == 0; }
+
+cudaError_t launch_fwd_update(const Params& p, const UpdArgs<__nv_bfloat16>& a, const float* coef, bool has_conv,
+                              int sms, cudaStream_t st) {
+  const Walk wk = make_walk(p, sms);
+  dim3 grid(wk.R, wk.ncb);
+  const int smem = (int)sizeof(FwdSmem);
+  timing_begin("fwd_update", st);
+  if (has_conv) {
+    cudaFuncSetAttribute(fwd_update_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaFuncSetAttribute(fwd_update_kernel<true>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    fwd_update_kernel<true><<<grid, THREADS, smem, st>>>(p, a, coef, wk);
+  } else {
+    fwd_update_kernel<false><<<grid, THREADS, 0, st>>>(p, a, coef, wk);
+  }
+  timing_end(st);
+  return cudaGetLastError();
+}
+
+size_t bwd_col_pdot_floats(const Params& p) {
+  return (size_t)p.B * p.S * (size_t)((p.C + CB - 1) / CB) * PDOT;
+}
+size_t bwd_col_cpart_floats(const Params& p, int sms) {
+  return (size_t)make_walk(p, sms).R * NTAPS * (size_t)p.C;
+}
+int bwd_col_cpart_rows(const Params& p, int sms) { return make_walk(p, sms).R; }
+
+cudaError_t launch_bwd_col(const Params& p, const BwdArgs<__nv_bfloat16>& a, const float* coef, bool has_conv,
+                           float* pdot, float* cpart, int sms, cudaStream_t st) {
+  const Walk wk = make_walk(p, sms);
+  dim3 grid(wk.R, wk.ncb);
+  const int smem = (int)sizeof(ColSmem);
+  timing_begin("bwd_col", st);
+  if (has_conv) {
+    cudaFuncSetAttribute(bwd_col_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaFuncSetAttribute(bwd_col_kernel<true>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    bwd_col_kernel<true><<<grid, THREADS, smem, st>>>(p, a, coef, pdot, cpart, wk);
+  } else {
+    cudaFuncSetAttribute(bwd_col_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaFuncSetAttribute(bwd_col_kernel<false>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    bwd_col_kernel<false><<<grid, THREADS, smem, st>>>(p, a, coef, pdot, cpart, wk);
+  }
+  timing_end(st);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_dz(const Params& p, const float* saved, const float* pdot, bool has_dxin,
+                          __nv_bfloat16* dP, float* rec, cudaStream_t st) {
+  const size_t T_all = (size_t)p.B * p.S;
+  const int ncb = (p.C + CB - 1) / CB;
+  const size_t smem = (size_t)16 * std::max(p.iters, 1) * 32 * sizeof(float);
+  cudaFuncSetAttribute(bwd_dz_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  timing_begin("bwd_dz", st);
+  bwd_dz_kernel<<<(unsigned)((T_all + 15) / 16), 256, smem, st>>>(p, saved, pdot, ncb, has_dxin ? 1 : 0, dP, rec,
+                                                                   T_all);
+  timing_end(st);
+  return cudaGetLastError();
+}
+
+}  // namespace xhc

@@ -1,0 +1,29 @@
+// Bandwidth-bound CUDA-core passes for bf16 state (see xhc_stream.cu).
+#pragma once
+
+#include "xhc_kernels.cuh"
+
+namespace xhc {
+
+// Coefficient block [T, COEF_STRIDE] from saved logits [T, P + 1].
+cudaError_t launch_coef(const Params& p, const float* saved, float* coef, cudaStream_t st);
+
+// Forward update from a coefficient block: x_in, saved active rows, sparse write.
+bool stream_update_supported(const Params& p);
+cudaError_t launch_fwd_update(const Params& p, const UpdArgs<__nv_bfloat16>& a, const float* coef, bool has_conv,
+                              int sms, cudaStream_t st);
+
+// Backward column pass: active-stream mix into dX, dout, conv-weight partials
+// (rows of [24][C], one per CTA of a channel block) and coefficient dots.
+size_t bwd_col_pdot_floats(const Params& p);
+size_t bwd_col_cpart_floats(const Params& p, int sms);
+int bwd_col_cpart_rows(const Params& p, int sms);
+cudaError_t launch_bwd_col(const Params& p, const BwdArgs<__nv_bfloat16>& a, const float* coef, bool has_conv,
+                           float* pdot, float* cpart, int sms, cudaStream_t st);
+
+// Backward per-token reverse: dp (bf16, 64 per token) and records
+// [alpha | hpre (N) | unused (4k)].
+cudaError_t launch_bwd_dz(const Params& p, const float* saved, const float* pdot, bool has_dxin,
+                          __nv_bfloat16* dP, float* rec, cudaStream_t st);
+
+}  // namespace xhc

@@ -112,6 +112,7 @@ struct CoeffsOut {
   float* hpost;
   float* hres;
   float* saved;
+  float* coef;    // [T, COEF_STRIDE] coefficient block, or nullptr
 };
 
 __global__ void __launch_bounds__(coeffs::THREADS, 1)
@@ -278,49 +279,49 @@ __global__ void __launch_bounds__(coeffs::THREADS, 1)
           if (q < P) sv[q] = rstd * pz[q];
         sv[P] = rstd;
       }
+      float zl[PMAX];
+#pragma unroll
+      for (int q = 0; q < W_ROWS; ++q) zl[q] = rstd * pz[q];
       if (o.hpre) {
 #pragma unroll
         for (int q = 0; q < NMAX; ++q)
-          if (q < N) o.hpre[t * N + q] = sigmoidf_(rstd * pz[q]);
+          if (q < N) o.hpre[t * N + q] = sigmoidf_(zl[q]);
       }
       if (o.hpost) {
 #pragma unroll
         for (int q = 0; q < 4 * KMAX; ++q)
-          if (q < 4 * k) o.hpost[t * 4 * k + q] = sigmoidf_(rstd * pz[N + q]);
+          if (q < 4 * k) o.hpost[t * 4 * k + q] = sigmoidf_(zl[N + q]);
       }
-      if (o.hres) {
+      if (o.hres || o.coef) {
         // Sinkhorn of this token's k x k logits in registers (one thread)
         float M[KMAX][KMAX];
-        float zmax = -INFINITY;
+        sinkhorn_thread(zl + N + 4 * k, k, p.iters, M);
+        if (o.hres) {
 #pragma unroll
-        for (int i = 0; i < KMAX; ++i)
+          for (int i = 0; i < KMAX; ++i)
 #pragma unroll
-          for (int j = 0; j < KMAX; ++j)
-            if (i < k && j < k) zmax = fmaxf(zmax, rstd * pz[N + 4 * k + k * i + j]);
-#pragma unroll
-        for (int i = 0; i < KMAX; ++i)
-#pragma unroll
-          for (int j = 0; j < KMAX; ++j)
-            M[i][j] = (i < k && j < k) ? expf(rstd * pz[N + 4 * k + k * i + j] - zmax) : 0.0f;
-        for (int itr = 0; itr < p.iters; ++itr) {
-#pragma unroll
-          for (int i = 0; i < KMAX; ++i) {
-            const float s = (M[i][0] + M[i][1]) + (M[i][2] + M[i][3]);
-#pragma unroll
-            for (int j = 0; j < KMAX; ++j) M[i][j] = (i < k && j < k) ? M[i][j] / s : 0.0f;
-          }
-#pragma unroll
-          for (int j = 0; j < KMAX; ++j) {
-            const float s = (M[0][j] + M[2][j]) + (M[1][j] + M[3][j]);
-#pragma unroll
-            for (int i = 0; i < KMAX; ++i) M[i][j] = (i < k && j < k) ? M[i][j] / s : 0.0f;
-          }
+            for (int j = 0; j < KMAX; ++j)
+              if (i < k && j < k) o.hres[t * k * k + k * i + j] = M[i][j];
         }
+        if (o.coef) {
+          float4* cf = reinterpret_cast<float4*>(o.coef + t * COEF_STRIDE);
 #pragma unroll
-        for (int i = 0; i < KMAX; ++i)
+          for (int v = 0; v < 4; ++v) {
+            float h[4];
 #pragma unroll
-          for (int j = 0; j < KMAX; ++j)
-            if (i < k && j < k) o.hres[t * k * k + k * i + j] = M[i][j];
+            for (int e = 0; e < 4; ++e) h[e] = (4 * v + e < N) ? sigmoidf_(zl[4 * v + e]) : 0.0f;
+            cf[v] = make_float4(h[0], h[1], h[2], h[3]);
+          }
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            float h[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) h[e] = (4 * v + e < 4 * k) ? sigmoidf_(zl[N + 4 * v + e]) : 0.0f;
+            cf[4 + v] = make_float4(h[0], h[1], h[2], h[3]);
+          }
+#pragma unroll
+          for (int i = 0; i < KMAX; ++i) cf[8 + i] = make_float4(M[i][0], M[i][1], M[i][2], M[i][3]);
+        }
       }
     }
   }
@@ -334,7 +335,7 @@ __global__ void __launch_bounds__(coeffs::THREADS, 1)
 bool tc_coeffs_supported(const Params& p) { return p.C % coeffs::KC == 0 && p.P <= coeffs::W_ROWS; }
 
 cudaError_t launch_coeffs_tc(const Params& p, const void* X, const float* W, float* hpre, float* hpost,
-                             float* hres, float* saved, cudaStream_t st) {
+                             float* hres, float* saved, float* coef, cudaStream_t st) {
   using namespace coeffs;
   const size_t T_all = (size_t)p.B * p.S;
   const size_t NC = (size_t)p.N * p.C;
@@ -355,7 +356,7 @@ cudaError_t launch_coeffs_tc(const Params& p, const void* X, const float* W, flo
   const int ntiles = (int)((T_all + TILE_T - 1) / TILE_T);
   const int grid = std::min(ntiles, sm_count());
   cudaFuncSetAttribute(coeffs_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
-  CoeffsOut o{hpre, hpost, hres, saved};
+  CoeffsOut o{hpre, hpost, hres, saved, coef};
   timing_begin("coeffs_tc", st);
   coeffs_tc_kernel<<<grid, THREADS, SMEM, st>>>(mx, mw, p, o, ntiles);
   timing_end(st);
@@ -700,11 +701,6 @@ cudaError_t launch_bwd_stream_tc(const Params& p, const BwdArgs<__nv_bfloat16>& 
   bwd_stream_tc_kernel<<<grid, THREADS, SMEM, st>>>(m, p, a, ranges, range_len, wpart);
   timing_end(st);
   return cudaGetLastError();
-}
-
-bool tc_update_supported(const Params&) { return false; }
-cudaError_t launch_update_tc(const Params&, const UpdArgs<__nv_bfloat16>&, bool, cudaStream_t) {
-  return cudaErrorNotSupported;
 }
 
 bool tc_bwd_supported(const Params& p) { return p.C % bwdtc::CB == 0 && p.P <= 48; }

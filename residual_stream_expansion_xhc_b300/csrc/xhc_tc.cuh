@@ -6,16 +6,13 @@
 namespace xhc {
 
 bool tc_coeffs_supported(const Params& p);
-// Coefficients of every token (any of the outputs may be nullptr).  The dense
-// read x_in is not computed here.
+// Coefficients of every token (any of the outputs may be nullptr; `coef` is
+// the [T, COEF_STRIDE] block).  The dense read x_in is not computed here.
 cudaError_t launch_coeffs_tc(const Params& p, const void* X, const float* W, float* hpre, float* hpost, float* hres,
-                             float* saved, cudaStream_t st);
+                             float* saved, float* coef, cudaStream_t st);
 // Status recorded by bounded device-side waits (0: none); synchronises `st`
 // and clears the record.
 int read_device_error(cudaStream_t st);
-
-bool tc_update_supported(const Params& p);
-cudaError_t launch_update_tc(const Params& p, const UpdArgs<__nv_bfloat16>& a, bool has_conv, cudaStream_t st);
 
 // The bf16 backward built from the token pass, the TFA pass, the tensor-core
 // stream pass and the reduction (see xhc_bwd.cuh) serves these shapes.

@@ -60,6 +60,8 @@ WORKLOADS = {
     "fwdbwd_bf16": Workload("fwdbwd_bf16", 4, B=4, S=4096, N=16, C=2048, k=4, dtype="bf16", backward=True),
     "mhc_bf16": Workload("mhc_bf16", 5, B=4, S=4096, N=4, C=2048, k=4, dtype="bf16",
                          conv="none", identity_idx=True, backward=True),
+    # a quarter of the forward + backward workload (state 268 MB, above L2) for profiler captures
+    "quarter_bf16": Workload("quarter_bf16", 6, B=1, S=4096, N=16, C=2048, k=4, dtype="bf16", backward=True),
 }
 
 

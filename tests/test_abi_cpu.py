@@ -89,6 +89,21 @@ def test_null_and_alignment_rejected(lib):
     need = lib.LIB.xhc_fwd_workspace_bytes(ctypes.byref(sh))
     assert need >= 2 * 8 * 49 * 4
     assert fwd(lib, sh, idx(0, 1, 2, 3), ws=FAKE, ws_bytes=need - 1) == 5
+    # with the logits kept by the caller, the bf16 path still needs the coefficient block
+    assert fwd(lib, sh, idx(0, 1, 2, 3), saved=FAKE) == 5
+
+
+def test_forward_workspace_sizes(lib):
+    L = lib.LIB
+    sh = shape(lib, B=3, S=100)                       # bf16, 300 tokens, P = 48
+    up = lambda b: (b + 255) // 256 * 256             # noqa: E731
+    coef, z = up(300 * 48 * 4), up(300 * 49 * 4)
+    assert L.xhc_fwd_workspace_need(ctypes.byref(sh), 1) == coef
+    assert L.xhc_fwd_workspace_need(ctypes.byref(sh), 0) == coef + z
+    assert L.xhc_fwd_workspace_bytes(ctypes.byref(sh)) == coef + z
+    f32 = shape(lib, B=3, S=100, dtype=0)             # the fp32 path keeps no coefficient block
+    assert L.xhc_fwd_workspace_need(ctypes.byref(f32), 1) == 0
+    assert L.xhc_fwd_workspace_need(ctypes.byref(f32), 0) == z
 
 
 def test_empty_forward_launches_nothing(lib):

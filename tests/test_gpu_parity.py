@@ -45,7 +45,8 @@ def run_fwd(wl, t, inplace=True, want_x_in=True, want_saved=True, want_active=Tr
     x_in = torch.empty(wl.B, wl.S, wl.C, dtype=tdtype(wl), device="cuda") if want_x_in else None
     saved = torch.empty(wl.B, wl.S, wl.P + 1, dtype=torch.float32, device="cuda") if want_saved else None
     act = torch.empty(wl.B, wl.S, wl.k, wl.C, dtype=tdtype(wl), device="cuda") if want_active else None
-    ws = None if want_saved else api.workspace(api.xhc_fwd_workspace_bytes(sh))
+    need = api.xhc_fwd_workspace_need(sh, want_saved)
+    ws = api.workspace(need) if need else None
     Xo = X if inplace else torch.full_like(X, float("nan"))
     api.xhc_sublayer_fwd(sh, X, Xo, out, conv, W, t.idx, x_in=x_in, saved=saved, saved_active=act, workspace=ws)
     torch.cuda.synchronize()

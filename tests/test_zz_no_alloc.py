@@ -44,7 +44,7 @@ def _run(wl, t, use_noalloc):
     if use_noalloc:
         api.xhc_sublayer_fwd_noalloc(sh, X, X, out, conv, W, t.idx, x_in=x_in, saved=None, saved_active=act)
     else:
-        ws = api.workspace(api.xhc_fwd_workspace_bytes(sh))
+        ws = api.workspace(api.xhc_fwd_workspace_need(sh, False))
         api.xhc_sublayer_fwd(sh, X, X, out, conv, W, t.idx, x_in=x_in, saved=None, saved_active=act, workspace=ws)
     torch.cuda.synchronize()
     api.xhc_device_status()
@@ -64,14 +64,17 @@ def test_noalloc_matches_workspace_path_twice(wl):
 
 
 def test_noalloc_refuses_calls_beyond_its_scratch():
-    # 50,000 tokens x 49 logits x 4 bytes > 8 MiB: refused before any launch
-    sh = _lib.XhcShape(1, 50000, 16, 256, 4, _lib.XHC_BF16, 20, 1e-6)
+    # 30,000 bf16 tokens need 30,000 x (48 + 49) x 4 bytes > 8 MiB without
+    # `saved`: refused before any launch; with `saved` (48 x 4 bytes per
+    # token) they fit
+    sh = _lib.XhcShape(1, 30000, 16, 256, 4, _lib.XHC_BF16, 20, 1e-6)
+    assert api.xhc_fwd_workspace_need(sh, False) > 8 << 20 >= api.xhc_fwd_workspace_need(sh, True)
     idx = (ctypes.c_int32 * 4)(0, 1, 2, 3)
     fake = ctypes.c_void_p(1 << 20)
     st = _lib.LIB.xhc_sublayer_fwd_noalloc(ctypes.byref(sh), fake, fake, fake, None, None, None, fake, idx, None,
                                            None, None, None)
     assert st == 5                     # XHC_ERR_WORKSPACE
-    # the same call fits when the caller keeps the logits itself
+    # a call that keeps its logits runs
     wl = xin.Workload("noalloc_saved", 42, B=1, S=40, N=16, C=256, k=4, dtype="bf16")
     t = xin.make(wl)
     shp = api.make_shape(wl.B, wl.S, wl.N, wl.C, wl.k, torch.bfloat16)
