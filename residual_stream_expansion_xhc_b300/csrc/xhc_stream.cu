@@ -17,11 +17,10 @@
 // N streams, only the k active streams are rewritten.
 //
 // Layout of the work.  A CTA owns CB = 256 channels of the state (one channel
-// per thread in the channel phases) and walks token segments of one sequence
-// in chunks of TT = 8 tokens (one token per warp in the token phases, eight
-// channels = one 16-byte vector per lane).  The causal halo of `out` lives in
-// a ring of rows in shared memory, so every row of `out` is read from HBM
-// once per segment; the conv taps of the CTA's channels are read once per CTA.
+// per thread in the channel phases) and walks a contiguous range of chunks of
+// TT = 8 tokens (one token per warp in the token phases, eight channels = one
+// 16-byte vector per lane).  The causal halo of `out` lives in a ring of rows
+// in shared memory, so every row of `out` is read from HBM once per walk.
 #include <algorithm>
 
 #include "xhc_stream.cuh"
@@ -33,7 +32,6 @@ constexpr int CB = 256;        // channels per CTA
 constexpr int TT = 8;          // tokens per chunk
 constexpr int THREADS = 256;
 constexpr int ORING = 32;      // rows in the `out` ring (power of two)
-constexpr int SEG = 64;        // tokens per segment (one job)
 constexpr int PDOT = 48;       // floats per token and channel block of dots
 }  // namespace stream
 
@@ -74,16 +72,36 @@ __device__ __forceinline__ void load_taps(const float* const (&w)[3], int c, int
   for (int g = 0; g < NTAPS; ++g) tap[g] = v[g];
 }
 
-// Warp `warp` loads rows r_beg + warp, r_beg + warp + TT, ... < r_end of the
-// sequence's `out` (channels of this CTA) into the ring; rows outside [0, S)
-// are zero (the causal padding before the sequence start).
+// Ring refill split in two, so that the global load of the row is in flight
+// while the warp issues its other loads: warp `warp` fetches row r_beg + warp
+// (r_beg + TT rows per chunk, one row per warp) into a register, and commits it
+// to the ring later.
+__device__ __forceinline__ uint4 fetch_out_row(const __nv_bfloat16* __restrict__ out, size_t seq_base, int S, int C,
+                                               int c_lane, int r) {
+  uint4 v = make_uint4(0, 0, 0, 0);
+  if (r >= 0 && r < S && c_lane < C) v = *reinterpret_cast<const uint4*>(out + (seq_base + r) * C + c_lane);
+  return v;
+}
+__device__ __forceinline__ void commit_out_row(uint16_t (*ring)[CB], int r, int lane, const uint4& v) {
+  *reinterpret_cast<uint4*>(&ring[r & (ORING - 1)][8 * lane]) = v;
+}
+
+// Rows r_beg .. r_end - 1 (at most 3 TT) of the sequence's `out` into the ring:
+// warp w takes rows r_beg + w, r_beg + w + TT, ...; all its loads are issued
+// before the first store.  Rows outside [0, S) are zero (the causal padding).
 __device__ __forceinline__ void load_out_rows(uint16_t (*ring)[CB], const __nv_bfloat16* __restrict__ out,
                                               size_t seq_base, int S, int C, int c_lane, int r_beg, int r_end,
                                               int warp, int lane) {
-  for (int r = r_beg + warp; r < r_end; r += TT) {
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (r >= 0 && r < S && c_lane < C) v = *reinterpret_cast<const uint4*>(out + (seq_base + r) * C + c_lane);
-    *reinterpret_cast<uint4*>(&ring[r & (ORING - 1)][8 * lane]) = v;
+  uint4 v[3];
+#pragma unroll
+  for (int q = 0; q < 3; ++q) {
+    const int r = r_beg + warp + q * TT;
+    v[q] = r < r_end ? fetch_out_row(out, seq_base, S, C, c_lane, r) : make_uint4(0, 0, 0, 0);
+  }
+#pragma unroll
+  for (int q = 0; q < 3; ++q) {
+    const int r = r_beg + warp + q * TT;
+    if (r < r_end) commit_out_row(ring, r, lane, v[q]);
   }
 }
 
@@ -103,19 +121,27 @@ __device__ __forceinline__ float warp_transpose_sum32(float (&v)[32], int lane) 
   return v[0];
 }
 
+// Work split: the chunks of every sequence, numbered g = b * nch + m (chunk m
+// of sequence b), are cut into R contiguous ranges of `per` chunks; CTA
+// (r, channel block) walks range r chunk by chunk (the forward upwards, the
+// backward downwards), carrying the `out` and du rings from one chunk to the
+// next, and restarts only where its range starts or a sequence ends.
 struct Walk {
-  int nseg;       // segments per sequence
-  int R;          // CTAs per channel block (grid.x)
+  int nch;        // chunks per sequence
   int ncb;        // channel blocks (grid.y)
+  int R;          // ranges = CTAs per channel block (grid.x)
+  long per;       // chunks per range
 };
 
 Walk make_walk(const Params& p, int sms) {
   Walk w;
-  w.nseg = (p.S + SEG - 1) / SEG;
+  w.nch = (p.S + TT - 1) / TT;
   w.ncb = (p.C + CB - 1) / CB;
-  const long jobs = (long)p.B * w.nseg;
+  const long total = std::max(1L, (long)p.B * w.nch);
   const long slots = std::max(1L, (long)(2 * sms) / w.ncb);
-  w.R = (int)std::max(1L, std::min(jobs, slots));
+  const long R = std::min(total, slots);
+  w.per = (total + R - 1) / R;
+  w.R = (int)((total + w.per - 1) / w.per);   // no empty range
   return w;
 }
 
@@ -216,7 +242,9 @@ __global__ void __launch_bounds__(THREADS, 2) fwd_update_kernel(Params p, UpdArg
   const bool lane_ok = c_lane < C;
   if (HAS_CONV) stage_taps(sm.tap, a.w, cb0 + ch, C, ch);
   const bool need_all = a.x_in != nullptr || a.copy_inactive;
-  const int jobs = p.B * wk.nseg;
+  const long g_beg = (long)blockIdx.x * wk.per;
+  const long g_total = (long)p.B * wk.nch;
+  const long g_end = g_beg + wk.per < g_total ? g_beg + wk.per : g_total;
 
   auto channel_phase = [&](int t0, int s_end) {
     float tap[NTAPS];
@@ -225,23 +253,27 @@ __global__ void __launch_bounds__(THREADS, 2) fwd_update_kernel(Params p, UpdArg
     tfa_chunk_s<float>(sm.ring, sm.u, tap, t0, s_end, ch);
   };
 
-  for (int job = blockIdx.x; job < jobs; job += gridDim.x) {
-    const int b = job / wk.nseg;
-    const int s_beg = (job % wk.nseg) * SEG;
-    const int s_end = min(s_beg + SEG, S);
+  bool start = true;
+  for (long g = g_beg; g < g_end; ++g) {
+    const int b = (int)(g / wk.nch), m = (int)(g % wk.nch);
+    const int t0 = m * TT;
+    const int s_end = min(t0 + TT, S);         // tokens of this chunk: t0 .. s_end - 1
     const size_t seq_base = (size_t)b * S;
-    const int nchunks = (s_end - s_beg + TT - 1) / TT;
-    __syncthreads();                           // previous job is done with the ring; taps staged
-    if (HAS_CONV) {
-      load_out_rows(sm.ring, a.out, seq_base, S, C, c_lane, s_beg - HALO, s_beg + TT, warp, lane);
-      __syncthreads();
-      channel_phase(s_beg, s_end);
-      __syncthreads();
+    const bool has_next = g + 1 < g_end && m + 1 < wk.nch;
+    if (start) {
+      __syncthreads();                         // the previous walk is done with the ring; taps staged
+      if (HAS_CONV) {
+        load_out_rows(sm.ring, a.out, seq_base, S, C, c_lane, t0 - HALO, t0 + TT, warp, lane);
+        __syncthreads();
+        channel_phase(t0, s_end);
+        __syncthreads();
+      }
     }
-    for (int m = 0; m < nchunks; ++m) {
-      const int t0 = s_beg + m * TT;
-      if (HAS_CONV && m + 1 < nchunks)
-        load_out_rows(sm.ring, a.out, seq_base, S, C, c_lane, t0 + TT, t0 + 2 * TT, warp, lane);
+    start = !has_next;
+    {
+      const bool refill = HAS_CONV && has_next;
+      uint4 next_row;
+      if (refill) next_row = fetch_out_row(a.out, seq_base, S, C, c_lane, t0 + TT + warp);
       const int t = t0 + warp;
       if (t < s_end && lane_ok) {
         const size_t tok = seq_base + t;
@@ -341,11 +373,12 @@ __global__ void __launch_bounds__(THREADS, 2) fwd_update_kernel(Params p, UpdArg
           st_stream(yrow + (size_t)p.idx[i] * C, pack8(y));
         }
       }
-      if (HAS_CONV) {
-        __syncthreads();                       // u of this chunk consumed; next rows in the ring
-        if (m + 1 < nchunks) channel_phase(t0 + TT, s_end);
-        __syncthreads();
-      }
+      if (refill) commit_out_row(sm.ring, t0 + TT + warp, lane, next_row);
+    }
+    if (HAS_CONV) {
+      __syncthreads();                         // u of this chunk consumed; next rows in the ring
+      if (has_next) channel_phase(t0 + TT, min(t0 + 2 * TT, S));
+      __syncthreads();
     }
   }
 }
@@ -360,10 +393,11 @@ __global__ void __launch_bounds__(THREADS, 2) fwd_update_kernel(Params p, UpdArg
 //     dots  <G_i, Xa_j>, <G_i, u_c> (and <dx_in, X_n> with dx_in), reduced over
 //           the CTA's channels -> pdot[t][channel block]
 //     (and loads the `out` rows the next chunk's channel phase needs)
-//   channel phase (thread = channel)
+//   channel phase (thread = channel; tokens t and t + 4 of the chunk paired in
+//   float2 lanes)
+//     u_1..u_3 of the next (earlier) chunk
 //     dout[t] = du_0[t] + sum_j sum_tau w_j[tau] du_j[t + tau]   (inside the sequence)
 //     dw_j[tau] += du_j[t] out[t - tau]
-//     u_1..u_3 of the next (earlier) chunk
 // The du rows of the tokens after a segment that its convolutions reach (3, 7
 // and 11 for K = 4, 8, 12) are computed first: the anti-causal halo.  Each
 // du_j ring holds K_j - 1 + TT rows or more.  Conv-weight partials: one row
@@ -381,9 +415,41 @@ struct ColSmem {
   float dw[NTAPS][CB];               // conv-weight gradient of the CTA's channels
 };
 
-__device__ __forceinline__ void store8f(float* d, const float (&v)[8]) {
-  *reinterpret_cast<float4*>(d) = make_float4(v[0], v[1], v[2], v[3]);
-  *reinterpret_cast<float4*>(d + 4) = make_float4(v[4], v[5], v[6], v[7]);
+__device__ __forceinline__ void store8f(float* d, const float2 (&v)[4]) {
+  *reinterpret_cast<float4*>(d) = make_float4(v[0].x, v[0].y, v[1].x, v[1].y);
+  *reinterpret_cast<float4*>(d + 4) = make_float4(v[2].x, v[2].y, v[3].x, v[3].y);
+}
+__device__ __forceinline__ void unpack8x2(const uint4& a, float2 (&v)[4]) {
+  v[0] = make_float2(bf_lo(a.x), bf_hi(a.x));
+  v[1] = make_float2(bf_lo(a.y), bf_hi(a.y));
+  v[2] = make_float2(bf_lo(a.z), bf_hi(a.z));
+  v[3] = make_float2(bf_lo(a.w), bf_hi(a.w));
+}
+__device__ __forceinline__ uint4 pack8x2(const float2 (&v)[4]) {
+  return make_uint4(pack_bf2(v[0].x, v[0].y), pack_bf2(v[1].x, v[1].y), pack_bf2(v[2].x, v[2].y),
+                    pack_bf2(v[3].x, v[3].y));
+}
+// Streaming read that does not allocate in L1 (L1 keeps the conv taps).
+__device__ __forceinline__ uint4 ld_na(const __nv_bfloat16* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+__device__ __forceinline__ float2 f2(float a) { return make_float2(a, a); }
+// dot of two 8-vectors held as float2 pairs
+__device__ __forceinline__ float dot8(const float2 (&a)[4], const float2 (&b)[4]) {
+  float2 s = __fmul2_rn(a[0], b[0]);
+  s = __ffma2_rn(a[1], b[1], s);
+  s = __ffma2_rn(a[2], b[2], s);
+  s = __ffma2_rn(a[3], b[3], s);
+  return s.x + s.y;
+}
+// ring slot of row base + i for a ring of R rows, base in [0, R), 0 <= i < R
+__device__ __forceinline__ int wrap(int base, int i, int R) {
+  const int r = base + i;
+  return r >= R ? r - R : r;
 }
 
 template <bool HAS_CONV>
@@ -403,31 +469,57 @@ __global__ void __launch_bounds__(THREADS, 2) bwd_col_kernel(Params p, BwdArgs<_
 #pragma unroll
     for (int g = 0; g < NTAPS; ++g) sm.dw[g][ch] = 0.0f;
   }
-  const int jobs = p.B * wk.nseg;
   const int ncb = wk.ncb;
 
-  auto taps = [&](float (&tap)[NTAPS]) { load_taps(a.w, c_ch, C, tap); };
+  // u_1..u_3 of the chunk t0 .. t0+7 (tokens < s_end) from ring rows t0-11 .. t0+7
+  auto tfa_pairs = [&](const float (&tap)[NTAPS], int t0, int s_end) {
+    float2 Q[TT / 2 + HALO];                   // (row t0-11+i, row t0-7+i)
+#pragma unroll
+    for (int i = 0; i < TT / 2 + HALO; ++i)
+      Q[i] = make_float2(bf16_bits(sm.ring[(t0 - HALO + i) & (ORING - 1)][ch]),
+                         bf16_bits(sm.ring[(t0 - HALO + 4 + i) & (ORING - 1)][ch]));
+#pragma unroll
+    for (int tt = 0; tt < TT / 2; ++tt) {
+      float2 u1 = make_float2(0.0f, 0.0f), u2 = u1, u3 = u1;
+#pragma unroll
+      for (int tau = 0; tau < 4; ++tau) u1 = __ffma2_rn(f2(tap[tau]), Q[tt + HALO - tau], u1);
+#pragma unroll
+      for (int tau = 0; tau < 8; ++tau) u2 = __ffma2_rn(f2(tap[4 + tau]), Q[tt + HALO - tau], u2);
+#pragma unroll
+      for (int tau = 0; tau < 12; ++tau) u3 = __ffma2_rn(f2(tap[12 + tau]), Q[tt + HALO - tau], u3);
+      if (t0 + tt < s_end) {
+        sm.u[0][tt][ch] = __bfloat16_as_ushort(__float2bfloat16_rn(u1.x));
+        sm.u[1][tt][ch] = __bfloat16_as_ushort(__float2bfloat16_rn(u2.x));
+        sm.u[2][tt][ch] = __bfloat16_as_ushort(__float2bfloat16_rn(u3.x));
+      }
+      if (t0 + tt + 4 < s_end) {
+        sm.u[0][tt + 4][ch] = __bfloat16_as_ushort(__float2bfloat16_rn(u1.y));
+        sm.u[1][tt + 4][ch] = __bfloat16_as_ushort(__float2bfloat16_rn(u2.y));
+        sm.u[2][tt + 4][ch] = __bfloat16_as_ushort(__float2bfloat16_rn(u3.y));
+      }
+    }
+  };
 
   // du_1..du_3 of a halo token t (lane's channels): rows the convolutions reach
   auto du_halo = [&](size_t seq_base, int t, int s_end) {
     const size_t tok = seq_base + t;
     const float* cf = coef + tok * COEF_STRIDE;
-    float du[3][8];
+    float2 du[3][4];
 #pragma unroll
     for (int c = 0; c < 3; ++c)
 #pragma unroll
-      for (int x = 0; x < 8; ++x) du[c][x] = 0.0f;
+      for (int q = 0; q < 4; ++q) du[c][q] = make_float2(0.0f, 0.0f);
 #pragma unroll
     for (int i = 0; i < KMAX; ++i) {
       if (i < k) {
-        float g[8];
-        unpack8(ld_stream(a.dXp + tok * NC + (size_t)p.idx[i] * C + c_lane), g);
+        float2 g[4];
+        unpack8x2(ld_na(a.dXp + tok * NC + (size_t)p.idx[i] * C + c_lane), g);
         const float4 hp = *reinterpret_cast<const float4*>(cf + COEF_POST + 4 * i);
 #pragma unroll
-        for (int x = 0; x < 8; ++x) {
-          du[0][x] = fmaf(hp.y, g[x], du[0][x]);
-          du[1][x] = fmaf(hp.z, g[x], du[1][x]);
-          du[2][x] = fmaf(hp.w, g[x], du[2][x]);
+        for (int q = 0; q < 4; ++q) {
+          du[0][q] = __ffma2_rn(f2(hp.y), g[q], du[0][q]);
+          du[1][q] = __ffma2_rn(f2(hp.z), g[q], du[1][q]);
+          du[2][q] = __ffma2_rn(f2(hp.w), g[q], du[2][q]);
         }
       }
     }
@@ -437,88 +529,103 @@ __global__ void __launch_bounds__(THREADS, 2) bwd_col_kernel(Params p, BwdArgs<_
     store8f(&sm.du3[t % DR3][8 * lane], du[2]);
   };
 
-  for (int job = blockIdx.x; job < jobs; job += gridDim.x) {
-    const int b = job / wk.nseg;
-    const int s_beg = (job % wk.nseg) * SEG;
-    const int s_end = min(s_beg + SEG, S);
+  const long g_beg = (long)blockIdx.x * wk.per;
+  const long g_total = (long)p.B * wk.nch;
+  const long g_end = g_beg + wk.per < g_total ? g_beg + wk.per : g_total;
+  bool start = true;
+  for (long g = g_end - 1; g >= g_beg; --g) {
+    const int b = (int)(g / wk.nch), m = (int)(g % wk.nch);
+    const int t0 = m * TT;
+    const int s_end = min(t0 + TT, S);         // tokens of this chunk: t0 .. s_end - 1
     const size_t seq_base = (size_t)b * S;
-    const int nchunks = (s_end - s_beg + TT - 1) / TT;
-    const int t_top = s_beg + (nchunks - 1) * TT;
-    __syncthreads();                           // previous job is done with shared memory
-    if (HAS_CONV) {
-      // out rows of the top chunk and the du rows of the halo after the segment
-      load_out_rows(sm.ring, a.out, seq_base, S, C, c_lane, t_top - HALO, t_top + TT, warp, lane);
-      if (lane_ok) {
-        for (int t = s_end + warp; t < min(s_end + HALO, S); t += TT) du_halo(seq_base, t, s_end);
+    const bool has_next = g - 1 >= g_beg && m > 0;    // the next chunk walked is t0 - TT, same sequence
+    if (start) {
+      __syncthreads();                         // the previous walk is done with shared memory
+      if (HAS_CONV) {
+        // out rows of this chunk and the du rows of the tokens above it that
+        // its convolutions reach
+        load_out_rows(sm.ring, a.out, seq_base, S, C, c_lane, t0 - HALO, t0 + TT, warp, lane);
+        if (lane_ok) {
+          for (int t = s_end + warp; t < min(s_end + HALO, S); t += TT) du_halo(seq_base, t, s_end);
+        }
+        __syncthreads();
+        if (c_ch < C) {
+          float tap[NTAPS];
+          load_taps(a.w, c_ch, C, tap);
+          tfa_pairs(tap, t0, s_end);
+        }
+        __syncthreads();
       }
-      __syncthreads();
-      if (c_ch < C) {
-        float tap[NTAPS];
-        taps(tap);
-        tfa_chunk_s<uint16_t>(sm.ring, sm.u, tap, t_top, s_end, ch);
-      }
-      __syncthreads();
     }
-    for (int m = nchunks - 1; m >= 0; --m) {
-      const int t0 = s_beg + m * TT;
+    start = !has_next;
+    {
       // ------------------------------------------------ token phase
-      if (HAS_CONV && m > 0)
-        load_out_rows(sm.ring, a.out, seq_base, S, C, c_lane, t0 - TT - HALO, t0 - HALO, warp, lane);
+      const bool refill = HAS_CONV && has_next;
+      uint4 next_row;
+      if (refill) next_row = fetch_out_row(a.out, seq_base, S, C, c_lane, t0 - TT - HALO + warp);
       const int t = t0 + warp;
       if (t < s_end) {                         // warp-uniform
         const size_t tok = seq_base + t;
         const float* cf = coef + tok * COEF_STRIDE;
-        uint4 gr[KMAX], xr[KMAX];
+        float2 G[KMAX][4];
+        uint4 xr[KMAX];
 #pragma unroll
-        for (int i = 0; i < KMAX; ++i) gr[i] = xr[i] = make_uint4(0, 0, 0, 0);
+        for (int i = 0; i < KMAX; ++i) {
+          xr[i] = make_uint4(0, 0, 0, 0);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) G[i][q] = make_float2(0.0f, 0.0f);
+        }
         if (lane_ok) {
+          uint4 gr[KMAX];
 #pragma unroll
           for (int i = 0; i < KMAX; ++i) {
             if (i < k) {
-              gr[i] = ld_stream(a.dXp + tok * NC + (size_t)p.idx[i] * C + c_lane);
-              xr[i] = a.saved_active ? ld_stream(a.saved_active + (tok * k + i) * C + c_lane)
-                                     : ld_stream(a.X + tok * NC + (size_t)p.idx[i] * C + c_lane);
+              gr[i] = ld_na(a.dXp + tok * NC + (size_t)p.idx[i] * C + c_lane);
+              xr[i] = a.saved_active ? ld_na(a.saved_active + (tok * k + i) * C + c_lane)
+                                     : ld_na(a.X + tok * NC + (size_t)p.idx[i] * C + c_lane);
             }
           }
+#pragma unroll
+          for (int i = 0; i < KMAX; ++i)
+            if (i < k) unpack8x2(gr[i], G[i]);
           // active-stream mix: dX[a_j] = sum_i Hres[i][j] G_i
+          float hres[KMAX][KMAX];
+#pragma unroll
+          for (int i = 0; i < KMAX; ++i) {
+            const float4 h = *reinterpret_cast<const float4*>(cf + COEF_RES + 4 * i);
+            hres[i][0] = h.x; hres[i][1] = h.y; hres[i][2] = h.z; hres[i][3] = h.w;
+          }
 #pragma unroll
           for (int j = 0; j < KMAX; ++j) {
             if (j < k) {
-              float mx[8];
+              float2 mx[4];
 #pragma unroll
-              for (int x = 0; x < 8; ++x) mx[x] = 0.0f;
+              for (int q = 0; q < 4; ++q) mx[q] = make_float2(0.0f, 0.0f);
 #pragma unroll
-              for (int i = 0; i < KMAX; ++i) {
-                if (i < k) {
-                  const float h = cf[COEF_RES + 4 * i + j];
-                  float g[8];
-                  unpack8(gr[i], g);
+              for (int i = 0; i < KMAX; ++i)
+                if (i < k)
 #pragma unroll
-                  for (int x = 0; x < 8; ++x) mx[x] = fmaf(h, g[x], mx[x]);
-                }
-              }
-              st_stream(a.dX + tok * NC + (size_t)p.idx[j] * C + c_lane, pack8(mx));
+                  for (int q = 0; q < 4; ++q) mx[q] = __ffma2_rn(f2(hres[i][j]), G[i][q], mx[q]);
+              st_stream(a.dX + tok * NC + (size_t)p.idx[j] * C + c_lane, pack8x2(mx));
             }
           }
           // du_c = sum_i hpost[i][c] G_i
           {
-            float du[4][8];
+            float2 du[4][4];
 #pragma unroll
             for (int c = 0; c < 4; ++c)
 #pragma unroll
-              for (int x = 0; x < 8; ++x) du[c][x] = 0.0f;
+              for (int q = 0; q < 4; ++q) du[c][q] = make_float2(0.0f, 0.0f);
 #pragma unroll
             for (int i = 0; i < KMAX; ++i) {
               if (i < k) {
                 const float4 hp = *reinterpret_cast<const float4*>(cf + COEF_POST + 4 * i);
-                float g[8];
-                unpack8(gr[i], g);
 #pragma unroll
-                for (int x = 0; x < 8; ++x) {
-                  du[0][x] = fmaf(hp.x, g[x], du[0][x]);
-                  du[1][x] = fmaf(hp.y, g[x], du[1][x]);
-                  du[2][x] = fmaf(hp.z, g[x], du[2][x]);
-                  du[3][x] = fmaf(hp.w, g[x], du[3][x]);
+                for (int q = 0; q < 4; ++q) {
+                  du[0][q] = __ffma2_rn(f2(hp.x), G[i][q], du[0][q]);
+                  du[1][q] = __ffma2_rn(f2(hp.y), G[i][q], du[1][q]);
+                  du[2][q] = __ffma2_rn(f2(hp.z), G[i][q], du[2][q]);
+                  du[3][q] = __ffma2_rn(f2(hp.w), G[i][q], du[3][q]);
                 }
               }
             }
@@ -528,7 +635,7 @@ __global__ void __launch_bounds__(THREADS, 2) bwd_col_kernel(Params p, BwdArgs<_
               store8f(&sm.du2[t % DR2][8 * lane], du[2]);
               store8f(&sm.du3[t % DR3][8 * lane], du[3]);
             } else {
-              st_stream(a.dout + tok * C + c_lane, pack8(du[0]));
+              st_stream(a.dout + tok * C + c_lane, pack8x2(du[0]));
             }
           }
         }
@@ -540,43 +647,26 @@ __global__ void __launch_bounds__(THREADS, 2) bwd_col_kernel(Params p, BwdArgs<_
 #pragma unroll
           for (int j = 0; j < KMAX; ++j) {
             if (j < k) {
-              float xv[8];
-              unpack8(xr[j], xv);
+              float2 xv[4];
+              unpack8x2(xr[j], xv);
 #pragma unroll
-              for (int i = 0; i < KMAX; ++i) {
-                if (i < k) {
-                  float g[8];
-                  unpack8(gr[i], g);
-                  float d = 0.0f;
-#pragma unroll
-                  for (int x = 0; x < 8; ++x) d = fmaf(g[x], xv[x], d);
-                  v[4 * i + j] = d;
-                }
-              }
+              for (int i = 0; i < KMAX; ++i)
+                if (i < k) v[4 * i + j] = dot8(G[i], xv);
             }
           }
 #pragma unroll
           for (int c = 0; c < 4; ++c) {
-            float uv[8];
+            if (!HAS_CONV && c > 0) break;
+            float2 uv[4];
             if (c == 0) {
-              if (HAS_CONV) unpack8(*reinterpret_cast<const uint4*>(&sm.ring[t & (ORING - 1)][8 * lane]), uv);
-              else unpack8(*reinterpret_cast<const uint4*>(a.out + tok * C + c_lane), uv);
-            } else if (HAS_CONV) {
-              unpack8(*reinterpret_cast<const uint4*>(&sm.u[c - 1][warp][8 * lane]), uv);
+              if (HAS_CONV) unpack8x2(*reinterpret_cast<const uint4*>(&sm.ring[t & (ORING - 1)][8 * lane]), uv);
+              else unpack8x2(ld_na(a.out + tok * C + c_lane), uv);
             } else {
-              break;
+              unpack8x2(*reinterpret_cast<const uint4*>(&sm.u[c - 1][warp][8 * lane]), uv);
             }
 #pragma unroll
-            for (int i = 0; i < KMAX; ++i) {
-              if (i < k) {
-                float g[8];
-                unpack8(gr[i], g);
-                float d = 0.0f;
-#pragma unroll
-                for (int x = 0; x < 8; ++x) d = fmaf(g[x], uv[x], d);
-                v[16 + 4 * i + c] = d;
-              }
-            }
+            for (int i = 0; i < KMAX; ++i)
+              if (i < k) v[16 + 4 * i + c] = dot8(G[i], uv);
           }
         }
         // sum over the CTA's channels (all lanes take part)
@@ -587,24 +677,18 @@ __global__ void __launch_bounds__(THREADS, 2) bwd_col_kernel(Params p, BwdArgs<_
 #pragma unroll
           for (int q = 0; q < 32; ++q) v[q] = 0.0f;
           if (lane_ok) {
-            float g[8];
-            unpack8(ld_stream(a.dx_in + tok * C + c_lane), g);
+            float2 g[4];
+            unpack8x2(ld_na(a.dx_in + tok * C + c_lane), g);
 #pragma unroll
             for (int n = 0; n < NMAX; ++n) {
               if (n < N) {
                 const int slot = p.is_active[n];
-                float xv[8];
-                if (slot) {
-                  const __nv_bfloat16* src = a.saved_active ? a.saved_active + (tok * k + slot - 1) * C + c_lane
-                                                            : a.X + tok * NC + (size_t)n * C + c_lane;
-                  unpack8(*reinterpret_cast<const uint4*>(src), xv);
-                } else {
-                  unpack8(ld_stream(a.X + tok * NC + (size_t)n * C + c_lane), xv);
-                }
-                float d = 0.0f;
-#pragma unroll
-                for (int x = 0; x < 8; ++x) d = fmaf(g[x], xv[x], d);
-                v[n] = d;
+                const __nv_bfloat16* src = slot ? (a.saved_active ? a.saved_active + (tok * k + slot - 1) * C + c_lane
+                                                                  : a.X + tok * NC + (size_t)n * C + c_lane)
+                                                : a.X + tok * NC + (size_t)n * C + c_lane;
+                float2 xv[4];
+                unpack8x2(ld_na(src), xv);
+                v[n] = dot8(g, xv);
               }
             }
           }
@@ -613,53 +697,62 @@ __global__ void __launch_bounds__(THREADS, 2) bwd_col_kernel(Params p, BwdArgs<_
         }
       }
       if (!HAS_CONV) continue;
+      if (refill) commit_out_row(sm.ring, t0 - TT - HALO + warp, lane, next_row);
+      float tap[NTAPS];
+      load_taps(a.w, c_ch, C, tap);            // in flight across the barrier
       __syncthreads();
       // ------------------------------------------------ channel phase
       if (c_ch < C) {
-        float tap[NTAPS];
-        taps(tap);
-        // dout of the chunk tokens: du rows t0 .. t0 + 18 (zero past the sequence end)
-        float d1[TT + 3], d2[TT + 7], d3[TT + 11];
+        if (has_next) tfa_pairs(tap, t0 - TT, t0);
+        // dout of the chunk tokens: pairs of du rows (t0 + i, t0 + 4 + i), zero past the sequence end
+        const int b1 = t0 % DR1, b2 = t0 % DR2, b3 = t0 % DR3;
+        float2 P1[TT / 2 + 3], P2[TT / 2 + 7], P3[TT / 2 + 11];
 #pragma unroll
-        for (int i = 0; i < TT + 11; ++i) {
-          const int tr = t0 + i;
-          const bool in = tr < S;
-          if (i < TT + 3) d1[i] = in ? sm.du1[tr % DR1][ch] : 0.0f;
-          if (i < TT + 7) d2[i] = in ? sm.du2[tr % DR2][ch] : 0.0f;
-          d3[i] = in ? sm.du3[tr % DR3][ch] : 0.0f;
+        for (int i = 0; i < TT / 2 + 11; ++i) {
+          const bool in0 = t0 + i < S, in1 = t0 + 4 + i < S;
+          if (i < TT / 2 + 3)
+            P1[i] = make_float2(in0 ? sm.du1[wrap(b1, i, DR1)][ch] : 0.0f, in1 ? sm.du1[wrap(b1, i + 4, DR1)][ch] : 0.0f);
+          if (i < TT / 2 + 7)
+            P2[i] = make_float2(in0 ? sm.du2[wrap(b2, i, DR2)][ch] : 0.0f, in1 ? sm.du2[wrap(b2, i + 4, DR2)][ch] : 0.0f);
+          P3[i] = make_float2(in0 ? sm.du3[wrap(b3, i, DR3)][ch] : 0.0f, in1 ? sm.du3[wrap(b3, i + 4, DR3)][ch] : 0.0f);
         }
 #pragma unroll
-        for (int tt = 0; tt < TT; ++tt) {
-          if (t0 + tt >= s_end) break;
-          float d = sm.du0[tt][ch];
+        for (int tt = 0; tt < TT / 2; ++tt) {
+          float2 d = make_float2(sm.du0[tt][ch], sm.du0[tt + 4][ch]);
 #pragma unroll
-          for (int tau = 0; tau < 4; ++tau) d = fmaf(tap[tau], d1[tt + tau], d);
+          for (int tau = 0; tau < 4; ++tau) d = __ffma2_rn(f2(tap[tau]), P1[tt + tau], d);
 #pragma unroll
-          for (int tau = 0; tau < 8; ++tau) d = fmaf(tap[4 + tau], d2[tt + tau], d);
+          for (int tau = 0; tau < 8; ++tau) d = __ffma2_rn(f2(tap[4 + tau]), P2[tt + tau], d);
 #pragma unroll
-          for (int tau = 0; tau < 12; ++tau) d = fmaf(tap[12 + tau], d3[tt + tau], d);
-          a.dout[(seq_base + t0 + tt) * C + c_ch] = __float2bfloat16_rn(d);
+          for (int tau = 0; tau < 12; ++tau) d = __ffma2_rn(f2(tap[12 + tau]), P3[tt + tau], d);
+          if (t0 + tt < s_end) a.dout[(seq_base + t0 + tt) * C + c_ch] = __float2bfloat16_rn(d.x);
+          if (t0 + tt + 4 < s_end) a.dout[(seq_base + t0 + tt + 4) * C + c_ch] = __float2bfloat16_rn(d.y);
         }
-        // dw_j[tau] += du_j[t] out[t - tau] over the chunk tokens
-        float ow[TT + HALO];
+        // dw_j[tau] += du_j[t] out[t - tau] over the chunk tokens (tokens >= s_end masked)
+        float2 O[TT / 2 + HALO];               // (row t0-11+i, row t0-7+i)
 #pragma unroll
-        for (int i = 0; i < TT + HALO; ++i) ow[i] = bf16_bits(sm.ring[(t0 - HALO + i) & (ORING - 1)][ch]);
-        float dwl[NTAPS];
+        for (int i = 0; i < TT / 2 + HALO; ++i)
+          O[i] = make_float2(bf16_bits(sm.ring[(t0 - HALO + i) & (ORING - 1)][ch]),
+                             bf16_bits(sm.ring[(t0 - HALO + 4 + i) & (ORING - 1)][ch]));
+        float2 E1[TT / 2], E2[TT / 2], E3[TT / 2];
 #pragma unroll
-        for (int g = 0; g < NTAPS; ++g) dwl[g] = 0.0f;
-#pragma unroll
-        for (int tt = 0; tt < TT; ++tt) {
-          if (t0 + tt >= s_end) break;
-#pragma unroll
-          for (int tau = 0; tau < 4; ++tau) dwl[tau] = fmaf(d1[tt], ow[tt + HALO - tau], dwl[tau]);
-#pragma unroll
-          for (int tau = 0; tau < 8; ++tau) dwl[4 + tau] = fmaf(d2[tt], ow[tt + HALO - tau], dwl[4 + tau]);
-#pragma unroll
-          for (int tau = 0; tau < 12; ++tau) dwl[12 + tau] = fmaf(d3[tt], ow[tt + HALO - tau], dwl[12 + tau]);
+        for (int tt = 0; tt < TT / 2; ++tt) {
+          const bool v0 = t0 + tt < s_end, v1 = t0 + tt + 4 < s_end;
+          E1[tt] = make_float2(v0 ? P1[tt].x : 0.0f, v1 ? P1[tt].y : 0.0f);
+          E2[tt] = make_float2(v0 ? P2[tt].x : 0.0f, v1 ? P2[tt].y : 0.0f);
+          E3[tt] = make_float2(v0 ? P3[tt].x : 0.0f, v1 ? P3[tt].y : 0.0f);
         }
 #pragma unroll
-        for (int g = 0; g < NTAPS; ++g) sm.dw[g][ch] += dwl[g];
-        if (m > 0) tfa_chunk_s<uint16_t>(sm.ring, sm.u, tap, t0 - TT, s_end, ch);
+        for (int g = 0; g < NTAPS; ++g) {
+          const int tau = g < 4 ? g : (g < 12 ? g - 4 : g - 12);
+          float2 acc = make_float2(0.0f, 0.0f);
+#pragma unroll
+          for (int tt = 0; tt < TT / 2; ++tt) {
+            const float2 e = g < 4 ? E1[tt] : (g < 12 ? E2[tt] : E3[tt]);
+            acc = __ffma2_rn(e, O[tt + HALO - tau], acc);
+          }
+          sm.dw[g][ch] += acc.x + acc.y;
+        }
       }
       __syncthreads();
     }
@@ -764,7 +857,6 @@ cudaError_t launch_fwd_update(const Params& p, const UpdArgs<__nv_bfloat16>& a, 
   timing_begin("fwd_update", st);
   if (has_conv) {
     cudaFuncSetAttribute(fwd_update_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    cudaFuncSetAttribute(fwd_update_kernel<true>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     fwd_update_kernel<true><<<grid, THREADS, smem, st>>>(p, a, coef, wk);
   } else {
     fwd_update_kernel<false><<<grid, THREADS, 0, st>>>(p, a, coef, wk);

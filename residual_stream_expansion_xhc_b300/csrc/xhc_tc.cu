@@ -93,8 +93,8 @@ int sm_count() {
 namespace coeffs {
 constexpr int TILE_T = 128;
 constexpr int KC = 64;                  // state entries per stage (128 bytes of bf16)
-constexpr int STAGES = 4;
-constexpr int X_BYTES = TILE_T * KC * 2;          // 16 KB
+constexpr int STAGES = 5;
+constexpr int X_BYTES = TILE_T * KC * 2;          // 16 KB (a tile of `rows` <= 128 tokens uses the first rows)
 constexpr int W_ROWS = 48;                        // padded P
 constexpr int WRAW_BYTES = W_ROWS * KC * 4;       // 12 KB fp32 tile from TMA
 constexpr int W_BYTES = W_ROWS * KC * 2;          // 6 KB per bf16 part
@@ -117,7 +117,7 @@ struct CoeffsOut {
 
 __global__ void __launch_bounds__(coeffs::THREADS, 1)
     coeffs_tc_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__ CUtensorMap mapW, Params p,
-                     CoeffsOut o, int ntiles) {
+                     CoeffsOut o, int ntiles, int rows) {
   using namespace coeffs;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
@@ -163,9 +163,9 @@ __global__ void __launch_bounds__(coeffs::THREADS, 1)
           const uint32_t ph = (it / STAGES) & 1;
           if (it >= STAGES && !mbar_wait(&empty[s], ph ^ 1, err, 11)) goto done_prod;
           uint8_t* st = smem + s * STAGE_BYTES;
-          mbar_expect_tx(&full[s], X_BYTES + p.P * KC * 4);
+          mbar_expect_tx(&full[s], rows * KC * 2 + p.P * KC * 4);
           const int n = kc / cchunks, c0 = (kc % cchunks) * KC;
-          tma_load_3d(st, &mapX, &full[s], c0, n, tile * TILE_T, pol_x);
+          tma_load_3d(st, &mapX, &full[s], c0, n, tile * rows, pol_x);
           tma_load_2d_f32(st + OFF_WRAW, &mapW, &full[s], kc * KC, 0, pol_w);
         }
       }
@@ -239,7 +239,9 @@ __global__ void __launch_bounds__(coeffs::THREADS, 1)
         const uint8_t* xr = stg + row * 128;
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
-          const uint4 v = *reinterpret_cast<const uint4*>(xr + 16 * c);
+          // physical 16-byte chunk (c + row) mod 8: the eight rows read by a
+          // phase of eight lanes fall in eight different bank groups
+          const uint4 v = *reinterpret_cast<const uint4*>(xr + 16 * ((c + row) & 7));
           const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
           for (int h = 0; h < 4; ++h) {
@@ -268,8 +270,8 @@ __global__ void __launch_bounds__(coeffs::THREADS, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[buf]);
 
-      const size_t t = (size_t)tile * TILE_T + row;
-      if (t >= (size_t)p.B * p.S) continue;
+      const size_t t = (size_t)tile * rows + row;
+      if (row >= rows || t >= (size_t)p.B * p.S) continue;
       const int N = p.N, k = p.k, P = p.P;
       const float rstd = 1.0f / sqrtf(ss / (float)(N * p.C) + p.eps);
       if (o.saved) {
@@ -339,11 +341,16 @@ cudaError_t launch_coeffs_tc(const Params& p, const void* X, const float* W, flo
   using namespace coeffs;
   const size_t T_all = (size_t)p.B * p.S;
   const size_t NC = (size_t)p.N * p.C;
+  // Tokens per tile: spread the tokens over every SM in one wave where that
+  // keeps at least 64 tokens per tile (W is re-read from L2 once per tile);
+  // the MMA always computes 128 rows and rows >= `rows` are ignored.
+  const size_t per_sm = (T_all + sm_count() - 1) / sm_count();
+  const int rows = (int)std::min<size_t>(TILE_T, std::max<size_t>(64, (per_sm + 7) / 8 * 8));
   CUtensorMap mx, mw;
   {
     const uint64_t dims[3] = {(uint64_t)p.C, (uint64_t)p.N, T_all};
     const uint64_t strides[2] = {(uint64_t)p.C * 2, NC * 2};
-    const uint32_t box[3] = {KC, 1, TILE_T};
+    const uint32_t box[3] = {KC, 1, (uint32_t)rows};
     if (!make_map(&mx, X, 3, dims, strides, box)) return cudaErrorInvalidValue;
   }
   {
@@ -353,12 +360,12 @@ cudaError_t launch_coeffs_tc(const Params& p, const void* X, const float* W, flo
     if (!make_map(&mw, W, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_DATA_TYPE_FLOAT32))
       return cudaErrorInvalidValue;
   }
-  const int ntiles = (int)((T_all + TILE_T - 1) / TILE_T);
+  const int ntiles = (int)((T_all + rows - 1) / rows);
   const int grid = std::min(ntiles, sm_count());
   cudaFuncSetAttribute(coeffs_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
   CoeffsOut o{hpre, hpost, hres, saved, coef};
   timing_begin("coeffs_tc", st);
-  coeffs_tc_kernel<<<grid, THREADS, SMEM, st>>>(mx, mw, p, o, ntiles);
+  coeffs_tc_kernel<<<grid, THREADS, SMEM, st>>>(mx, mw, p, o, ntiles, rows);
   timing_end(st);
   return cudaGetLastError();
 }
