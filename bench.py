@@ -361,7 +361,7 @@ def run_gpu(args, wl):
     per_launch_ms = dtotal / dcount
     alg = (ALG_C.get(dname, 0) * cunit + ALG_SIDE.get(dname, 0)) * wl.tokens
     achieved = alg / (per_launch_ms * 1e-3) / 1e9
-    traffic = load_traffic(dname)
+    traffic = load_traffic(dname, wl.tokens)
     e2e = None
     if not args.no_e2e:
         e2e = e2e_run(step, tensors, args.e2e_steps)
@@ -399,15 +399,20 @@ def run_gpu(args, wl):
     print(json.dumps(line), flush=True)
 
 
-def load_traffic(kernel: str):
-    """DRAM bytes per launch of the kernel from a committed ncu summary, or None."""
-    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+def load_traffic(kernel: str, tokens: int):
+    """DRAM bytes (read + write) per launch of a kernel, from the committed ncu
+    summary ``profiles/dram_traffic.txt`` (lines: kernel, measured bytes per
+    launch, tokens of the captured launch), scaled to ``tokens``; None when the
+    kernel has no entry there."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(path):
         return None
     with open(path) as f:
-        d = json.load(f)
-    v = d.get(kernel)
-    return None if v is None else v.get("bytes_per_launch")
+        for line in f:
+            parts = line.split()
+            if len(parts) >= 3 and not line.startswith("#") and parts[0] == kernel:
+                return float(parts[1]) * tokens / float(parts[2])
+    return None
 
 
 def main():

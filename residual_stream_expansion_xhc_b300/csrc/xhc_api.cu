@@ -80,6 +80,8 @@ Params make_params(const xhc_shape_t* sh, const int32_t* idx) {
       p.idx[i] = idx[i];
       p.is_active[idx[i]] = i + 1;
     }
+    for (int n = 0; n < sh->N; ++n)
+      if (!p.is_active[n]) p.inactive[p.n_inactive++] = n;
   }
   return p;
 }
@@ -339,8 +341,8 @@ int xhc_sublayer_fwd(const xhc_shape_t* sh, const void* X_in, void* X_out, const
 namespace {
 // Workspace of the backward.  CUDA-core path: per-token records (2P+1 floats),
 // recomputed logits, conv partials.  bf16 tensor-core path: records
-// (1+N+4k floats), recomputed logits, dp (bf16, 64 per token), W^T (bf16, 64
-// per column), the coefficient block, the column pass's coefficient dots and
+// (1+N+4k floats), recomputed logits, dp (bf16 hi and lo parts, 64 each per
+// token), W^T (bf16 hi and lo parts, 64 each per column), the coefficient block, the column pass's coefficient dots and
 // conv partials, dW partials (one per token range).
 struct BwdLayout {
   size_t rec, saved, dP, Wt, coef, pdot, cpart, wpart, total;
@@ -358,8 +360,8 @@ BwdLayout bwd_layout(const xhc_shape_t* sh) {
     L.rec = 0;
     L.saved = L.rec + round_up(T * (size_t)(1 + p.N + 4 * p.k) * sizeof(float));
     L.dP = L.saved + round_up(T * (size_t)(p.P + 1) * sizeof(float));
-    L.Wt = L.dP + round_up(T * 64 * sizeof(uint16_t));
-    L.coef = L.Wt + round_up(NC * 64 * sizeof(uint16_t));
+    L.Wt = L.dP + round_up(2 * T * 64 * sizeof(uint16_t));
+    L.coef = L.Wt + round_up(2 * NC * 64 * sizeof(uint16_t));
     L.pdot = L.coef + round_up(T * COEF_STRIDE * sizeof(float));
     L.cpart = L.pdot + round_up(bwd_col_pdot_floats(p) * sizeof(float));
     L.wpart = L.cpart + round_up(bwd_col_cpart_floats(p, sms) * sizeof(float));

@@ -17,7 +17,8 @@ namespace xhc {
 // ============================================================== W^T in bf16
 //
 // Wt[col][q] = bf16(W[q][col]) for q < P, zero for P <= q < 64: the K-major
-// operand of dV = dP . W in the stream pass.
+// operand of dV = dP . W in the stream pass, as a hi part and a lo part
+// (Wt + NC * 64 holds bf16(W - hi)), so that hi + lo keeps about 16 bits of W.
 
 __global__ void wt_prep_kernel(const float* __restrict__ W, __nv_bfloat16* __restrict__ Wt, int P, size_t NC) {
   __shared__ float tile[64][65];
@@ -27,10 +28,15 @@ __global__ void wt_prep_kernel(const float* __restrict__ W, __nv_bfloat16* __res
     tile[q][c] = (q < P && col0 + c < NC) ? W[(size_t)q * NC + col0 + c] : 0.0f;
   }
   __syncthreads();
+  __nv_bfloat16* Wt_lo = Wt + NC * 64;
   for (int i = threadIdx.x; i < 64 * 32; i += blockDim.x) {
     const int c = i / 32, q2 = (i % 32) * 2;
-    if (col0 + c < NC)
-      *reinterpret_cast<uint32_t*>(Wt + (col0 + c) * 64 + q2) = pack_bf2(tile[q2][c], tile[q2 + 1][c]);
+    if (col0 + c < NC) {
+      const float a = tile[q2][c], b = tile[q2 + 1][c];
+      const uint32_t h = pack_bf2(a, b);
+      *reinterpret_cast<uint32_t*>(Wt + (col0 + c) * 64 + q2) = h;
+      *reinterpret_cast<uint32_t*>(Wt_lo + (col0 + c) * 64 + q2) = pack_bf2(a - bf_lo(h), b - bf_hi(h));
+    }
   }
 }
 

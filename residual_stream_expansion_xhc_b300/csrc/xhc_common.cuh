@@ -24,6 +24,8 @@ struct Params {
   float eps;
   int idx[KMAX];
   int is_active[NMAX];    // slot+1 of stream n if active, else 0
+  int n_inactive;         // N - k
+  int inactive[NMAX];     // the inactive streams in increasing order
 };
 
 // ---------------------------------------------------------------- element access

@@ -230,7 +230,8 @@ __device__ __forceinline__ void tfa_chunk_s(const uint16_t (*ring)[CB], U (*u_s)
   }
 }
 
-template <bool HAS_CONV>
+// NI > 0: exactly NI inactive streams, all loaded in one wave; NI = 0: any count.
+template <bool HAS_CONV, int NI>
 __global__ void __launch_bounds__(THREADS, 2) fwd_update_kernel(Params p, UpdArgs<__nv_bfloat16> a,
                                                                 const float* __restrict__ coef, Walk wk) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
@@ -288,24 +289,27 @@ __global__ void __launch_bounds__(THREADS, 2) fwd_update_kernel(Params p, UpdArg
 #pragma unroll
         for (int x = 0; x < 8; ++x) acc[x] = 0.0f;
         if (need_all) {
-          // the inactive streams, eight rows at a time
+          // the inactive streams, NI (or at most 8) rows per wave of loads
+          constexpr int WAVE = NI > 0 ? NI : 8;
+          const int ni = NI > 0 ? NI : p.n_inactive;
+#pragma unroll 1
+          for (int q0 = 0; q0 < ni; q0 += WAVE) {
+            uint4 xr[WAVE];
 #pragma unroll
-          for (int nb = 0; nb < NMAX; nb += 8) {
-            uint4 xr[8];
+            for (int q = 0; q < WAVE; ++q)
+              if (q0 + q < ni) xr[q] = ld_stream(xrow + (size_t)p.inactive[q0 + q] * C);
 #pragma unroll
-            for (int q = 0; q < 8; ++q)
-              if (nb + q < N && !p.is_active[nb + q]) xr[q] = ld_stream(xrow + (size_t)(nb + q) * C);
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              if (nb + q < N && !p.is_active[nb + q]) {
+            for (int q = 0; q < WAVE; ++q) {
+              if (q0 + q < ni) {
+                const int n = p.inactive[q0 + q];
                 if (a.x_in) {
-                  const float h = cf[nb + q];
+                  const float h = cf[n];
                   float v[8];
                   unpack8(xr[q], v);
 #pragma unroll
                   for (int x = 0; x < 8; ++x) acc[x] = fmaf(h, v[x], acc[x]);
                 }
-                if (a.copy_inactive) st_stream(yrow + (size_t)(nb + q) * C, xr[q]);
+                if (a.copy_inactive) st_stream(yrow + (size_t)n * C, xr[q]);
               }
             }
           }
@@ -771,7 +775,7 @@ __global__ void __launch_bounds__(THREADS, 2) bwd_col_kernel(Params p, BwdArgs<_
 // partials of every channel block, reruns the Sinkhorn iterations keeping the
 // iterates, reverses them, and forms
 //   dz  (sigmoid' for H^pre / H^post, Sinkhorn reverse for H^res)
-//   dp  = rstd * dz                       -> dP[t][0..63] bf16 (zero padded)
+//   dp  = rstd * dz                       -> dP[t][0..63] bf16 hi + lo (zero padded)
 //   alpha = <dz, z / rstd> * (-rstd^3 / (N C))   -> rec[t][0]
 //   hpre[n]                               -> rec[t][1 + n]
 
@@ -826,11 +830,19 @@ __global__ void __launch_bounds__(256) bwd_dz_kernel(Params p, const float* __re
   part += __shfl_xor_sync(FULL, part, 4);
   part += __shfl_xor_sync(FULL, part, 8);
   if (!live) return;
+  // dp as a bf16 hi part (dP) and lo part (dP + T * 64): hi + lo keeps about
+  // 16 bits of dp for the tensor-core contractions
   __nv_bfloat16* dprow = dP + t * 64;
-  if (e < N) dprow[e] = __float2bfloat16_rn(rstd * dz_pre);
-  if (e < 4 * k) dprow[N + e] = __float2bfloat16_rn(rstd * dz_post);
-  if (valid) dprow[N + 4 * k + k * i + j] = __float2bfloat16_rn(rstd * dz_res);
-  for (int q = P + e; q < 64; q += 16) dprow[q] = __float2bfloat16_rn(0.0f);
+  __nv_bfloat16* dplow = dP + T_all * 64 + t * 64;
+  auto put = [&](int q, float v) {
+    const __nv_bfloat16 h = __float2bfloat16_rn(v);
+    dprow[q] = h;
+    dplow[q] = __float2bfloat16_rn(v - __bfloat162float(h));
+  };
+  if (e < N) put(e, rstd * dz_pre);
+  if (e < 4 * k) put(N + e, rstd * dz_post);
+  if (valid) put(N + 4 * k + k * i + j, rstd * dz_res);
+  for (int q = P + e; q < 64; q += 16) put(q, 0.0f);
   const int rl = 1 + N + 4 * k;
   float* rc = rec + t * rl;
   if (e == 0) rc[0] = -part * rstd * rstd / (float)((size_t)N * p.C);
@@ -855,11 +867,17 @@ cudaError_t launch_fwd_update(const Params& p, const UpdArgs<__nv_bfloat16>& a, 
   dim3 grid(wk.R, wk.ncb);
   const int smem = (int)sizeof(FwdSmem);
   timing_begin("fwd_update", st);
-  if (has_conv) {
-    cudaFuncSetAttribute(fwd_update_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    fwd_update_kernel<true><<<grid, THREADS, smem, st>>>(p, a, coef, wk);
+  const bool twelve = p.n_inactive == 12;      // N = 16, k = 4
+  if (has_conv && twelve) {
+    cudaFuncSetAttribute(fwd_update_kernel<true, 12>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    fwd_update_kernel<true, 12><<<grid, THREADS, smem, st>>>(p, a, coef, wk);
+  } else if (has_conv) {
+    cudaFuncSetAttribute(fwd_update_kernel<true, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    fwd_update_kernel<true, 0><<<grid, THREADS, smem, st>>>(p, a, coef, wk);
+  } else if (twelve) {
+    fwd_update_kernel<false, 12><<<grid, THREADS, 0, st>>>(p, a, coef, wk);
   } else {
-    fwd_update_kernel<false><<<grid, THREADS, 0, st>>>(p, a, coef, wk);
+    fwd_update_kernel<false, 0><<<grid, THREADS, 0, st>>>(p, a, coef, wk);
   }
   timing_end(st);
   return cudaGetLastError();

@@ -133,7 +133,7 @@ __global__ void __launch_bounds__(coeffs::THREADS, 1)
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);                   // TMA transaction
       mbar_init(&bready[s], 4);                 // W split done by the 4 math warps
-      mbar_init(&empty[s], 1);                  // MMA commit
+      mbar_init(&empty[s], 1 + 4);              // MMA commit + the 4 math warps done reading X
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
@@ -236,6 +236,8 @@ __global__ void __launch_bounds__(coeffs::THREADS, 1)
           *reinterpret_cast<uint4*>(stg + OFF_WLO + sw128_offset(q, g * 16)) = l;
         }
         fence_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bready[s]);   // the MMA may start; X is read below
         const uint8_t* xr = stg + row * 128;
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
@@ -251,7 +253,7 @@ __global__ void __launch_bounds__(coeffs::THREADS, 1)
           }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bready[s]);
+        if (lane == 0) mbar_arrive(&empty[s]);
       }
       if (!ok) break;
       const int buf = tl & 1;
@@ -390,8 +392,10 @@ int read_device_error(cudaStream_t st) {
 //                                     boxes, 128-byte swizzle)
 //   Bt   [128 x 128]                 dX' (inactive n) or the active-stream mix
 //                                     written to dX by the token pass
-//   Pt   [128 tokens x 64]           dp (bf16, P <= 48 entries, zero padded)
-// and the tensor cores compute
+//   Pt   [128 tokens x 64]           dp (bf16 hi and lo parts, P <= 48 entries,
+//                                     zero padded)
+// and the tensor cores compute, with hi + lo parts of dp and of W (about 16
+// bits each; the lo x lo product is dropped)
 //   dV [128 tokens x 128 cols] = Pt . Wt_blk^T   (A K-major, B K-major; K = 48)
 //   dW [128 cols x 48]        += Xt^T . Pt       (A and B MN-major: the same
 //                                                 tiles, read along tokens)
@@ -409,17 +413,18 @@ constexpr int STAGES = 2;
 constexpr int HALF = TT * 64 * 2;                 // one 64-column box: 16 KB
 constexpr int OFF_X = 0;
 constexpr int OFF_B = 2 * HALF;
-constexpr int OFF_P = 4 * HALF;
-constexpr int STAGE_BYTES = 5 * HALF;             // 80 KB
-constexpr int WT_BYTES = CB * 64 * 2;             // 16 KB
-constexpr int SMEM = STAGES * STAGE_BYTES + WT_BYTES + 1024;
+constexpr int OFF_P = 4 * HALF;                   // dp, hi part
+constexpr int OFF_PL = 5 * HALF;                  // dp, lo part
+constexpr int STAGE_BYTES = 6 * HALF;             // 96 KB
+constexpr int WT_BYTES = CB * 64 * 2;             // 16 KB per part of W^T
+constexpr int SMEM = STAGES * STAGE_BYTES + 2 * WT_BYTES + 1024;
 constexpr int THREADS = 192;
 constexpr int TMEM_COLS = 512;                    // dV: 2 x 128, dW: 48 at column 256
 constexpr int D2_COL = 256;
 }  // namespace bwdtc
 
 struct StreamMaps {
-  CUtensorMap X, Xa, dXp, dX, dP, Wt;
+  CUtensorMap X, Xa, dXp, dX, dP, dPl, Wt, Wtl;
 };
 
 __global__ void __launch_bounds__(bwdtc::THREADS, 1)
@@ -476,8 +481,9 @@ __global__ void __launch_bounds__(bwdtc::THREADS, 1)
         const size_t t_beg = (size_t)r * range_len;
         const size_t t_end = (t_beg + range_len < T_all) ? t_beg + range_len : T_all;
         if (ii > 0 && !mbar_wait(&wt_empty, (ii - 1) & 1, err, 21)) break;
-        mbar_expect_tx(&wt_full, WT_BYTES);
+        mbar_expect_tx(&wt_full, 2 * WT_BYTES);
         tma_load_2d(wt_s, &m.Wt, &wt_full, 0, (int)((size_t)n * C + c0), pol_keep);
+        tma_load_2d(wt_s + WT_BYTES, &m.Wtl, &wt_full, 0, (int)((size_t)n * C + c0), pol_keep);
         bool ok = true;
         for (size_t t0 = t_beg; t0 < t_end; t0 += TT, ++it) {
           const int s = it % STAGES;
@@ -494,6 +500,7 @@ __global__ void __launch_bounds__(bwdtc::THREADS, 1)
             else tma_load_3d(st + OFF_B + h * HALF, &m.dXp, &full[s], c0 + 64 * h, n, tt, pol_stream);
           }
           tma_load_2d(st + OFF_P, &m.dP, &full[s], 0, tt, pol_keep);
+          tma_load_2d(st + OFF_PL, &m.dPl, &full[s], 0, tt, pol_keep);
         }
         if (!ok) break;
       }
@@ -519,20 +526,27 @@ __global__ void __launch_bounds__(bwdtc::THREADS, 1)
           if (tl >= 2 && !mbar_wait(&tempty[buf], ((tl >> 1) & 1) ^ 1, err, 26)) { ok = false; break; }
           tc_fence_after();
           const uint32_t st = smem_u32(smem + s * STAGE_BYTES);
-          // dV = dP . Wt^T  (K = 48: three K16 steps inside the 128-byte rows)
+          // dV = dP . Wt^T  (K = 48: three K16 steps inside the 128-byte rows);
+          // hi.hi + hi.lo + lo.hi
 #pragma unroll
           for (int ks = 0; ks < 3; ++ks) {
-            const uint64_t da = sdesc_sw128(st + OFF_P + ks * 32, 16, 1024);
-            const uint64_t db = sdesc_sw128(wt_addr + ks * 32, 16, 1024);
-            umma_bf16(tmem + buf * 128, da, db, idesc_v, ks > 0);
+            const uint64_t ph = sdesc_sw128(st + OFF_P + ks * 32, 16, 1024);
+            const uint64_t pl = sdesc_sw128(st + OFF_PL + ks * 32, 16, 1024);
+            const uint64_t wh = sdesc_sw128(wt_addr + ks * 32, 16, 1024);
+            const uint64_t wl = sdesc_sw128(wt_addr + WT_BYTES + ks * 32, 16, 1024);
+            umma_bf16(tmem + buf * 128, ph, wh, idesc_v, ks > 0);
+            umma_bf16(tmem + buf * 128, ph, wl, idesc_v, 1);
+            umma_bf16(tmem + buf * 128, pl, wh, idesc_v, 1);
           }
           umma_commit(&tfull[buf]);
-          // dW += X^T . dP  (K = 128 tokens: eight K16 steps of 16 rows)
+          // dW += X^T . dP  (K = 128 tokens: eight K16 steps of 16 rows); hi + lo of dp
 #pragma unroll
           for (int ks = 0; ks < TT / 16; ++ks) {
             const uint64_t da = sdesc_sw128(st + OFF_X + ks * 2048, HALF, 1024);
-            const uint64_t db = sdesc_sw128(st + OFF_P + ks * 2048, HALF, 1024);
-            umma_bf16(tmem + D2_COL, da, db, idesc_w, (first && ks == 0) ? 0u : 1u);
+            const uint64_t dh = sdesc_sw128(st + OFF_P + ks * 2048, HALF, 1024);
+            const uint64_t dl = sdesc_sw128(st + OFF_PL + ks * 2048, HALF, 1024);
+            umma_bf16(tmem + D2_COL, da, dh, idesc_w, (first && ks == 0) ? 0u : 1u);
+            umma_bf16(tmem + D2_COL, da, dl, idesc_w, 1);
           }
           umma_commit(&empty[s]);
           first = false;
@@ -692,12 +706,14 @@ cudaError_t launch_bwd_stream_tc(const Params& p, const BwdArgs<__nv_bfloat16>& 
     const uint64_t strides[1] = {128};
     const uint32_t box[2] = {64, TT};
     if (!make_map(&m.dP, dP, 2, dims, strides, box)) return cudaErrorInvalidValue;
+    if (!make_map(&m.dPl, dP + T_all * 64, 2, dims, strides, box)) return cudaErrorInvalidValue;
   }
   {
     const uint64_t dims[2] = {64, NC};
     const uint64_t strides[1] = {128};
     const uint32_t box[2] = {64, CB};
     if (!make_map(&m.Wt, Wt, 2, dims, strides, box)) return cudaErrorInvalidValue;
+    if (!make_map(&m.Wtl, Wt + NC * 64, 2, dims, strides, box)) return cudaErrorInvalidValue;
   }
   const size_t tiles = (T_all + TT - 1) / TT;
   const int range_len = (int)(((tiles + ranges - 1) / ranges) * TT);

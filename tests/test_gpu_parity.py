@@ -28,6 +28,12 @@ CASES = {
     "mhc_bf16_small": xin.Workload("mhc_bf16_small", 14, B=2, S=70, N=4, C=256, k=4, dtype="bf16",
                                    conv="none", identity_idx=True),
     "bf16_odd_c": xin.Workload("bf16_odd_c", 15, B=1, S=33, N=6, C=72, k=2, dtype="bf16"),
+    # degenerate lengths: one token, shorter than the longest convolution, exactly its length
+    "bf16_s1": xin.Workload("bf16_s1", 16, B=3, S=1, N=16, C=256, k=4, dtype="bf16"),
+    "bf16_s5": xin.Workload("bf16_s5", 17, B=2, S=5, N=16, C=256, k=4, dtype="bf16"),
+    "bf16_s12": xin.Workload("bf16_s12", 18, B=2, S=12, N=16, C=256, k=4, dtype="bf16"),
+    # fewest streams: one active of two
+    "bf16_n2k1": xin.Workload("bf16_n2k1", 19, B=2, S=40, N=2, C=256, k=1, dtype="bf16"),
 }
 
 
@@ -181,7 +187,8 @@ def run_bwd(wl, t, use_saved=True, use_active=True, dx_in=True, dX_alias=False):
     return dict(dX=dX, dout=dout, dconv=dconv, dW=dW)
 
 
-BWD_CASES = ["tiny_f32", "bf16_ragged", "f32_ragged", "mhc_bf16_small", "bf16_c2048", "bf16_odd_c"]
+BWD_CASES = ["tiny_f32", "bf16_ragged", "f32_ragged", "mhc_bf16_small", "bf16_c2048", "bf16_odd_c", "bf16_s1",
+             "bf16_s5", "bf16_s12", "bf16_n2k1"]
 
 
 @pytest.mark.parametrize("name", BWD_CASES)
