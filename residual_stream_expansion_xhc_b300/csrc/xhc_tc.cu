@@ -82,10 +82,11 @@ int sm_count() {
 //   warp 0      TMA producer: X tile [128 tokens x 64 state entries] and the
 //               matching fp32 W tile [P x 64] per stage
 //   warp 1      MMA issuer (one thread) and TMEM owner
-//   warps 2..5  split the W tile into bf16 W_hi = bf16(W) and W_lo =
-//               bf16(W - W_hi) (swizzled K-major tiles), and, one thread per
-//               token, accumulate the sum of squares of each X stage; then the
-//               epilogue (rstd, logits, sigmoid, Sinkhorn, stores)
+//   warps 2..9  split the W tile into bf16 W_hi = bf16(W) and W_lo =
+//               bf16(W - W_hi) (swizzled K-major tiles), and accumulate the
+//               sum of squares of each X stage (warps 2..5 and 6..9 each take
+//               half of every token row); warps 2..5 then run the epilogue
+//               (rstd, logits, sigmoid, Sinkhorn, stores)
 // D[128 x 48] (fp32, TMEM) accumulates X.W_hi^T + X.W_lo^T over all N*C / 64
 // stages of a tile, which keeps about 16 mantissa bits of W; two TMEM buffers
 // let the epilogue of tile i overlap the MMAs of tile i+1.
@@ -103,7 +104,8 @@ constexpr int OFF_WHI = X_BYTES + WRAW_BYTES;
 constexpr int OFF_WLO = OFF_WHI + W_BYTES;
 constexpr int STAGE_BYTES = OFF_WLO + W_BYTES;    // 40 KB
 constexpr int SMEM = STAGES * STAGE_BYTES + 1024;
-constexpr int THREADS = 192;
+constexpr int MATH_WARPS = 8;                     // two per scheduler: W split + sum of squares
+constexpr int THREADS = 64 + 32 * MATH_WARPS;     // producer, MMA issuer, math warps
 constexpr int TMEM_COLS = 128;                    // 2 buffers x 64 columns
 }  // namespace coeffs
 
@@ -121,8 +123,9 @@ __global__ void __launch_bounds__(coeffs::THREADS, 1)
   using namespace coeffs;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
-  __shared__ uint64_t full[STAGES], bready[STAGES], empty[STAGES], tfull[2], tempty[2];
+  __shared__ uint64_t full[STAGES], bready[STAGES], empty[STAGES], tfull[2], tempty[2], ssfull[2], ssempty[2];
   __shared__ uint32_t tmem_slot;
+  __shared__ float ss_half[2][TILE_T];          // second halves of the row sums of squares
   int* err = &g_device_error;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -132,12 +135,14 @@ __global__ void __launch_bounds__(coeffs::THREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);                   // TMA transaction
-      mbar_init(&bready[s], 4);                 // W split done by the 4 math warps
-      mbar_init(&empty[s], 1 + 4);              // MMA commit + the 4 math warps done reading X
+      mbar_init(&bready[s], MATH_WARPS);        // W split done by the math warps
+      mbar_init(&empty[s], 1 + MATH_WARPS);     // MMA commit + the math warps done reading X
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
       mbar_init(&tempty[b], 4);
+      mbar_init(&ssfull[b], 4);                 // warps 6..9 wrote their halves
+      mbar_init(&ssempty[b], 4);                // warps 2..5 read them
     }
     fence_mbar_init();
     tma_prefetch_desc(&mapX);
@@ -204,6 +209,8 @@ __global__ void __launch_bounds__(coeffs::THREADS, 1)
   } else {
     // ------------------------------------------------ sum of squares + epilogue
     const int row = 32 * (warp & 3) + lane;             // token row == TMEM lane
+    const int half = (warp - 2) >> 2;                   // which four 16-byte chunks of the row
+    const int mt = threadIdx.x - 64;                    // math thread 0 .. 32 * MATH_WARPS - 1
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
     int it = 0, tl = 0;
     for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++tl) {
@@ -213,8 +220,8 @@ __global__ void __launch_bounds__(coeffs::THREADS, 1)
         const int s = it % STAGES;
         if (!mbar_wait(&full[s], (it / STAGES) & 1, err, 14)) { ok = false; break; }
         uint8_t* stg = smem + s * STAGE_BYTES;
-        // split W: 48 rows x 8 groups of 8 entries, 3 groups per thread
-        for (int u = threadIdx.x - 64; u < W_ROWS * 8; u += 128) {
+        // split W: 48 rows x 8 groups of 8 entries over the math threads
+        for (int u = mt; u < W_ROWS * 8; u += 32 * MATH_WARPS) {
           const int q = u >> 3, g = u & 7;
           uint4 h = make_uint4(0, 0, 0, 0), l = make_uint4(0, 0, 0, 0);
           if (q < p.P) {
@@ -240,10 +247,10 @@ __global__ void __launch_bounds__(coeffs::THREADS, 1)
         if (lane == 0) mbar_arrive(&bready[s]);   // the MMA may start; X is read below
         const uint8_t* xr = stg + row * 128;
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          // physical 16-byte chunk (c + row) mod 8: the eight rows read by a
-          // phase of eight lanes fall in eight different bank groups
-          const uint4 v = *reinterpret_cast<const uint4*>(xr + 16 * ((c + row) & 7));
+        for (int c = 0; c < 4; ++c) {
+          // physical 16-byte chunk (4 half + c + row) mod 8: the eight rows read
+          // by a phase of eight lanes fall in eight different bank groups
+          const uint4 v = *reinterpret_cast<const uint4*>(xr + 16 * ((4 * half + c + row) & 7));
           const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
           for (int h = 0; h < 4; ++h) {
@@ -256,6 +263,19 @@ __global__ void __launch_bounds__(coeffs::THREADS, 1)
         if (lane == 0) mbar_arrive(&empty[s]);
       }
       if (!ok) break;
+      const int sb = tl & 1;
+      if (half == 1) {
+        // hand the second half of the row sums to warps 2..5 (double-buffered)
+        if (tl >= 2 && !mbar_wait(&ssempty[sb], ((tl >> 1) & 1) ^ 1, err, 16)) break;
+        ss_half[sb][row] = ss;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ssfull[sb]);
+        continue;
+      }
+      if (!mbar_wait(&ssfull[sb], (tl >> 1) & 1, err, 17)) break;
+      ss += ss_half[sb][row];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ssempty[sb]);
       const int buf = tl & 1;
       if (!mbar_wait(&tfull[buf], (tl >> 1) & 1, err, 15)) break;
       tc_fence_after();
