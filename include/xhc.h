@@ -152,7 +152,8 @@ int xhc_sparse_update(const xhc_shape_t* sh, const void* X_in, void* X_out,
  * for every call of the shape; xhc_fwd_workspace_need() is what a call needs
  * when the caller keeps the logits (keeps_saved != 0: `saved` is non-NULL) or
  * not.  The bf16 path uses it for a per-token coefficient block (48 fp32 per
- * token) and, when `saved` is NULL, for the logits (P + 1 fp32 per token).
+ * token) and a bf16 hi/lo split copy of W (2 x 48 x N*C bf16), and, when
+ * `saved` is NULL, for the logits (P + 1 fp32 per token).
  */
 size_t xhc_fwd_workspace_bytes(const xhc_shape_t* sh);
 size_t xhc_fwd_workspace_need(const xhc_shape_t* sh, int keeps_saved);
@@ -185,13 +186,14 @@ int xhc_sublayer_fwd(const xhc_shape_t* sh, const void* X_in, void* X_out,
  * may not call the CUDA allocator (a plugin or custom-op hook running inside
  * another framework's memory pool, a C caller without a workspace of its
  * own).  This entry point takes the same arguments as xhc_sublayer_fwd minus
- * the workspace, and uses a fixed 8 MiB scratch area built into the library
+ * the workspace, and uses a fixed 32 MiB scratch area built into the library
  * (a device array that every GPU which loads the library keeps until the
  * process exits) in place of the workspace.
- *   Limit: xhc_fwd_workspace_need(sh, saved != NULL) must be at most 8 MiB:
- *          43,690 tokens at N = 16, k = 4 with `saved` given, 21,620 without
- *          (bf16; the fp32 path needs no scratch when `saved` is given).
- *          Larger calls return XHC_ERR_WORKSPACE before touching the GPU.
+ *   Limit: xhc_fwd_workspace_need(sh, saved != NULL) must be at most 32 MiB.
+ *          At N = 16, k = 4 in bf16 a call needs 3072 * C bytes (a bf16 split
+ *          copy of W) plus 192 bytes per token with `saved` given, 388
+ *          without: at C = 2048 about 141,000 and 70,000 tokens.  Larger
+ *          calls return XHC_ERR_WORKSPACE before touching the GPU.
  *   The first call on each device looks up the scratch address on that
  *   device (no allocation); make that first call before any stream capture.
  *   Every call shares the one scratch area: calls whose work overlaps on the

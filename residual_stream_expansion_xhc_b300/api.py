@@ -102,7 +102,7 @@ def xhc_sublayer_fwd(sh, X_in, X_out, out, conv, W, idx, x_in=None, saved=None, 
 def xhc_sublayer_fwd_noalloc(sh, X_in, X_out, out, conv, W, idx, x_in=None, saved=None, saved_active=None,
                              stream=None):
     """xhc_sublayer_fwd without a workspace: for callers that may not allocate
-    device memory.  Uses the library's built-in 8 MiB scratch (see the C
+    device memory.  Uses the library's built-in 32 MiB scratch (see the C
     header for the token limit and the rule that overlapping calls race)."""
     w4, w8, w12 = _conv(conv)
     _check("xhc_sublayer_fwd_noalloc",

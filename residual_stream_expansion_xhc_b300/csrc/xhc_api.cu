@@ -108,7 +108,7 @@ int run_coeffs(const xhc_shape_t* sh, const Params& p, const void* X, const floa
   if (sh->dtype == XHC_BF16) {
     using T = __nv_bfloat16;
     if (tc_coeffs_supported(p)) {
-      int s = cuda_status(launch_coeffs_tc(p, X, W, hpre, hpost, hres, saved, nullptr, st));
+      int s = cuda_status(launch_coeffs_tc(p, X, W, nullptr, hpre, hpost, hres, saved, nullptr, st));
       if (s || !x_in) return s;
       UpdArgs<T> a{(const T*)X, nullptr, nullptr, {nullptr, nullptr, nullptr}, hpre, nullptr, nullptr,
                    hpre ? nullptr : saved, (T*)x_in, nullptr, 0};
@@ -277,26 +277,32 @@ int xhc_sparse_update(const xhc_shape_t* sh, const void* X_in, void* X_out, cons
 }
 
 namespace {
-// Forward workspace: the coefficient block [T, COEF_STRIDE] (bf16 tensor-core
-// path) followed by the logits [T, P + 1] when the caller keeps none.
-size_t fwd_coef_bytes(const xhc_shape_t* sh) { return round_up(tokens(sh) * COEF_STRIDE * sizeof(float)); }
-size_t fwd_z_bytes(const xhc_shape_t* sh) {
-  return round_up(tokens(sh) * (size_t)(sh->N + 4 * sh->k + sh->k * sh->k + 1) * sizeof(float));
-}
+// Forward workspace: the coefficient block [T, COEF_STRIDE] and the bf16 hi/lo
+// split of W (bf16 tensor-core path), followed by the logits [T, P + 1] when
+// the caller keeps none.
 bool fwd_uses_coef(const xhc_shape_t* sh, const Params& p) {
   return sh->dtype == XHC_BF16 && tc_coeffs_supported(p) && stream_update_supported(p);
+}
+size_t fwd_coef_bytes(const xhc_shape_t* sh) { return round_up(tokens(sh) * COEF_STRIDE * sizeof(float)); }
+size_t fwd_wsplit_bytes(const xhc_shape_t* sh) {
+  const Params p = make_params(sh, nullptr);
+  return fwd_uses_coef(sh, p) ? round_up(coeffs_wsplit_bytes(p)) : 0;
+}
+size_t fwd_z_bytes(const xhc_shape_t* sh) {
+  return round_up(tokens(sh) * (size_t)(sh->N + 4 * sh->k + sh->k * sh->k + 1) * sizeof(float));
 }
 }  // namespace
 
 size_t xhc_fwd_workspace_bytes(const xhc_shape_t* sh) {
   if (check_shape(sh)) return 0;
-  return fwd_coef_bytes(sh) + fwd_z_bytes(sh);
+  const Params p = make_params(sh, nullptr);
+  return (fwd_uses_coef(sh, p) ? fwd_coef_bytes(sh) : 0) + fwd_wsplit_bytes(sh) + fwd_z_bytes(sh);
 }
 
 size_t xhc_fwd_workspace_need(const xhc_shape_t* sh, int keeps_saved) {
   if (check_shape(sh)) return 0;
   const Params p = make_params(sh, nullptr);
-  return (fwd_uses_coef(sh, p) ? fwd_coef_bytes(sh) : 0) + (keeps_saved ? 0 : fwd_z_bytes(sh));
+  return (fwd_uses_coef(sh, p) ? fwd_coef_bytes(sh) : 0) + fwd_wsplit_bytes(sh) + (keeps_saved ? 0 : fwd_z_bytes(sh));
 }
 
 int xhc_sublayer_fwd(const xhc_shape_t* sh, const void* X_in, void* X_out, const void* out, const float* w4,
@@ -315,13 +321,14 @@ int xhc_sublayer_fwd(const xhc_shape_t* sh, const void* X_in, void* X_out, const
   if (need > 0 && (!workspace || ws_bytes < need)) return XHC_ERR_WORKSPACE;
   char* ws = (char*)workspace;
   float* coef = use_coef ? (float*)ws : nullptr;
-  float* z = saved ? saved : (float*)(ws + (use_coef ? fwd_coef_bytes(sh) : 0));
+  void* wsplit = use_coef ? (void*)(ws + fwd_coef_bytes(sh)) : nullptr;
+  float* z = saved ? saved : (float*)(ws + (use_coef ? fwd_coef_bytes(sh) + fwd_wsplit_bytes(sh) : 0));
   cudaStream_t st = (cudaStream_t)stream;
   if (use_coef) {
     // coefficients on the tensor cores, then one streaming pass: dense read,
     // TFA and sparse write
     using T = __nv_bfloat16;
-    if ((s = cuda_status(launch_coeffs_tc(p, X_in, W, nullptr, nullptr, nullptr, z, coef, st)))) return s;
+    if ((s = cuda_status(launch_coeffs_tc(p, X_in, W, wsplit, nullptr, nullptr, nullptr, z, coef, st)))) return s;
     UpdArgs<T> a{(const T*)X_in, (T*)X_out, (const T*)out, {w4, w8, w12}, nullptr, nullptr, nullptr, z,
                  (T*)x_in, (T*)saved_active, X_out != X_in};
     return cuda_status(launch_fwd_update(p, a, coef, has_conv, num_sms(), st));
@@ -345,7 +352,7 @@ namespace {
 // token), W^T (bf16 hi and lo parts, 64 each per column), the coefficient block, the column pass's coefficient dots and
 // conv partials, dW partials (one per token range).
 struct BwdLayout {
-  size_t rec, saved, dP, Wt, coef, pdot, cpart, wpart, total;
+  size_t rec, saved, dP, Wt, coef, pdot, cpart, wpart, wsplit, total;
   int ranges, cpart_rows;
 };
 BwdLayout bwd_layout(const xhc_shape_t* sh) {
@@ -365,7 +372,8 @@ BwdLayout bwd_layout(const xhc_shape_t* sh) {
     L.pdot = L.coef + round_up(T * COEF_STRIDE * sizeof(float));
     L.cpart = L.pdot + round_up(bwd_col_pdot_floats(p) * sizeof(float));
     L.wpart = L.cpart + round_up(bwd_col_cpart_floats(p, sms) * sizeof(float));
-    L.total = L.wpart + round_up((size_t)L.ranges * p.P * NC * sizeof(float));
+    L.wsplit = L.wpart + round_up((size_t)L.ranges * p.P * NC * sizeof(float));
+    L.total = L.wsplit + (tc_coeffs_supported(p) ? round_up(coeffs_wsplit_bytes(p)) : 0);
   } else {
     L.rec = 0;
     L.saved = round_up(T * (size_t)(2 * p.P + 1) * sizeof(float));
@@ -421,7 +429,8 @@ int xhc_sublayer_bwd(const xhc_shape_t* sh, const void* X_state, const void* sav
   if (!z) {
     float* zw = (float*)(ws + L.saved);
     if (tc_path && tc_coeffs_supported(p)) {
-      if ((s = cuda_status(launch_coeffs_tc(p, X_state, W, nullptr, nullptr, nullptr, zw, coef, st)))) return s;
+      if ((s = cuda_status(launch_coeffs_tc(p, X_state, W, ws + L.wsplit, nullptr, nullptr, nullptr, zw, coef, st))))
+        return s;
       have_coef = true;
     } else if ((s = run_coeffs(sh, p, X_state, W, nullptr, nullptr, nullptr, zw, nullptr, st))) {
       return s;

@@ -1,8 +1,9 @@
 // xhc_sublayer_fwd_noalloc: the fused forward for callers that cannot
 // allocate device memory.
 //
-// The fused forward needs scratch: a per-token coefficient block, and the
-// per-token logits when the caller does not keep them (`saved` == NULL).
+// The fused forward needs scratch: a per-token coefficient block, a bf16 split
+// copy of W, and the per-token logits when the caller does not keep them
+// (`saved` == NULL).
 // Normally the caller hands that scratch in as a workspace.  Some callers have no way to obtain one: code running
 // inside a framework's custom-op or plugin hook that may not call the CUDA
 // allocator, a process whose memory is owned by a pool it cannot reach from
@@ -17,9 +18,10 @@
 namespace {
 
 // Capacity of the built-in scratch.  At N = 16, k = 4 (P = 48) a bf16 call
-// needs 192 bytes per token with `saved` given (43,690 tokens fit) and 388
-// bytes per token without (21,620 tokens fit).
-constexpr size_t kScratchBytes = size_t(8) << 20;
+// needs 3072 * C bytes for the split copy of W, plus 192 bytes per token with
+// `saved` given or 388 without: at C = 2048 about 141,000 tokens fit with
+// `saved` and 70,000 without.
+constexpr size_t kScratchBytes = size_t(32) << 20;
 
 static __device__ __align__(256) unsigned char g_fwd_scratch[kScratchBytes];
 

@@ -94,19 +94,33 @@ int sm_count() {
 namespace coeffs {
 constexpr int TILE_T = 128;
 constexpr int KC = 64;                  // state entries per stage (128 bytes of bf16)
-constexpr int STAGES = 5;
 constexpr int X_BYTES = TILE_T * KC * 2;          // 16 KB (a tile of `rows` <= 128 tokens uses the first rows)
 constexpr int W_ROWS = 48;                        // padded P
 constexpr int WRAW_BYTES = W_ROWS * KC * 4;       // 12 KB fp32 tile from TMA
 constexpr int W_BYTES = W_ROWS * KC * 2;          // 6 KB per bf16 part
-constexpr int OFF_WRAW = X_BYTES;
-constexpr int OFF_WHI = X_BYTES + WRAW_BYTES;
-constexpr int OFF_WLO = OFF_WHI + W_BYTES;
-constexpr int STAGE_BYTES = OFF_WLO + W_BYTES;    // 40 KB
-constexpr int SMEM = STAGES * STAGE_BYTES + 1024;
 constexpr int MATH_WARPS = 8;                     // two per scheduler: W split + sum of squares
 constexpr int THREADS = 64 + 32 * MATH_WARPS;     // producer, MMA issuer, math warps
 constexpr int TMEM_COLS = 128;                    // 2 buffers x 64 columns
+// Stage layouts.  PRESPLIT: W arrives as bf16 hi and lo tiles split once per
+// call (w_split_kernel), so a stage is X + hi + lo.  Otherwise the fp32 W
+// tile arrives and the math warps split it into hi and lo in the stage.
+template <bool PRESPLIT> struct Layout;
+template <> struct Layout<true> {
+  static constexpr int STAGES = 7;
+  static constexpr int OFF_WHI = X_BYTES;
+  static constexpr int OFF_WLO = OFF_WHI + W_BYTES;
+  static constexpr int OFF_WRAW = 0;                // unused
+  static constexpr int STAGE_BYTES = OFF_WLO + W_BYTES;   // 28 KB
+};
+template <> struct Layout<false> {
+  static constexpr int STAGES = 5;
+  static constexpr int OFF_WRAW = X_BYTES;
+  static constexpr int OFF_WHI = X_BYTES + WRAW_BYTES;
+  static constexpr int OFF_WLO = OFF_WHI + W_BYTES;
+  static constexpr int STAGE_BYTES = OFF_WLO + W_BYTES;   // 40 KB
+};
+template <bool PRESPLIT>
+constexpr int smem_bytes() { return Layout<PRESPLIT>::STAGES * Layout<PRESPLIT>::STAGE_BYTES + 1024; }
 }  // namespace coeffs
 
 struct CoeffsOut {
@@ -117,10 +131,14 @@ struct CoeffsOut {
   float* coef;    // [T, COEF_STRIDE] coefficient block, or nullptr
 };
 
+template <bool PRESPLIT>
 __global__ void __launch_bounds__(coeffs::THREADS, 1)
-    coeffs_tc_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__ CUtensorMap mapW, Params p,
-                     CoeffsOut o, int ntiles, int rows) {
+    coeffs_tc_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__ CUtensorMap mapW,
+                     const __grid_constant__ CUtensorMap mapWlo, Params p, CoeffsOut o, int ntiles, int rows) {
   using namespace coeffs;
+  using L = Layout<PRESPLIT>;
+  constexpr int STAGES = L::STAGES, STAGE_BYTES = L::STAGE_BYTES;
+  constexpr int OFF_WRAW = L::OFF_WRAW, OFF_WHI = L::OFF_WHI, OFF_WLO = L::OFF_WLO;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   __shared__ uint64_t full[STAGES], bready[STAGES], empty[STAGES], tfull[2], tempty[2], ssfull[2], ssempty[2];
@@ -147,6 +165,7 @@ __global__ void __launch_bounds__(coeffs::THREADS, 1)
     fence_mbar_init();
     tma_prefetch_desc(&mapX);
     tma_prefetch_desc(&mapW);
+    if (PRESPLIT) tma_prefetch_desc(&mapWlo);
   }
   if (warp == 1) {
     tmem_alloc(&tmem_slot, TMEM_COLS);
@@ -168,10 +187,15 @@ __global__ void __launch_bounds__(coeffs::THREADS, 1)
           const uint32_t ph = (it / STAGES) & 1;
           if (it >= STAGES && !mbar_wait(&empty[s], ph ^ 1, err, 11)) goto done_prod;
           uint8_t* st = smem + s * STAGE_BYTES;
-          mbar_expect_tx(&full[s], rows * KC * 2 + p.P * KC * 4);
+          mbar_expect_tx(&full[s], rows * KC * 2 + (PRESPLIT ? 2 * W_BYTES : p.P * KC * 4));
           const int n = kc / cchunks, c0 = (kc % cchunks) * KC;
           tma_load_3d(st, &mapX, &full[s], c0, n, tile * rows, pol_x);
-          tma_load_2d_f32(st + OFF_WRAW, &mapW, &full[s], kc * KC, 0, pol_w);
+          if (PRESPLIT) {
+            tma_load_2d(st + OFF_WHI, &mapW, &full[s], kc * KC, 0, pol_w);
+            tma_load_2d(st + OFF_WLO, &mapWlo, &full[s], kc * KC, 0, pol_w);
+          } else {
+            tma_load_2d_f32(st + OFF_WRAW, &mapW, &full[s], kc * KC, 0, pol_w);
+          }
         }
       }
     done_prod:;
@@ -189,7 +213,7 @@ __global__ void __launch_bounds__(coeffs::THREADS, 1)
         bool ok = true;
         for (int kc = 0; kc < nk; ++kc, ++it) {
           const int s = it % STAGES;
-          if (!mbar_wait(&bready[s], (it / STAGES) & 1, err, 13)) { ok = false; break; }
+          if (!mbar_wait(PRESPLIT ? &full[s] : &bready[s], (it / STAGES) & 1, err, 13)) { ok = false; break; }
           tc_fence_after();
           const uint32_t xs = smem_u32(smem + s * STAGE_BYTES);
 #pragma unroll
@@ -221,7 +245,7 @@ __global__ void __launch_bounds__(coeffs::THREADS, 1)
         if (!mbar_wait(&full[s], (it / STAGES) & 1, err, 14)) { ok = false; break; }
         uint8_t* stg = smem + s * STAGE_BYTES;
         // split W: 48 rows x 8 groups of 8 entries over the math threads
-        for (int u = mt; u < W_ROWS * 8; u += 32 * MATH_WARPS) {
+        for (int u = mt; !PRESPLIT && u < W_ROWS * 8; u += 32 * MATH_WARPS) {
           const int q = u >> 3, g = u & 7;
           uint4 h = make_uint4(0, 0, 0, 0), l = make_uint4(0, 0, 0, 0);
           if (q < p.P) {
@@ -242,9 +266,11 @@ __global__ void __launch_bounds__(coeffs::THREADS, 1)
           *reinterpret_cast<uint4*>(stg + OFF_WHI + sw128_offset(q, g * 16)) = h;
           *reinterpret_cast<uint4*>(stg + OFF_WLO + sw128_offset(q, g * 16)) = l;
         }
-        fence_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&bready[s]);   // the MMA may start; X is read below
+        if (!PRESPLIT) {
+          fence_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bready[s]);   // the MMA may start; X is read below
+        }
         const uint8_t* xr = stg + row * 128;
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
@@ -358,8 +384,35 @@ __global__ void __launch_bounds__(coeffs::THREADS, 1)
 
 bool tc_coeffs_supported(const Params& p) { return p.C % coeffs::KC == 0 && p.P <= coeffs::W_ROWS; }
 
-cudaError_t launch_coeffs_tc(const Params& p, const void* X, const float* W, float* hpre, float* hpost,
-                             float* hres, float* saved, float* coef, cudaStream_t st) {
+// W [P, N*C] fp32 -> bf16 hi and lo parts, each [48][N*C] (rows >= P zero):
+// Ws[col] = bf16(W), Ws[48 * NC + col] = bf16(W - hi).  One thread per 8
+// consecutive columns of one row.
+__global__ void w_split_kernel(const float* __restrict__ W, __nv_bfloat16* __restrict__ Ws, int P, size_t NC) {
+  const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const size_t groups = NC / 8;
+  if (i >= (size_t)coeffs::W_ROWS * groups) return;
+  const int q = (int)(i / groups);
+  const size_t c = (i % groups) * 8;
+  float w[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+  if (q < P) {
+    const float4 a = *reinterpret_cast<const float4*>(W + (size_t)q * NC + c);
+    const float4 b = *reinterpret_cast<const float4*>(W + (size_t)q * NC + c + 4);
+    w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w; w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+  }
+  uint32_t h[4], l[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    h[e] = pack_bf2(w[2 * e], w[2 * e + 1]);
+    l[e] = pack_bf2(w[2 * e] - bf_lo(h[e]), w[2 * e + 1] - bf_hi(h[e]));
+  }
+  *reinterpret_cast<uint4*>(Ws + (size_t)q * NC + c) = make_uint4(h[0], h[1], h[2], h[3]);
+  *reinterpret_cast<uint4*>(Ws + ((size_t)coeffs::W_ROWS + q) * NC + c) = make_uint4(l[0], l[1], l[2], l[3]);
+}
+
+size_t coeffs_wsplit_bytes(const Params& p) { return (size_t)2 * coeffs::W_ROWS * p.N * p.C * sizeof(uint16_t); }
+
+cudaError_t launch_coeffs_tc(const Params& p, const void* X, const float* W, void* Wsplit, float* hpre,
+                             float* hpost, float* hres, float* saved, float* coef, cudaStream_t st) {
   using namespace coeffs;
   const size_t T_all = (size_t)p.B * p.S;
   const size_t NC = (size_t)p.N * p.C;
@@ -368,26 +421,47 @@ cudaError_t launch_coeffs_tc(const Params& p, const void* X, const float* W, flo
   // the MMA always computes 128 rows and rows >= `rows` are ignored.
   const size_t per_sm = (T_all + sm_count() - 1) / sm_count();
   const int rows = (int)std::min<size_t>(TILE_T, std::max<size_t>(64, (per_sm + 7) / 8 * 8));
-  CUtensorMap mx, mw;
+  CUtensorMap mx, mw, mwl;
   {
     const uint64_t dims[3] = {(uint64_t)p.C, (uint64_t)p.N, T_all};
     const uint64_t strides[2] = {(uint64_t)p.C * 2, NC * 2};
     const uint32_t box[3] = {KC, 1, (uint32_t)rows};
     if (!make_map(&mx, X, 3, dims, strides, box)) return cudaErrorInvalidValue;
   }
-  {
+  const bool presplit = Wsplit != nullptr;
+  if (presplit) {
+    const __nv_bfloat16* ws = reinterpret_cast<const __nv_bfloat16*>(Wsplit);
+    const uint64_t dims[2] = {NC, (uint64_t)W_ROWS};
+    const uint64_t strides[1] = {NC * 2};
+    const uint32_t box[2] = {KC, (uint32_t)W_ROWS};
+    if (!make_map(&mw, ws, 2, dims, strides, box)) return cudaErrorInvalidValue;
+    if (!make_map(&mwl, ws + (size_t)W_ROWS * NC, 2, dims, strides, box)) return cudaErrorInvalidValue;
+  } else {
     const uint64_t dims[2] = {NC, (uint64_t)p.P};
     const uint64_t strides[1] = {NC * 4};
     const uint32_t box[2] = {KC, (uint32_t)p.P};
     if (!make_map(&mw, W, 2, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_DATA_TYPE_FLOAT32))
       return cudaErrorInvalidValue;
+    mwl = mw;
   }
   const int ntiles = (int)((T_all + rows - 1) / rows);
   const int grid = std::min(ntiles, sm_count());
-  cudaFuncSetAttribute(coeffs_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
   CoeffsOut o{hpre, hpost, hres, saved, coef};
-  timing_begin("coeffs_tc", st);
-  coeffs_tc_kernel<<<grid, THREADS, SMEM, st>>>(mx, mw, p, o, ntiles, rows);
+  if (presplit) {
+    const size_t threads = (size_t)W_ROWS * (NC / 8);
+    timing_begin("w_split", st);
+    w_split_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, st>>>(W, (__nv_bfloat16*)Wsplit, p.P, NC);
+    timing_end(st);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    cudaFuncSetAttribute(coeffs_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<true>());
+    timing_begin("coeffs_tc", st);
+    coeffs_tc_kernel<true><<<grid, THREADS, smem_bytes<true>(), st>>>(mx, mw, mwl, p, o, ntiles, rows);
+  } else {
+    cudaFuncSetAttribute(coeffs_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<false>());
+    timing_begin("coeffs_tc", st);
+    coeffs_tc_kernel<false><<<grid, THREADS, smem_bytes<false>(), st>>>(mx, mw, mwl, p, o, ntiles, rows);
+  }
   timing_end(st);
   return cudaGetLastError();
 }

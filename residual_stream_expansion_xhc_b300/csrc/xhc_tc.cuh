@@ -8,8 +8,12 @@ namespace xhc {
 bool tc_coeffs_supported(const Params& p);
 // Coefficients of every token (any of the outputs may be nullptr; `coef` is
 // the [T, COEF_STRIDE] block).  The dense read x_in is not computed here.
-cudaError_t launch_coeffs_tc(const Params& p, const void* X, const float* W, float* hpre, float* hpost, float* hres,
-                             float* saved, float* coef, cudaStream_t st);
+// With Wsplit (coeffs_wsplit_bytes() of scratch) W is split into bf16 hi and
+// lo parts once, by a small kernel, and the projection streams them; without
+// it the projection splits each fp32 W tile on chip.
+size_t coeffs_wsplit_bytes(const Params& p);
+cudaError_t launch_coeffs_tc(const Params& p, const void* X, const float* W, void* Wsplit, float* hpre,
+                             float* hpost, float* hres, float* saved, float* coef, cudaStream_t st);
 // Status recorded by bounded device-side waits (0: none); synchronises `st`
 // and clears the record.
 int read_device_error(cudaStream_t st);

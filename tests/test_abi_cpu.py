@@ -95,12 +95,13 @@ def test_null_and_alignment_rejected(lib):
 
 def test_forward_workspace_sizes(lib):
     L = lib.LIB
-    sh = shape(lib, B=3, S=100)                       # bf16, 300 tokens, P = 48
+    sh = shape(lib, B=3, S=100)                       # bf16, 300 tokens, P = 48, C = 256
     up = lambda b: (b + 255) // 256 * 256             # noqa: E731
     coef, z = up(300 * 48 * 4), up(300 * 49 * 4)
-    assert L.xhc_fwd_workspace_need(ctypes.byref(sh), 1) == coef
-    assert L.xhc_fwd_workspace_need(ctypes.byref(sh), 0) == coef + z
-    assert L.xhc_fwd_workspace_bytes(ctypes.byref(sh)) == coef + z
+    wsplit = up(2 * 48 * 16 * 256 * 2)                # bf16 hi and lo parts of W, 48 rows each
+    assert L.xhc_fwd_workspace_need(ctypes.byref(sh), 1) == coef + wsplit
+    assert L.xhc_fwd_workspace_need(ctypes.byref(sh), 0) == coef + wsplit + z
+    assert L.xhc_fwd_workspace_bytes(ctypes.byref(sh)) == coef + wsplit + z
     f32 = shape(lib, B=3, S=100, dtype=0)             # the fp32 path keeps no coefficient block
     assert L.xhc_fwd_workspace_need(ctypes.byref(f32), 1) == 0
     assert L.xhc_fwd_workspace_need(ctypes.byref(f32), 0) == z

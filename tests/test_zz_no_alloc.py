@@ -64,11 +64,11 @@ def test_noalloc_matches_workspace_path_twice(wl):
 
 
 def test_noalloc_refuses_calls_beyond_its_scratch():
-    # 30,000 bf16 tokens need 30,000 x (48 + 49) x 4 bytes > 8 MiB without
+    # 100,000 bf16 tokens need 100,000 x (48 + 49) x 4 bytes > 32 MiB without
     # `saved`: refused before any launch; with `saved` (48 x 4 bytes per
-    # token) they fit
-    sh = _lib.XhcShape(1, 30000, 16, 256, 4, _lib.XHC_BF16, 20, 1e-6)
-    assert api.xhc_fwd_workspace_need(sh, False) > 8 << 20 >= api.xhc_fwd_workspace_need(sh, True)
+    # token, plus the split copy of W) they fit
+    sh = _lib.XhcShape(1, 100000, 16, 256, 4, _lib.XHC_BF16, 20, 1e-6)
+    assert api.xhc_fwd_workspace_need(sh, False) > 32 << 20 >= api.xhc_fwd_workspace_need(sh, True)
     idx = (ctypes.c_int32 * 4)(0, 1, 2, 3)
     fake = ctypes.c_void_p(1 << 20)
     st = _lib.LIB.xhc_sublayer_fwd_noalloc(ctypes.byref(sh), fake, fake, fake, None, None, None, fake, idx, None,
