@@ -93,6 +93,16 @@ __device__ __forceinline__ void tma_load_2d_f32(void* dst, const CUtensorMap* ma
                                                 uint64_t policy) {
   tma_load_2d(dst, map, bar, x, y, policy);
 }
+// Non-tensor bulk copy of `bytes` contiguous bytes (16-byte aligned, a
+// multiple of 16) from global memory into this CTA's shared memory; completes
+// `bytes` transactions on `bar`.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                          uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;"
+      ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int x, int y, int z) {
   asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(map),
                "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)

@@ -102,17 +102,22 @@ constexpr int MATH_WARPS = 8;                     // two per scheduler: W split 
 constexpr int THREADS = 64 + 32 * MATH_WARPS;     // producer, MMA issuer, math warps
 constexpr int TMEM_COLS = 128;                    // 2 buffers x 64 columns
 // Stage layouts.  PRESPLIT: W arrives as bf16 hi and lo tiles split once per
-// call (w_split_kernel), so a stage is X + hi + lo.  Otherwise the fp32 W
+// call (w_split_kernel, which stores each stage's 12 KB as one contiguous,
+// already swizzled image), so a stage is X + hi + lo.  Otherwise the fp32 W
 // tile arrives and the math warps split it into hi and lo in the stage.
 template <bool PRESPLIT> struct Layout;
 template <> struct Layout<true> {
-  static constexpr int STAGES = 7;
-  static constexpr int OFF_WHI = X_BYTES;
+  static constexpr int BOXES = 2;                   // 64-entry chunks per stage: 256 contiguous bytes per row
+  static constexpr int STAGES = 4;
+  static constexpr int OFF_WHI = BOXES * X_BYTES;   // chunk b: hi at OFF_WHI + b WBOX, lo W_BYTES later
   static constexpr int OFF_WLO = OFF_WHI + W_BYTES;
+  static constexpr int WBOX = 2 * W_BYTES;
   static constexpr int OFF_WRAW = 0;                // unused
-  static constexpr int STAGE_BYTES = OFF_WLO + W_BYTES;   // 28 KB
+  static constexpr int STAGE_BYTES = OFF_WHI + BOXES * WBOX;   // 56 KB
 };
 template <> struct Layout<false> {
+  static constexpr int BOXES = 1;
+  static constexpr int WBOX = 0;
   static constexpr int STAGES = 5;
   static constexpr int OFF_WRAW = X_BYTES;
   static constexpr int OFF_WHI = X_BYTES + WRAW_BYTES;
@@ -129,6 +134,7 @@ struct CoeffsOut {
   float* hres;
   float* saved;
   float* coef;    // [T, COEF_STRIDE] coefficient block, or nullptr
+  const uint8_t* wsplit;   // stage images of the bf16 hi/lo split of W, or nullptr
 };
 
 template <bool PRESPLIT>
@@ -137,7 +143,7 @@ __global__ void __launch_bounds__(coeffs::THREADS, 1)
                      const __grid_constant__ CUtensorMap mapWlo, Params p, CoeffsOut o, int ntiles, int rows) {
   using namespace coeffs;
   using L = Layout<PRESPLIT>;
-  constexpr int STAGES = L::STAGES, STAGE_BYTES = L::STAGE_BYTES;
+  constexpr int STAGES = L::STAGES, STAGE_BYTES = L::STAGE_BYTES, BOXES = L::BOXES;
   constexpr int OFF_WRAW = L::OFF_WRAW, OFF_WHI = L::OFF_WHI, OFF_WLO = L::OFF_WLO;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
@@ -147,7 +153,7 @@ __global__ void __launch_bounds__(coeffs::THREADS, 1)
   int* err = &g_device_error;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int cchunks = p.C / KC;
+  const int cchunks = p.C / (KC * BOXES);
   const int nk = p.N * cchunks;                 // stages per tile
 
   if (threadIdx.x == 0) {
@@ -164,8 +170,7 @@ __global__ void __launch_bounds__(coeffs::THREADS, 1)
     }
     fence_mbar_init();
     tma_prefetch_desc(&mapX);
-    tma_prefetch_desc(&mapW);
-    if (PRESPLIT) tma_prefetch_desc(&mapWlo);
+    if (!PRESPLIT) tma_prefetch_desc(&mapW);
   }
   if (warp == 1) {
     tmem_alloc(&tmem_slot, TMEM_COLS);
@@ -187,12 +192,12 @@ __global__ void __launch_bounds__(coeffs::THREADS, 1)
           const uint32_t ph = (it / STAGES) & 1;
           if (it >= STAGES && !mbar_wait(&empty[s], ph ^ 1, err, 11)) goto done_prod;
           uint8_t* st = smem + s * STAGE_BYTES;
-          mbar_expect_tx(&full[s], rows * KC * 2 + (PRESPLIT ? 2 * W_BYTES : p.P * KC * 4));
-          const int n = kc / cchunks, c0 = (kc % cchunks) * KC;
-          tma_load_3d(st, &mapX, &full[s], c0, n, tile * rows, pol_x);
+          mbar_expect_tx(&full[s], BOXES * rows * KC * 2 + (PRESPLIT ? BOXES * 2 * W_BYTES : p.P * KC * 4));
+          const int n = kc / cchunks, c0 = (kc % cchunks) * KC * BOXES;
+#pragma unroll
+          for (int b = 0; b < BOXES; ++b) tma_load_3d(st + b * X_BYTES, &mapX, &full[s], c0 + b * KC, n, tile * rows, pol_x);
           if (PRESPLIT) {
-            tma_load_2d(st + OFF_WHI, &mapW, &full[s], kc * KC, 0, pol_w);
-            tma_load_2d(st + OFF_WLO, &mapWlo, &full[s], kc * KC, 0, pol_w);
+            bulk_load(st + OFF_WHI, o.wsplit + (size_t)kc * BOXES * 2 * W_BYTES, BOXES * 2 * W_BYTES, &full[s], pol_w);
           } else {
             tma_load_2d_f32(st + OFF_WRAW, &mapW, &full[s], kc * KC, 0, pol_w);
           }
@@ -217,12 +222,15 @@ __global__ void __launch_bounds__(coeffs::THREADS, 1)
           tc_fence_after();
           const uint32_t xs = smem_u32(smem + s * STAGE_BYTES);
 #pragma unroll
-          for (int ks = 0; ks < KC / 16; ++ks) {
-            const uint64_t a = sdesc_sw128(xs + ks * 32, 16, 1024);
-            const uint64_t bh = sdesc_sw128(xs + OFF_WHI + ks * 32, 16, 1024);
-            const uint64_t bl = sdesc_sw128(xs + OFF_WLO + ks * 32, 16, 1024);
-            umma_bf16(d, a, bh, idesc, (kc | ks) != 0);
-            umma_bf16(d, a, bl, idesc, 1);
+          for (int b = 0; b < BOXES; ++b) {
+#pragma unroll
+            for (int ks = 0; ks < KC / 16; ++ks) {
+              const uint64_t a = sdesc_sw128(xs + b * X_BYTES + ks * 32, 16, 1024);
+              const uint64_t bh = sdesc_sw128(xs + OFF_WHI + b * L::WBOX + ks * 32, 16, 1024);
+              const uint64_t bl = sdesc_sw128(xs + OFF_WLO + b * L::WBOX + ks * 32, 16, 1024);
+              umma_bf16(d, a, bh, idesc, (kc | b | ks) != 0);
+              umma_bf16(d, a, bl, idesc, 1);
+            }
           }
           umma_commit(&empty[s]);
         }
@@ -271,12 +279,14 @@ __global__ void __launch_bounds__(coeffs::THREADS, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(&bready[s]);   // the MMA may start; X is read below
         }
-        const uint8_t* xr = stg + row * 128;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          // physical 16-byte chunk (4 half + c + row) mod 8: the eight rows read
-          // by a phase of eight lanes fall in eight different bank groups
-          const uint4 v = *reinterpret_cast<const uint4*>(xr + 16 * ((4 * half + c + row) & 7));
+        for (int c = 0; c < 4 * BOXES; ++c) {
+          // the row's 8 BOXES 16-byte groups, half of them per math half;
+          // physical group (lin + row) mod 8 of box lin / 8: the eight rows
+          // read by a phase of eight lanes fall in eight different bank groups
+          const int lin = half * 4 * BOXES + c;
+          const uint8_t* xr = stg + (lin >> 3) * X_BYTES + row * 128;
+          const uint4 v = *reinterpret_cast<const uint4*>(xr + 16 * ((lin + row) & 7));
           const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
           for (int h = 0; h < 4; ++h) {
@@ -384,10 +394,13 @@ __global__ void __launch_bounds__(coeffs::THREADS, 1)
 
 bool tc_coeffs_supported(const Params& p) { return p.C % coeffs::KC == 0 && p.P <= coeffs::W_ROWS; }
 
-// W [P, N*C] fp32 -> bf16 hi and lo parts, each [48][N*C] (rows >= P zero):
-// Ws[col] = bf16(W), Ws[48 * NC + col] = bf16(W - hi).  One thread per 8
-// consecutive columns of one row.
-__global__ void w_split_kernel(const float* __restrict__ W, __nv_bfloat16* __restrict__ Ws, int P, size_t NC) {
+// W [P, N*C] fp32 -> bf16 hi and lo parts (rows >= P zero), stored tile by
+// tile in the exact shared-memory image a stage of the projection needs: for
+// each 64-column chunk kk, [hi: 48 rows x 128 B][lo: 48 rows x 128 B], each
+// row's eight 16-byte groups placed by the 128-byte swizzle (group g of row q
+// at (g ^ (q mod 8)) * 16).  One bulk copy then brings a stage's 12 KB.  One
+// thread per 8 consecutive columns of one row.
+__global__ void w_split_kernel(const float* __restrict__ W, uint8_t* __restrict__ Ws, int P, size_t NC) {
   const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
   const size_t groups = NC / 8;
   if (i >= (size_t)coeffs::W_ROWS * groups) return;
@@ -405,8 +418,12 @@ __global__ void w_split_kernel(const float* __restrict__ W, __nv_bfloat16* __res
     h[e] = pack_bf2(w[2 * e], w[2 * e + 1]);
     l[e] = pack_bf2(w[2 * e] - bf_lo(h[e]), w[2 * e + 1] - bf_hi(h[e]));
   }
-  *reinterpret_cast<uint4*>(Ws + (size_t)q * NC + c) = make_uint4(h[0], h[1], h[2], h[3]);
-  *reinterpret_cast<uint4*>(Ws + ((size_t)coeffs::W_ROWS + q) * NC + c) = make_uint4(l[0], l[1], l[2], l[3]);
+  const size_t kk = c / coeffs::KC;
+  const int g = (int)((c % coeffs::KC) / 8);
+  uint8_t* tile = Ws + kk * 2 * coeffs::W_BYTES;
+  const uint32_t off = sw128_offset(q, g * 16);
+  *reinterpret_cast<uint4*>(tile + off) = make_uint4(h[0], h[1], h[2], h[3]);
+  *reinterpret_cast<uint4*>(tile + coeffs::W_BYTES + off) = make_uint4(l[0], l[1], l[2], l[3]);
 }
 
 size_t coeffs_wsplit_bytes(const Params& p) { return (size_t)2 * coeffs::W_ROWS * p.N * p.C * sizeof(uint16_t); }
@@ -428,14 +445,10 @@ cudaError_t launch_coeffs_tc(const Params& p, const void* X, const float* W, voi
     const uint32_t box[3] = {KC, 1, (uint32_t)rows};
     if (!make_map(&mx, X, 3, dims, strides, box)) return cudaErrorInvalidValue;
   }
-  const bool presplit = Wsplit != nullptr;
+  const bool presplit = Wsplit != nullptr && p.C % (KC * Layout<true>::BOXES) == 0;
   if (presplit) {
-    const __nv_bfloat16* ws = reinterpret_cast<const __nv_bfloat16*>(Wsplit);
-    const uint64_t dims[2] = {NC, (uint64_t)W_ROWS};
-    const uint64_t strides[1] = {NC * 2};
-    const uint32_t box[2] = {KC, (uint32_t)W_ROWS};
-    if (!make_map(&mw, ws, 2, dims, strides, box)) return cudaErrorInvalidValue;
-    if (!make_map(&mwl, ws + (size_t)W_ROWS * NC, 2, dims, strides, box)) return cudaErrorInvalidValue;
+    mw = mx;                                    // unused: W comes by bulk copies
+    mwl = mx;
   } else {
     const uint64_t dims[2] = {NC, (uint64_t)p.P};
     const uint64_t strides[1] = {NC * 4};
@@ -446,11 +459,11 @@ cudaError_t launch_coeffs_tc(const Params& p, const void* X, const float* W, voi
   }
   const int ntiles = (int)((T_all + rows - 1) / rows);
   const int grid = std::min(ntiles, sm_count());
-  CoeffsOut o{hpre, hpost, hres, saved, coef};
+  CoeffsOut o{hpre, hpost, hres, saved, coef, (const uint8_t*)Wsplit};
   if (presplit) {
     const size_t threads = (size_t)W_ROWS * (NC / 8);
     timing_begin("w_split", st);
-    w_split_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, st>>>(W, (__nv_bfloat16*)Wsplit, p.P, NC);
+    w_split_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, st>>>(W, (uint8_t*)Wsplit, p.P, NC);
     timing_end(st);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
