@@ -50,8 +50,17 @@ __global__ void bwd_reduce_kernel(int conv_rows, int C, const float* __restrict_
   if (cpart) {
     for (size_t i = i0; i < (size_t)NTAPS * C; i += stride) {
       const int g = (int)(i / C), c = (int)(i % C);
+      // eight independent loads in flight, then a fixed-order sum
       float s = 0.0f;
-      for (int r = 0; r < conv_rows; ++r) s += cpart[((size_t)r * NTAPS + g) * C + c];
+      int r = 0;
+      for (; r + 8 <= conv_rows; r += 8) {
+        float v[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) v[q] = cpart[((size_t)(r + q) * NTAPS + g) * C + c];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) s += v[q];
+      }
+      for (; r < conv_rows; ++r) s += cpart[((size_t)r * NTAPS + g) * C + c];
       if (g < 4) dw4[(size_t)c * 4 + g] = s;
       else if (g < 12) dw8[(size_t)c * 8 + (g - 4)] = s;
       else dw12[(size_t)c * 12 + (g - 12)] = s;

@@ -104,13 +104,16 @@ __device__ __forceinline__ float sinkhorn_init(float z, bool valid) {
 }
 
 // One iteration; optionally records the matrices entering each step.
+// Each normalisation multiplies by the rounded reciprocal of the sum (one
+// reciprocal per row or column instead of a division per entry); the thread
+// version below does the same, so both produce identical values.
 __device__ __forceinline__ float sinkhorn_step(float M, bool valid, float* before_row, float* before_col) {
   if (before_row) *before_row = M;
   float s = rowsum16(M);
-  M = valid ? M / s : 0.0f;
+  M = valid ? M * __frcp_rn(s) : 0.0f;
   if (before_col) *before_col = M;
   s = colsum16(M);
-  M = valid ? M / s : 0.0f;
+  M = valid ? M * __frcp_rn(s) : 0.0f;
   return M;
 }
 
@@ -140,15 +143,15 @@ __device__ __forceinline__ void sinkhorn_thread(const float* z, int k, int iters
   for (int it = 0; it < iters; ++it) {
 #pragma unroll
     for (int i = 0; i < KMAX; ++i) {
-      const float s = (M[i][0] + M[i][1]) + (M[i][2] + M[i][3]);
+      const float r = __frcp_rn((M[i][0] + M[i][1]) + (M[i][2] + M[i][3]));
 #pragma unroll
-      for (int j = 0; j < KMAX; ++j) M[i][j] = (i < k && j < k) ? M[i][j] / s : 0.0f;
+      for (int j = 0; j < KMAX; ++j) M[i][j] = (i < k && j < k) ? M[i][j] * r : 0.0f;
     }
 #pragma unroll
     for (int j = 0; j < KMAX; ++j) {
-      const float s = (M[0][j] + M[1][j]) + (M[2][j] + M[3][j]);
+      const float r = __frcp_rn((M[0][j] + M[1][j]) + (M[2][j] + M[3][j]));
 #pragma unroll
-      for (int i = 0; i < KMAX; ++i) M[i][j] = (i < k && j < k) ? M[i][j] / s : 0.0f;
+      for (int i = 0; i < KMAX; ++i) M[i][j] = (i < k && j < k) ? M[i][j] * r : 0.0f;
     }
   }
 }

@@ -770,18 +770,20 @@ int bwd_stream_ranges(const Params& p) {
   const int blocks = p.N * (p.C / bwdtc::CB);
   const size_t tiles = ((size_t)p.B * p.S + bwdtc::TT - 1) / bwdtc::TT;
   if (tiles == 0) return 1;
+  // Fewest ranges whose last wave is within 2% of the best wave balance:
+  // every range writes a dW partial of P x N x C floats that the reduction
+  // reads back.
   const int sms = sm_count();
-  int best = 1;
+  double eff_r[17] = {0};
   double best_eff = 0.0;
   for (int r = 1; r <= 16 && (size_t)r <= tiles; ++r) {
     const long items = (long)blocks * r;
     const long waves = (items + sms - 1) / sms;
-    const double eff = (double)items / (double)(waves * sms);
-    if (eff > best_eff + 1e-3) {
-      best_eff = eff;
-      best = r;
-    }
+    eff_r[r] = (double)items / (double)(waves * sms);
+    best_eff = std::max(best_eff, eff_r[r]);
   }
+  int best = 1;
+  while (best < 16 && eff_r[best] < best_eff - 0.02) ++best;
   // no empty range: every range must own at least one tile
   const size_t per = (tiles + best - 1) / best;
   return (int)((tiles + per - 1) / per);
