@@ -389,35 +389,56 @@ __global__ void __launch_bounds__(THREADS, 2) fwd_update_kernel(Params p, UpdArg
 
 // ---------------------------------------------------------------- backward column pass
 //
-// Walks each segment from its last chunk to its first.  Per chunk:
-//   token phase (warp = token, lane = 8 channels)
+// CTA = 128 channels, 4 warps, three CTAs per SM; it walks a contiguous range
+// of 8-token chunks downwards (the anti-causal direction of the transposed
+// convolutions).  Per chunk:
+//   token phase (half-warp = token, lane = 8 channels)
 //     G_i = dX'[a_i], Xa_j (old active rows), u_c of the token
 //     mix   dX[a_j] = sum_i Hres[i][j] G_i
-//     du_c  = sum_i hpost[i][c] G_i  -> du rings (c >= 1), du0 (c = 0)
-//     dots  <G_i, Xa_j>, <G_i, u_c> (and <dx_in, X_n> with dx_in), reduced over
-//           the CTA's channels -> pdot[t][channel block]
-//     (and loads the `out` rows the next chunk's channel phase needs)
-//   channel phase (thread = channel; tokens t and t + 4 of the chunk paired in
-//   float2 lanes)
+//     du_c  = sum_i hpost[i][c] G_i: du_1..du_3 -> rings, du_0 kept in registers
+//     dots  <G_i, Xa_j>, <G_i, u_c> (and <dx_in, X_n> with dx_in) reduced over the
+//           CTA's channels -> pdot[t][channel block]
+//     dout of the previous chunk's token = du_0 + the convolution parts the
+//           channel phase left in shared memory
+//     (and the `out` rows the channel phase of this chunk needs next)
+//   channel phase (thread = two adjacent channels; threads 0-63 take the K = 4
+//   and K = 8 convolutions, threads 64-127 the K = 12 one: 12 taps each)
 //     u_1..u_3 of the next (earlier) chunk
-//     dout[t] = du_0[t] + sum_j sum_tau w_j[tau] du_j[t + tau]   (inside the sequence)
-//     dw_j[tau] += du_j[t] out[t - tau]
-// The du rows of the tokens after a segment that its convolutions reach (3, 7
-// and 11 for K = 4, 8, 12) are computed first: the anti-causal halo.  Each
-// du_j ring holds K_j - 1 + TT rows or more.  Conv-weight partials: one row
-// per CTA, [R][24][C].
+//     convolution parts of dout: sum_tau w_j[tau] du_j[t + tau] (inside the sequence)
+//     dw_j[tau] += du_j[t] out[t - tau], in registers for the whole walk
+// The du rows of the tokens after a walk's first chunk that its convolutions
+// reach (3, 7 and 11 for K = 4, 8, 12) are computed first: the anti-causal
+// halo.  Conv-weight partials: one row per CTA, [R][24][C].
 
-constexpr int DR1 = 12, DR2 = 16, DR3 = 20;
+namespace col {
+constexpr int CB = 128;                 // channels per CTA
+constexpr int THREADS = 128;
+constexpr int TT = 8;                   // tokens per chunk (4 warps x 2 half-warps)
+constexpr int ORING = 32;
+constexpr int D1 = 16, D2 = 16, D3 = 32;   // du ring rows: powers of two >= K_j - 1 + TT
+}  // namespace col
 
 struct ColSmem {
-  uint16_t ring[ORING][CB];          // out rows (bf16 bits)
-  uint16_t u[3][TT][CB];             // u_1..u_3 of the chunk (bf16: they only enter dots)
-  float du1[DR1][CB];
-  float du2[DR2][CB];
-  float du3[DR3][CB];
-  float du0[TT][CB];                 // du_0 of the chunk
-  float dw[NTAPS][CB];               // conv-weight gradient of the CTA's channels
+  uint16_t ring[col::ORING][col::CB];         // out rows (bf16 bits)
+  uint32_t u[3][col::TT][col::CB / 2];        // u_1..u_3 of the chunk, bf16 pairs (they only enter dots)
+  float du1[col::D1][col::CB];
+  float du2[col::D2][col::CB];
+  float du3[col::D3][col::CB];
+  float dconv[2][col::TT][col::CB];           // convolution parts of dout (K4 + K8 | K12)
+  float tap[NTAPS][col::CB];
 };
+
+Walk make_walk_col(const Params& p, int sms) {
+  Walk w;
+  w.nch = (p.S + col::TT - 1) / col::TT;
+  w.ncb = (p.C + col::CB - 1) / col::CB;
+  const long total = std::max(1L, (long)p.B * w.nch);
+  const long slots = std::max(1L, (long)(3 * sms) / w.ncb);
+  const long R = std::min(total, slots);
+  w.per = (total + R - 1) / R;
+  w.R = (int)((total + w.per - 1) / w.per);
+  return w;
+}
 
 __device__ __forceinline__ void store8f(float* d, const float2 (&v)[4]) {
   *reinterpret_cast<float4*>(d) = make_float4(v[0].x, v[0].y, v[1].x, v[1].y);
@@ -433,7 +454,7 @@ __device__ __forceinline__ uint4 pack8x2(const float2 (&v)[4]) {
   return make_uint4(pack_bf2(v[0].x, v[0].y), pack_bf2(v[1].x, v[1].y), pack_bf2(v[2].x, v[2].y),
                     pack_bf2(v[3].x, v[3].y));
 }
-// Streaming read that does not allocate in L1 (L1 keeps the conv taps).
+// Streaming read that does not allocate in L1.
 __device__ __forceinline__ uint4 ld_na(const __nv_bfloat16* p) {
   uint4 v;
   asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
@@ -442,6 +463,7 @@ __device__ __forceinline__ uint4 ld_na(const __nv_bfloat16* p) {
   return v;
 }
 __device__ __forceinline__ float2 f2(float a) { return make_float2(a, a); }
+__device__ __forceinline__ float2 bf2f(uint32_t w) { return make_float2(bf_lo(w), bf_hi(w)); }
 // dot of two 8-vectors held as float2 pairs
 __device__ __forceinline__ float dot8(const float2 (&a)[4], const float2 (&b)[4]) {
   float2 s = __fmul2_rn(a[0], b[0]);
@@ -450,58 +472,82 @@ __device__ __forceinline__ float dot8(const float2 (&a)[4], const float2 (&b)[4]
   s = __ffma2_rn(a[3], b[3], s);
   return s.x + s.y;
 }
-// ring slot of row base + i for a ring of R rows, base in [0, R), 0 <= i < R
-__device__ __forceinline__ int wrap(int base, int i, int R) {
-  const int r = base + i;
-  return r >= R ? r - R : r;
+// Sum 32 per-lane values over the 16 lanes of a half-warp: lane l ends with
+// the sums of values 2l and 2l + 1 (30 shuffles; both halves run it).
+__device__ __forceinline__ float2 half_transpose_sum32(float (&v)[32], int l16) {
+#pragma unroll
+  for (int o = 8; o >= 1; o >>= 1) {
+    const bool upper = (l16 & o) != 0;
+#pragma unroll
+    for (int i = 0; i < 2 * o; ++i) {
+      const float send = upper ? v[i] : v[i + 2 * o];
+      const float keep = upper ? v[i + 2 * o] : v[i];
+      v[i] = keep + __shfl_xor_sync(FULL, send, o);
+    }
+  }
+  return make_float2(v[0], v[1]);
+}
+// Sum 16 per-lane values over a half-warp: lane l ends with the sum of value l.
+__device__ __forceinline__ float half_transpose_sum16(float (&v)[16], int l16) {
+#pragma unroll
+  for (int o = 8; o >= 1; o >>= 1) {
+    const bool upper = (l16 & o) != 0;
+#pragma unroll
+    for (int i = 0; i < o; ++i) {
+      const float send = upper ? v[i] : v[i + o];
+      const float keep = upper ? v[i + o] : v[i];
+      v[i] = keep + __shfl_xor_sync(FULL, send, o);
+    }
+  }
+  return v[0];
 }
 
 template <bool HAS_CONV>
-__global__ void __launch_bounds__(THREADS, 2) bwd_col_kernel(Params p, BwdArgs<__nv_bfloat16> a,
-                                                             const float* __restrict__ coef, float* __restrict__ pdot,
-                                                             float* __restrict__ cpart, Walk wk) {
+__global__ void __launch_bounds__(col::THREADS, 3) bwd_col_kernel(Params p, BwdArgs<__nv_bfloat16> a,
+                                                                  const float* __restrict__ coef,
+                                                                  float* __restrict__ pdot, float* __restrict__ cpart,
+                                                                  Walk wk) {
+  constexpr int CBc = col::CB, TTc = col::TT, ORc = col::ORING;
   extern __shared__ __align__(16) uint8_t smem_raw[];
   ColSmem& sm = *reinterpret_cast<ColSmem*>(smem_raw);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, ch = threadIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int l16 = lane & 15, hw = 2 * warp + (lane >> 4);   // token slot of this half-warp
   const int N = p.N, k = p.k, C = p.C, S = p.S;
   const size_t NC = (size_t)N * C;
-  const int cb = blockIdx.y, cb0 = cb * CB;
-  const int c_lane = cb0 + 8 * lane;
+  const int cb = blockIdx.y, cb0 = cb * CBc;
+  const int c_lane = cb0 + 8 * l16;
   const bool lane_ok = c_lane < C;
-  const int c_ch = cb0 + ch;
-  if (HAS_CONV) {
-#pragma unroll
-    for (int g = 0; g < NTAPS; ++g) sm.dw[g][ch] = 0.0f;
-  }
+  const int pr = threadIdx.x & 63, grp = threadIdx.x >> 6;  // channel phase: pair, convolution group
+  const int c2 = cb0 + 2 * pr;
+  const bool pair_ok = c2 < C;
   const int ncb = wk.ncb;
+  if (HAS_CONV) {
+    float t[NTAPS];
+    load_taps(a.w, cb0 + threadIdx.x, C, t);
+#pragma unroll
+    for (int g = 0; g < NTAPS; ++g) sm.tap[g][threadIdx.x] = t[g];
+  }
+  float2 dw[12];                                            // this group's 12 taps, two channels
+#pragma unroll
+  for (int q = 0; q < 12; ++q) dw[q] = make_float2(0.0f, 0.0f);
+  float2 du0r[4];                                           // du_0 of the token awaiting its dout
+  bool fin = false;
+  size_t fin_tok = 0;
 
-  // u_1..u_3 of the chunk t0 .. t0+7 (tokens < s_end) from ring rows t0-11 .. t0+7
-  auto tfa_pairs = [&](const float (&tap)[NTAPS], int t0, int s_end) {
-    float2 Q[TT / 2 + HALO];                   // (row t0-11+i, row t0-7+i)
-#pragma unroll
-    for (int i = 0; i < TT / 2 + HALO; ++i)
-      Q[i] = make_float2(bf16_bits(sm.ring[(t0 - HALO + i) & (ORING - 1)][ch]),
-                         bf16_bits(sm.ring[(t0 - HALO + 4 + i) & (ORING - 1)][ch]));
-#pragma unroll
-    for (int tt = 0; tt < TT / 2; ++tt) {
-      float2 u1 = make_float2(0.0f, 0.0f), u2 = u1, u3 = u1;
-#pragma unroll
-      for (int tau = 0; tau < 4; ++tau) u1 = __ffma2_rn(f2(tap[tau]), Q[tt + HALO - tau], u1);
-#pragma unroll
-      for (int tau = 0; tau < 8; ++tau) u2 = __ffma2_rn(f2(tap[4 + tau]), Q[tt + HALO - tau], u2);
-#pragma unroll
-      for (int tau = 0; tau < 12; ++tau) u3 = __ffma2_rn(f2(tap[12 + tau]), Q[tt + HALO - tau], u3);
-      if (t0 + tt < s_end) {
-        sm.u[0][tt][ch] = __bfloat16_as_ushort(__float2bfloat16_rn(u1.x));
-        sm.u[1][tt][ch] = __bfloat16_as_ushort(__float2bfloat16_rn(u2.x));
-        sm.u[2][tt][ch] = __bfloat16_as_ushort(__float2bfloat16_rn(u3.x));
-      }
-      if (t0 + tt + 4 < s_end) {
-        sm.u[0][tt + 4][ch] = __bfloat16_as_ushort(__float2bfloat16_rn(u1.y));
-        sm.u[1][tt + 4][ch] = __bfloat16_as_ushort(__float2bfloat16_rn(u2.y));
-        sm.u[2][tt + 4][ch] = __bfloat16_as_ushort(__float2bfloat16_rn(u3.y));
-      }
+  auto finalize = [&]() {                                   // dout of token fin_tok (slot hw)
+    if (fin && lane_ok) {
+      const float4 a0 = *reinterpret_cast<const float4*>(&sm.dconv[0][hw][8 * l16]);
+      const float4 a1 = *reinterpret_cast<const float4*>(&sm.dconv[0][hw][8 * l16 + 4]);
+      const float4 b0 = *reinterpret_cast<const float4*>(&sm.dconv[1][hw][8 * l16]);
+      const float4 b1 = *reinterpret_cast<const float4*>(&sm.dconv[1][hw][8 * l16 + 4]);
+      float2 d[4];
+      d[0] = make_float2(du0r[0].x + (a0.x + b0.x), du0r[0].y + (a0.y + b0.y));
+      d[1] = make_float2(du0r[1].x + (a0.z + b0.z), du0r[1].y + (a0.w + b0.w));
+      d[2] = make_float2(du0r[2].x + (a1.x + b1.x), du0r[2].y + (a1.y + b1.y));
+      d[3] = make_float2(du0r[3].x + (a1.z + b1.z), du0r[3].y + (a1.w + b1.w));
+      st_stream(a.dout + fin_tok * C + c_lane, pack8x2(d));
     }
+    fin = false;
   };
 
   // du_1..du_3 of a halo token t (lane's channels): rows the convolutions reach
@@ -528,9 +574,43 @@ __global__ void __launch_bounds__(THREADS, 2) bwd_col_kernel(Params p, BwdArgs<_
       }
     }
     const int d = t - s_end;                   // 0 .. 10
-    if (d < 3) store8f(&sm.du1[t % DR1][8 * lane], du[0]);
-    if (d < 7) store8f(&sm.du2[t % DR2][8 * lane], du[1]);
-    store8f(&sm.du3[t % DR3][8 * lane], du[2]);
+    if (d < 3) store8f(&sm.du1[t & (col::D1 - 1)][8 * l16], du[0]);
+    if (d < 7) store8f(&sm.du2[t & (col::D2 - 1)][8 * l16], du[1]);
+    store8f(&sm.du3[t & (col::D3 - 1)][8 * l16], du[2]);
+  };
+
+  // u_1..u_3 of chunk tc (8 tokens, all < s_end) from ring rows tc - 11 .. tc + 7
+  auto tfa_chunk = [&](const float2 (&tp)[12], int tc, int s_end) {
+    float2 ow[TTc + HALO];
+#pragma unroll
+    for (int i = 0; i < TTc + HALO; ++i)
+      ow[i] = bf2f(*reinterpret_cast<const uint32_t*>(&sm.ring[(tc - HALO + i) & (ORc - 1)][2 * pr]));
+#pragma unroll
+    for (int tt = 0; tt < TTc; ++tt) {
+      float2 x = make_float2(0.0f, 0.0f), y = x;
+      if (grp == 0) {
+#pragma unroll
+        for (int tau = 0; tau < 4; ++tau) x = __ffma2_rn(tp[tau], ow[tt + HALO - tau], x);
+#pragma unroll
+        for (int tau = 0; tau < 8; ++tau) y = __ffma2_rn(tp[4 + tau], ow[tt + HALO - tau], y);
+      } else {
+#pragma unroll
+        for (int tau = 0; tau < 12; ++tau) x = __ffma2_rn(tp[tau], ow[tt + HALO - tau], x);
+      }
+      if (tc + tt < s_end) {
+        if (grp == 0) {
+          sm.u[0][tt][pr] = pack_bf2(x.x, x.y);
+          sm.u[1][tt][pr] = pack_bf2(y.x, y.y);
+        } else {
+          sm.u[2][tt][pr] = pack_bf2(x.x, x.y);
+        }
+      }
+    }
+  };
+
+  auto load_tap_pairs = [&](float2 (&tp)[12]) {
+#pragma unroll
+    for (int q = 0; q < 12; ++q) tp[q] = *reinterpret_cast<const float2*>(&sm.tap[12 * grp + q][2 * pr]);
   };
 
   const long g_beg = (long)blockIdx.x * wk.per;
@@ -539,233 +619,262 @@ __global__ void __launch_bounds__(THREADS, 2) bwd_col_kernel(Params p, BwdArgs<_
   bool start = true;
   for (long g = g_end - 1; g >= g_beg; --g) {
     const int b = (int)(g / wk.nch), m = (int)(g % wk.nch);
-    const int t0 = m * TT;
-    const int s_end = min(t0 + TT, S);         // tokens of this chunk: t0 .. s_end - 1
+    const int t0 = m * TTc;
+    const int s_end = min(t0 + TTc, S);        // tokens of this chunk: t0 .. s_end - 1
     const size_t seq_base = (size_t)b * S;
-    const bool has_next = g - 1 >= g_beg && m > 0;    // the next chunk walked is t0 - TT, same sequence
+    const bool has_next = g - 1 >= g_beg && m > 0;   // the next chunk walked is t0 - TT, same sequence
     if (start) {
       __syncthreads();                         // the previous walk is done with shared memory
       if (HAS_CONV) {
-        // out rows of this chunk and the du rows of the tokens above it that
-        // its convolutions reach
-        load_out_rows(sm.ring, a.out, seq_base, S, C, c_lane, t0 - HALO, t0 + TT, warp, lane);
+        // out rows t0 - 11 .. t0 + 7 (a half-warp per row), all loads before the stores
+        uint4 v[3];
+#pragma unroll
+        for (int q = 0; q < 3; ++q) {
+          const int r = t0 - HALO + hw + 8 * q;
+          v[q] = r < t0 + TTc ? fetch_out_row(a.out, seq_base, S, C, c_lane, r) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int q = 0; q < 3; ++q) {
+          const int r = t0 - HALO + hw + 8 * q;
+          if (r < t0 + TTc) *reinterpret_cast<uint4*>(&sm.ring[r & (ORc - 1)][8 * l16]) = v[q];
+        }
         if (lane_ok) {
-          for (int t = s_end + warp; t < min(s_end + HALO, S); t += TT) du_halo(seq_base, t, s_end);
+          for (int t = s_end + hw; t < min(s_end + HALO, S); t += TTc) du_halo(seq_base, t, s_end);
         }
         __syncthreads();
-        if (c_ch < C) {
-          float tap[NTAPS];
-          load_taps(a.w, c_ch, C, tap);
-          tfa_pairs(tap, t0, s_end);
+        if (pair_ok) {
+          float2 tp[12];
+          load_tap_pairs(tp);
+          tfa_chunk(tp, t0, s_end);
         }
         __syncthreads();
       }
     }
     start = !has_next;
-    {
-      // ------------------------------------------------ token phase
-      const bool refill = HAS_CONV && has_next;
-      uint4 next_row;
-      if (refill) next_row = fetch_out_row(a.out, seq_base, S, C, c_lane, t0 - TT - HALO + warp);
-      const int t = t0 + warp;
-      if (t < s_end) {                         // warp-uniform
-        const size_t tok = seq_base + t;
-        const float* cf = coef + tok * COEF_STRIDE;
-        float2 G[KMAX][4];
-        uint4 xr[KMAX];
+    // ------------------------------------------------ token phase
+    const bool refill = HAS_CONV && has_next;
+    uint4 next_row;
+    if (refill) next_row = fetch_out_row(a.out, seq_base, S, C, c_lane, t0 - TTc - HALO + hw);
+    if (HAS_CONV) finalize();                  // dout of the previous chunk's token of this slot
+    const int t = t0 + hw;
+    const bool tok_ok = t < s_end;             // per half-warp
+    const size_t tok = seq_base + (tok_ok ? t : t0);
+    const float* cf = coef + tok * COEF_STRIDE;
+    float2 G[KMAX][4];
+    uint4 xr[KMAX];
 #pragma unroll
-        for (int i = 0; i < KMAX; ++i) {
-          xr[i] = make_uint4(0, 0, 0, 0);
+    for (int i = 0; i < KMAX; ++i) {
+      xr[i] = make_uint4(0, 0, 0, 0);
 #pragma unroll
-          for (int q = 0; q < 4; ++q) G[i][q] = make_float2(0.0f, 0.0f);
+      for (int q = 0; q < 4; ++q) G[i][q] = make_float2(0.0f, 0.0f);
+    }
+    if (tok_ok && lane_ok) {
+      uint4 gr[KMAX];
+#pragma unroll
+      for (int i = 0; i < KMAX; ++i) {
+        if (i < k) {
+          gr[i] = ld_na(a.dXp + tok * NC + (size_t)p.idx[i] * C + c_lane);
+          xr[i] = a.saved_active ? ld_na(a.saved_active + (tok * k + i) * C + c_lane)
+                                 : ld_na(a.X + tok * NC + (size_t)p.idx[i] * C + c_lane);
         }
-        if (lane_ok) {
-          uint4 gr[KMAX];
+      }
 #pragma unroll
-          for (int i = 0; i < KMAX; ++i) {
-            if (i < k) {
-              gr[i] = ld_na(a.dXp + tok * NC + (size_t)p.idx[i] * C + c_lane);
-              xr[i] = a.saved_active ? ld_na(a.saved_active + (tok * k + i) * C + c_lane)
-                                     : ld_na(a.X + tok * NC + (size_t)p.idx[i] * C + c_lane);
-            }
-          }
+      for (int i = 0; i < KMAX; ++i)
+        if (i < k) unpack8x2(gr[i], G[i]);
+      // active-stream mix: dX[a_j] = sum_i Hres[i][j] G_i
+      float hres[KMAX][KMAX];
+#pragma unroll
+      for (int i = 0; i < KMAX; ++i) {
+        const float4 h = *reinterpret_cast<const float4*>(cf + COEF_RES + 4 * i);
+        hres[i][0] = h.x; hres[i][1] = h.y; hres[i][2] = h.z; hres[i][3] = h.w;
+      }
+#pragma unroll
+      for (int j = 0; j < KMAX; ++j) {
+        if (j < k) {
+          float2 mx[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) mx[q] = make_float2(0.0f, 0.0f);
 #pragma unroll
           for (int i = 0; i < KMAX; ++i)
-            if (i < k) unpack8x2(gr[i], G[i]);
-          // active-stream mix: dX[a_j] = sum_i Hres[i][j] G_i
-          float hres[KMAX][KMAX];
+            if (i < k)
 #pragma unroll
-          for (int i = 0; i < KMAX; ++i) {
-            const float4 h = *reinterpret_cast<const float4*>(cf + COEF_RES + 4 * i);
-            hres[i][0] = h.x; hres[i][1] = h.y; hres[i][2] = h.z; hres[i][3] = h.w;
-          }
-#pragma unroll
-          for (int j = 0; j < KMAX; ++j) {
-            if (j < k) {
-              float2 mx[4];
-#pragma unroll
-              for (int q = 0; q < 4; ++q) mx[q] = make_float2(0.0f, 0.0f);
-#pragma unroll
-              for (int i = 0; i < KMAX; ++i)
-                if (i < k)
-#pragma unroll
-                  for (int q = 0; q < 4; ++q) mx[q] = __ffma2_rn(f2(hres[i][j]), G[i][q], mx[q]);
-              st_stream(a.dX + tok * NC + (size_t)p.idx[j] * C + c_lane, pack8x2(mx));
-            }
-          }
-          // du_c = sum_i hpost[i][c] G_i
-          {
-            float2 du[4][4];
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-#pragma unroll
-              for (int q = 0; q < 4; ++q) du[c][q] = make_float2(0.0f, 0.0f);
-#pragma unroll
-            for (int i = 0; i < KMAX; ++i) {
-              if (i < k) {
-                const float4 hp = *reinterpret_cast<const float4*>(cf + COEF_POST + 4 * i);
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                  du[0][q] = __ffma2_rn(f2(hp.x), G[i][q], du[0][q]);
-                  du[1][q] = __ffma2_rn(f2(hp.y), G[i][q], du[1][q]);
-                  du[2][q] = __ffma2_rn(f2(hp.z), G[i][q], du[2][q]);
-                  du[3][q] = __ffma2_rn(f2(hp.w), G[i][q], du[3][q]);
-                }
-              }
-            }
-            if (HAS_CONV) {
-              store8f(&sm.du0[warp][8 * lane], du[0]);
-              store8f(&sm.du1[t % DR1][8 * lane], du[1]);
-              store8f(&sm.du2[t % DR2][8 * lane], du[2]);
-              store8f(&sm.du3[t % DR3][8 * lane], du[3]);
-            } else {
-              st_stream(a.dout + tok * C + c_lane, pack8x2(du[0]));
-            }
-          }
-        }
-        // dots over this lane's channels: [0,16) <G_i, Xa_j> at 4i+j, [16,32) <G_i, u_c> at 16+4i+c
-        float v[32];
-#pragma unroll
-        for (int q = 0; q < 32; ++q) v[q] = 0.0f;
-        if (lane_ok) {
-#pragma unroll
-          for (int j = 0; j < KMAX; ++j) {
-            if (j < k) {
-              float2 xv[4];
-              unpack8x2(xr[j], xv);
-#pragma unroll
-              for (int i = 0; i < KMAX; ++i)
-                if (i < k) v[4 * i + j] = dot8(G[i], xv);
-            }
-          }
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            if (!HAS_CONV && c > 0) break;
-            float2 uv[4];
-            if (c == 0) {
-              if (HAS_CONV) unpack8x2(*reinterpret_cast<const uint4*>(&sm.ring[t & (ORING - 1)][8 * lane]), uv);
-              else unpack8x2(ld_na(a.out + tok * C + c_lane), uv);
-            } else {
-              unpack8x2(*reinterpret_cast<const uint4*>(&sm.u[c - 1][warp][8 * lane]), uv);
-            }
-#pragma unroll
-            for (int i = 0; i < KMAX; ++i)
-              if (i < k) v[16 + 4 * i + c] = dot8(G[i], uv);
-          }
-        }
-        // sum over the CTA's channels (all lanes take part)
-        float* pd = pdot + (tok * ncb + cb) * PDOT;
-        pd[lane] = warp_transpose_sum32(v, lane);
-        if (a.dx_in) {
-          // <dx_in, X_n> for every stream n
-#pragma unroll
-          for (int q = 0; q < 32; ++q) v[q] = 0.0f;
-          if (lane_ok) {
-            float2 g[4];
-            unpack8x2(ld_na(a.dx_in + tok * C + c_lane), g);
-#pragma unroll
-            for (int n = 0; n < NMAX; ++n) {
-              if (n < N) {
-                const int slot = p.is_active[n];
-                const __nv_bfloat16* src = slot ? (a.saved_active ? a.saved_active + (tok * k + slot - 1) * C + c_lane
-                                                                  : a.X + tok * NC + (size_t)n * C + c_lane)
-                                                : a.X + tok * NC + (size_t)n * C + c_lane;
-                float2 xv[4];
-                unpack8x2(ld_na(src), xv);
-                v[n] = dot8(g, xv);
-              }
-            }
-          }
-          const float r = warp_transpose_sum32(v, lane);
-          if (lane < 16) pd[32 + lane] = r;
+              for (int q = 0; q < 4; ++q) mx[q] = __ffma2_rn(f2(hres[i][j]), G[i][q], mx[q]);
+          st_stream(a.dX + tok * NC + (size_t)p.idx[j] * C + c_lane, pack8x2(mx));
         }
       }
-      if (!HAS_CONV) continue;
-      if (refill) commit_out_row(sm.ring, t0 - TT - HALO + warp, lane, next_row);
-      float tap[NTAPS];
-      load_taps(a.w, c_ch, C, tap);            // in flight across the barrier
-      __syncthreads();
-      // ------------------------------------------------ channel phase
-      if (c_ch < C) {
-        if (has_next) tfa_pairs(tap, t0 - TT, t0);
-        // dout of the chunk tokens: pairs of du rows (t0 + i, t0 + 4 + i), zero past the sequence end
-        const int b1 = t0 % DR1, b2 = t0 % DR2, b3 = t0 % DR3;
-        float2 P1[TT / 2 + 3], P2[TT / 2 + 7], P3[TT / 2 + 11];
+      // du_c = sum_i hpost[i][c] G_i
+      float2 du[4][4];
 #pragma unroll
-        for (int i = 0; i < TT / 2 + 11; ++i) {
-          const bool in0 = t0 + i < S, in1 = t0 + 4 + i < S;
-          if (i < TT / 2 + 3)
-            P1[i] = make_float2(in0 ? sm.du1[wrap(b1, i, DR1)][ch] : 0.0f, in1 ? sm.du1[wrap(b1, i + 4, DR1)][ch] : 0.0f);
-          if (i < TT / 2 + 7)
-            P2[i] = make_float2(in0 ? sm.du2[wrap(b2, i, DR2)][ch] : 0.0f, in1 ? sm.du2[wrap(b2, i + 4, DR2)][ch] : 0.0f);
-          P3[i] = make_float2(in0 ? sm.du3[wrap(b3, i, DR3)][ch] : 0.0f, in1 ? sm.du3[wrap(b3, i + 4, DR3)][ch] : 0.0f);
-        }
+      for (int c = 0; c < 4; ++c)
 #pragma unroll
-        for (int tt = 0; tt < TT / 2; ++tt) {
-          float2 d = make_float2(sm.du0[tt][ch], sm.du0[tt + 4][ch]);
+        for (int q = 0; q < 4; ++q) du[c][q] = make_float2(0.0f, 0.0f);
 #pragma unroll
-          for (int tau = 0; tau < 4; ++tau) d = __ffma2_rn(f2(tap[tau]), P1[tt + tau], d);
+      for (int i = 0; i < KMAX; ++i) {
+        if (i < k) {
+          const float4 hp = *reinterpret_cast<const float4*>(cf + COEF_POST + 4 * i);
 #pragma unroll
-          for (int tau = 0; tau < 8; ++tau) d = __ffma2_rn(f2(tap[4 + tau]), P2[tt + tau], d);
-#pragma unroll
-          for (int tau = 0; tau < 12; ++tau) d = __ffma2_rn(f2(tap[12 + tau]), P3[tt + tau], d);
-          if (t0 + tt < s_end) a.dout[(seq_base + t0 + tt) * C + c_ch] = __float2bfloat16_rn(d.x);
-          if (t0 + tt + 4 < s_end) a.dout[(seq_base + t0 + tt + 4) * C + c_ch] = __float2bfloat16_rn(d.y);
-        }
-        // dw_j[tau] += du_j[t] out[t - tau] over the chunk tokens (tokens >= s_end masked)
-        float2 O[TT / 2 + HALO];               // (row t0-11+i, row t0-7+i)
-#pragma unroll
-        for (int i = 0; i < TT / 2 + HALO; ++i)
-          O[i] = make_float2(bf16_bits(sm.ring[(t0 - HALO + i) & (ORING - 1)][ch]),
-                             bf16_bits(sm.ring[(t0 - HALO + 4 + i) & (ORING - 1)][ch]));
-        float2 E1[TT / 2], E2[TT / 2], E3[TT / 2];
-#pragma unroll
-        for (int tt = 0; tt < TT / 2; ++tt) {
-          const bool v0 = t0 + tt < s_end, v1 = t0 + tt + 4 < s_end;
-          E1[tt] = make_float2(v0 ? P1[tt].x : 0.0f, v1 ? P1[tt].y : 0.0f);
-          E2[tt] = make_float2(v0 ? P2[tt].x : 0.0f, v1 ? P2[tt].y : 0.0f);
-          E3[tt] = make_float2(v0 ? P3[tt].x : 0.0f, v1 ? P3[tt].y : 0.0f);
-        }
-#pragma unroll
-        for (int g = 0; g < NTAPS; ++g) {
-          const int tau = g < 4 ? g : (g < 12 ? g - 4 : g - 12);
-          float2 acc = make_float2(0.0f, 0.0f);
-#pragma unroll
-          for (int tt = 0; tt < TT / 2; ++tt) {
-            const float2 e = g < 4 ? E1[tt] : (g < 12 ? E2[tt] : E3[tt]);
-            acc = __ffma2_rn(e, O[tt + HALO - tau], acc);
+          for (int q = 0; q < 4; ++q) {
+            du[0][q] = __ffma2_rn(f2(hp.x), G[i][q], du[0][q]);
+            du[1][q] = __ffma2_rn(f2(hp.y), G[i][q], du[1][q]);
+            du[2][q] = __ffma2_rn(f2(hp.z), G[i][q], du[2][q]);
+            du[3][q] = __ffma2_rn(f2(hp.w), G[i][q], du[3][q]);
           }
-          sm.dw[g][ch] += acc.x + acc.y;
         }
       }
-      __syncthreads();
+      if (HAS_CONV) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) du0r[q] = du[0][q];
+        store8f(&sm.du1[t & (col::D1 - 1)][8 * l16], du[1]);
+        store8f(&sm.du2[t & (col::D2 - 1)][8 * l16], du[2]);
+        store8f(&sm.du3[t & (col::D3 - 1)][8 * l16], du[3]);
+      } else {
+        st_stream(a.dout + tok * C + c_lane, pack8x2(du[0]));
+      }
     }
-  }
-  if (HAS_CONV && c_ch < C) {
-    __syncthreads();
-    float* dst = cpart + (size_t)blockIdx.x * NTAPS * C + c_ch;
+    if (HAS_CONV && tok_ok) {
+      fin = true;
+      fin_tok = tok;
+    }
+    // dots over this lane's channels: [0,16) <G_i, Xa_j> at 4i+j, [16,32) <G_i, u_c> at 16+4i+c
+    float v[32];
 #pragma unroll
-    for (int g = 0; g < NTAPS; ++g) dst[(size_t)g * C] = sm.dw[g][ch];
+    for (int q = 0; q < 32; ++q) v[q] = 0.0f;
+    if (tok_ok && lane_ok) {
+#pragma unroll
+      for (int j = 0; j < KMAX; ++j) {
+        if (j < k) {
+          float2 xv[4];
+          unpack8x2(xr[j], xv);
+#pragma unroll
+          for (int i = 0; i < KMAX; ++i)
+            if (i < k) v[4 * i + j] = dot8(G[i], xv);
+        }
+      }
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        if (!HAS_CONV && c > 0) break;
+        float2 uv[4];
+        if (c == 0) {
+          if (HAS_CONV) unpack8x2(*reinterpret_cast<const uint4*>(&sm.ring[t & (ORc - 1)][8 * l16]), uv);
+          else unpack8x2(ld_na(a.out + tok * C + c_lane), uv);
+        } else {
+          unpack8x2(*reinterpret_cast<const uint4*>(&sm.u[c - 1][hw][4 * l16]), uv);
+        }
+#pragma unroll
+        for (int i = 0; i < KMAX; ++i)
+          if (i < k) v[16 + 4 * i + c] = dot8(G[i], uv);
+      }
+    }
+    {
+      const float2 r = half_transpose_sum32(v, l16);
+      if (tok_ok) *reinterpret_cast<float2*>(pdot + (tok * ncb + cb) * PDOT + 2 * l16) = r;
+    }
+    if (a.dx_in) {
+      // <dx_in, X_n> for every stream n
+      float w2[16];
+#pragma unroll
+      for (int q = 0; q < 16; ++q) w2[q] = 0.0f;
+      if (tok_ok && lane_ok) {
+        float2 gx[4];
+        unpack8x2(ld_na(a.dx_in + tok * C + c_lane), gx);
+#pragma unroll
+        for (int n = 0; n < NMAX; ++n) {
+          if (n < N) {
+            const int slot = p.is_active[n];
+            const __nv_bfloat16* src = slot ? (a.saved_active ? a.saved_active + (tok * k + slot - 1) * C + c_lane
+                                                              : a.X + tok * NC + (size_t)n * C + c_lane)
+                                            : a.X + tok * NC + (size_t)n * C + c_lane;
+            float2 xv[4];
+            unpack8x2(ld_na(src), xv);
+            w2[n] = dot8(gx, xv);
+          }
+        }
+      }
+      const float r = half_transpose_sum16(w2, l16);
+      if (tok_ok) pdot[(tok * ncb + cb) * PDOT + 32 + l16] = r;
+    }
+    if (refill) *reinterpret_cast<uint4*>(&sm.ring[(t0 - TTc - HALO + hw) & (ORc - 1)][8 * l16]) = next_row;
+    if (!HAS_CONV) continue;
+    __syncthreads();
+    // ------------------------------------------------ channel phase
+    if (pair_ok) {
+      float2 tp[12];
+      load_tap_pairs(tp);
+      if (has_next) tfa_chunk(tp, t0 - TTc, t0);
+      // convolution parts of dout: du rows t0 .. t0 + 18, zero past the sequence end
+      float2 part[TTc];
+      if (grp == 0) {
+        float2 d1[TTc + 3], d2[TTc + 7];
+#pragma unroll
+        for (int i = 0; i < TTc + 7; ++i) {
+          const bool in = t0 + i < S;
+          if (i < TTc + 3) d1[i] = in ? *reinterpret_cast<const float2*>(&sm.du1[(t0 + i) & (col::D1 - 1)][2 * pr])
+                                      : make_float2(0.0f, 0.0f);
+          d2[i] = in ? *reinterpret_cast<const float2*>(&sm.du2[(t0 + i) & (col::D2 - 1)][2 * pr])
+                     : make_float2(0.0f, 0.0f);
+        }
+#pragma unroll
+        for (int tt = 0; tt < TTc; ++tt) {
+          float2 d = make_float2(0.0f, 0.0f);
+#pragma unroll
+          for (int tau = 0; tau < 4; ++tau) d = __ffma2_rn(tp[tau], d1[tt + tau], d);
+#pragma unroll
+          for (int tau = 0; tau < 8; ++tau) d = __ffma2_rn(tp[4 + tau], d2[tt + tau], d);
+          part[tt] = d;
+        }
+        // dw: this chunk's tokens only
+        float2 ow[TTc + HALO];
+#pragma unroll
+        for (int i = 0; i < TTc + HALO; ++i)
+          ow[i] = bf2f(*reinterpret_cast<const uint32_t*>(&sm.ring[(t0 - HALO + i) & (ORc - 1)][2 * pr]));
+#pragma unroll
+        for (int tt = 0; tt < TTc; ++tt) {
+          const bool ok = t0 + tt < s_end;
+          const float2 e1 = ok ? d1[tt] : make_float2(0.0f, 0.0f);
+          const float2 e2 = ok ? d2[tt] : make_float2(0.0f, 0.0f);
+#pragma unroll
+          for (int tau = 0; tau < 4; ++tau) dw[tau] = __ffma2_rn(e1, ow[tt + HALO - tau], dw[tau]);
+#pragma unroll
+          for (int tau = 0; tau < 8; ++tau) dw[4 + tau] = __ffma2_rn(e2, ow[tt + HALO - tau], dw[4 + tau]);
+        }
+      } else {
+        float2 d3[TTc + 11];
+#pragma unroll
+        for (int i = 0; i < TTc + 11; ++i)
+          d3[i] = t0 + i < S ? *reinterpret_cast<const float2*>(&sm.du3[(t0 + i) & (col::D3 - 1)][2 * pr])
+                             : make_float2(0.0f, 0.0f);
+#pragma unroll
+        for (int tt = 0; tt < TTc; ++tt) {
+          float2 d = make_float2(0.0f, 0.0f);
+#pragma unroll
+          for (int tau = 0; tau < 12; ++tau) d = __ffma2_rn(tp[tau], d3[tt + tau], d);
+          part[tt] = d;
+        }
+        float2 ow[TTc + HALO];
+#pragma unroll
+        for (int i = 0; i < TTc + HALO; ++i)
+          ow[i] = bf2f(*reinterpret_cast<const uint32_t*>(&sm.ring[(t0 - HALO + i) & (ORc - 1)][2 * pr]));
+#pragma unroll
+        for (int tt = 0; tt < TTc; ++tt) {
+          const float2 e3 = t0 + tt < s_end ? d3[tt] : make_float2(0.0f, 0.0f);
+#pragma unroll
+          for (int tau = 0; tau < 12; ++tau) dw[tau] = __ffma2_rn(e3, ow[tt + HALO - tau], dw[tau]);
+        }
+      }
+#pragma unroll
+      for (int tt = 0; tt < TTc; ++tt) *reinterpret_cast<float2*>(&sm.dconv[grp][tt][2 * pr]) = part[tt];
+    }
+    __syncthreads();
+    if (!has_next) finalize();                 // the walk ends here: no later token phase
+  }
+  if (HAS_CONV && pair_ok) {
+    float* dst = cpart + (size_t)blockIdx.x * NTAPS * C + c2;
+#pragma unroll
+    for (int q = 0; q < 12; ++q) {
+      float* row = dst + (size_t)(12 * grp + q) * C;
+      row[0] = dw[q].x;
+      row[1] = dw[q].y;
+    }
   }
 }
 
@@ -884,27 +993,25 @@ cudaError_t launch_fwd_update(const Params& p, const UpdArgs<__nv_bfloat16>& a, 
 }
 
 size_t bwd_col_pdot_floats(const Params& p) {
-  return (size_t)p.B * p.S * (size_t)((p.C + CB - 1) / CB) * PDOT;
+  return (size_t)p.B * p.S * (size_t)((p.C + col::CB - 1) / col::CB) * PDOT;
 }
 size_t bwd_col_cpart_floats(const Params& p, int sms) {
-  return (size_t)make_walk(p, sms).R * NTAPS * (size_t)p.C;
+  return (size_t)make_walk_col(p, sms).R * NTAPS * (size_t)p.C;
 }
-int bwd_col_cpart_rows(const Params& p, int sms) { return make_walk(p, sms).R; }
+int bwd_col_cpart_rows(const Params& p, int sms) { return make_walk_col(p, sms).R; }
 
 cudaError_t launch_bwd_col(const Params& p, const BwdArgs<__nv_bfloat16>& a, const float* coef, bool has_conv,
                            float* pdot, float* cpart, int sms, cudaStream_t st) {
-  const Walk wk = make_walk(p, sms);
+  const Walk wk = make_walk_col(p, sms);
   dim3 grid(wk.R, wk.ncb);
   const int smem = (int)sizeof(ColSmem);
   timing_begin("bwd_col", st);
   if (has_conv) {
     cudaFuncSetAttribute(bwd_col_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    cudaFuncSetAttribute(bwd_col_kernel<true>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-    bwd_col_kernel<true><<<grid, THREADS, smem, st>>>(p, a, coef, pdot, cpart, wk);
+    bwd_col_kernel<true><<<grid, col::THREADS, smem, st>>>(p, a, coef, pdot, cpart, wk);
   } else {
     cudaFuncSetAttribute(bwd_col_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    cudaFuncSetAttribute(bwd_col_kernel<false>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-    bwd_col_kernel<false><<<grid, THREADS, smem, st>>>(p, a, coef, pdot, cpart, wk);
+    bwd_col_kernel<false><<<grid, col::THREADS, smem, st>>>(p, a, coef, pdot, cpart, wk);
   }
   timing_end(st);
   return cudaGetLastError();
@@ -913,7 +1020,7 @@ cudaError_t launch_bwd_col(const Params& p, const BwdArgs<__nv_bfloat16>& a, con
 cudaError_t launch_bwd_dz(const Params& p, const float* saved, const float* pdot, bool has_dxin,
                           __nv_bfloat16* dP, float* rec, cudaStream_t st) {
   const size_t T_all = (size_t)p.B * p.S;
-  const int ncb = (p.C + CB - 1) / CB;
+  const int ncb = (p.C + col::CB - 1) / col::CB;
   const size_t smem = (size_t)16 * std::max(p.iters, 1) * 32 * sizeof(float);
   cudaFuncSetAttribute(bwd_dz_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   timing_begin("bwd_dz", st);
