@@ -150,34 +150,27 @@ Walk make_walk(const Params& p, int sms) {
 // One thread per token: hpre = sigmoid(z[0:N]), hpost = sigmoid(z[N:N+4k]),
 // Hres = Sinkhorn(exp(Z - max Z)) -> coefficient block.
 
-__global__ void __launch_bounds__(128) coef_kernel(Params p, const float* __restrict__ saved, float* __restrict__ coef,
+__global__ void __launch_bounds__(256) coef_kernel(Params p, const float* __restrict__ saved, float* __restrict__ coef,
                                                    size_t T_all) {
-  const size_t t = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (t >= T_all) return;
+  // half-warp per token: lane e computes hpre[e], hpost[e] and H^res entry e
+  // (e = 4 i + j) with the shuffle Sinkhorn, which gives the same values as
+  // the one-thread version used by the forward
+  const int lane = threadIdx.x & 31, e = lane & 15;
+  const size_t t = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) >> 4;
+  const bool live = t < T_all;
+  const size_t tc = live ? t : 0;
   const int N = p.N, k = p.k, P = p.P;
-  const float* z = saved + t * (P + 1);
-  float4* cf = reinterpret_cast<float4*>(coef + t * COEF_STRIDE);
-#pragma unroll
-  for (int v = 0; v < 4; ++v) {
-    float h[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) h[e] = (4 * v + e < N) ? sigmoidf_(z[4 * v + e]) : 0.0f;
-    cf[v] = make_float4(h[0], h[1], h[2], h[3]);
-  }
-#pragma unroll
-  for (int v = 0; v < 4; ++v) {
-    float h[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) h[e] = (4 * v + e < 4 * k) ? sigmoidf_(z[N + 4 * v + e]) : 0.0f;
-    cf[4 + v] = make_float4(h[0], h[1], h[2], h[3]);
-  }
-  float zr[KMAX * KMAX];
-#pragma unroll
-  for (int q = 0; q < KMAX * KMAX; ++q) zr[q] = q < k * k ? z[N + 4 * k + q] : 0.0f;
-  float M[KMAX][KMAX];
-  sinkhorn_thread(zr, k, p.iters, M);
-#pragma unroll
-  for (int i = 0; i < KMAX; ++i) cf[8 + i] = make_float4(M[i][0], M[i][1], M[i][2], M[i][3]);
+  const float* z = saved + tc * (P + 1);
+  const int i = e >> 2, j = e & 3;
+  const bool valid = i < k && j < k;
+  const float hpre = e < N ? sigmoidf_(z[e]) : 0.0f;
+  const float hpost = e < 4 * k ? sigmoidf_(z[N + e]) : 0.0f;
+  const float H = sinkhorn16(valid ? z[N + 4 * k + k * i + j] : 0.0f, valid, p.iters);
+  if (!live) return;
+  float* cf = coef + t * COEF_STRIDE;
+  cf[e] = hpre;
+  cf[COEF_POST + e] = hpost;
+  cf[COEF_RES + e] = valid ? H : 0.0f;
 }
 
 // ---------------------------------------------------------------- forward update
@@ -901,12 +894,29 @@ __global__ void __launch_bounds__(256) bwd_dz_kernel(Params p, const float* __re
   const int N = p.N, k = p.k, P = p.P;
   const float* zt = saved + tc * (P + 1);
   const float rstd = zt[P];
+  // sums over the channel blocks in block order, eight blocks' loads in flight at a time
   float dres = 0.0f, dpost = 0.0f, dpre = 0.0f;
-  for (int c = 0; c < ncb; ++c) {
-    const float* pd = pdot + (tc * ncb + c) * PDOT;
-    dres += pd[e];
-    dpost += pd[16 + e];
-    if (has_dxin) dpre += pd[32 + e];
+  const float* pd0 = pdot + tc * ncb * PDOT;
+  int c = 0;
+  for (; c + 8 <= ncb; c += 8) {
+    float a[8], b[8], d[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      a[q] = pd0[(c + q) * PDOT + e];
+      b[q] = pd0[(c + q) * PDOT + 16 + e];
+      d[q] = has_dxin ? pd0[(c + q) * PDOT + 32 + e] : 0.0f;
+    }
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      dres += a[q];
+      dpost += b[q];
+      dpre += d[q];
+    }
+  }
+  for (; c < ncb; ++c) {
+    dres += pd0[c * PDOT + e];
+    dpost += pd0[c * PDOT + 16 + e];
+    if (has_dxin) dpre += pd0[c * PDOT + 32 + e];
   }
   const int i = e >> 2, j = e & 3;
   const bool valid = i < k && j < k;
@@ -963,7 +973,7 @@ __global__ void __launch_bounds__(256) bwd_dz_kernel(Params p, const float* __re
 cudaError_t launch_coef(const Params& p, const float* saved, float* coef, cudaStream_t st) {
   const size_t T_all = (size_t)p.B * p.S;
   timing_begin("coef", st);
-  coef_kernel<<<(unsigned)((T_all + 127) / 128), 128, 0, st>>>(p, saved, coef, T_all);
+  coef_kernel<<<(unsigned)((T_all * 16 + 255) / 256), 256, 0, st>>>(p, saved, coef, T_all);
   timing_end(st);
   return cudaGetLastError();
 }
