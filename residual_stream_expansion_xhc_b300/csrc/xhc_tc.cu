@@ -509,6 +509,15 @@ int read_device_error(cudaStream_t st) {
 // dV goes to a double-buffered TMEM accumulator that the epilogue turns into
 // dX = dV + alpha X + base (+ hpre[n] dx_in); dW accumulates in TMEM over the
 // whole token range and is written as one partial per range.
+//
+// The epilogue writes the dX tile into the stage's Pt region (free once both
+// contractions have read it), in the same swizzled layout TMA uses, and a
+// store warp sends it out with two TMA stores: full 128-byte lines instead of
+// one 16-byte piece per token row per store instruction.  The stage's X and B
+// part is released as soon as the epilogue has read it, so the next tile's
+// HBM loads start while the store is still reading the Pt region; the Pt part
+// is released when the store has read it.
+//
 // Section "Scaling N" (coefficients come from the whole state, so every
 // stream receives the projection gradient); section "Dense read, sparse
 // write" (inactive streams pass dX' through, active ones receive the mix).
@@ -520,12 +529,14 @@ constexpr int STAGES = 2;
 constexpr int HALF = TT * 64 * 2;                 // one 64-column box: 16 KB
 constexpr int OFF_X = 0;
 constexpr int OFF_B = 2 * HALF;
-constexpr int OFF_P = 4 * HALF;                   // dp, hi part
-constexpr int OFF_PL = 5 * HALF;                  // dp, lo part
+constexpr int OFF_P = 4 * HALF;                   // dp, hi part; then dX box 0
+constexpr int OFF_PL = 5 * HALF;                  // dp, lo part; then dX box 1
 constexpr int STAGE_BYTES = 6 * HALF;             // 96 KB
 constexpr int WT_BYTES = CB * 64 * 2;             // 16 KB per part of W^T
 constexpr int SMEM = STAGES * STAGE_BYTES + 2 * WT_BYTES + 1024;
-constexpr int THREADS = 192;
+constexpr int EPI_WARPS = 8;
+constexpr int THREADS = 32 * (3 + EPI_WARPS);     // producer, MMA issuer, epilogue, store
+constexpr int STORE_WARP = 2 + EPI_WARPS;
 constexpr int TMEM_COLS = 512;                    // dV: 2 x 128, dW: 48 at column 256
 constexpr int D2_COL = 256;
 }  // namespace bwdtc
@@ -541,7 +552,11 @@ __global__ void __launch_bounds__(bwdtc::THREADS, 1)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   uint8_t* wt_s = smem + STAGES * STAGE_BYTES;
-  __shared__ uint64_t full[STAGES], empty[STAGES], tfull[2], tempty[2], wt_full, wt_empty, d2full, d2empty;
+  // full: stage loaded; xb_free: X and B read (MMA + epilogue); mma_done: both
+  // contractions done with the stage; out_ready: dX tile written to the Pt
+  // region; p_free: the store has read it
+  __shared__ uint64_t full[STAGES], xb_free[STAGES], mma_done[STAGES], out_ready[STAGES], p_free[STAGES];
+  __shared__ uint64_t tfull[2], tempty[2], wt_full, wt_empty, d2full, d2empty;
   __shared__ uint32_t tmem_slot;
   int* err = &g_device_error;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -555,16 +570,19 @@ __global__ void __launch_bounds__(bwdtc::THREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1 + 4);              // MMA commit + 4 epilogue warps
+      mbar_init(&xb_free[s], 1 + EPI_WARPS);    // MMA commit + epilogue warps
+      mbar_init(&mma_done[s], 1);
+      mbar_init(&out_ready[s], EPI_WARPS);
+      mbar_init(&p_free[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], 4);
+      mbar_init(&tempty[b], EPI_WARPS);
     }
     mbar_init(&wt_full, 1);
     mbar_init(&wt_empty, 1);
     mbar_init(&d2full, 1);
-    mbar_init(&d2empty, 4);
+    mbar_init(&d2empty, EPI_WARPS);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -587,14 +605,11 @@ __global__ void __launch_bounds__(bwdtc::THREADS, 1)
         const int slot = p.is_active[n];
         const size_t t_beg = (size_t)r * range_len;
         const size_t t_end = (t_beg + range_len < T_all) ? t_beg + range_len : T_all;
-        if (ii > 0 && !mbar_wait(&wt_empty, (ii - 1) & 1, err, 21)) break;
-        mbar_expect_tx(&wt_full, 2 * WT_BYTES);
-        tma_load_2d(wt_s, &m.Wt, &wt_full, 0, (int)((size_t)n * C + c0), pol_keep);
-        tma_load_2d(wt_s + WT_BYTES, &m.Wtl, &wt_full, 0, (int)((size_t)n * C + c0), pol_keep);
         bool ok = true;
         for (size_t t0 = t_beg; t0 < t_end; t0 += TT, ++it) {
           const int s = it % STAGES;
-          if (it >= STAGES && !mbar_wait(&empty[s], ((it / STAGES) & 1) ^ 1, err, 22)) { ok = false; break; }
+          const uint32_t ph = ((it / STAGES) & 1) ^ 1;
+          if (it >= STAGES && !mbar_wait(&xb_free[s], ph, err, 22)) { ok = false; break; }
           uint8_t* st = smem + s * STAGE_BYTES;
           mbar_expect_tx(&full[s], STAGE_BYTES);
           const int tt = (int)t0;
@@ -606,8 +621,16 @@ __global__ void __launch_bounds__(bwdtc::THREADS, 1)
             if (slot) tma_load_3d(st + OFF_B + h * HALF, &m.dX, &full[s], c0 + 64 * h, n, tt, pol_stream);
             else tma_load_3d(st + OFF_B + h * HALF, &m.dXp, &full[s], c0 + 64 * h, n, tt, pol_stream);
           }
+          if (it >= STAGES && !mbar_wait(&p_free[s], ph, err, 31)) { ok = false; break; }
           tma_load_2d(st + OFF_P, &m.dP, &full[s], 0, tt, pol_keep);
           tma_load_2d(st + OFF_PL, &m.dPl, &full[s], 0, tt, pol_keep);
+          if (t0 == t_beg) {
+            // this item's W^T block, once the previous item's contractions are done
+            if (ii > 0 && !mbar_wait(&wt_empty, (ii - 1) & 1, err, 21)) { ok = false; break; }
+            mbar_expect_tx(&wt_full, 2 * WT_BYTES);
+            tma_load_2d(wt_s, &m.Wt, &wt_full, 0, (int)((size_t)n * C + c0), pol_keep);
+            tma_load_2d(wt_s + WT_BYTES, &m.Wtl, &wt_full, 0, (int)((size_t)n * C + c0), pol_keep);
+          }
         }
         if (!ok) break;
       }
@@ -623,13 +646,11 @@ __global__ void __launch_bounds__(bwdtc::THREADS, 1)
         const int r = item % ranges;
         const size_t t_beg = (size_t)r * range_len;
         const size_t t_end = (t_beg + range_len < T_all) ? t_beg + range_len : T_all;
-        if (!mbar_wait(&wt_full, ii & 1, err, 23)) break;
-        if (ii > 0 && !mbar_wait(&d2empty, (ii - 1) & 1, err, 24)) break;
-        tc_fence_after();
-        bool ok = true, first = true;
+        bool ok = true;
         for (size_t t0 = t_beg; t0 < t_end; t0 += TT, ++it, ++tl) {
           const int s = it % STAGES, buf = tl & 1;
           if (!mbar_wait(&full[s], (it / STAGES) & 1, err, 25)) { ok = false; break; }
+          if (t0 == t_beg && !mbar_wait(&wt_full, ii & 1, err, 23)) { ok = false; break; }
           if (tl >= 2 && !mbar_wait(&tempty[buf], ((tl >> 1) & 1) ^ 1, err, 26)) { ok = false; break; }
           tc_fence_after();
           const uint32_t st = smem_u32(smem + s * STAGE_BYTES);
@@ -646,26 +667,60 @@ __global__ void __launch_bounds__(bwdtc::THREADS, 1)
             umma_bf16(tmem + buf * 128, pl, wh, idesc_v, 1);
           }
           umma_commit(&tfull[buf]);
+          // the previous item's dW partial must be drained before this item's
+          // first accumulation
+          if (t0 == t_beg && ii > 0) {
+            if (!mbar_wait(&d2empty, (ii - 1) & 1, err, 24)) { ok = false; break; }
+            tc_fence_after();
+          }
           // dW += X^T . dP  (K = 128 tokens: eight K16 steps of 16 rows); hi + lo of dp
 #pragma unroll
           for (int ks = 0; ks < TT / 16; ++ks) {
             const uint64_t da = sdesc_sw128(st + OFF_X + ks * 2048, HALF, 1024);
             const uint64_t dh = sdesc_sw128(st + OFF_P + ks * 2048, HALF, 1024);
             const uint64_t dl = sdesc_sw128(st + OFF_PL + ks * 2048, HALF, 1024);
-            umma_bf16(tmem + D2_COL, da, dh, idesc_w, (first && ks == 0) ? 0u : 1u);
+            umma_bf16(tmem + D2_COL, da, dh, idesc_w, (t0 == t_beg && ks == 0) ? 0u : 1u);
             umma_bf16(tmem + D2_COL, da, dl, idesc_w, 1);
           }
-          umma_commit(&empty[s]);
-          first = false;
+          umma_commit(&mma_done[s]);
+          umma_commit(&xb_free[s]);
         }
         if (!ok) break;
         umma_commit(&d2full);
         umma_commit(&wt_empty);
       }
     }
+  } else if (warp == STORE_WARP) {
+    // ------------------------------------------------ dX tile stores
+    if (lane == 0) {
+      int it = 0;
+      for (int item = blockIdx.x; item < nitems; item += gridDim.x) {
+        const int blk = item / ranges, r = item % ranges;
+        const int n = blk / cblocks, c0 = (blk % cblocks) * CB;
+        const size_t t_beg = (size_t)r * range_len;
+        const size_t t_end = (t_beg + range_len < T_all) ? t_beg + range_len : T_all;
+        bool ok = true;
+        for (size_t t0 = t_beg; t0 < t_end; t0 += TT, ++it) {
+          const int s = it % STAGES;
+          if (!mbar_wait(&out_ready[s], (it / STAGES) & 1, err, 30)) { ok = false; break; }
+          const uint8_t* st = smem + s * STAGE_BYTES;
+          // rows past the last token are clipped by the tensor map
+          tma_store_3d(&m.dX, st + OFF_P, c0, n, (int)t0);
+          tma_store_3d(&m.dX, st + OFF_PL, c0 + 64, n, (int)t0);
+          tma_store_commit();
+          tma_store_wait_read0();
+          mbar_arrive(&p_free[s]);
+        }
+        if (!ok) break;
+      }
+      tma_store_wait0();
+    }
   } else {
     // ------------------------------------------------ epilogue: one thread per token / per column
-    const int q4 = warp & 3;
+    // warp w reads TMEM lanes 32 (w % 4) .. +31 (its sub-partition); with
+    // eight epilogue warps, two share a sub-partition and split the columns
+    constexpr int SPLIT = EPI_WARPS / 4, CC = CB / 16 / SPLIT;
+    const int q4 = warp & 3, part = (warp - 2) / 4;
     const int row = 32 * q4 + lane;
     const uint32_t lane_base = (uint32_t)(32 * q4) << 16;
     const int rl = 1 + N + 4 * k;
@@ -678,30 +733,32 @@ __global__ void __launch_bounds__(bwdtc::THREADS, 1)
       bool ok = true;
       for (size_t t0 = t_beg; t0 < t_end; t0 += TT, ++it, ++tl) {
         const int s = it % STAGES, buf = tl & 1;
-        if (!mbar_wait(&full[s], (it / STAGES) & 1, err, 27)) { ok = false; break; }
-        if (!mbar_wait(&tfull[buf], (tl >> 1) & 1, err, 28)) { ok = false; break; }
-        tc_fence_after();
-        const uint8_t* st = smem + s * STAGE_BYTES;
+        const uint32_t ph = (it / STAGES) & 1;
         const size_t t = t0 + row;
         const bool live = t < T_all;
-        float alpha = 0.0f, hp = 0.0f;
+        float alpha = 0.0f, hp = 0.0f;           // loaded before the waits
         if (live) {
           alpha = a.rec[t * rl];
           if (a.dx_in) hp = a.rec[t * rl + 1 + n];
         }
+        if (!mbar_wait(&full[s], ph, err, 27)) { ok = false; break; }
+        if (!mbar_wait(&tfull[buf], (tl >> 1) & 1, err, 28)) { ok = false; break; }
+        if (!mbar_wait(&mma_done[s], ph, err, 32)) { ok = false; break; }
+        tc_fence_after();
+        uint8_t* st = smem + s * STAGE_BYTES;
 #pragma unroll 1
-        for (int cc = 0; cc < CB / 16; ++cc) {
+        for (int cc = part * CC; cc < (part + 1) * CC; ++cc) {
           uint32_t d[16];
           tmem_ld16(tmem + lane_base + buf * 128 + cc * 16, d);
-          tmem_wait_ld();
           const int h = cc >> 2;                        // which 64-column box
           const int byte0 = (cc & 3) * 32;              // 16 columns = 32 bytes
+          const uint32_t o0 = sw128_offset(row, byte0), o1 = sw128_offset(row, byte0 + 16);
           const uint8_t* xr = st + OFF_X + h * HALF;
           const uint8_t* br = st + OFF_B + h * HALF;
-          const uint4 x0 = *reinterpret_cast<const uint4*>(xr + sw128_offset(row, byte0));
-          const uint4 x1 = *reinterpret_cast<const uint4*>(xr + sw128_offset(row, byte0 + 16));
-          const uint4 b0 = *reinterpret_cast<const uint4*>(br + sw128_offset(row, byte0));
-          const uint4 b1 = *reinterpret_cast<const uint4*>(br + sw128_offset(row, byte0 + 16));
+          const uint4 x0 = *reinterpret_cast<const uint4*>(xr + o0);
+          const uint4 x1 = *reinterpret_cast<const uint4*>(xr + o1);
+          const uint4 b0 = *reinterpret_cast<const uint4*>(br + o0);
+          const uint4 b1 = *reinterpret_cast<const uint4*>(br + o1);
           const uint32_t xw[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
           const uint32_t bw[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
           float g[16];
@@ -718,6 +775,7 @@ __global__ void __launch_bounds__(bwdtc::THREADS, 1)
 #pragma unroll
             for (int e = 0; e < 16; ++e) g[e] = 0.0f;
           }
+          tmem_wait_ld();
           uint32_t o[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
@@ -729,17 +787,17 @@ __global__ void __launch_bounds__(bwdtc::THREADS, 1)
             yb = fmaf(hp, g[2 * e + 1], yb);
             o[e] = pack_bf2(ya, yb);
           }
-          if (live) {
-            uint4* dst = reinterpret_cast<uint4*>(a.dX + (t * N + n) * (size_t)C + c0 + cc * 16);
-            dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-            dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
-          }
+          uint8_t* orow = st + OFF_P + h * HALF;        // dX box h, same swizzle as the loads
+          *reinterpret_cast<uint4*>(orow + o0) = make_uint4(o[0], o[1], o[2], o[3]);
+          *reinterpret_cast<uint4*>(orow + o1) = make_uint4(o[4], o[5], o[6], o[7]);
         }
         tc_fence_before();
+        fence_async_smem();                             // the tile is read by TMA next
         __syncwarp();
         if (lane == 0) {
           mbar_arrive(&tempty[buf]);
-          mbar_arrive(&empty[s]);
+          mbar_arrive(&xb_free[s]);
+          mbar_arrive(&out_ready[s]);
         }
       }
       if (!ok) break;
@@ -748,7 +806,7 @@ __global__ void __launch_bounds__(bwdtc::THREADS, 1)
       tc_fence_after();
       float* dst = wpart + (size_t)r * P * NC + (size_t)n * C + c0 + row;
 #pragma unroll
-      for (int qc = 0; qc < 48; qc += 16) {
+      for (int qc = 16 * part; qc < 48; qc += 16 * SPLIT) {
         uint32_t d[16];
         tmem_ld16(tmem + lane_base + D2_COL + qc, d);
         tmem_wait_ld();
