@@ -411,15 +411,42 @@ constexpr int ORING = 32;
 constexpr int D1 = 16, D2 = 16, D3 = 32;   // du ring rows: powers of two >= K_j - 1 + TT
 }  // namespace col
 
+// Rows that feed the coefficient dots on the tensor cores are read eight at a
+// time by ldmatrix; each such row stores its 16 16-byte chunks rotated by a
+// row-specific amount (logical chunk q at physical chunk (q + rot) mod 16), so
+// that the eight rows of one ldmatrix fall in eight different bank groups:
+//   A rows: G_i of slot s                    rot = i + 4 (s mod 2)
+//   B rows: Xa_j (rot j + 1), out (ring, rot 0), u_1..u_3 (rot 5..7)
 struct ColSmem {
   uint16_t ring[col::ORING][col::CB];         // out rows (bf16 bits)
-  uint32_t u[3][col::TT][col::CB / 2];        // u_1..u_3 of the chunk, bf16 pairs (they only enter dots)
+  uint32_t u[3][col::TT][col::CB / 2];        // u_1..u_3 of the chunk, bf16 pairs, rotated (they only enter dots)
   float du1[col::D1][col::CB];
   float du2[col::D2][col::CB];
   float du3[col::D3][col::CB];
-  float dconv[2][col::TT][col::CB];           // convolution parts of dout (K4 + K8 | K12)
+  float dconv[col::TT][2][col::CB];           // per token slot: convolution parts of dout (K4 + K8 | K12);
+                                              // in the token phase, after they are consumed: the slot's G rows
+  uint32_t xa[col::TT][KMAX][col::CB / 2];    // the slot's old active rows Xa_j, rotated
   float tap[NTAPS][col::CB];
 };
+
+// ldmatrix of four 8 x 8 bf16 matrices; mma.sync m16n8k16 bf16 -> fp32
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(addr)
+               : "memory");
+}
+__device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
+  // rows 8..15 of A are zero
+  asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+               "{%8, %9}, {%0, %1, %2, %3};"
+               : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+               : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t rot_chunk(int q, int rot) { return (uint32_t)((q + rot) & 15) << 4; }
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
 
 Walk make_walk_col(const Params& p, int sms) {
   Walk w;
@@ -465,21 +492,6 @@ __device__ __forceinline__ float dot8(const float2 (&a)[4], const float2 (&b)[4]
   s = __ffma2_rn(a[3], b[3], s);
   return s.x + s.y;
 }
-// Sum 32 per-lane values over the 16 lanes of a half-warp: lane l ends with
-// the sums of values 2l and 2l + 1 (30 shuffles; both halves run it).
-__device__ __forceinline__ float2 half_transpose_sum32(float (&v)[32], int l16) {
-#pragma unroll
-  for (int o = 8; o >= 1; o >>= 1) {
-    const bool upper = (l16 & o) != 0;
-#pragma unroll
-    for (int i = 0; i < 2 * o; ++i) {
-      const float send = upper ? v[i] : v[i + 2 * o];
-      const float keep = upper ? v[i + 2 * o] : v[i];
-      v[i] = keep + __shfl_xor_sync(FULL, send, o);
-    }
-  }
-  return make_float2(v[0], v[1]);
-}
 // Sum 16 per-lane values over a half-warp: lane l ends with the sum of value l.
 __device__ __forceinline__ float half_transpose_sum16(float (&v)[16], int l16) {
 #pragma unroll
@@ -514,6 +526,11 @@ __global__ void __launch_bounds__(col::THREADS, 3) bwd_col_kernel(Params p, BwdA
   const int c2 = cb0 + 2 * pr;
   const bool pair_ok = c2 < C;
   const int ncb = wk.ncb;
+  // rows the dots read but no pass writes (channels past C, tokens past the
+  // sequence end, the zero row) must hold finite values: start from zero
+  for (int q = threadIdx.x; q < (int)(sizeof(ColSmem) / 16); q += col::THREADS)
+    reinterpret_cast<uint4*>(smem_raw)[q] = make_uint4(0, 0, 0, 0);
+  __syncthreads();
   if (HAS_CONV) {
     float t[NTAPS];
     load_taps(a.w, cb0 + threadIdx.x, C, t);
@@ -529,10 +546,10 @@ __global__ void __launch_bounds__(col::THREADS, 3) bwd_col_kernel(Params p, BwdA
 
   auto finalize = [&]() {                                   // dout of token fin_tok (slot hw)
     if (fin && lane_ok) {
-      const float4 a0 = *reinterpret_cast<const float4*>(&sm.dconv[0][hw][8 * l16]);
-      const float4 a1 = *reinterpret_cast<const float4*>(&sm.dconv[0][hw][8 * l16 + 4]);
-      const float4 b0 = *reinterpret_cast<const float4*>(&sm.dconv[1][hw][8 * l16]);
-      const float4 b1 = *reinterpret_cast<const float4*>(&sm.dconv[1][hw][8 * l16 + 4]);
+      const float4 a0 = *reinterpret_cast<const float4*>(&sm.dconv[hw][0][8 * l16]);
+      const float4 a1 = *reinterpret_cast<const float4*>(&sm.dconv[hw][0][8 * l16 + 4]);
+      const float4 b0 = *reinterpret_cast<const float4*>(&sm.dconv[hw][1][8 * l16]);
+      const float4 b1 = *reinterpret_cast<const float4*>(&sm.dconv[hw][1][8 * l16 + 4]);
       float2 d[4];
       d[0] = make_float2(du0r[0].x + (a0.x + b0.x), du0r[0].y + (a0.y + b0.y));
       d[1] = make_float2(du0r[1].x + (a0.z + b0.z), du0r[1].y + (a0.w + b0.w));
@@ -592,10 +609,10 @@ __global__ void __launch_bounds__(col::THREADS, 3) bwd_col_kernel(Params p, BwdA
       }
       if (tc + tt < s_end) {
         if (grp == 0) {
-          sm.u[0][tt][pr] = pack_bf2(x.x, x.y);
-          sm.u[1][tt][pr] = pack_bf2(y.x, y.y);
+          sm.u[0][tt][(pr + 20) & 63] = pack_bf2(x.x, x.y);   // rotations 5 and 6
+          sm.u[1][tt][(pr + 24) & 63] = pack_bf2(y.x, y.y);
         } else {
-          sm.u[2][tt][pr] = pack_bf2(x.x, x.y);
+          sm.u[2][tt][(pr + 28) & 63] = pack_bf2(x.x, x.y);   // rotation 7
         }
       }
     }
@@ -654,15 +671,15 @@ __global__ void __launch_bounds__(col::THREADS, 3) bwd_col_kernel(Params p, BwdA
     const size_t tok = seq_base + (tok_ok ? t : t0);
     const float* cf = coef + tok * COEF_STRIDE;
     float2 G[KMAX][4];
-    uint4 xr[KMAX];
+    uint4 gr[KMAX], xr[KMAX];                 // raw bf16 rows; zero where absent
 #pragma unroll
     for (int i = 0; i < KMAX; ++i) {
+      gr[i] = make_uint4(0, 0, 0, 0);
       xr[i] = make_uint4(0, 0, 0, 0);
 #pragma unroll
       for (int q = 0; q < 4; ++q) G[i][q] = make_float2(0.0f, 0.0f);
     }
     if (tok_ok && lane_ok) {
-      uint4 gr[KMAX];
 #pragma unroll
       for (int i = 0; i < KMAX; ++i) {
         if (i < k) {
@@ -728,39 +745,65 @@ __global__ void __launch_bounds__(col::THREADS, 3) bwd_col_kernel(Params p, BwdA
       fin = true;
       fin_tok = tok;
     }
-    // dots over this lane's channels: [0,16) <G_i, Xa_j> at 4i+j, [16,32) <G_i, u_c> at 16+4i+c
-    float v[32];
-#pragma unroll
-    for (int q = 0; q < 32; ++q) v[q] = 0.0f;
-    if (tok_ok && lane_ok) {
-#pragma unroll
-      for (int j = 0; j < KMAX; ++j) {
-        if (j < k) {
-          float2 xv[4];
-          unpack8x2(xr[j], xv);
-#pragma unroll
-          for (int i = 0; i < KMAX; ++i)
-            if (i < k) v[4 * i + j] = dot8(G[i], xv);
-        }
-      }
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        if (!HAS_CONV && c > 0) break;
-        float2 uv[4];
-        if (c == 0) {
-          if (HAS_CONV) unpack8x2(*reinterpret_cast<const uint4*>(&sm.ring[t & (ORc - 1)][8 * l16]), uv);
-          else unpack8x2(ld_na(a.out + tok * C + c_lane), uv);
-        } else {
-          unpack8x2(*reinterpret_cast<const uint4*>(&sm.u[c - 1][hw][4 * l16]), uv);
-        }
-#pragma unroll
-        for (int i = 0; i < KMAX; ++i)
-          if (i < k) v[16 + 4 * i + c] = dot8(G[i], uv);
-      }
-    }
+    // Coefficient dots of this CTA's channels, per token: [0,16) <G_i, Xa_j>
+    // at 4i+j, [16,32) <G_i, u_c> at 16+4i+c.  Per warp (two tokens, slots
+    // 2w and 2w+1) they are two small contractions over the 128 channels,
+    //   D_T[i][n] = sum_ch G_T,i[ch] Y_T,n[ch],  Y_T = (Xa_0..Xa_3, u_0..u_3),
+    // run as mma.sync m16n8k16 (bf16 in, fp32 sums): A rows 0-3 hold G of
+    // slot 2w, rows 4-7 G of slot 2w+1 (rows 8-15 zero), B holds one token's
+    // Y; the token's own rows of D are kept.  The bf16 products are exact and
+    // the sums are fp32, as with the CUDA-core dots they replace.
     {
-      const float2 r = half_transpose_sum32(v, l16);
-      if (tok_ok) *reinterpret_cast<float2*>(pdot + (tok * ncb + cb) * PDOT + 2 * l16) = r;
+      if (!HAS_CONV) {
+        // u_0 = out row of the token (staged in the unused ring); ring[ORING - 1] stays zero
+        const uint4 ov = (tok_ok && lane_ok) ? ld_na(a.out + tok * C + c_lane) : make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(&sm.ring[hw][8 * l16]) = ov;
+      }
+      __syncwarp();                            // finalize() has read this slot's dconv rows
+      uint32_t* gs = reinterpret_cast<uint32_t*>(&sm.dconv[hw][0][0]);
+      const int rot_g = 4 * (hw & 1);
+#pragma unroll
+      for (int i = 0; i < KMAX; ++i) {
+        *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(gs + 64 * i) + rot_chunk(l16, i + rot_g)) = gr[i];
+        *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(&sm.xa[hw][i][0]) + rot_chunk(l16, i + 1)) = xr[i];
+      }
+      __syncwarp();
+      const int mq = lane >> 3, rr = lane & 7;  // ldmatrix: this lane addresses row rr of matrix mq
+      const int sa = 2 * warp + (rr >> 2), ia = rr & 3;
+      const uint32_t a_row = smem_u32(&sm.dconv[sa][0][0]) + 256 * ia;
+      const int a_rot = mq + ia + 4 * (sa & 1);
+      uint32_t b_row[2];
+      int b_rot;
+#pragma unroll
+      for (int T = 0; T < 2; ++T) {
+        const int sb = 2 * warp + T;
+        if (rr < 4) {
+          b_row[T] = smem_u32(&sm.xa[sb][rr][0]);
+        } else if (rr == 4) {
+          b_row[T] = HAS_CONV ? smem_u32(&sm.ring[(t0 + sb) & (ORc - 1)][0]) : smem_u32(&sm.ring[sb][0]);
+        } else {
+          b_row[T] = HAS_CONV ? smem_u32(&sm.u[rr - 5][sb][0]) : smem_u32(&sm.ring[ORc - 1][0]);
+        }
+      }
+      b_rot = mq + (rr < 4 ? rr + 1 : (rr == 4 ? 0 : (HAS_CONV ? rr : 0)));
+      float dA[4] = {0.0f, 0.0f, 0.0f, 0.0f}, dB[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll
+      for (int pp = 0; pp < CBc / 32; ++pp) {   // two 16-channel K steps per ldmatrix
+        uint32_t fa[4], fb[4];
+        ldsm_x4(a_row + rot_chunk(4 * pp, a_rot), fa);
+        ldsm_x4(b_row[0] + rot_chunk(4 * pp, b_rot), fb);
+        mma_16816(dA, fa[0], fa[1], fb[0], fb[1]);
+        mma_16816(dA, fa[2], fa[3], fb[2], fb[3]);
+        ldsm_x4(b_row[1] + rot_chunk(4 * pp, b_rot), fb);
+        mma_16816(dB, fa[0], fa[1], fb[0], fb[1]);
+        mma_16816(dB, fa[2], fa[3], fb[2], fb[3]);
+      }
+      // lane = 4 g + t holds D[g][2t], D[g][2t + 1]; rows g = 0-3 are slot 2w's
+      // tokens (from dA), rows 4-7 slot 2w+1's (from dB): i = g mod 4
+      const float2 r = lane < 16 ? make_float2(dA[0], dA[1]) : make_float2(dB[0], dB[1]);
+      const int gi = (lane >> 2) & 3, n0 = 2 * (lane & 3);
+      const int at = n0 < 4 ? 4 * gi + n0 : 16 + 4 * gi + (n0 - 4);
+      if (tok_ok) *reinterpret_cast<float2*>(pdot + (tok * ncb + cb) * PDOT + at) = r;
     }
     if (a.dx_in) {
       // <dx_in, X_n> for every stream n
@@ -855,7 +898,7 @@ __global__ void __launch_bounds__(col::THREADS, 3) bwd_col_kernel(Params p, BwdA
         }
       }
 #pragma unroll
-      for (int tt = 0; tt < TTc; ++tt) *reinterpret_cast<float2*>(&sm.dconv[grp][tt][2 * pr]) = part[tt];
+      for (int tt = 0; tt < TTc; ++tt) *reinterpret_cast<float2*>(&sm.dconv[tt][grp][2 * pr]) = part[tt];
     }
     __syncthreads();
     if (!has_next) finalize();                 // the walk ends here: no later token phase
