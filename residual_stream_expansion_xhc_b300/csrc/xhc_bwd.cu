@@ -41,14 +41,15 @@ __global__ void wt_prep_kernel(const float* __restrict__ W, __nv_bfloat16* __res
 }
 
 // Fixed-order sums: conv-weight partials [rows][24][C] and dW partials
-// [ranges][P][N C].
+// [ranges][P][N C].  The first `cblocks` blocks take the conv-weight sums,
+// the others the dW sums, four consecutive entries (one 16-byte vector) per
+// thread and step.
 __global__ void bwd_reduce_kernel(int conv_rows, int C, const float* __restrict__ cpart, float* __restrict__ dw4,
-                                  float* __restrict__ dw8, float* __restrict__ dw12, int w_ranges, size_t PNC,
-                                  const float* __restrict__ wpart, float* __restrict__ dW) {
-  const size_t stride = (size_t)gridDim.x * blockDim.x;
-  const size_t i0 = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (cpart) {
-    for (size_t i = i0; i < (size_t)NTAPS * C; i += stride) {
+                                  float* __restrict__ dw8, float* __restrict__ dw12, int cblocks, int w_ranges,
+                                  size_t PNC, const float* __restrict__ wpart, float* __restrict__ dW) {
+  if ((int)blockIdx.x < cblocks) {
+    const size_t stride = (size_t)cblocks * blockDim.x;
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < (size_t)NTAPS * C; i += stride) {
       const int g = (int)(i / C), c = (int)(i % C);
       // eight independent loads in flight, then a fixed-order sum
       float s = 0.0f;
@@ -65,11 +66,22 @@ __global__ void bwd_reduce_kernel(int conv_rows, int C, const float* __restrict_
       else if (g < 12) dw8[(size_t)c * 8 + (g - 4)] = s;
       else dw12[(size_t)c * 12 + (g - 12)] = s;
     }
+    return;
   }
-  for (size_t i = i0; i < PNC; i += stride) {
-    float s = 0.0f;
-    for (int r = 0; r < w_ranges; ++r) s += wpart[(size_t)r * PNC + i];
-    dW[i] = s;
+  // PNC is a multiple of 4 (C is a multiple of 8) and the buffers are 16-byte aligned
+  const size_t n4 = PNC / 4;
+  const size_t stride = (size_t)(gridDim.x - cblocks) * blockDim.x;
+  const float4* wp = reinterpret_cast<const float4*>(wpart);
+  for (size_t i = (size_t)(blockIdx.x - cblocks) * blockDim.x + threadIdx.x; i < n4; i += stride) {
+    float4 s = wp[i];
+    for (int r = 1; r < w_ranges; ++r) {
+      const float4 v = wp[(size_t)r * n4 + i];
+      s.x += v.x;
+      s.y += v.y;
+      s.z += v.z;
+      s.w += v.w;
+    }
+    reinterpret_cast<float4*>(dW)[i] = s;
   }
 }
 
@@ -87,8 +99,11 @@ cudaError_t launch_bwd_reduce(const Params& p, const BwdArgs<__nv_bfloat16>& a, 
                               int conv_rows, int w_ranges, const float* wpart, cudaStream_t st) {
   const size_t PNC = (size_t)p.P * p.N * p.C;
   timing_begin("bwd_reduce", st);
-  bwd_reduce_kernel<<<592, 256, 0, st>>>(conv_rows, p.C, has_conv ? cpart : nullptr, a.dw[0],
-                                         a.dw[1], a.dw[2], w_ranges, PNC, wpart, a.dW);
+  // conv sums: one thread per output (24 C of them); dW: about two float4 per thread
+  const int cblocks = has_conv ? (int)((NTAPS * (size_t)p.C + 255) / 256) : 0;
+  const int wblocks = (int)std::min<size_t>(2 * 148 * 8, (PNC / 4 + 511) / 512);
+  bwd_reduce_kernel<<<cblocks + std::max(wblocks, 1), 256, 0, st>>>(conv_rows, p.C, cpart, a.dw[0], a.dw[1], a.dw[2],
+                                                                   cblocks, w_ranges, PNC, wpart, a.dW);
   timing_end(st);
   return cudaGetLastError();
 }

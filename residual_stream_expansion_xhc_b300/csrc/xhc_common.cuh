@@ -166,16 +166,17 @@ constexpr int COEF_POST = 16;
 constexpr int COEF_RES = 32;
 
 // Reverse of one normalisation y = x / s (s = sum of x along the axis):
-// dx = dy / s - sum(dy * x) / s^2.
+// dx = dy / s - sum(dy * x) / s^2 = (dy - sum(dy * x) / s) / s, with 1 / s
+// taken once as a rounded reciprocal.
 __device__ __forceinline__ float norm_reverse_row(float g, float x, bool valid) {
-  float s = rowsum16(x);
-  float gx = rowsum16(g * x);
-  return valid ? (g / s - gx / (s * s)) : 0.0f;
+  const float r = __frcp_rn(rowsum16(x));
+  const float gx = rowsum16(g * x);
+  return valid ? (g - gx * r) * r : 0.0f;
 }
 __device__ __forceinline__ float norm_reverse_col(float g, float x, bool valid) {
-  float s = colsum16(x);
-  float gx = colsum16(g * x);
-  return valid ? (g / s - gx / (s * s)) : 0.0f;
+  const float r = __frcp_rn(colsum16(x));
+  const float gx = colsum16(g * x);
+  return valid ? (g - gx * r) * r : 0.0f;
 }
 
 }  // namespace xhc

@@ -627,8 +627,9 @@ __global__ void __launch_bounds__(col::THREADS, 3) bwd_col_kernel(Params p, BwdA
   const long g_total = (long)p.B * wk.nch;
   const long g_end = g_beg + wk.per < g_total ? g_beg + wk.per : g_total;
   bool start = true;
-  for (long g = g_end - 1; g >= g_beg; --g) {
-    const int b = (int)(g / wk.nch), m = (int)(g % wk.nch);
+  // (b, m) = (g / nch, g mod nch), stepped down with g
+  int b = (int)((g_end - 1) / wk.nch), m = (int)((g_end - 1) % wk.nch);
+  for (long g = g_end - 1; g >= g_beg; --g, (m == 0 ? (m = wk.nch - 1, --b) : --m)) {
     const int t0 = m * TTc;
     const int s_end = min(t0 + TTc, S);        // tokens of this chunk: t0 .. s_end - 1
     const size_t seq_base = (size_t)b * S;
