@@ -35,8 +35,16 @@ pages are silent (each is listed in the design notes):
 * X'[a_i] = sum_j H^res[i, j] X[a_j] + sum_c H^post[i, c] u_c for slot i of
   the ordered index list a; other streams unchanged.
 * conv tap tau multiplies out[t - tau] (tau = 0 is the current token), zero
-  padding before the start of each sequence, no bias.  No Gram-Schmidt, router
-  score s = 1 (the active indices are given).
+  padding before the start of each sequence, no bias.  Router score s = 1 (the
+  active indices are given).
+* Gram-Schmidt ([xHC] "Conv / Gram-Schmidt"; optional, ``gs=True``): per token,
+  modified Gram-Schmidt over the four components in the order u_0, u_1, u_2,
+  u_3: u~_0 = u_0 is kept, and each later component has its projections onto
+  the earlier u~_d removed one at a time, each projection taken from the
+  partly reduced vector.  The write-back then combines u~_c instead of u_c.
+  The pages leave a zero (or vanishing) component undefined; reading: a
+  projection onto u~_d is skipped when |u~_d|^2 <= GS_EPS (the coefficient is
+  taken as 0), so a zero component stays zero and removes nothing.
 
 All arrays are float64 numpy arrays.  The backward is the exact reverse mode of
 the forward, hand-derived step by step (the Sinkhorn reverse recomputes and
@@ -48,6 +56,7 @@ from __future__ import annotations
 import numpy as np
 
 CONV_KS = (4, 8, 12)
+GS_EPS = 1e-12      # squared norm at or below which a component is treated as zero
 
 
 def n_logits(N: int, k: int) -> int:
@@ -121,6 +130,63 @@ def tfa_components(out_seq, conv):
     return u
 
 
+def gram_schmidt(u, eps=GS_EPS):
+    """Modified Gram-Schmidt of the four components of every token.
+
+    u: [4, S, C] (component, token, channel).  Returns (ut, steps): ut[0] =
+    u[0]; for c = 1, 2, 3 the vector v starts as u[c] and, for d = 0 .. c-1 in
+    turn, loses its projection onto ut[d]:
+        alpha = <v, ut[d]> / <ut[d], ut[d]>   (0 when <ut[d], ut[d]> <= eps)
+        v    <- v - alpha ut[d]
+    and ut[c] is the final v.  ``steps`` keeps, per (c, d), the vector before
+    the step, alpha, the squared norm and the skip mask for the reverse pass.
+    """
+    ut = np.empty_like(u)
+    ut[0] = u[0]
+    norms = [np.einsum("sc,sc->s", u[0], u[0])]
+    steps = []
+    for c in range(1, 4):
+        v = u[c].copy()
+        for d in range(c):
+            n = norms[d]
+            use = n > eps
+            alpha = np.where(use, np.einsum("sc,sc->s", v, ut[d]) / np.where(use, n, 1.0), 0.0)
+            steps.append((c, d, v.copy(), alpha, n, use))
+            v = v - alpha[:, None] * ut[d]
+        ut[c] = v
+        norms.append(np.einsum("sc,sc->s", v, v))
+    return ut, steps
+
+
+def gram_schmidt_reverse(dut, ut, steps):
+    """Reverse mode of ``gram_schmidt``: dL/dut [4, S, C] -> dL/du.
+
+    Steps are undone last to first.  For v' = v - alpha ut_d with alpha =
+    <v, ut_d> / n_d and n_d = <ut_d, ut_d> (the skip decision is a constant):
+        dL/dalpha = -<g, ut_d>
+        dL/dv    += g + dL/dalpha ut_d / n_d
+        dL/dut_d += -alpha g + dL/dalpha (v / n_d - 2 alpha ut_d / n_d)
+    where g = dL/dv'.
+    """
+    acc = dut.copy()                  # dL/dut, growing as later steps are undone
+    du = np.zeros_like(dut)
+    by_c = {}
+    for st in steps:
+        by_c.setdefault(st[0], []).append(st)
+    for c in (3, 2, 1):
+        g = acc[c].copy()             # dL/d(final v of component c)
+        for (_, d, v, alpha, n, use) in reversed(by_c[c]):
+            da = -np.einsum("sc,sc->s", g, ut[d])
+            inv = np.where(use, 1.0 / np.where(use, n, 1.0), 0.0)
+            acc[d] += (-alpha[:, None] * g
+                       + (da * inv)[:, None] * v
+                       - (2.0 * da * alpha * inv)[:, None] * ut[d])
+            g = g + (da * inv)[:, None] * ut[d]
+        du[c] = g
+    du[0] = acc[0]
+    return du
+
+
 def _check(X, out, conv, W, idx):
     B, S, N, C = X.shape
     k = len(idx)
@@ -146,15 +212,17 @@ def _coeffs_seq(Xs, W, N, C, k, iters, eps):
     return dict(v=v, rstd=rstd, p=p, z=z, hpre=hpre, hpost=hpost, hres=hres, trace=trace)
 
 
-def forward(X, out, conv, W, idx, iters=20, eps=1e-6):
+def forward(X, out, conv, W, idx, iters=20, eps=1e-6, gs=False):
     """One xHC sublayer update (forward).
 
     X: [B, S, N, C]; out: [B, S, C]; conv: (w4, w8, w12) or None;
-    W: [P, N*C]; idx: the k active stream indices (ordered, slot i <-> idx[i]).
+    W: [P, N*C]; idx: the k active stream indices (ordered, slot i <-> idx[i]);
+    gs: orthogonalise the components by modified Gram-Schmidt first.
 
     Returns a dict with Xp (updated state [B,S,N,C]), x_in (dense read
     [B,S,C]), z (logits [B,S,P]), rstd [B,S], hpre [B,S,N], hpost [B,S,k,4],
-    hres [B,S,k,k], u (components [B,4,S,C]).
+    hres [B,S,k,k], u (the components written back, after Gram-Schmidt when
+    gs, [B,4,S,C]).
     """
     B, S, N, C, k = _check(X, out, conv, W, idx)
     idx = [int(a) for a in idx]
@@ -168,6 +236,8 @@ def forward(X, out, conv, W, idx, iters=20, eps=1e-6):
         # dense read over all N streams
         x_in = np.einsum("sn,snc->sc", cf["hpre"], X[b])
         u = tfa_components(out[b], conv)
+        if gs:
+            u, _ = gram_schmidt(u)
         Xa = X[b][:, idx, :]                                     # [S, k, C]
         mix = np.einsum("sij,sjc->sic", cf["hres"], Xa)
         write = np.einsum("sic,csx->six", cf["hpost"], u)       # sum over components
@@ -179,7 +249,7 @@ def forward(X, out, conv, W, idx, iters=20, eps=1e-6):
     return res
 
 
-def backward(X, out, conv, W, idx, dXp, dx_in=None, iters=20, eps=1e-6, keep=False):
+def backward(X, out, conv, W, idx, dXp, dx_in=None, iters=20, eps=1e-6, keep=False, gs=False):
     """Exact reverse mode of ``forward``.
 
     X is the state BEFORE the update.  dXp = dL/dX' [B,S,N,C]; dx_in = dL/dx_in
@@ -187,7 +257,9 @@ def backward(X, out, conv, W, idx, dXp, dx_in=None, iters=20, eps=1e-6, keep=Fal
 
     Returns dict with dX [B,S,N,C], dout [B,S,C], dconv (three arrays, or None
     when conv is None), dW [P, N*C]; with keep=True also dz [B,S,P] (gradient
-    at the logits) and the per-token dp [B,S,P] and drstd [B,S].
+    at the logits) and the per-token dp [B,S,P] and drstd [B,S].  gs: the
+    forward orthogonalised the components (``gram_schmidt``); the gradient
+    at the orthogonalised components is taken back through it.
     """
     B, S, N, C, k = _check(X, out, conv, W, idx)
     idx = [int(a) for a in idx]
@@ -202,6 +274,9 @@ def backward(X, out, conv, W, idx, dXp, dx_in=None, iters=20, eps=1e-6, keep=Fal
         Xs = X[b]
         cf = _coeffs_seq(Xs, W, N, C, k, iters, eps)
         u = tfa_components(out[b], conv)                        # [4, S, C]
+        if gs:
+            u_raw = u
+            u, gs_steps = gram_schmidt(u_raw)
         G = dXp[b][:, idx, :]                                   # [S, k, C]
         Xa = Xs[:, idx, :]                                      # [S, k, C]
         # gradients at the coefficients
@@ -235,6 +310,8 @@ def backward(X, out, conv, W, idx, dXp, dx_in=None, iters=20, eps=1e-6, keep=Fal
         dX[b] = dXs
         # components: du_c = sum_i hpost[i, c] G_i
         du = np.einsum("six,sic->xsc", hpost, G)                # [4, S, C]
+        if gs:
+            du = gram_schmidt_reverse(du, u, gs_steps)
         dout_b = du[0].copy()
         if conv is not None:
             for j, w in enumerate(conv, start=1):
