@@ -43,8 +43,10 @@ pages are silent (each is listed in the design notes):
   the earlier u~_d removed one at a time, each projection taken from the
   partly reduced vector.  The write-back then combines u~_c instead of u_c.
   The pages leave a zero (or vanishing) component undefined; reading: a
-  projection onto u~_d is skipped when |u~_d|^2 <= GS_EPS (the coefficient is
-  taken as 0), so a zero component stays zero and removes nothing.
+  projection onto u~_d is skipped (its coefficient taken as 0) when
+  |u~_d|^2 <= GS_EPS |u_d|^2, i.e. when u_d is zero or lies (to within a
+  relative 1e-3 in norm) in the span of the components before it.  A zero
+  component then stays zero and removes nothing.
 
 All arrays are float64 numpy arrays.  The backward is the exact reverse mode of
 the forward, hand-derived step by step (the Sinkhorn reverse recomputes and
@@ -56,7 +58,7 @@ from __future__ import annotations
 import numpy as np
 
 CONV_KS = (4, 8, 12)
-GS_EPS = 1e-12      # squared norm at or below which a component is treated as zero
+GS_EPS = 1e-6       # relative squared residual at or below which a component is treated as zero
 
 
 def n_logits(N: int, k: int) -> int:
@@ -136,20 +138,21 @@ def gram_schmidt(u, eps=GS_EPS):
     u: [4, S, C] (component, token, channel).  Returns (ut, steps): ut[0] =
     u[0]; for c = 1, 2, 3 the vector v starts as u[c] and, for d = 0 .. c-1 in
     turn, loses its projection onto ut[d]:
-        alpha = <v, ut[d]> / <ut[d], ut[d]>   (0 when <ut[d], ut[d]> <= eps)
+        alpha = <v, ut[d]> / <ut[d], ut[d]>   (0 when <ut[d], ut[d]> <= eps <u_d, u_d>)
         v    <- v - alpha ut[d]
     and ut[c] is the final v.  ``steps`` keeps, per (c, d), the vector before
     the step, alpha, the squared norm and the skip mask for the reverse pass.
     """
     ut = np.empty_like(u)
     ut[0] = u[0]
-    norms = [np.einsum("sc,sc->s", u[0], u[0])]
+    raw = np.einsum("xsc,xsc->xs", u, u)
+    norms = [raw[0]]
     steps = []
     for c in range(1, 4):
         v = u[c].copy()
         for d in range(c):
             n = norms[d]
-            use = n > eps
+            use = n > eps * raw[d]
             alpha = np.where(use, np.einsum("sc,sc->s", v, ut[d]) / np.where(use, n, 1.0), 0.0)
             steps.append((c, d, v.copy(), alpha, n, use))
             v = v - alpha[:, None] * ut[d]

@@ -129,3 +129,15 @@ def test_gs_backward_finite_differences(with_dxin):
     num, it = fd(L, W, picks=picks)
     for ix in it:
         assert abs(num[ix] - g["dW"][ix]) <= 1e-6 * max(1.0, abs(num[ix])), ix
+
+
+def test_gs_dependent_component_is_skipped():
+    # u_2 in the span of u_0, u_1: its residual vanishes (relative to |u_2|)
+    # and nothing is projected onto it
+    u = _rows((4, 3, 8), 12)
+    u[2] = 2.0 * u[1] - u[0]
+    ut, steps = xo.gram_schmidt(u)
+    assert np.abs(ut[2]).max() < 1e-12 * np.abs(u[2]).max()
+    assert not any(st[5].any() for st in steps if st[1] == 2)
+    ref, _ = xo.gram_schmidt(np.stack([u[0], u[1], u[3], np.zeros_like(u[0])]))
+    np.testing.assert_allclose(ut[3], ref[2], rtol=0, atol=1e-12)
