@@ -154,8 +154,8 @@ def time_oracle(sample, wl):
     from oracle import xhc_oracle as xo
     X, out, conv, W, idx, dXp = sample
     t0 = time.perf_counter()
-    xo.forward(X, out, conv, W, idx, iters=wl.iters, eps=wl.eps)
-    xo.backward(X, out, conv, W, idx, dXp, None, iters=wl.iters, eps=wl.eps)
+    xo.forward(X, out, conv, W, idx, iters=wl.iters, eps=wl.eps, gs=wl.gram_schmidt)
+    xo.backward(X, out, conv, W, idx, dXp, None, iters=wl.iters, eps=wl.eps, gs=wl.gram_schmidt)
     return time.perf_counter() - t0
 
 
@@ -199,8 +199,9 @@ def run_reference(args, wl):
 
 
 def wl_desc(wl):
+    gs = "; Gram-Schmidt of the TFA components" if wl.gram_schmidt else ""
     return (f"{wl.name}: B={wl.B} S={wl.S} N={wl.N} C={wl.C} k={wl.k} {wl.dtype}; forward (training mode: in "
-            f"place, x_in, saved logits, saved active rows) + backward (dX', no dx_in)")
+            f"place, x_in, saved logits, saved active rows) + backward (dX', no dx_in){gs}")
 
 
 # ----------------------------------------------------------------------------- GPU arm
@@ -219,7 +220,7 @@ class Step:
                 return torch.from_numpy(a).to(dev)
             return torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
 
-        self.sh = api.make_shape(wl.B, wl.S, wl.N, wl.C, wl.k, dt, wl.iters, wl.eps)
+        self.sh = api.make_shape(wl.B, wl.S, wl.N, wl.C, wl.k, dt, wl.iters, wl.eps, wl.gram_schmidt)
         self.X = act(tensors.X)
         self.out = act(tensors.out)
         self.dXp = act(tensors.dXp)

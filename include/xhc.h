@@ -83,6 +83,10 @@ typedef struct xhc_shape {
   int dtype;          /* XHC_F32 or XHC_BF16 */
   int sinkhorn_iters; /* 20 in the method's setting */
   float eps;          /* rmsnorm epsilon, 1e-6 in the method's setting */
+  int gram_schmidt;   /* 0: write back u_0..u_3 as they are (default);
+                         1: orthogonalise them first by modified Gram-Schmidt
+                         (section "Conv / Gram-Schmidt"), see
+                         xhc_sublayer_fwd.  Other values: XHC_ERR_SHAPE. */
 } xhc_shape_t;
 
 /* Human-readable name of a status code.  Never NULL. */
@@ -161,6 +165,19 @@ size_t xhc_fwd_workspace_need(const xhc_shape_t* sh, int keeps_saved);
 /*
  * xhc_sublayer_fwd -- the whole per-sublayer update: coefficients, dense
  * read, TFA and sparse write (all sections cited above).
+ *   With sh->gram_schmidt = 1 the four components are orthogonalised per
+ *   token before the write-back (section "Conv / Gram-Schmidt"): u_0 is kept
+ *   and each of u_1, u_2, u_3 in turn loses its projection onto every
+ *   orthogonalised component before it; a projection onto a component whose
+ *   residual is at most 1e-6 of its own squared norm (a zero or dependent
+ *   component) is skipped.  The library forms the per-token Gram matrix of
+ *   the components and applies the steps to the coefficients (exact up to
+ *   rounding).  Supported with conv weights on the bf16 path: the forward
+ *   for C a multiple of 64, the backward for C a multiple of 128
+ *   (XHC_ERR_DTYPE otherwise); without conv weights it changes nothing.  The
+ *   forward workspace grows by 48 bytes per token per 256 channels.
+ *   xhc_tfa and xhc_sparse_update (with conv weights) return XHC_ERR_ARG for
+ *   such a shape: they handle raw components only.
  *   X_in, X_out  as in xhc_sparse_update (X_out == X_in: in place).
  *   out, w4, w8, w12, idx  as in xhc_sparse_update.
  *   W      [P, N*C] fp32.
@@ -223,7 +240,10 @@ size_t xhc_bwd_workspace_bytes(const xhc_shape_t* sh);
  *   saved    [B,S,P+1] fp32 from the forward, or NULL to recompute it.
  *   dXp      [B,S,N,C] dtype: dL/dX', read.
  *   dx_in    [B,S,C] dtype: dL/dx_in, or NULL when x_in carries no gradient.
- *   dX       [B,S,N,C] dtype: dL/dX, written.  dX may equal dXp.
+ *   dX       [B,S,N,C] dtype: dL/dX, written.  dX must not be dXp
+ *            (XHC_ERR_ARG).
+ *   With sh->gram_schmidt = 1 the gradient is taken back through the
+ *   Gram-Schmidt step of the forward (same support as xhc_sublayer_fwd).
  *   dout     [B,S,C] dtype: dL/dout, written.
  *   dw4, dw8, dw12  [C,4], [C,8], [C,12] fp32, written (NULL when the conv
  *            weights are NULL).

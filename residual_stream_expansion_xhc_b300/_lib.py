@@ -24,7 +24,7 @@ EXPORTS = ("xhc_status_string", "xhc_last_cuda_error", "xhc_device_status", "xhc
 class XhcShape(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int), ("S", ctypes.c_int), ("N", ctypes.c_int), ("C", ctypes.c_int),
                 ("k", ctypes.c_int), ("dtype", ctypes.c_int), ("sinkhorn_iters", ctypes.c_int),
-                ("eps", ctypes.c_float)]
+                ("eps", ctypes.c_float), ("gram_schmidt", ctypes.c_int)]
 
 
 class XhcError(RuntimeError):

@@ -18,13 +18,16 @@ Tensor = torch.Tensor
 _DT = {torch.float32: XHC_F32, torch.bfloat16: XHC_BF16}
 
 
-def make_shape(B: int, S: int, N: int, C: int, k: int, dtype, iters: int = 20, eps: float = 1e-6) -> XhcShape:
-    """Build an ``xhc_shape_t``; ``dtype`` is a torch dtype or "f32"/"bf16"."""
+def make_shape(B: int, S: int, N: int, C: int, k: int, dtype, iters: int = 20, eps: float = 1e-6,
+               gram_schmidt: bool = False) -> XhcShape:
+    """Build an ``xhc_shape_t``; ``dtype`` is a torch dtype or "f32"/"bf16";
+    ``gram_schmidt`` orthogonalises the TFA components in the fused sublayer
+    forward and backward."""
     if isinstance(dtype, str):
         dt = {"f32": XHC_F32, "bf16": XHC_BF16}[dtype]
     else:
         dt = _DT[dtype]
-    return XhcShape(B, S, N, C, k, dt, iters, eps)
+    return XhcShape(B, S, N, C, k, dt, iters, eps, 1 if gram_schmidt else 0)
 
 
 def num_logits(sh: XhcShape) -> int:

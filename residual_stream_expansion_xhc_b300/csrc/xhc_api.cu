@@ -10,6 +10,7 @@
 #include "xhc_bwd.cuh"
 #include "xhc_tc.cuh"
 #include "xhc_stream.cuh"
+#include "xhc_gs.cuh"
 
 using namespace xhc;
 
@@ -36,6 +37,7 @@ int check_shape(const xhc_shape_t* sh) {
   if (!(sh->eps > 0.0f)) return XHC_ERR_SHAPE;
   if (((size_t)sh->C * esize(sh)) % 16 != 0) return XHC_ERR_ALIGN;
   if ((size_t)sh->B * (size_t)sh->S > (size_t)INT32_MAX) return XHC_ERR_SHAPE;
+  if (sh->gram_schmidt != 0 && sh->gram_schmidt != 1) return XHC_ERR_SHAPE;
   return XHC_OK;
 }
 
@@ -246,6 +248,7 @@ int xhc_tfa(const xhc_shape_t* sh, const void* out, const float* w4, const float
   int s = check_shape(sh);
   if (s) return s;
   if (tokens(sh) == 0) return XHC_OK;
+  if (sh->gram_schmidt) return XHC_ERR_ARG;          // returns the raw components only
   if ((s = check_ptrs({out, w4, w8, w12, u}, {}))) return s;
   const Params p = make_params(sh, nullptr);
   cudaStream_t st = (cudaStream_t)stream;
@@ -262,6 +265,7 @@ int xhc_sparse_update(const xhc_shape_t* sh, const void* X_in, void* X_out, cons
   bool has_conv = false;
   if ((s = check_conv(w4, w8, w12, &has_conv))) return s;
   if (tokens(sh) == 0) return XHC_OK;
+  if (sh->gram_schmidt && has_conv) return XHC_ERR_ARG;   // use xhc_sublayer_fwd
   if ((s = check_ptrs({X_in, X_out, out, hpost, hres}, {w4, w8, w12}))) return s;
   const Params p = make_params(sh, idx);
   cudaStream_t st = (cudaStream_t)stream;
@@ -291,18 +295,26 @@ size_t fwd_wsplit_bytes(const xhc_shape_t* sh) {
 size_t fwd_z_bytes(const xhc_shape_t* sh) {
   return round_up(tokens(sh) * (size_t)(sh->N + 4 * sh->k + sh->k * sh->k + 1) * sizeof(float));
 }
+// Gram-Schmidt: per-token Gram partials, one set per 256-channel block
+size_t gs_gpart_bytes(const xhc_shape_t* sh) {
+  if (!sh->gram_schmidt) return 0;
+  const Params p = make_params(sh, nullptr);
+  return round_up(tokens(sh) * (size_t)gs_gram_blocks(p) * GS_PSTRIDE * sizeof(float));
+}
 }  // namespace
 
 size_t xhc_fwd_workspace_bytes(const xhc_shape_t* sh) {
   if (check_shape(sh)) return 0;
   const Params p = make_params(sh, nullptr);
-  return (fwd_uses_coef(sh, p) ? fwd_coef_bytes(sh) : 0) + fwd_wsplit_bytes(sh) + fwd_z_bytes(sh);
+  return (fwd_uses_coef(sh, p) ? fwd_coef_bytes(sh) : 0) + fwd_wsplit_bytes(sh) + fwd_z_bytes(sh) +
+         gs_gpart_bytes(sh);
 }
 
 size_t xhc_fwd_workspace_need(const xhc_shape_t* sh, int keeps_saved) {
   if (check_shape(sh)) return 0;
   const Params p = make_params(sh, nullptr);
-  return (fwd_uses_coef(sh, p) ? fwd_coef_bytes(sh) : 0) + fwd_wsplit_bytes(sh) + (keeps_saved ? 0 : fwd_z_bytes(sh));
+  return (fwd_uses_coef(sh, p) ? fwd_coef_bytes(sh) : 0) + fwd_wsplit_bytes(sh) + (keeps_saved ? 0 : fwd_z_bytes(sh)) +
+         gs_gpart_bytes(sh);
 }
 
 int xhc_sublayer_fwd(const xhc_shape_t* sh, const void* X_in, void* X_out, const void* out, const float* w4,
@@ -317,18 +329,28 @@ int xhc_sublayer_fwd(const xhc_shape_t* sh, const void* X_in, void* X_out, const
   if ((s = check_ptrs({X_in, X_out, out, W}, {w4, w8, w12, x_in, saved, saved_active, workspace}))) return s;
   const Params p = make_params(sh, idx);
   const bool use_coef = fwd_uses_coef(sh, p);
+  const bool gs = sh->gram_schmidt && has_conv;
+  if (gs && !use_coef) return XHC_ERR_DTYPE;
   const size_t need = xhc_fwd_workspace_need(sh, saved != nullptr);
   if (need > 0 && (!workspace || ws_bytes < need)) return XHC_ERR_WORKSPACE;
   char* ws = (char*)workspace;
   float* coef = use_coef ? (float*)ws : nullptr;
   void* wsplit = use_coef ? (void*)(ws + fwd_coef_bytes(sh)) : nullptr;
-  float* z = saved ? saved : (float*)(ws + (use_coef ? fwd_coef_bytes(sh) + fwd_wsplit_bytes(sh) : 0));
+  const size_t z_off = use_coef ? fwd_coef_bytes(sh) + fwd_wsplit_bytes(sh) : 0;
+  float* z = saved ? saved : (float*)(ws + z_off);
+  float* gpart = gs ? (float*)(ws + z_off + (saved ? 0 : fwd_z_bytes(sh))) : nullptr;
   cudaStream_t st = (cudaStream_t)stream;
   if (use_coef) {
     // coefficients on the tensor cores, then one streaming pass: dense read,
     // TFA and sparse write
     using T = __nv_bfloat16;
     if ((s = cuda_status(launch_coeffs_tc(p, X_in, W, wsplit, nullptr, nullptr, nullptr, z, coef, st)))) return s;
+    if (gs) {
+      // Gram-Schmidt folded into H^post (section "Conv / Gram-Schmidt")
+      const float* const w[3] = {w4, w8, w12};
+      if ((s = cuda_status(launch_gs_gram(p, (const T*)out, w, gpart, st)))) return s;
+      if ((s = cuda_status(launch_gs_fold(p, gpart, coef, nullptr, st)))) return s;
+    }
     UpdArgs<T> a{(const T*)X_in, (T*)X_out, (const T*)out, {w4, w8, w12}, nullptr, nullptr, nullptr, z,
                  (T*)x_in, (T*)saved_active, X_out != X_in};
     return cuda_status(launch_fwd_update(p, a, coef, has_conv, num_sms(), st));
@@ -352,8 +374,8 @@ namespace {
 // token), W^T (bf16 hi and lo parts, 64 each per column), the coefficient block, the column pass's coefficient dots and
 // conv partials, dW partials (one per token range).
 struct BwdLayout {
-  size_t rec, saved, dP, Wt, coef, pdot, cpart, wpart, wsplit, total;
-  int ranges, cpart_rows;
+  size_t rec, saved, dP, Wt, coef, pdot, cpart, wpart, wsplit, gpart, gsrec, sgram, total;
+  int ranges, cpart_rows, col_rows;
 };
 BwdLayout bwd_layout(const xhc_shape_t* sh) {
   const Params p = make_params(sh, nullptr);
@@ -363,7 +385,9 @@ BwdLayout bwd_layout(const xhc_shape_t* sh) {
   if (sh->dtype == XHC_BF16 && tc_bwd_supported(p)) {
     const int sms = num_sms();
     L.ranges = bwd_stream_ranges(p);
-    L.cpart_rows = bwd_col_cpart_rows(p, sms);
+    L.col_rows = bwd_col_cpart_rows(p, sms);
+    // Gram-Schmidt adds one conv-weight partial row per token range of its pass
+    L.cpart_rows = L.col_rows + (sh->gram_schmidt ? gs_bwd_rows(p) : 0);
     L.rec = 0;
     L.saved = L.rec + round_up(T * (size_t)(1 + p.N + 4 * p.k) * sizeof(float));
     L.dP = L.saved + round_up(T * (size_t)(p.P + 1) * sizeof(float));
@@ -371,9 +395,12 @@ BwdLayout bwd_layout(const xhc_shape_t* sh) {
     L.coef = L.Wt + round_up(2 * NC * 64 * sizeof(uint16_t));
     L.pdot = L.coef + round_up(T * COEF_STRIDE * sizeof(float));
     L.cpart = L.pdot + round_up(bwd_col_pdot_floats(p) * sizeof(float));
-    L.wpart = L.cpart + round_up(bwd_col_cpart_floats(p, sms) * sizeof(float));
+    L.wpart = L.cpart + round_up((size_t)L.cpart_rows * NTAPS * p.C * sizeof(float));
     L.wsplit = L.wpart + round_up((size_t)L.ranges * p.P * NC * sizeof(float));
-    L.total = L.wsplit + (tc_coeffs_supported(p) ? round_up(coeffs_wsplit_bytes(p)) : 0);
+    L.gpart = L.wsplit + (tc_coeffs_supported(p) ? round_up(coeffs_wsplit_bytes(p)) : 0);
+    L.gsrec = L.gpart + gs_gpart_bytes(sh);
+    L.sgram = L.gsrec + (sh->gram_schmidt ? round_up(T * GS_REC * sizeof(float)) : 0);
+    L.total = L.sgram + (sh->gram_schmidt ? round_up(T * 16 * sizeof(float)) : 0);
   } else {
     L.rec = 0;
     L.saved = round_up(T * (size_t)(2 * p.P + 1) * sizeof(float));
@@ -423,6 +450,8 @@ int xhc_sublayer_bwd(const xhc_shape_t* sh, const void* X_state, const void* sav
   cudaStream_t st = (cudaStream_t)stream;
   float* rec = (float*)(ws + L.rec);
   const bool tc_path = sh->dtype == XHC_BF16 && tc_bwd_supported(p);
+  const bool gs = sh->gram_schmidt && has_conv;
+  if (gs && !tc_path) return XHC_ERR_DTYPE;
   float* coef = tc_path ? (float*)(ws + L.coef) : nullptr;
   bool have_coef = false;
   const float* z = saved;
@@ -448,10 +477,21 @@ int xhc_sublayer_bwd(const xhc_shape_t* sh, const void* X_state, const void* sav
       float* cpart = (float*)(ws + L.cpart);
       float* wpart = (float*)(ws + L.wpart);
       const int sms = num_sms();
+      float* gsrec = gs ? (float*)(ws + L.gsrec) : nullptr;
+      float* sgram = gs ? (float*)(ws + L.sgram) : nullptr;
+      const float* const w[3] = {w4, w8, w12};
       if ((s = cuda_status(launch_wt_prep(p, W, Wt, st)))) return s;
       if (!have_coef && (s = cuda_status(launch_coef(p, z, coef, st)))) return s;
+      if (gs) {
+        // the forward's Gram-Schmidt coefficients again: H^post' in the block, T and M per token
+        if ((s = cuda_status(launch_gs_gram(p, (const T*)out, w, (float*)(ws + L.gpart), st)))) return s;
+        if ((s = cuda_status(launch_gs_fold(p, (const float*)(ws + L.gpart), coef, gsrec, st)))) return s;
+      }
       if ((s = cuda_status(launch_bwd_col(p, a, coef, has_conv, pdot, cpart, sms, st)))) return s;
-      if ((s = cuda_status(launch_bwd_dz(p, z, pdot, dx_in != nullptr, dP, rec, st)))) return s;
+      if ((s = cuda_status(launch_bwd_dz(p, z, pdot, dx_in != nullptr, dP, rec, gsrec, sgram, st)))) return s;
+      if (gs && (s = cuda_status(launch_gs_bwd(p, (const T*)out, w, sgram, (T*)dout,
+                                               cpart + (size_t)L.col_rows * NTAPS * p.C, st))))
+        return s;
       if ((s = cuda_status(launch_bwd_stream_tc(p, a, Wt, dP, L.ranges, wpart, st)))) return s;
       return cuda_status(launch_bwd_reduce(p, a, has_conv, cpart, L.cpart_rows, L.ranges, wpart, st));
     }

@@ -23,6 +23,7 @@
 // in shared memory, so every row of `out` is read from HBM once per walk.
 #include <algorithm>
 
+#include "xhc_gs.cuh"
 #include "xhc_stream.cuh"
 
 namespace xhc {
@@ -925,9 +926,11 @@ __global__ void __launch_bounds__(col::THREADS, 3) bwd_col_kernel(Params p, BwdA
 //   alpha = <dz, z / rstd> * (-rstd^3 / (N C))   -> rec[t][0]
 //   hpre[n]                               -> rec[t][1 + n]
 
+template <bool GS>
 __global__ void __launch_bounds__(256) bwd_dz_kernel(Params p, const float* __restrict__ saved,
                                                      const float* __restrict__ pdot, int ncb, int has_dxin,
                                                      __nv_bfloat16* __restrict__ dP, float* __restrict__ rec,
+                                                     const float* __restrict__ gsrec, float* __restrict__ sgram,
                                                      size_t T_all) {
   extern __shared__ float trace_s[];           // [16 tokens][iters][32]
   const int lane = threadIdx.x & 31, e = lane & 15;
@@ -976,8 +979,55 @@ __global__ void __launch_bounds__(256) bwd_dz_kernel(Params p, const float* __re
   }
   const float dz_res = valid ? g * M0 : 0.0f;
   float dz_post = 0.0f, dz_pre = 0.0f, hpre = 0.0f;
-  if (e < 4 * k) {
-    const float h = sigmoidf_(zt[N + e]);
+  const float h = e < 4 * k ? sigmoidf_(zt[N + e]) : 0.0f;
+  if (GS) {
+    // The write-back used H^post' = H^post T (Gram-Schmidt coefficients T of
+    // this token); dpost holds dL/dH^post'[i][d] at lane 4 i + d.
+    //   dL/dH^post[i][c] = sum_d dL/dH^post'[i][d] T[c][d]
+    //   dL/dT[c][d]     = sum_i H^post[i][c] dL/dH^post'[i][d]
+    // then back through the Gram-Schmidt steps to dL/dM, and S = dM + dM^T
+    // (the Gram term of dL/du, applied by the Gram pass) to sgram.
+    const int base = lane & 16;
+    float D[16], H[16];
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+      D[q] = __shfl_sync(FULL, dpost, base + q);
+      H[q] = __shfl_sync(FULL, h, base + q);
+    }
+    const float* gr = gsrec + tc * GS_REC;
+    float T[4][4], M[4][4], dT[4][4], dM[4][4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      const float4 a = *reinterpret_cast<const float4*>(gr + 4 * c);
+      const float4 b = *reinterpret_cast<const float4*>(gr + 16 + 4 * c);
+      T[c][0] = a.x; T[c][1] = a.y; T[c][2] = a.z; T[c][3] = a.w;
+      M[c][0] = b.x; M[c][1] = b.y; M[c][2] = b.z; M[c][3] = b.w;
+    }
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+#pragma unroll
+      for (int d = 0; d < 4; ++d) {
+        float s = 0.0f;
+#pragma unroll
+        for (int i = 0; i < KMAX; ++i) s = fmaf(H[4 * i + c], D[4 * i + d], s);
+        dT[c][d] = s;
+      }
+    gs_coeffs_reverse(M, dT, dM);
+    float dh = 0.0f, sg = 0.0f;
+#pragma unroll
+    for (int q = 0; q < 16; ++q) {
+      const int i = q >> 2, c = q & 3;
+      float s = 0.0f;
+#pragma unroll
+      for (int d = 0; d < 4; ++d) s = fmaf(D[4 * i + d], T[c][d], s);
+      if (q == e) {
+        dh = s;
+        sg = dM[i][c] + dM[c][i];
+      }
+    }
+    if (live) sgram[t * 16 + e] = sg;
+    if (e < 4 * k) dz_post = dh * h * (1.0f - h);
+  } else if (e < 4 * k) {
     dz_post = dpost * h * (1.0f - h);
   }
   if (e < N) {
@@ -1072,14 +1122,20 @@ cudaError_t launch_bwd_col(const Params& p, const BwdArgs<__nv_bfloat16>& a, con
 }
 
 cudaError_t launch_bwd_dz(const Params& p, const float* saved, const float* pdot, bool has_dxin,
-                          __nv_bfloat16* dP, float* rec, cudaStream_t st) {
+                          __nv_bfloat16* dP, float* rec, const float* gsrec, float* sgram, cudaStream_t st) {
   const size_t T_all = (size_t)p.B * p.S;
   const int ncb = (p.C + col::CB - 1) / col::CB;
   const size_t smem = (size_t)16 * std::max(p.iters, 1) * 32 * sizeof(float);
-  cudaFuncSetAttribute(bwd_dz_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  const unsigned grid = (unsigned)((T_all + 15) / 16);
   timing_begin("bwd_dz", st);
-  bwd_dz_kernel<<<(unsigned)((T_all + 15) / 16), 256, smem, st>>>(p, saved, pdot, ncb, has_dxin ? 1 : 0, dP, rec,
-                                                                   T_all);
+  if (gsrec) {
+    cudaFuncSetAttribute(bwd_dz_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    bwd_dz_kernel<true><<<grid, 256, smem, st>>>(p, saved, pdot, ncb, has_dxin ? 1 : 0, dP, rec, gsrec, sgram, T_all);
+  } else {
+    cudaFuncSetAttribute(bwd_dz_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    bwd_dz_kernel<false><<<grid, 256, smem, st>>>(p, saved, pdot, ncb, has_dxin ? 1 : 0, dP, rec, nullptr, nullptr,
+                                                  T_all);
+  }
   timing_end(st);
   return cudaGetLastError();
 }

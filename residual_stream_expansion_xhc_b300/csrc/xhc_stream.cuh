@@ -22,8 +22,9 @@ cudaError_t launch_bwd_col(const Params& p, const BwdArgs<__nv_bfloat16>& a, con
                            float* pdot, float* cpart, int sms, cudaStream_t st);
 
 // Backward per-token reverse: dp (bf16, 64 per token) and records
-// [alpha | hpre (N) | unused (4k)].
+// [alpha | hpre (N) | unused (4k)].  With Gram-Schmidt (gsrec = the per-token
+// T and M records, non-NULL) also the Gram term S [T, 16] into sgram.
 cudaError_t launch_bwd_dz(const Params& p, const float* saved, const float* pdot, bool has_dxin,
-                          __nv_bfloat16* dP, float* rec, cudaStream_t st);
+                          __nv_bfloat16* dP, float* rec, const float* gsrec, float* sgram, cudaStream_t st);
 
 }  // namespace xhc

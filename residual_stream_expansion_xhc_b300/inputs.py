@@ -39,6 +39,7 @@ class Workload:
     conv_std: float = 0.02
     iters: int = 20
     eps: float = 1e-6
+    gram_schmidt: bool = False    # orthogonalise the TFA components
 
     @property
     def P(self) -> int:
@@ -62,6 +63,11 @@ WORKLOADS = {
                          conv="none", identity_idx=True, backward=True),
     # a quarter of the forward + backward workload (state 268 MB, above L2) for profiler captures
     "quarter_bf16": Workload("quarter_bf16", 6, B=1, S=4096, N=16, C=2048, k=4, dtype="bf16", backward=True),
+    # forward + backward with Gram-Schmidt of the TFA components; conv weights
+    # large enough (std 0.3) that the components are of the size of `out` and
+    # correlated with it, so the orthogonalisation changes the write-back
+    "gs_bf16": Workload("gs_bf16", 7, B=4, S=4096, N=16, C=2048, k=4, dtype="bf16", backward=True,
+                        conv_std=0.3, gram_schmidt=True),
 }
 
 

@@ -138,3 +138,43 @@ def test_copy_rejections(lib):
     assert lib.LIB.xhc_copy(FAKE, FAKE, 24, None) == 3
     assert lib.LIB.xhc_copy(None, FAKE, 32, None) == 8
     assert lib.LIB.xhc_copy(FAKE, FAKE, 0, None) == 0
+
+
+# ---------------------------------------------------------------- Gram-Schmidt flag
+
+def gs_shape(lib, **kw):
+    sh = shape(lib, **kw)
+    sh.gram_schmidt = 1
+    return sh
+
+
+def test_gram_schmidt_flag_validated(lib):
+    sh = shape(lib)
+    sh.gram_schmidt = 2
+    assert fwd(lib, sh, idx(0, 1, 2, 3)) == 1
+    assert lib.LIB.xhc_fwd_workspace_bytes(ctypes.byref(sh)) == 0
+
+
+def test_gram_schmidt_workspace_sizes(lib):
+    L = lib.LIB
+    up = lambda b: (b + 255) // 256 * 256             # noqa: E731
+    plain, gs = shape(lib, B=3, S=100, C=512), gs_shape(lib, B=3, S=100, C=512)
+    gpart = up(300 * 2 * 12 * 4)                      # 12 floats per token and 256-channel block
+    for keeps in (0, 1):
+        assert L.xhc_fwd_workspace_need(ctypes.byref(gs), keeps) == L.xhc_fwd_workspace_need(ctypes.byref(plain), keeps) + gpart
+    assert L.xhc_bwd_workspace_bytes(ctypes.byref(gs)) > L.xhc_bwd_workspace_bytes(ctypes.byref(plain)) + gpart
+
+
+def test_gram_schmidt_rejections(lib):
+    L = lib.LIB
+    conv = (FAKE, FAKE, FAKE)
+    # the fp32 path and a C the tensor-core passes do not tile have no Gram-Schmidt
+    assert fwd(lib, gs_shape(lib, dtype=0), idx(0, 1, 2, 3), conv=conv) == 4
+    assert fwd(lib, gs_shape(lib, C=72), idx(0, 1, 2, 3), conv=conv) == 4
+    # without conv weights the flag changes nothing (missing workspace reported as usual)
+    assert fwd(lib, gs_shape(lib, dtype=0), idx(0, 1, 2, 3)) == 5
+    # building blocks handle raw components only
+    sh = gs_shape(lib)
+    assert L.xhc_tfa(ctypes.byref(sh), FAKE, FAKE, FAKE, FAKE, FAKE, None) == 8
+    assert L.xhc_sparse_update(ctypes.byref(sh), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                               idx(0, 1, 2, 3), None) == 8

@@ -9,6 +9,8 @@ saved active rows, no gradient through x_in).
   conv-weight gradients, which sum over all tokens, in full.
 * B=4, S=4096, C=2048, N=4, k=4 with no convolution branches (the mHC shape):
   forward + backward in full.
+* B=4, S=4096, C=2048, N=16, k=4 with Gram-Schmidt of the TFA components
+  (conv weights std 0.3): forward + backward in full.
 * B=2, S=8192, C=4096, 8 sublayers with the state carried in place: on
   sampled tokens, every sublayer against the oracle fed the state the GPU
   carried into it.  A token's update reads only its own state and the last 12
@@ -38,7 +40,7 @@ HALO = 11
 
 
 def _shape(wl):
-    return api.make_shape(wl.B, wl.S, wl.N, wl.C, wl.k, tdtype(wl), wl.iters, wl.eps)
+    return api.make_shape(wl.B, wl.S, wl.N, wl.C, wl.k, tdtype(wl), wl.iters, wl.eps, wl.gram_schmidt)
 
 
 def _conv64(t):
@@ -84,7 +86,8 @@ def _check_forward(wl, t, X0_host, sub):
     conv, W = _conv64(t), np.asarray(t.W, np.float64)
     for b in range(wl.B):
         Xb = xin.to_f64(wl, X0_host[b:b + 1])
-        ref = xo.forward(Xb, xin.to_f64(wl, t.out[b:b + 1]), conv, W, idx, iters=wl.iters, eps=wl.eps)
+        ref = xo.forward(Xb, xin.to_f64(wl, t.out[b:b + 1]), conv, W, idx, iters=wl.iters, eps=wl.eps,
+                         gs=wl.gram_schmidt)
         Xp = sub.X[b:b + 1]
         got_bits = Xp[:, :, inactive].view(torch.int16).cpu().numpy()
         assert np.array_equal(got_bits, X0_host[b:b + 1][:, :, inactive].view(np.int16)), f"seq {b}: inactive rows"
@@ -108,7 +111,7 @@ def test_fullsize_forward_bf16():
     _check_forward(wl, t, t.X, sub)
 
 
-@pytest.mark.parametrize("name", ["fwdbwd_bf16", "mhc_bf16"])
+@pytest.mark.parametrize("name", ["fwdbwd_bf16", "mhc_bf16", "gs_bf16"])
 def test_fullsize_forward_backward(name):
     wl = xin.WORKLOADS[name]
     t = xin.make(wl, grads=True)
@@ -124,7 +127,7 @@ def test_fullsize_forward_backward(name):
     dconv_ref = None if conv is None else [np.zeros_like(w) for w in conv]
     for b in range(wl.B):
         ref = xo.backward(xin.to_f64(wl, t.X[b:b + 1]), xin.to_f64(wl, t.out[b:b + 1]), conv, W, t.idx,
-                          xin.to_f64(wl, t.dXp[b:b + 1]), None, iters=wl.iters, eps=wl.eps)
+                          xin.to_f64(wl, t.dXp[b:b + 1]), None, iters=wl.iters, eps=wl.eps, gs=wl.gram_schmidt)
         for key, got in (("dX", dX[b:b + 1]), ("dout", dout[b:b + 1])):
             e = xo.max_rel_err(host_f64(got), ref[key])
             assert e <= tol, f"seq {b}: {key} err {e}"
