@@ -374,7 +374,7 @@ namespace {
 // token), W^T (bf16 hi and lo parts, 64 each per column), the coefficient block, the column pass's coefficient dots and
 // conv partials, dW partials (one per token range).
 struct BwdLayout {
-  size_t rec, saved, dP, Wt, coef, pdot, cpart, wpart, wsplit, gpart, gsrec, sgram, total;
+  size_t rec, saved, dP, Wt, coef, pdot, cpart, wpart, wsplit, gpart, gsrec, sgram, gsdh, total;
   int ranges, cpart_rows, col_rows;
 };
 BwdLayout bwd_layout(const xhc_shape_t* sh) {
@@ -400,7 +400,8 @@ BwdLayout bwd_layout(const xhc_shape_t* sh) {
     L.gpart = L.wsplit + (tc_coeffs_supported(p) ? round_up(coeffs_wsplit_bytes(p)) : 0);
     L.gsrec = L.gpart + gs_gpart_bytes(sh);
     L.sgram = L.gsrec + (sh->gram_schmidt ? round_up(T * GS_REC * sizeof(float)) : 0);
-    L.total = L.sgram + (sh->gram_schmidt ? round_up(T * 16 * sizeof(float)) : 0);
+    L.gsdh = L.sgram + (sh->gram_schmidt ? round_up(T * 16 * sizeof(float)) : 0);
+    L.total = L.gsdh + (sh->gram_schmidt ? round_up(T * 16 * sizeof(float)) : 0);
   } else {
     L.rec = 0;
     L.saved = round_up(T * (size_t)(2 * p.P + 1) * sizeof(float));
@@ -479,6 +480,7 @@ int xhc_sublayer_bwd(const xhc_shape_t* sh, const void* X_state, const void* sav
       const int sms = num_sms();
       float* gsrec = gs ? (float*)(ws + L.gsrec) : nullptr;
       float* sgram = gs ? (float*)(ws + L.sgram) : nullptr;
+      float* gsdh = gs ? (float*)(ws + L.gsdh) : nullptr;
       const float* const w[3] = {w4, w8, w12};
       if ((s = cuda_status(launch_wt_prep(p, W, Wt, st)))) return s;
       if (!have_coef && (s = cuda_status(launch_coef(p, z, coef, st)))) return s;
@@ -488,7 +490,8 @@ int xhc_sublayer_bwd(const xhc_shape_t* sh, const void* X_state, const void* sav
         if ((s = cuda_status(launch_gs_fold(p, (const float*)(ws + L.gpart), coef, gsrec, st)))) return s;
       }
       if ((s = cuda_status(launch_bwd_col(p, a, coef, has_conv, pdot, cpart, sms, st)))) return s;
-      if ((s = cuda_status(launch_bwd_dz(p, z, pdot, dx_in != nullptr, dP, rec, gsrec, sgram, st)))) return s;
+      if (gs && (s = cuda_status(launch_gs_rev(p, z, pdot, gsrec, gsdh, sgram, st)))) return s;
+      if ((s = cuda_status(launch_bwd_dz(p, z, pdot, dx_in != nullptr, dP, rec, gsdh, st)))) return s;
       if (gs && (s = cuda_status(launch_gs_bwd(p, (const T*)out, w, sgram, (T*)dout,
                                                cpart + (size_t)L.col_rows * NTAPS * p.C, st))))
         return s;

@@ -930,8 +930,7 @@ template <bool GS>
 __global__ void __launch_bounds__(256) bwd_dz_kernel(Params p, const float* __restrict__ saved,
                                                      const float* __restrict__ pdot, int ncb, int has_dxin,
                                                      __nv_bfloat16* __restrict__ dP, float* __restrict__ rec,
-                                                     const float* __restrict__ gsrec, float* __restrict__ sgram,
-                                                     size_t T_all) {
+                                                     const float* __restrict__ gsdh, size_t T_all) {
   extern __shared__ float trace_s[];           // [16 tokens][iters][32]
   const int lane = threadIdx.x & 31, e = lane & 15;
   const int slot = (threadIdx.x >> 5) * 2 + (lane >> 4);
@@ -981,52 +980,8 @@ __global__ void __launch_bounds__(256) bwd_dz_kernel(Params p, const float* __re
   float dz_post = 0.0f, dz_pre = 0.0f, hpre = 0.0f;
   const float h = e < 4 * k ? sigmoidf_(zt[N + e]) : 0.0f;
   if (GS) {
-    // The write-back used H^post' = H^post T (Gram-Schmidt coefficients T of
-    // this token); dpost holds dL/dH^post'[i][d] at lane 4 i + d.
-    //   dL/dH^post[i][c] = sum_d dL/dH^post'[i][d] T[c][d]
-    //   dL/dT[c][d]     = sum_i H^post[i][c] dL/dH^post'[i][d]
-    // then back through the Gram-Schmidt steps to dL/dM, and S = dM + dM^T
-    // (the Gram term of dL/du, applied by the Gram pass) to sgram.
-    const int base = lane & 16;
-    float D[16], H[16];
-#pragma unroll
-    for (int q = 0; q < 16; ++q) {
-      D[q] = __shfl_sync(FULL, dpost, base + q);
-      H[q] = __shfl_sync(FULL, h, base + q);
-    }
-    const float* gr = gsrec + tc * GS_REC;
-    float T[4][4], M[4][4], dT[4][4], dM[4][4];
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      const float4 a = *reinterpret_cast<const float4*>(gr + 4 * c);
-      const float4 b = *reinterpret_cast<const float4*>(gr + 16 + 4 * c);
-      T[c][0] = a.x; T[c][1] = a.y; T[c][2] = a.z; T[c][3] = a.w;
-      M[c][0] = b.x; M[c][1] = b.y; M[c][2] = b.z; M[c][3] = b.w;
-    }
-#pragma unroll
-    for (int c = 0; c < 4; ++c)
-#pragma unroll
-      for (int d = 0; d < 4; ++d) {
-        float s = 0.0f;
-#pragma unroll
-        for (int i = 0; i < KMAX; ++i) s = fmaf(H[4 * i + c], D[4 * i + d], s);
-        dT[c][d] = s;
-      }
-    gs_coeffs_reverse(M, dT, dM);
-    float dh = 0.0f, sg = 0.0f;
-#pragma unroll
-    for (int q = 0; q < 16; ++q) {
-      const int i = q >> 2, c = q & 3;
-      float s = 0.0f;
-#pragma unroll
-      for (int d = 0; d < 4; ++d) s = fmaf(D[4 * i + d], T[c][d], s);
-      if (q == e) {
-        dh = s;
-        sg = dM[i][c] + dM[c][i];
-      }
-    }
-    if (live) sgram[t * 16 + e] = sg;
-    if (e < 4 * k) dz_post = dh * h * (1.0f - h);
+    // dL/dH^post through the Gram-Schmidt fold, from gs_rev_kernel
+    if (e < 4 * k) dz_post = gsdh[tc * 16 + e] * h * (1.0f - h);
   } else if (e < 4 * k) {
     dz_post = dpost * h * (1.0f - h);
   }
@@ -1060,6 +1015,94 @@ __global__ void __launch_bounds__(256) bwd_dz_kernel(Params p, const float* __re
   float* rc = rec + t * rl;
   if (e == 0) rc[0] = -part * rstd * rstd / (float)((size_t)N * p.C);
   if (e < N) rc[1 + e] = hpre;
+}
+
+// ---------------------------------------------------------------- Gram-Schmidt reverse
+//
+// One thread per token.  The write-back used H^post' = H^post T (T: the
+// token's Gram-Schmidt coefficients); the column pass's dots give
+// D[i][d] = dL/dH^post'[i][d] (summed over the channel blocks here).
+//   dL/dH^post[i][c] = sum_d D[i][d] T[c][d]            -> gsdh (read by bwd_dz)
+//   dL/dT[c][d]      = sum_i H^post[i][c] D[i][d]
+// then back through the Gram-Schmidt steps to dL/dM and S = dM + dM^T, the
+// Gram term of dL/du, to sgram (applied by gs_bwd_kernel).
+
+__global__ void __launch_bounds__(64) gs_rev_kernel(Params p, const float* __restrict__ saved,
+                                                     const float* __restrict__ pdot, int ncb,
+                                                     const float* __restrict__ gsrec, float* __restrict__ gsdh,
+                                                     float* __restrict__ sgram, size_t T_all) {
+  const size_t t = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= T_all) return;
+  float D[KMAX][4];
+#pragma unroll
+  for (int i = 0; i < KMAX; ++i)
+#pragma unroll
+    for (int d = 0; d < 4; ++d) D[i][d] = 0.0f;
+  const float* pd = pdot + t * ncb * PDOT + 16;
+  for (int c = 0; c < ncb; ++c) {
+#pragma unroll
+    for (int i = 0; i < KMAX; ++i) {
+      const float4 v = *reinterpret_cast<const float4*>(pd + (size_t)c * PDOT + 4 * i);
+      D[i][0] += v.x;
+      D[i][1] += v.y;
+      D[i][2] += v.z;
+      D[i][3] += v.w;
+    }
+  }
+  const float* zt = saved + t * (p.P + 1) + p.N;
+  float H[KMAX][4];
+#pragma unroll
+  for (int i = 0; i < KMAX; ++i)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      H[i][c] = i < p.k ? sigmoidf_(zt[4 * i + c]) : 0.0f;
+      if (i >= p.k) D[i][c] = 0.0f;
+    }
+  const float* gr = gsrec + t * GS_REC;
+  float T[4][4], M[4][4], dT[4][4], dM[4][4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const float4 a = *reinterpret_cast<const float4*>(gr + 4 * c);
+    const float4 b = *reinterpret_cast<const float4*>(gr + 16 + 4 * c);
+    T[c][0] = a.x; T[c][1] = a.y; T[c][2] = a.z; T[c][3] = a.w;
+    M[c][0] = b.x; M[c][1] = b.y; M[c][2] = b.z; M[c][3] = b.w;
+  }
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+#pragma unroll
+    for (int d = 0; d < 4; ++d) {
+      float s = 0.0f;
+#pragma unroll
+      for (int i = 0; i < KMAX; ++i) s = fmaf(H[i][c], D[i][d], s);
+      dT[c][d] = s;
+    }
+  gs_coeffs_reverse(M, dT, dM);
+  float* dh = gsdh + t * 16;
+  float* sg = sgram + t * 16;
+#pragma unroll
+  for (int i = 0; i < KMAX; ++i) {
+    float o[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      float s = 0.0f;
+#pragma unroll
+      for (int d = 0; d < 4; ++d) s = fmaf(D[i][d], T[c][d], s);
+      o[c] = s;
+    }
+    *reinterpret_cast<float4*>(dh + 4 * i) = make_float4(o[0], o[1], o[2], o[3]);
+    *reinterpret_cast<float4*>(sg + 4 * i) =
+        make_float4(dM[i][0] + dM[0][i], dM[i][1] + dM[1][i], dM[i][2] + dM[2][i], dM[i][3] + dM[3][i]);
+  }
+}
+
+cudaError_t launch_gs_rev(const Params& p, const float* saved, const float* pdot, const float* gsrec, float* gsdh,
+                          float* sgram, cudaStream_t st) {
+  const size_t T_all = (size_t)p.B * p.S;
+  const int ncb = (p.C + col::CB - 1) / col::CB;
+  timing_begin("gs_rev", st);
+  gs_rev_kernel<<<(unsigned)((T_all + 63) / 64), 64, 0, st>>>(p, saved, pdot, ncb, gsrec, gsdh, sgram, T_all);
+  timing_end(st);
+  return cudaGetLastError();
 }
 
 // ---------------------------------------------------------------- launchers
@@ -1122,19 +1165,18 @@ cudaError_t launch_bwd_col(const Params& p, const BwdArgs<__nv_bfloat16>& a, con
 }
 
 cudaError_t launch_bwd_dz(const Params& p, const float* saved, const float* pdot, bool has_dxin,
-                          __nv_bfloat16* dP, float* rec, const float* gsrec, float* sgram, cudaStream_t st) {
+                          __nv_bfloat16* dP, float* rec, const float* gsdh, cudaStream_t st) {
   const size_t T_all = (size_t)p.B * p.S;
   const int ncb = (p.C + col::CB - 1) / col::CB;
   const size_t smem = (size_t)16 * std::max(p.iters, 1) * 32 * sizeof(float);
   const unsigned grid = (unsigned)((T_all + 15) / 16);
   timing_begin("bwd_dz", st);
-  if (gsrec) {
+  if (gsdh) {
     cudaFuncSetAttribute(bwd_dz_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    bwd_dz_kernel<true><<<grid, 256, smem, st>>>(p, saved, pdot, ncb, has_dxin ? 1 : 0, dP, rec, gsrec, sgram, T_all);
+    bwd_dz_kernel<true><<<grid, 256, smem, st>>>(p, saved, pdot, ncb, has_dxin ? 1 : 0, dP, rec, gsdh, T_all);
   } else {
     cudaFuncSetAttribute(bwd_dz_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    bwd_dz_kernel<false><<<grid, 256, smem, st>>>(p, saved, pdot, ncb, has_dxin ? 1 : 0, dP, rec, nullptr, nullptr,
-                                                  T_all);
+    bwd_dz_kernel<false><<<grid, 256, smem, st>>>(p, saved, pdot, ncb, has_dxin ? 1 : 0, dP, rec, nullptr, T_all);
   }
   timing_end(st);
   return cudaGetLastError();

@@ -22,9 +22,15 @@ cudaError_t launch_bwd_col(const Params& p, const BwdArgs<__nv_bfloat16>& a, con
                            float* pdot, float* cpart, int sms, cudaStream_t st);
 
 // Backward per-token reverse: dp (bf16, 64 per token) and records
-// [alpha | hpre (N) | unused (4k)].  With Gram-Schmidt (gsrec = the per-token
-// T and M records, non-NULL) also the Gram term S [T, 16] into sgram.
+// [alpha | hpre (N) | unused (4k)].  With Gram-Schmidt, gsdh [T, 16] holds
+// dL/dH^post (from launch_gs_rev) in place of the column pass's dots.
 cudaError_t launch_bwd_dz(const Params& p, const float* saved, const float* pdot, bool has_dxin,
-                          __nv_bfloat16* dP, float* rec, const float* gsrec, float* sgram, cudaStream_t st);
+                          __nv_bfloat16* dP, float* rec, const float* gsdh, cudaStream_t st);
+
+// Gram-Schmidt reverse per token: dL/dH^post [T, 16] into gsdh and the Gram
+// term S = dM + dM^T [T, 16] into sgram, from the column pass's dots, the
+// saved logits and the per-token T and M records of launch_gs_fold.
+cudaError_t launch_gs_rev(const Params& p, const float* saved, const float* pdot, const float* gsrec, float* gsdh,
+                          float* sgram, cudaStream_t st);
 
 }  // namespace xhc
