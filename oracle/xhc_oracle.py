@@ -333,6 +333,32 @@ def backward(X, out, conv, W, idx, dXp, dx_in=None, iters=20, eps=1e-6, keep=Fal
     return res
 
 
+def expand_hres_active(W_pp, W_ra, idx, N, C):
+    """H^res logits from the k active streams only ([xHC] "Dense read, sparse
+    write": only the active streams take part in the residual mixing, so the
+    mixing logits need only their k*C entries -- the O(k^3 C) reading).
+
+    W_pp: [N + 4k, N*C] (H^pre and H^post rows over the whole state);
+    W_ra: [k*k, k*C] (H^res rows over vec(X[a_0], ..., X[a_{k-1}]), slot
+    order).  Returns the full projection [P, N*C] whose H^res rows carry W_ra
+    in the columns of the active streams and zeros elsewhere, so that
+    z_res = rstd * vec(X_A) . W_ra^T through the plain forward.
+    """
+    k = len(idx)
+    W = np.zeros((N + 4 * k + k * k, N * C))
+    W[: N + 4 * k] = W_pp
+    for j, a in enumerate(idx):
+        W[N + 4 * k:, int(a) * C:(int(a) + 1) * C] = W_ra[:, j * C:(j + 1) * C]
+    return W
+
+
+def gather_hres_active(dW, idx, N, C):
+    """dL/dW_ra from dL/dW of the expanded projection: the active streams'
+    columns of the H^res rows, in slot order."""
+    k = len(idx)
+    return np.concatenate([dW[N + 4 * k:, int(a) * C:(int(a) + 1) * C] for a in idx], axis=1)
+
+
 def max_rel_err(got, ref):
     """Error measure used by every parity check: max_i |g_i - r_i| /
     max(|r_i|, rms(r)) -- elementwise relative, floored at the tensor's RMS so

@@ -361,3 +361,44 @@ def test_max_rel_err_definition():
     rms = np.sqrt((1 + 4 + 1e-18) / 4)
     got = ref + np.array([0.01, 0.0, 0.001, 0.0])
     assert abs(xo.max_rel_err(got, ref) - max(0.01 / max(1.0, rms), 0.001 / rms)) < 1e-15
+
+
+# ---------------------------------------------------------------- H^res from the active rows only
+
+def test_hres_active_logits_definition():
+    # z_res = rstd * vec(X[a_0], .., X[a_{k-1}]) . W_ra^T, the other logits over the whole state
+    B, S, N, C, k = 1, 6, 16, 5, 4
+    X, out, cv, _, idx = case(B=B, S=S, N=N, C=C, k=k, seed=130)
+    rng = np.random.default_rng(3)
+    W_pp = rng.standard_normal((N + 4 * k, N * C)) * 0.05
+    W_ra = rng.standard_normal((k * k, k * C)) * 0.05
+    r = xo.forward(X, out, cv, xo.expand_hres_active(W_pp, W_ra, idx, N, C), idx)
+    v = X[0].reshape(S, N * C)
+    va = X[0][:, list(idx), :].reshape(S, k * C)
+    rstd = 1.0 / np.sqrt((v * v).mean(axis=1) + 1e-6)
+    np.testing.assert_allclose(r["z"][0, :, : N + 4 * k], rstd[:, None] * (v @ W_pp.T), rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(r["z"][0, :, N + 4 * k:], rstd[:, None] * (va @ W_ra.T), rtol=1e-12, atol=1e-14)
+    # the inactive streams' state does not reach the mixing logits
+    X2 = X.copy()
+    inactive = [n for n in range(N) if n not in idx]
+    X2[:, :, inactive] *= 3.0
+    r2 = xo.forward(X2, out, cv, xo.expand_hres_active(W_pp, W_ra, idx, N, C), idx)
+    np.testing.assert_allclose(r2["z"][..., N + 4 * k:] / r2["rstd"][..., None],
+                               r["z"][..., N + 4 * k:] / r["rstd"][..., None], rtol=1e-12)
+
+
+def test_hres_active_gradient_finite_differences():
+    B, S, N, C, k = 1, 8, 16, 3, 4
+    X, out, cv, _, idx = case(B=B, S=S, N=N, C=C, k=k, seed=131, wstd=0.3)
+    rng = np.random.default_rng(4)
+    W_pp = rng.standard_normal((N + 4 * k, N * C)) * 0.3
+    W_ra = rng.standard_normal((k * k, k * C)) * 0.3
+    dXp = rng.standard_normal(X.shape)
+    g = xo.backward(X, out, cv, xo.expand_hres_active(W_pp, W_ra, idx, N, C), idx, dXp)
+    dW_ra = xo.gather_hres_active(g["dW"], idx, N, C)
+
+    def L():
+        return (xo.forward(X, out, cv, xo.expand_hres_active(W_pp, W_ra, idx, N, C), idx)["Xp"] * dXp).sum()
+
+    num, _ = fd(L, W_ra)
+    np.testing.assert_allclose(dW_ra, num, rtol=1e-6, atol=1e-8)
