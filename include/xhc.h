@@ -259,6 +259,33 @@ int xhc_sublayer_bwd(const xhc_shape_t* sh, const void* X_state,
                      void* workspace, size_t ws_bytes, xhc_stream_t stream);
 
 /*
+ * xhc_hres_active_weights -- H^res logits from the k active streams only.
+ * Section "Dense read, sparse write": only the k active streams take part in
+ * the residual mixing, so its logits can be generated from their k*C state
+ * entries alone (cost O(k^3 C) instead of growing with N).  This builds the
+ * full projection that every other entry point takes, so the variant runs
+ * through them unchanged:
+ *   W_pp   [N + 4k, N*C] fp32, read: the H^pre and H^post rows (whole state).
+ *   W_ra   [k*k, k*C] fp32, read: the H^res rows over vec(X[a_0], ..,
+ *          X[a_{k-1}]) (slot order of idx).
+ *   idx    host, k entries (as in xhc_sparse_update).
+ *   W      [P, N*C] fp32, written: W_pp, then the H^res rows with W_ra in the
+ *          columns of the active streams and zeros elsewhere.
+ * rstd stays the rmsnorm scale of the whole state.
+ */
+int xhc_hres_active_weights(const xhc_shape_t* sh, const float* W_pp,
+                            const float* W_ra, const int32_t* idx, float* W,
+                            xhc_stream_t stream);
+
+/*
+ * xhc_hres_active_grad -- dL/dW_ra [k*k, k*C] fp32 (written) from the
+ * gradient dW [P, N*C] (read) of the projection built by
+ * xhc_hres_active_weights: the active streams' columns of its H^res rows.
+ */
+int xhc_hres_active_grad(const xhc_shape_t* sh, const float* dW,
+                         const int32_t* idx, float* dW_ra, xhc_stream_t stream);
+
+/*
  * xhc_copy -- device-to-device copy of `bytes` bytes with 16-byte vector
  * loads and stores.  Used to measure the HBM copy bandwidth in the same
  * process as the update kernels.  Both pointers 16-byte aligned, bytes a

@@ -124,6 +124,19 @@ def xhc_sublayer_bwd(sh, X_state, saved_active, out, conv, W, idx, saved, dXp, d
                                                     ws_bytes, _s(stream)))
 
 
+def xhc_hres_active_weights(sh, W_pp, W_ra, idx, W, stream=None):
+    """Full projection W [P, N*C] for H^res logits from the k active rows
+    only: W_pp [N+4k, N*C] and W_ra [k*k, k*C] (see the C header)."""
+    _check("xhc_hres_active_weights",
+           LIB.xhc_hres_active_weights(ctypes.byref(sh), _p(W_pp), _p(W_ra), _idx(idx), _p(W), _s(stream)))
+
+
+def xhc_hres_active_grad(sh, dW, idx, dW_ra, stream=None):
+    """dL/dW_ra [k*k, k*C] from the full projection's gradient dW."""
+    _check("xhc_hres_active_grad", LIB.xhc_hres_active_grad(ctypes.byref(sh), _p(dW), _idx(idx), _p(dW_ra),
+                                                            _s(stream)))
+
+
 def xhc_copy(src: Tensor, dst: Tensor, nbytes: Optional[int] = None, stream=None):
     n = src.numel() * src.element_size() if nbytes is None else nbytes
     _check("xhc_copy", LIB.xhc_copy(_p(src), _p(dst), n, _s(stream)))

@@ -505,6 +505,26 @@ int xhc_sublayer_bwd(const xhc_shape_t* sh, const void* X_state, const void* sav
   return cuda_status(launch_bwd_simt<float>(p, a, has_conv, (float*)(ws + L.cpart), true, st));
 }
 
+int xhc_hres_active_weights(const xhc_shape_t* sh, const float* W_pp, const float* W_ra, const int32_t* idx,
+                            float* W, xhc_stream_t stream) {
+  int s = check_shape(sh);
+  if (s) return s;
+  if ((s = check_idx(sh, idx))) return s;
+  if (sh->C % 4) return XHC_ERR_ALIGN;
+  if ((s = check_ptrs({W_pp, W_ra, W}, {}))) return s;
+  return cuda_status(launch_hres_active_weights(make_params(sh, idx), W_pp, W_ra, W, (cudaStream_t)stream));
+}
+
+int xhc_hres_active_grad(const xhc_shape_t* sh, const float* dW, const int32_t* idx, float* dW_ra,
+                         xhc_stream_t stream) {
+  int s = check_shape(sh);
+  if (s) return s;
+  if ((s = check_idx(sh, idx))) return s;
+  if (sh->C % 4) return XHC_ERR_ALIGN;
+  if ((s = check_ptrs({dW, dW_ra}, {}))) return s;
+  return cuda_status(launch_hres_active_grad(make_params(sh, idx), dW, dW_ra, (cudaStream_t)stream));
+}
+
 int xhc_copy(const void* src, void* dst, size_t bytes, xhc_stream_t stream) {
   if (!src || !dst) return XHC_ERR_ARG;
   if (!aligned16(src) || !aligned16(dst) || bytes % 16) return XHC_ERR_ALIGN;

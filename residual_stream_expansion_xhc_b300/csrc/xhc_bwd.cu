@@ -85,6 +85,59 @@ __global__ void bwd_reduce_kernel(int conv_rows, int C, const float* __restrict_
   }
 }
 
+// ============================================================== H^res from the active rows
+//
+// Section "Dense read, sparse write": the mixing logits generated from the k
+// active streams only.  The full projection W [P, N*C] carries W_ra in the
+// active streams' columns of its H^res rows (zeros elsewhere); the gradient
+// of W_ra is read back from the same columns.  One thread per 4 columns.
+
+__global__ void hres_active_weights_kernel(Params p, const float* __restrict__ W_pp, const float* __restrict__ W_ra,
+                                           float* __restrict__ W) {
+  const size_t NC = (size_t)p.N * p.C;
+  const size_t n4 = (size_t)p.P * NC / 4;
+  const int R0 = p.N + 4 * p.k;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x) {
+    const size_t r = (4 * i) / NC, col = (4 * i) % NC;
+    float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    if ((int)r < R0) {
+      v = *reinterpret_cast<const float4*>(W_pp + r * NC + col);
+    } else {
+      const int n = (int)(col / p.C), c = (int)(col % p.C), slot = p.is_active[n];
+      if (slot) v = *reinterpret_cast<const float4*>(W_ra + (r - R0) * ((size_t)p.k * p.C) + (size_t)(slot - 1) * p.C + c);
+    }
+    *reinterpret_cast<float4*>(W + r * NC + col) = v;
+  }
+}
+
+__global__ void hres_active_grad_kernel(Params p, const float* __restrict__ dW, float* __restrict__ dW_ra) {
+  const size_t kC = (size_t)p.k * p.C;
+  const size_t n4 = (size_t)p.k * p.k * kC / 4;
+  const size_t NC = (size_t)p.N * p.C;
+  const int R0 = p.N + 4 * p.k;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x) {
+    const size_t q = (4 * i) / kC, col = (4 * i) % kC;
+    const int j = (int)(col / p.C), c = (int)(col % p.C);
+    *reinterpret_cast<float4*>(dW_ra + q * kC + col) =
+        *reinterpret_cast<const float4*>(dW + (R0 + q) * NC + (size_t)p.idx[j] * p.C + c);
+  }
+}
+
+cudaError_t launch_hres_active_weights(const Params& p, const float* W_pp, const float* W_ra, float* W,
+                                       cudaStream_t st) {
+  const size_t n4 = (size_t)p.P * p.N * p.C / 4;
+  const unsigned grid = (unsigned)std::min<size_t>((n4 + 255) / 256, 148 * 16);
+  hres_active_weights_kernel<<<grid, 256, 0, st>>>(p, W_pp, W_ra, W);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_hres_active_grad(const Params& p, const float* dW, float* dW_ra, cudaStream_t st) {
+  const size_t n4 = (size_t)p.k * p.k * p.k * p.C / 4;
+  const unsigned grid = (unsigned)std::min<size_t>((n4 + 255) / 256, 148 * 16);
+  hres_active_grad_kernel<<<grid, 256, 0, st>>>(p, dW, dW_ra);
+  return cudaGetLastError();
+}
+
 // ============================================================== launchers
 
 cudaError_t launch_wt_prep(const Params& p, const float* W, __nv_bfloat16* Wt, cudaStream_t st) {

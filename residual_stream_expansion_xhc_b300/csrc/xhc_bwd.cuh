@@ -17,4 +17,10 @@ int bwd_stream_ranges(const Params& p);
 cudaError_t launch_bwd_stream_tc(const Params& p, const BwdArgs<__nv_bfloat16>& a, const __nv_bfloat16* Wt,
                                  const __nv_bfloat16* dP, int ranges, float* wpart, cudaStream_t st);
 
+// H^res logits from the active rows: full projection from W_pp, W_ra; and
+// the gradient of W_ra from the full dW (C a multiple of 4).
+cudaError_t launch_hres_active_weights(const Params& p, const float* W_pp, const float* W_ra, float* W,
+                                       cudaStream_t st);
+cudaError_t launch_hres_active_grad(const Params& p, const float* dW, float* dW_ra, cudaStream_t st);
+
 }  // namespace xhc

@@ -66,6 +66,9 @@ WORKLOADS = {
     # forward + backward with Gram-Schmidt of the TFA components; conv weights
     # large enough (std 0.3) that the components are of the size of `out` and
     # correlated with it, so the orthogonalisation changes the write-back
+    # the sublayer without TFA (u_0 = out only) at N = 16, k = 4
+    "noconv_bf16": Workload("noconv_bf16", 8, B=4, S=4096, N=16, C=2048, k=4, dtype="bf16", conv="none",
+                            backward=True),
     "gs_bf16": Workload("gs_bf16", 7, B=4, S=4096, N=16, C=2048, k=4, dtype="bf16", backward=True,
                         conv_std=0.3, gram_schmidt=True),
 }

@@ -34,6 +34,8 @@ CASES = {
     "bf16_s12": xin.Workload("bf16_s12", 18, B=2, S=12, N=16, C=256, k=4, dtype="bf16"),
     # fewest streams: one active of two
     "bf16_n2k1": xin.Workload("bf16_n2k1", 19, B=2, S=40, N=2, C=256, k=1, dtype="bf16"),
+    # the sublayer without TFA (u_0 = out only) at N = 16, k = 4
+    "bf16_noconv16": xin.Workload("bf16_noconv16", 21, B=2, S=77, N=16, C=512, k=4, dtype="bf16", conv="none"),
 }
 
 
@@ -188,7 +190,7 @@ def run_bwd(wl, t, use_saved=True, use_active=True, dx_in=True, dX_alias=False):
 
 
 BWD_CASES = ["tiny_f32", "bf16_ragged", "f32_ragged", "mhc_bf16_small", "bf16_c2048", "bf16_odd_c", "bf16_s1",
-             "bf16_s5", "bf16_s12", "bf16_n2k1"]
+             "bf16_s5", "bf16_s12", "bf16_n2k1", "bf16_noconv16"]
 
 
 @pytest.mark.parametrize("name", BWD_CASES)
