@@ -590,8 +590,9 @@ __global__ void __launch_bounds__(col::THREADS, 3) bwd_col_kernel(Params p, BwdA
     store8f(&sm.du3[t & (col::D3 - 1)][8 * l16], du[2]);
   };
 
-  // u_1..u_3 of chunk tc (8 tokens, all < s_end) from ring rows tc - 11 .. tc + 7
-  auto tfa_chunk = [&](const float2 (&tp)[12], int tc, int s_end) {
+  // u_1..u_3 of chunk tc from ring rows tc - 11 .. tc + 7 (rows of tokens past
+  // the sequence end get finite values that no dot uses: their G rows are zero)
+  auto tfa_chunk = [&](const float2 (&tp)[12], int tc) {
     float2 ow[TTc + HALO];
 #pragma unroll
     for (int i = 0; i < TTc + HALO; ++i)
@@ -608,13 +609,11 @@ __global__ void __launch_bounds__(col::THREADS, 3) bwd_col_kernel(Params p, BwdA
 #pragma unroll
         for (int tau = 0; tau < 12; ++tau) x = __ffma2_rn(tp[tau], ow[tt + HALO - tau], x);
       }
-      if (tc + tt < s_end) {
-        if (grp == 0) {
-          sm.u[0][tt][(pr + 20) & 63] = pack_bf2(x.x, x.y);   // rotations 5 and 6
-          sm.u[1][tt][(pr + 24) & 63] = pack_bf2(y.x, y.y);
-        } else {
-          sm.u[2][tt][(pr + 28) & 63] = pack_bf2(x.x, x.y);   // rotation 7
-        }
+      if (grp == 0) {
+        sm.u[0][tt][(pr + 20) & 63] = pack_bf2(x.x, x.y);     // rotations 5 and 6
+        sm.u[1][tt][(pr + 24) & 63] = pack_bf2(y.x, y.y);
+      } else {
+        sm.u[2][tt][(pr + 28) & 63] = pack_bf2(x.x, x.y);     // rotation 7
       }
     }
   };
@@ -653,11 +652,24 @@ __global__ void __launch_bounds__(col::THREADS, 3) bwd_col_kernel(Params p, BwdA
         if (lane_ok) {
           for (int t = s_end + hw; t < min(s_end + HALO, S); t += TTc) du_halo(seq_base, t, s_end);
         }
+        // du rows of tokens past the sequence end that this walk's windows
+        // reach (t0 + 10, + 14, + 18 for K = 4, 8, 12) are zero: the channel
+        // phase then needs no bounds tests.  No later token of the walk is
+        // stored in these ring rows while a window still reads them.
+        {
+          const float2 z[4] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f),
+                               make_float2(0.0f, 0.0f)};
+          for (int t = S + hw; t < t0 + TTc + HALO; t += TTc) {
+            if (t < t0 + TTc + 3) store8f(&sm.du1[t & (col::D1 - 1)][8 * l16], z);
+            if (t < t0 + TTc + 7) store8f(&sm.du2[t & (col::D2 - 1)][8 * l16], z);
+            store8f(&sm.du3[t & (col::D3 - 1)][8 * l16], z);
+          }
+        }
         __syncthreads();
         if (pair_ok) {
           float2 tp[12];
           load_tap_pairs(tp);
-          tfa_chunk(tp, t0, s_end);
+          tfa_chunk(tp, t0);
         }
         __syncthreads();
       }
@@ -838,18 +850,16 @@ __global__ void __launch_bounds__(col::THREADS, 3) bwd_col_kernel(Params p, BwdA
     if (pair_ok) {
       float2 tp[12];
       load_tap_pairs(tp);
-      if (has_next) tfa_chunk(tp, t0 - TTc, t0);
-      // convolution parts of dout: du rows t0 .. t0 + 18, zero past the sequence end
+      if (has_next) tfa_chunk(tp, t0 - TTc);
+      // convolution parts of dout: du rows t0 .. t0 + 18 (rows past the
+      // sequence end hold zeros)
       float2 part[TTc];
       if (grp == 0) {
         float2 d1[TTc + 3], d2[TTc + 7];
 #pragma unroll
         for (int i = 0; i < TTc + 7; ++i) {
-          const bool in = t0 + i < S;
-          if (i < TTc + 3) d1[i] = in ? *reinterpret_cast<const float2*>(&sm.du1[(t0 + i) & (col::D1 - 1)][2 * pr])
-                                      : make_float2(0.0f, 0.0f);
-          d2[i] = in ? *reinterpret_cast<const float2*>(&sm.du2[(t0 + i) & (col::D2 - 1)][2 * pr])
-                     : make_float2(0.0f, 0.0f);
+          if (i < TTc + 3) d1[i] = *reinterpret_cast<const float2*>(&sm.du1[(t0 + i) & (col::D1 - 1)][2 * pr]);
+          d2[i] = *reinterpret_cast<const float2*>(&sm.du2[(t0 + i) & (col::D2 - 1)][2 * pr]);
         }
 #pragma unroll
         for (int tt = 0; tt < TTc; ++tt) {
@@ -860,27 +870,23 @@ __global__ void __launch_bounds__(col::THREADS, 3) bwd_col_kernel(Params p, BwdA
           for (int tau = 0; tau < 8; ++tau) d = __ffma2_rn(tp[4 + tau], d2[tt + tau], d);
           part[tt] = d;
         }
-        // dw: this chunk's tokens only
+        // dw: this chunk's tokens (du of tokens past the end is zero)
         float2 ow[TTc + HALO];
 #pragma unroll
         for (int i = 0; i < TTc + HALO; ++i)
           ow[i] = bf2f(*reinterpret_cast<const uint32_t*>(&sm.ring[(t0 - HALO + i) & (ORc - 1)][2 * pr]));
 #pragma unroll
         for (int tt = 0; tt < TTc; ++tt) {
-          const bool ok = t0 + tt < s_end;
-          const float2 e1 = ok ? d1[tt] : make_float2(0.0f, 0.0f);
-          const float2 e2 = ok ? d2[tt] : make_float2(0.0f, 0.0f);
 #pragma unroll
-          for (int tau = 0; tau < 4; ++tau) dw[tau] = __ffma2_rn(e1, ow[tt + HALO - tau], dw[tau]);
+          for (int tau = 0; tau < 4; ++tau) dw[tau] = __ffma2_rn(d1[tt], ow[tt + HALO - tau], dw[tau]);
 #pragma unroll
-          for (int tau = 0; tau < 8; ++tau) dw[4 + tau] = __ffma2_rn(e2, ow[tt + HALO - tau], dw[4 + tau]);
+          for (int tau = 0; tau < 8; ++tau) dw[4 + tau] = __ffma2_rn(d2[tt], ow[tt + HALO - tau], dw[4 + tau]);
         }
       } else {
         float2 d3[TTc + 11];
 #pragma unroll
         for (int i = 0; i < TTc + 11; ++i)
-          d3[i] = t0 + i < S ? *reinterpret_cast<const float2*>(&sm.du3[(t0 + i) & (col::D3 - 1)][2 * pr])
-                             : make_float2(0.0f, 0.0f);
+          d3[i] = *reinterpret_cast<const float2*>(&sm.du3[(t0 + i) & (col::D3 - 1)][2 * pr]);
 #pragma unroll
         for (int tt = 0; tt < TTc; ++tt) {
           float2 d = make_float2(0.0f, 0.0f);
@@ -894,9 +900,8 @@ __global__ void __launch_bounds__(col::THREADS, 3) bwd_col_kernel(Params p, BwdA
           ow[i] = bf2f(*reinterpret_cast<const uint32_t*>(&sm.ring[(t0 - HALO + i) & (ORc - 1)][2 * pr]));
 #pragma unroll
         for (int tt = 0; tt < TTc; ++tt) {
-          const float2 e3 = t0 + tt < s_end ? d3[tt] : make_float2(0.0f, 0.0f);
 #pragma unroll
-          for (int tau = 0; tau < 12; ++tau) dw[tau] = __ffma2_rn(e3, ow[tt + HALO - tau], dw[tau]);
+          for (int tau = 0; tau < 12; ++tau) dw[tau] = __ffma2_rn(d3[tt], ow[tt + HALO - tau], dw[tau]);
         }
       }
 #pragma unroll
