@@ -194,32 +194,33 @@ __device__ __forceinline__ void stage_taps(float (*tap_s)[CB], const float* cons
   for (int g = 0; g < NTAPS; ++g) tap_s[g][ch] = t[g];
 }
 
-// u_1..u_3 of one channel for the chunk tokens t0 .. t0+7 (< s_end) from the
-// ring rows t0 - 11 .. t0 + 7; U is float (forward) or bf16 bits (backward).
+// u_1..u_3 of one channel for the chunk tokens t0 .. t0+7 from the ring rows
+// t0 - 11 .. t0 + 7 (tokens past the sequence end get values that are never
+// read); U is float or bf16 bits.  Tap-outer loops keep eight independent
+// accumulators per tap.
 template <typename U>
 __device__ __forceinline__ void tfa_chunk_s(const uint16_t (*ring)[CB], U (*u_s)[TT][CB], const float (&tap)[NTAPS],
-                                            int t0, int s_end, int ch) {
+                                            int t0, int ch) {
   float ow[TT + HALO];
 #pragma unroll
   for (int i = 0; i < TT + HALO; ++i) ow[i] = bf16_bits(ring[(t0 - HALO + i) & (ORING - 1)][ch]);
 #pragma unroll
-  for (int tt = 0; tt < TT; ++tt) {
-    if (t0 + tt >= s_end) break;
-    float u1 = 0.0f, u2 = 0.0f, u3 = 0.0f;
+  for (int j = 0; j < 3; ++j) {
+    const int K = 4 * (j + 1), g0 = (j == 0) ? 0 : (j == 1 ? 4 : 12);
+    float u[TT];
 #pragma unroll
-    for (int tau = 0; tau < 4; ++tau) u1 = fmaf(tap[tau], ow[tt + HALO - tau], u1);
+    for (int tt = 0; tt < TT; ++tt) u[tt] = 0.0f;
 #pragma unroll
-    for (int tau = 0; tau < 8; ++tau) u2 = fmaf(tap[4 + tau], ow[tt + HALO - tau], u2);
+    for (int tau = 0; tau < K; ++tau)
 #pragma unroll
-    for (int tau = 0; tau < 12; ++tau) u3 = fmaf(tap[12 + tau], ow[tt + HALO - tau], u3);
-    if constexpr (sizeof(U) == 4) {
-      u_s[0][tt][ch] = u1;
-      u_s[1][tt][ch] = u2;
-      u_s[2][tt][ch] = u3;
-    } else {
-      u_s[0][tt][ch] = __bfloat16_as_ushort(__float2bfloat16_rn(u1));
-      u_s[1][tt][ch] = __bfloat16_as_ushort(__float2bfloat16_rn(u2));
-      u_s[2][tt][ch] = __bfloat16_as_ushort(__float2bfloat16_rn(u3));
+      for (int tt = 0; tt < TT; ++tt) u[tt] = fmaf(tap[g0 + tau], ow[tt + HALO - tau], u[tt]);
+#pragma unroll
+    for (int tt = 0; tt < TT; ++tt) {
+      if constexpr (sizeof(U) == 4) {
+        u_s[j][tt][ch] = u[tt];
+      } else {
+        u_s[j][tt][ch] = __bfloat16_as_ushort(__float2bfloat16_rn(u[tt]));
+      }
     }
   }
 }
@@ -241,16 +242,17 @@ __global__ void __launch_bounds__(THREADS, 2) fwd_update_kernel(Params p, UpdArg
   const long g_total = (long)p.B * wk.nch;
   const long g_end = g_beg + wk.per < g_total ? g_beg + wk.per : g_total;
 
-  auto channel_phase = [&](int t0, int s_end) {
+  auto channel_phase = [&](int t0) {
     float tap[NTAPS];
 #pragma unroll
     for (int g = 0; g < NTAPS; ++g) tap[g] = sm.tap[g][ch];
-    tfa_chunk_s<float>(sm.ring, sm.u, tap, t0, s_end, ch);
+    tfa_chunk_s<float>(sm.ring, sm.u, tap, t0, ch);
   };
 
   bool start = true;
-  for (long g = g_beg; g < g_end; ++g) {
-    const int b = (int)(g / wk.nch), m = (int)(g % wk.nch);
+  // (b, m) = (g / nch, g mod nch), stepped up with g
+  int b = (int)(g_beg / wk.nch), m = (int)(g_beg % wk.nch);
+  for (long g = g_beg; g < g_end; ++g, (m + 1 == wk.nch ? (m = 0, ++b) : ++m)) {
     const int t0 = m * TT;
     const int s_end = min(t0 + TT, S);         // tokens of this chunk: t0 .. s_end - 1
     const size_t seq_base = (size_t)b * S;
@@ -260,7 +262,7 @@ __global__ void __launch_bounds__(THREADS, 2) fwd_update_kernel(Params p, UpdArg
       if (HAS_CONV) {
         load_out_rows(sm.ring, a.out, seq_base, S, C, c_lane, t0 - HALO, t0 + TT, warp, lane);
         __syncthreads();
-        channel_phase(t0, s_end);
+        channel_phase(t0);
         __syncthreads();
       }
     }
@@ -375,7 +377,7 @@ __global__ void __launch_bounds__(THREADS, 2) fwd_update_kernel(Params p, UpdArg
     }
     if (HAS_CONV) {
       __syncthreads();                         // u of this chunk consumed; next rows in the ring
-      if (has_next) channel_phase(t0 + TT, min(t0 + 2 * TT, S));
+      if (has_next) channel_phase(t0 + TT);
       __syncthreads();
     }
   }
@@ -597,24 +599,34 @@ __global__ void __launch_bounds__(col::THREADS, 3) bwd_col_kernel(Params p, BwdA
 #pragma unroll
     for (int i = 0; i < TTc + HALO; ++i)
       ow[i] = bf2f(*reinterpret_cast<const uint32_t*>(&sm.ring[(tc - HALO + i) & (ORc - 1)][2 * pr]));
+    // tap-outer loops: eight independent accumulators per tap
+    float2 x[TTc], y[TTc];
 #pragma unroll
     for (int tt = 0; tt < TTc; ++tt) {
-      float2 x = make_float2(0.0f, 0.0f), y = x;
-      if (grp == 0) {
+      x[tt] = make_float2(0.0f, 0.0f);
+      y[tt] = x[tt];
+    }
+    if (grp == 0) {
 #pragma unroll
-        for (int tau = 0; tau < 4; ++tau) x = __ffma2_rn(tp[tau], ow[tt + HALO - tau], x);
+      for (int tau = 0; tau < 4; ++tau)
 #pragma unroll
-        for (int tau = 0; tau < 8; ++tau) y = __ffma2_rn(tp[4 + tau], ow[tt + HALO - tau], y);
-      } else {
+        for (int tt = 0; tt < TTc; ++tt) x[tt] = __ffma2_rn(tp[tau], ow[tt + HALO - tau], x[tt]);
 #pragma unroll
-        for (int tau = 0; tau < 12; ++tau) x = __ffma2_rn(tp[tau], ow[tt + HALO - tau], x);
+      for (int tau = 0; tau < 8; ++tau)
+#pragma unroll
+        for (int tt = 0; tt < TTc; ++tt) y[tt] = __ffma2_rn(tp[4 + tau], ow[tt + HALO - tau], y[tt]);
+#pragma unroll
+      for (int tt = 0; tt < TTc; ++tt) {
+        sm.u[0][tt][(pr + 20) & 63] = pack_bf2(x[tt].x, x[tt].y);   // rotations 5 and 6
+        sm.u[1][tt][(pr + 24) & 63] = pack_bf2(y[tt].x, y[tt].y);
       }
-      if (grp == 0) {
-        sm.u[0][tt][(pr + 20) & 63] = pack_bf2(x.x, x.y);     // rotations 5 and 6
-        sm.u[1][tt][(pr + 24) & 63] = pack_bf2(y.x, y.y);
-      } else {
-        sm.u[2][tt][(pr + 28) & 63] = pack_bf2(x.x, x.y);     // rotation 7
-      }
+    } else {
+#pragma unroll
+      for (int tau = 0; tau < 12; ++tau)
+#pragma unroll
+        for (int tt = 0; tt < TTc; ++tt) x[tt] = __ffma2_rn(tp[tau], ow[tt + HALO - tau], x[tt]);
+#pragma unroll
+      for (int tt = 0; tt < TTc; ++tt) sm.u[2][tt][(pr + 28) & 63] = pack_bf2(x[tt].x, x[tt].y);   // rotation 7
     }
   };
 
@@ -862,14 +874,15 @@ __global__ void __launch_bounds__(col::THREADS, 3) bwd_col_kernel(Params p, BwdA
           d2[i] = *reinterpret_cast<const float2*>(&sm.du2[(t0 + i) & (col::D2 - 1)][2 * pr]);
         }
 #pragma unroll
-        for (int tt = 0; tt < TTc; ++tt) {
-          float2 d = make_float2(0.0f, 0.0f);
+        for (int tt = 0; tt < TTc; ++tt) part[tt] = make_float2(0.0f, 0.0f);
 #pragma unroll
-          for (int tau = 0; tau < 4; ++tau) d = __ffma2_rn(tp[tau], d1[tt + tau], d);
+        for (int tau = 0; tau < 4; ++tau)
 #pragma unroll
-          for (int tau = 0; tau < 8; ++tau) d = __ffma2_rn(tp[4 + tau], d2[tt + tau], d);
-          part[tt] = d;
-        }
+          for (int tt = 0; tt < TTc; ++tt) part[tt] = __ffma2_rn(tp[tau], d1[tt + tau], part[tt]);
+#pragma unroll
+        for (int tau = 0; tau < 8; ++tau)
+#pragma unroll
+          for (int tt = 0; tt < TTc; ++tt) part[tt] = __ffma2_rn(tp[4 + tau], d2[tt + tau], part[tt]);
         // dw: this chunk's tokens (du of tokens past the end is zero)
         float2 ow[TTc + HALO];
 #pragma unroll
@@ -888,12 +901,11 @@ __global__ void __launch_bounds__(col::THREADS, 3) bwd_col_kernel(Params p, BwdA
         for (int i = 0; i < TTc + 11; ++i)
           d3[i] = *reinterpret_cast<const float2*>(&sm.du3[(t0 + i) & (col::D3 - 1)][2 * pr]);
 #pragma unroll
-        for (int tt = 0; tt < TTc; ++tt) {
-          float2 d = make_float2(0.0f, 0.0f);
+        for (int tt = 0; tt < TTc; ++tt) part[tt] = make_float2(0.0f, 0.0f);
 #pragma unroll
-          for (int tau = 0; tau < 12; ++tau) d = __ffma2_rn(tp[tau], d3[tt + tau], d);
-          part[tt] = d;
-        }
+        for (int tau = 0; tau < 12; ++tau)
+#pragma unroll
+          for (int tt = 0; tt < TTc; ++tt) part[tt] = __ffma2_rn(tp[tau], d3[tt + tau], part[tt]);
         float2 ow[TTc + HALO];
 #pragma unroll
         for (int i = 0; i < TTc + HALO; ++i)
