@@ -194,6 +194,12 @@ __device__ __forceinline__ void stage_taps(float (*tap_s)[CB], const float* cons
   for (int g = 0; g < NTAPS; ++g) tap_s[g][ch] = t[g];
 }
 
+__device__ __forceinline__ float2 fx2(float a) { return make_float2(a, a); }
+// bf16 pair (low half first) -> two floats
+__device__ __forceinline__ float2 bfx2(uint32_t w) {
+  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+
 // u_1..u_3 of one channel for the chunk tokens t0 .. t0+7 from the ring rows
 // t0 - 11 .. t0 + 7 (tokens past the sequence end get values that are never
 // read); U is float or bf16 bits.  Tap-outer loops keep eight independent
@@ -281,9 +287,14 @@ __global__ void __launch_bounds__(THREADS, 2) fwd_update_kernel(Params p, UpdArg
 #pragma unroll
         for (int j = 0; j < KMAX; ++j)
           if (j < k) xa[j] = ld_stream(xrow + (size_t)p.idx[j] * C);
-        float acc[8];
+        // x_in partial sums in fp32x2: even and odd inactive rows apart (two
+        // independent chains), the active rows into the first
+        float2 acc[2][4];
 #pragma unroll
-        for (int x = 0; x < 8; ++x) acc[x] = 0.0f;
+        for (int x = 0; x < 4; ++x) {
+          acc[0][x] = make_float2(0.0f, 0.0f);
+          acc[1][x] = acc[0][x];
+        }
         if (need_all) {
           // the inactive streams, NI (or at most 8) rows per wave of loads
           constexpr int WAVE = NI > 0 ? NI : 8;
@@ -299,11 +310,10 @@ __global__ void __launch_bounds__(THREADS, 2) fwd_update_kernel(Params p, UpdArg
               if (q0 + q < ni) {
                 const int n = p.inactive[q0 + q];
                 if (a.x_in) {
-                  const float h = cf[n];
-                  float v[8];
-                  unpack8(xr[q], v);
+                  const float2 h = fx2(cf[n]);
+                  const uint32_t w[4] = {xr[q].x, xr[q].y, xr[q].z, xr[q].w};
 #pragma unroll
-                  for (int x = 0; x < 8; ++x) acc[x] = fmaf(h, v[x], acc[x]);
+                  for (int x = 0; x < 4; ++x) acc[q & 1][x] = __ffma2_rn(h, bfx2(w[x]), acc[q & 1][x]);
                 }
                 if (a.copy_inactive) st_stream(yrow + (size_t)n * C, xr[q]);
               }
@@ -314,14 +324,19 @@ __global__ void __launch_bounds__(THREADS, 2) fwd_update_kernel(Params p, UpdArg
 #pragma unroll
           for (int j = 0; j < KMAX; ++j) {
             if (j < k) {
-              const float h = cf[p.idx[j]];
-              float v[8];
-              unpack8(xa[j], v);
+              const float2 h = fx2(cf[p.idx[j]]);
+              const uint32_t w[4] = {xa[j].x, xa[j].y, xa[j].z, xa[j].w};
 #pragma unroll
-              for (int x = 0; x < 8; ++x) acc[x] = fmaf(h, v[x], acc[x]);
+              for (int x = 0; x < 4; ++x) acc[0][x] = __ffma2_rn(h, bfx2(w[x]), acc[0][x]);
             }
           }
-          st_stream(a.x_in + tok * C + c_lane, pack8(acc));
+          float o[8];
+#pragma unroll
+          for (int x = 0; x < 4; ++x) {
+            o[2 * x] = acc[0][x].x + acc[1][x].x;
+            o[2 * x + 1] = acc[0][x].y + acc[1][x].y;
+          }
+          st_stream(a.x_in + tok * C + c_lane, pack8(o));
         }
         if (a.saved_active) {
 #pragma unroll
@@ -345,32 +360,39 @@ __global__ void __launch_bounds__(THREADS, 2) fwd_update_kernel(Params p, UpdArg
 #pragma unroll
             for (int x = 0; x < 8; ++x) u[j][x] = 0.0f;
         }
+        // the k new active rows: independent across i (no early exit), fp32x2
 #pragma unroll
         for (int i = 0; i < KMAX; ++i) {
-          if (i >= k) break;
-          const float4 hp = *reinterpret_cast<const float4*>(cf + COEF_POST + 4 * i);
-          const float4 hr = *reinterpret_cast<const float4*>(cf + COEF_RES + 4 * i);
-          const float hrv[4] = {hr.x, hr.y, hr.z, hr.w};
-          float y[8];
+          if (i < k) {
+            const float4 hp = *reinterpret_cast<const float4*>(cf + COEF_POST + 4 * i);
+            const float4 hr = *reinterpret_cast<const float4*>(cf + COEF_RES + 4 * i);
+            const float hrv[4] = {hr.x, hr.y, hr.z, hr.w};
+            float2 y[4];
 #pragma unroll
-          for (int x = 0; x < 8; ++x) y[x] = 0.0f;
+            for (int x = 0; x < 4; ++x) y[x] = make_float2(0.0f, 0.0f);
 #pragma unroll
-          for (int j = 0; j < KMAX; ++j) {
-            if (j < k) {
-              float v[8];
-              unpack8(xa[j], v);
+            for (int j = 0; j < KMAX; ++j) {
+              if (j < k) {
+                const uint32_t w[4] = {xa[j].x, xa[j].y, xa[j].z, xa[j].w};
 #pragma unroll
-              for (int x = 0; x < 8; ++x) y[x] = fmaf(hrv[j], v[x], y[x]);
+                for (int x = 0; x < 4; ++x) y[x] = __ffma2_rn(fx2(hrv[j]), bfx2(w[x]), y[x]);
+              }
             }
-          }
 #pragma unroll
-          for (int x = 0; x < 8; ++x) {
-            y[x] = fmaf(hp.x, u[0][x], y[x]);
-            y[x] = fmaf(hp.y, u[1][x], y[x]);
-            y[x] = fmaf(hp.z, u[2][x], y[x]);
-            y[x] = fmaf(hp.w, u[3][x], y[x]);
+            for (int x = 0; x < 4; ++x) {
+              y[x] = __ffma2_rn(fx2(hp.x), make_float2(u[0][2 * x], u[0][2 * x + 1]), y[x]);
+              y[x] = __ffma2_rn(fx2(hp.y), make_float2(u[1][2 * x], u[1][2 * x + 1]), y[x]);
+              y[x] = __ffma2_rn(fx2(hp.z), make_float2(u[2][2 * x], u[2][2 * x + 1]), y[x]);
+              y[x] = __ffma2_rn(fx2(hp.w), make_float2(u[3][2 * x], u[3][2 * x + 1]), y[x]);
+            }
+            float o[8];
+#pragma unroll
+            for (int x = 0; x < 4; ++x) {
+              o[2 * x] = y[x].x;
+              o[2 * x + 1] = y[x].y;
+            }
+            st_stream(yrow + (size_t)p.idx[i] * C, pack8(o));
           }
-          st_stream(yrow + (size_t)p.idx[i] * C, pack8(y));
         }
       }
       if (refill) commit_out_row(sm.ring, t0 + TT + warp, lane, next_row);
