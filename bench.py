@@ -278,43 +278,85 @@ def copy_peak(dev):
 
 
 def e2e_run(step, tensors, steps):
-    """Host buffers through the public API: pinned host -> device copies of the
-    step's inputs (X, out, dX'), forward + backward, device -> host reads of
-    its results (X', dX, dout, dW, conv-weight gradients)."""
+    """Host buffers through the public API: every step copies its inputs
+    (X, out, dX') from pinned host memory to the device, runs the forward +
+    backward, and reads its results (X', dX, dout, dW, conv-weight gradients)
+    back to pinned host memory.
+
+    Steps are pipelined the way a training loop would: two sets of device
+    buffers, host-to-device copies on one stream, the update on another and
+    device-to-host reads on a third, so that step i + 1's inputs travel while
+    step i's results come back (the link is full duplex).  The timed region
+    starts before the first step's copies and ends after the last step's
+    reads have landed."""
     torch = step.torch
     wl = step.wl
+    dev = step.X.device
 
     def pinned(a):
         t = torch.from_numpy(a if wl.dtype == "f32" else a.view(np.int16))
         return t.pin_memory()
 
     hX, hout, hdXp = pinned(tensors.X), pinned(tensors.out), pinned(tensors.dXp)
-    rX, rdX = torch.empty_like(hX).pin_memory(), torch.empty_like(hdXp).pin_memory()
-    rdout = torch.empty_like(hout).pin_memory()
-    rdW = torch.empty(step.W.shape, dtype=torch.float32).pin_memory()
-    rdc = None if step.dconv is None else [torch.empty(w.shape, dtype=torch.float32).pin_memory() for w in step.dconv]
     as_raw = (lambda t: t) if wl.dtype == "f32" else (lambda t: t.view(torch.int16))
+    sets = [step, Step(wl, tensors, dev)]
+    res = []
+    for _ in sets:
+        rdc = None if step.dconv is None else [torch.empty(w.shape, dtype=torch.float32).pin_memory()
+                                               for w in step.dconv]
+        res.append(dict(X=torch.empty_like(hX).pin_memory(), dX=torch.empty_like(hdXp).pin_memory(),
+                        dout=torch.empty_like(hout).pin_memory(),
+                        dW=torch.empty(step.W.shape, dtype=torch.float32).pin_memory(), dconv=rdc))
+    s_in, s_comp, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    done_out = [None, None]                       # D2H of the last step that used each set
 
-    def one():
-        as_raw(step.X).copy_(hX, non_blocking=True)
-        as_raw(step.out).copy_(hout, non_blocking=True)
-        as_raw(step.dXp).copy_(hdXp, non_blocking=True)
-        step()
-        rX.copy_(as_raw(step.X), non_blocking=True)
-        rdX.copy_(as_raw(step.dX), non_blocking=True)
-        rdout.copy_(as_raw(step.dout), non_blocking=True)
-        rdW.copy_(step.dW, non_blocking=True)
-        if rdc is not None:
-            for h, d in zip(rdc, step.dconv):
-                h.copy_(d, non_blocking=True)
+    def one(i):
+        st, r = sets[i % 2], res[i % 2]
+        ev_free = done_out[i % 2]
+        with torch.cuda.stream(s_in):
+            if ev_free is not None:
+                s_in.wait_event(ev_free)
+            as_raw(st.X).copy_(hX, non_blocking=True)
+            as_raw(st.out).copy_(hout, non_blocking=True)
+            as_raw(st.dXp).copy_(hdXp, non_blocking=True)
+            ev_in = torch.cuda.Event()
+            ev_in.record(s_in)
+        with torch.cuda.stream(s_comp):
+            s_comp.wait_event(ev_in)
+            st()
+            ev_c = torch.cuda.Event()
+            ev_c.record(s_comp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_c)
+            r["X"].copy_(as_raw(st.X), non_blocking=True)
+            r["dX"].copy_(as_raw(st.dX), non_blocking=True)
+            r["dout"].copy_(as_raw(st.dout), non_blocking=True)
+            r["dW"].copy_(st.dW, non_blocking=True)
+            if r["dconv"] is not None:
+                for h, d in zip(r["dconv"], st.dconv):
+                    h.copy_(d, non_blocking=True)
+            ev_o = torch.cuda.Event()
+            ev_o.record(s_out)
+            done_out[i % 2] = ev_o
 
-    one()
-    ms = timed(one, steps)
+    one(0)
+    one(1)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(s_in)
+    for i in range(steps):
+        one(i)
+    s_in.wait_stream(s_out)
+    e1.record(s_in)
+    e1.synchronize()
+    ms = e0.elapsed_time(e1)
     h2d = sum(t.numel() * t.element_size() for t in (hX, hout, hdXp))
-    d2h = sum(t.numel() * t.element_size() for t in (rX, rdX, rdout, rdW)) + (
-        0 if rdc is None else sum(t.numel() * 4 for t in rdc))
+    r = res[0]
+    d2h = sum(r[k].numel() * r[k].element_size() for k in ("X", "dX", "dout", "dW")) + (
+        0 if r["dconv"] is None else sum(t.numel() * 4 for t in r["dconv"]))
     return {"value": wl.tokens * steps / (ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
-            "d2h_bytes_per_step": int(d2h), "ms_per_step": ms / steps}
+            "d2h_bytes_per_step": int(d2h), "ms_per_step": ms / steps,
+            "pipeline": "two buffer sets; H2D, compute and D2H on three streams"}
 
 
 def run_gpu(args, wl):
@@ -424,7 +466,7 @@ def main():
     ap.add_argument("--impl", choices=["xhc", "reference"], default="xhc")
     ap.add_argument("--workload", default="fwdbwd_bf16", choices=sorted(xin.WORKLOADS))
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--e2e-steps", type=int, default=8)
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--cpu-tokens", type=int, default=8192)
     ap.add_argument("--ref-tokens", type=int, default=256)
