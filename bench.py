@@ -36,9 +36,9 @@ METRIC = "tokens/s per xHC sublayer (fwd, fwd+bwd) and achieved HBM GB/s vs peak
 #                     + 1 (write x_in) + 4 (write saved active rows) = 26
 #   backward, token:  4 (dX' active) + 4 (old active rows) + 1 (out) = 9
 #   backward, stream: 16 (X) + 16 (dX') + 1 (out) + 16 (dX) + 1 (dout) = 50
-ALG_C = {
-    "coeffs_tc": 16, "coeffs_simt": 17, "update_simt": 26,
-    "bwd_token": 13, "bwd_tfa": 6, "bwd_stream_tc": 48,
+ALG_C = {  # algorithmic bytes per token in C-units (one row of C state elements)
+    "coeffs_tc": 16, "fwd_update": 26, "bwd_col": 14, "bwd_stream_tc": 48,
+    "coeffs_simt": 17, "update_simt": 26,
     "bwd_token_simt": 9, "bwd_dx_simt": 48, "bwd_dw_simt": 16, "bwd_tfa_simt": 6,
 }
 ALG_SIDE = {  # fp32 bytes per token

@@ -482,8 +482,11 @@ int xhc_sublayer_bwd(const xhc_shape_t* sh, const void* X_state, const void* sav
       float* sgram = gs ? (float*)(ws + L.sgram) : nullptr;
       float* gsdh = gs ? (float*)(ws + L.gsdh) : nullptr;
       const float* const w[3] = {w4, w8, w12};
-      if ((s = cuda_status(launch_wt_prep(p, W, Wt, st)))) return s;
-      if (!have_coef && (s = cuda_status(launch_coef(p, z, coef, st)))) return s;
+      if (have_coef) {
+        if ((s = cuda_status(launch_wt_prep(p, W, Wt, st)))) return s;
+      } else if ((s = cuda_status(launch_bwd_prep(p, W, Wt, z, coef, st)))) {
+        return s;
+      }
       if (gs) {
         // the forward's Gram-Schmidt coefficients again: H^post' in the block, T and M per token
         if ((s = cuda_status(launch_gs_gram(p, (const T*)out, w, (float*)(ws + L.gpart), st)))) return s;

@@ -20,9 +20,10 @@ namespace xhc {
 // operand of dV = dP . W in the stream pass, as a hi part and a lo part
 // (Wt + NC * 64 holds bf16(W - hi)), so that hi + lo keeps about 16 bits of W.
 
-__global__ void wt_prep_kernel(const float* __restrict__ W, __nv_bfloat16* __restrict__ Wt, int P, size_t NC) {
+__device__ __forceinline__ void wt_prep_block(const float* __restrict__ W, __nv_bfloat16* __restrict__ Wt, int P,
+                                              size_t NC, size_t blk) {
   __shared__ float tile[64][65];
-  const size_t col0 = (size_t)blockIdx.x * 64;
+  const size_t col0 = blk * 64;
   for (int i = threadIdx.x; i < 64 * 64; i += blockDim.x) {
     const int q = i / 64, c = i % 64;
     tile[q][c] = (q < P && col0 + c < NC) ? W[(size_t)q * NC + col0 + c] : 0.0f;
@@ -38,6 +39,21 @@ __global__ void wt_prep_kernel(const float* __restrict__ W, __nv_bfloat16* __res
       *reinterpret_cast<uint32_t*>(Wt_lo + (col0 + c) * 64 + q2) = pack_bf2(a - bf_lo(h), b - bf_hi(h));
     }
   }
+}
+
+__global__ void __launch_bounds__(256) wt_prep_kernel(const float* __restrict__ W, __nv_bfloat16* __restrict__ Wt,
+                                                      int P, size_t NC) {
+  wt_prep_block(W, Wt, P, NC, blockIdx.x);
+}
+
+// The two independent preparations of the backward in one launch: blocks
+// [0, nwt) build W^T, the others the coefficient block from the saved logits.
+__global__ void __launch_bounds__(256) bwd_prep_kernel(Params p, const float* __restrict__ W,
+                                                       __nv_bfloat16* __restrict__ Wt, unsigned nwt,
+                                                       const float* __restrict__ saved, float* __restrict__ coef,
+                                                       size_t T_all) {
+  if (blockIdx.x < nwt) wt_prep_block(W, Wt, p.P, (size_t)p.N * p.C, blockIdx.x);
+  else coef_block(p, saved, coef, T_all, blockIdx.x - nwt);
 }
 
 // Fixed-order sums: conv-weight partials [rows][24][C] and dW partials
@@ -144,6 +160,18 @@ cudaError_t launch_wt_prep(const Params& p, const float* W, __nv_bfloat16* Wt, c
   const size_t NC = (size_t)p.N * p.C;
   timing_begin("bwd_wt_prep", st);
   wt_prep_kernel<<<(unsigned)((NC + 63) / 64), 256, 0, st>>>(W, Wt, p.P, NC);
+  timing_end(st);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_prep(const Params& p, const float* W, __nv_bfloat16* Wt, const float* saved, float* coef,
+                            cudaStream_t st) {
+  const size_t NC = (size_t)p.N * p.C;
+  const size_t T_all = (size_t)p.B * p.S;
+  const unsigned nwt = (unsigned)((NC + 63) / 64);
+  const unsigned ncoef = (unsigned)((T_all * 16 + 255) / 256);
+  timing_begin("bwd_prep", st);
+  bwd_prep_kernel<<<nwt + ncoef, 256, 0, st>>>(p, W, Wt, nwt, saved, coef, T_all);
   timing_end(st);
   return cudaGetLastError();
 }

@@ -6,6 +6,10 @@
 namespace xhc {
 
 cudaError_t launch_wt_prep(const Params& p, const float* W, __nv_bfloat16* Wt, cudaStream_t st);
+// W^T (as launch_wt_prep) and the coefficient block from saved logits (as
+// launch_coef) in one launch.
+cudaError_t launch_bwd_prep(const Params& p, const float* W, __nv_bfloat16* Wt, const float* saved, float* coef,
+                            cudaStream_t st);
 // Fixed-order sums of the conv-weight partials [conv_rows][24][C] and the dW
 // partials [w_ranges][P][N C].
 cudaError_t launch_bwd_reduce(const Params& p, const BwdArgs<__nv_bfloat16>& a, bool has_conv, const float* cpart,

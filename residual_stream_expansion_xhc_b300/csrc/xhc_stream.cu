@@ -153,25 +153,7 @@ Walk make_walk(const Params& p, int sms) {
 
 __global__ void __launch_bounds__(256) coef_kernel(Params p, const float* __restrict__ saved, float* __restrict__ coef,
                                                    size_t T_all) {
-  // half-warp per token: lane e computes hpre[e], hpost[e] and H^res entry e
-  // (e = 4 i + j) with the shuffle Sinkhorn, which gives the same values as
-  // the one-thread version used by the forward
-  const int lane = threadIdx.x & 31, e = lane & 15;
-  const size_t t = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) >> 4;
-  const bool live = t < T_all;
-  const size_t tc = live ? t : 0;
-  const int N = p.N, k = p.k, P = p.P;
-  const float* z = saved + tc * (P + 1);
-  const int i = e >> 2, j = e & 3;
-  const bool valid = i < k && j < k;
-  const float hpre = e < N ? sigmoidf_(z[e]) : 0.0f;
-  const float hpost = e < 4 * k ? sigmoidf_(z[N + e]) : 0.0f;
-  const float H = sinkhorn16(valid ? z[N + 4 * k + k * i + j] : 0.0f, valid, p.iters);
-  if (!live) return;
-  float* cf = coef + t * COEF_STRIDE;
-  cf[e] = hpre;
-  cf[COEF_POST + e] = hpost;
-  cf[COEF_RES + e] = valid ? H : 0.0f;
+  coef_block(p, saved, coef, T_all, blockIdx.x);
 }
 
 // ---------------------------------------------------------------- forward update
