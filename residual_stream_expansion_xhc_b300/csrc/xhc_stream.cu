@@ -106,22 +106,6 @@ __device__ __forceinline__ void load_out_rows(uint16_t (*ring)[CB], const __nv_b
   }
 }
 
-// Reduce 32 per-lane values across the warp so that lane l ends with the sum
-// over all lanes of value l (31 shuffles: each level halves the values held).
-__device__ __forceinline__ float warp_transpose_sum32(float (&v)[32], int lane) {
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) {
-    const bool upper = (lane & o) != 0;
-#pragma unroll
-    for (int i = 0; i < o; ++i) {
-      const float send = upper ? v[i] : v[i + o];
-      const float keep = upper ? v[i + o] : v[i];
-      v[i] = keep + __shfl_xor_sync(FULL, send, o);
-    }
-  }
-  return v[0];
-}
-
 // Work split: the chunks of every sequence, numbered g = b * nch + m (chunk m
 // of sequence b), are cut into R contiguous ranges of `per` chunks; CTA
 // (r, channel block) walks range r chunk by chunk (the forward upwards, the
@@ -396,8 +380,9 @@ __global__ void __launch_bounds__(THREADS, 2) fwd_update_kernel(Params p, UpdArg
 //     G_i = dX'[a_i], Xa_j (old active rows), u_c of the token
 //     mix   dX[a_j] = sum_i Hres[i][j] G_i
 //     du_c  = sum_i hpost[i][c] G_i: du_1..du_3 -> rings, du_0 kept in registers
-//     dots  <G_i, Xa_j>, <G_i, u_c> (and <dx_in, X_n> with dx_in) reduced over the
-//           CTA's channels -> pdot[t][channel block]
+//     dots  <G_i, Xa_j>, <G_i, u_c> over the CTA's channels on mma.sync (the
+//           rows staged in shared memory) -> pdot[t][channel block]; with
+//           dx_in also <dx_in, X_n> (CUDA cores, half-warp sums)
 //     dout of the previous chunk's token = du_0 + the convolution parts the
 //           channel phase left in shared memory
 //     (and the `out` rows the channel phase of this chunk needs next)
@@ -408,7 +393,8 @@ __global__ void __launch_bounds__(THREADS, 2) fwd_update_kernel(Params p, UpdArg
 //     dw_j[tau] += du_j[t] out[t - tau], in registers for the whole walk
 // The du rows of the tokens after a walk's first chunk that its convolutions
 // reach (3, 7 and 11 for K = 4, 8, 12) are computed first: the anti-causal
-// halo.  Conv-weight partials: one row per CTA, [R][24][C].
+// halo; rows past the sequence end are zeroed.  Conv-weight partials: one row
+// per CTA, [R][24][C].
 
 namespace col {
 constexpr int CB = 128;                 // channels per CTA
