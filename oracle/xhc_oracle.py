@@ -359,6 +359,148 @@ def gather_hres_active(dW, idx, N, C):
     return np.concatenate([dW[N + 4 * k:, int(a) * C:(int(a) + 1) * C] for a in idx], axis=1)
 
 
+# ---------------------------------------------------------------- router with per-token active sets
+#
+# [xHC] "Dense read, sparse write": the router reads the LayerNorm-ed whole
+# state vec X and gives every stream a sigmoid score; some streams are always
+# active (fixed) and the others are chosen per token by top-k of the scores.
+# For a chosen (routed) stream the score multiplies that stream's new
+# write-back, so the router learns through the write-back's size; unchosen
+# scores get no gradient in this sublayer.  Readings (the pages give no
+# formulas): LayerNorm over all N*C entries without gain or bias, eps as the
+# rmsnorm's; router weights W_r [N, N*C], no bias; the fixed streams are a
+# caller-given ordered list and take the first slots; the routed slots follow
+# in descending score (ties to the lower stream index); H^post and H^res rows
+# belong to slots as in the plain update.
+
+
+def router_scores(Xs, W_r, eps):
+    """Scores of one sequence.  Xs [S, N, C], W_r [N, N*C].  Returns
+    (s [S, N] sigmoid scores, r [S, N] logits, y [S, N*C] LayerNorm-ed state,
+    sd [S] its standard deviation sqrt(var + eps))."""
+    S, N, C = Xs.shape
+    v = Xs.reshape(S, N * C)
+    mu = v.mean(axis=1)
+    sd = np.sqrt(((v - mu[:, None]) ** 2).mean(axis=1) + eps)
+    y = (v - mu[:, None]) / sd[:, None]
+    r = y @ W_r.T
+    return sigmoid(r), r, y, sd
+
+
+def route(scores, fixed, k):
+    """Per-token active slots: the fixed streams in the given order, then the
+    top (k - len(fixed)) other streams by score (descending, ties to the lower
+    index).  scores [S, N] -> idx [S, k] (int)."""
+    S, N = scores.shape
+    fixed = [int(a) for a in fixed]
+    others = [n for n in range(N) if n not in fixed]
+    idx = np.zeros((S, k), dtype=np.int64)
+    for t in range(S):
+        order = sorted(others, key=lambda n: (-scores[t, n], n))
+        idx[t] = fixed + order[: k - len(fixed)]
+    return idx
+
+
+def _routed_weights(s, idx, nfixed):
+    """w[t, i] = 1 for fixed slots, the routed stream's score otherwise."""
+    w = np.take_along_axis(s, idx, axis=1).copy()
+    w[:, :nfixed] = 1.0
+    return w
+
+
+def forward_routed(X, out, conv, W, W_r, fixed, k, iters=20, eps=1e-6):
+    """The sublayer update with per-token active sets chosen by the router.
+    X [B,S,N,C], out [B,S,C], conv as in ``forward``, W [P, N*C] (P for k
+    slots), W_r [N, N*C], fixed: the always-active streams (ordered).
+    Returns Xp, x_in, idx [B,S,k], s [B,S,N]."""
+    B, S, N, C = X.shape
+    res = dict(Xp=X.copy(), x_in=np.zeros((B, S, C)), idx=np.zeros((B, S, k), dtype=np.int64),
+               s=np.zeros((B, S, N)))
+    for b in range(B):
+        cf = _coeffs_seq(X[b], W, N, C, k, iters, eps)
+        s, _, _, _ = router_scores(X[b], W_r, eps)
+        idx = route(s, fixed, k)
+        w = _routed_weights(s, idx, len(fixed))
+        u = tfa_components(out[b], conv)
+        Xa = np.take_along_axis(X[b], idx[:, :, None], axis=1)              # [S, k, C]
+        mix = np.einsum("sij,sjc->sic", cf["hres"], Xa)
+        write = np.einsum("sic,csx->six", cf["hpost"], u) * w[:, :, None]
+        Xp = X[b].copy()
+        np.put_along_axis(Xp, idx[:, :, None], mix + write, axis=1)
+        res["Xp"][b] = Xp
+        res["x_in"][b] = np.einsum("sn,snc->sc", cf["hpre"], X[b])
+        res["idx"][b] = idx
+        res["s"][b] = s
+    return res
+
+
+def backward_routed(X, out, conv, W, W_r, fixed, k, dXp, dx_in=None, iters=20, eps=1e-6):
+    """Exact reverse mode of ``forward_routed`` (the active sets are the
+    forward's, a constant; unchosen scores get no gradient).  Returns dX, dout,
+    dconv, dW, dW_r."""
+    B, S, N, C = X.shape
+    nf = len(fixed)
+    dX = np.zeros_like(X)
+    dout = np.zeros_like(out)
+    dW = np.zeros_like(W)
+    dW_r = np.zeros_like(W_r)
+    dconv = None if conv is None else [np.zeros_like(w) for w in conv]
+    for b in range(B):
+        Xs = X[b]
+        cf = _coeffs_seq(Xs, W, N, C, k, iters, eps)
+        s, r, y, sd = router_scores(Xs, W_r, eps)
+        idx = route(s, fixed, k)
+        w = _routed_weights(s, idx, nf)
+        u = tfa_components(out[b], conv)
+        G = np.take_along_axis(dXp[b], idx[:, :, None], axis=1)             # [S, k, C]
+        Xa = np.take_along_axis(Xs, idx[:, :, None], axis=1)
+        hpre, hpost = cf["hpre"], cf["hpost"]
+        D = np.einsum("sic,xsc->six", G, u)                                  # <G_i, u_c>
+        d_hres = np.einsum("sic,sjc->sij", G, Xa)
+        d_hpost = D * w[:, :, None]
+        d_w = np.einsum("six,six->si", hpost, D)                             # dL/dw_i
+        d_hpre = np.einsum("sc,snc->sn", dx_in[b], Xs) if dx_in is not None else np.zeros((S, N))
+        dZ = sinkhorn_reverse(d_hres, cf["trace"])
+        dz = np.concatenate([d_hpre * hpre * (1.0 - hpre),
+                             (d_hpost * hpost * (1.0 - hpost)).reshape(S, 4 * k),
+                             dZ.reshape(S, k * k)], axis=1)
+        rstd, p, v = cf["rstd"], cf["p"], cf["v"]
+        dp = rstd[:, None] * dz
+        drstd = (dz * p).sum(axis=1)
+        dv = dp @ W + (drstd * (-(rstd ** 3) / (N * C)))[:, None] * v
+        dW += dp.T @ v
+        # router: scores of the routed slots scale their write-back
+        ds = np.zeros((S, N))
+        rows = np.arange(S)
+        for i in range(nf, k):
+            ds[rows, idx[:, i]] += d_w[:, i]
+        dr = ds * s * (1.0 - s)
+        dW_r += dr.T @ y
+        dy = dr @ W_r
+        dv += (dy - dy.mean(axis=1, keepdims=True) - y * (dy * y).mean(axis=1, keepdims=True)) / sd[:, None]
+        dXs = dv.reshape(S, N, C).copy()
+        if dx_in is not None:
+            dXs += hpre[:, :, None] * dx_in[b][:, None, :]
+        # per-token sparse write: a stream passes dX' through unless active
+        active = np.zeros((S, N), dtype=bool)
+        np.put_along_axis(active, idx, True, axis=1)
+        dXs += np.where(active[:, :, None], 0.0, dXp[b])
+        back = np.einsum("sij,sic->sjc", cf["hres"], G)                      # to X[a_j]
+        for j in range(k):
+            dXs[rows, idx[:, j]] += back[:, j]
+        dX[b] = dXs
+        du = np.einsum("six,sic->xsc", hpost * w[:, :, None], G)
+        dout_b = du[0].copy()
+        if conv is not None:
+            for j, wj in enumerate(conv, start=1):
+                K = wj.shape[1]
+                for tau in range(min(K, S)):
+                    dout_b[: S - tau, :] += wj[None, :, tau] * du[j, tau:, :]
+                    dconv[j - 1][:, tau] += (du[j, tau:, :] * out[b][: S - tau, :]).sum(axis=0)
+        dout[b] = dout_b
+    return dict(dX=dX, dout=dout, dconv=dconv, dW=dW, dW_r=dW_r)
+
+
 def max_rel_err(got, ref):
     """Error measure used by every parity check: max_i |g_i - r_i| /
     max(|r_i|, rms(r)) -- elementwise relative, floored at the tensor's RMS so
