@@ -225,6 +225,38 @@ int xhc_sublayer_fwd_noalloc(const xhc_shape_t* sh, const void* X_in,
                              const int32_t* idx, void* x_in, float* saved,
                              void* saved_active, xhc_stream_t stream);
 
+/*
+ * xhc_sublayer_fwd_routed -- the sublayer update with per-token active sets
+ * chosen by a router (section "Dense read, sparse write").  Per token:
+ *   scores  s = sigmoid(W_r . LN(vec X)), LN over all N*C entries, no gain
+ *           or bias, eps = sh->eps;
+ *   slots   the n_fixed streams `fixed` (host, ordered) first, then the top
+ *           k - n_fixed other streams by score (descending, ties to the lower
+ *           index);
+ *   update  as xhc_sublayer_fwd with those slots, a routed slot's write-back
+ *           sum_c H^post[i][c] u_c multiplied by its stream's score.
+ *   W_r      [N, N*C] fp32, read.
+ *   tok_idx  [B,S,k] int32 device, written: the slots.
+ *   scores   [B,S,N] fp32 device, written.
+ *   saved_active  [B,S,k,C], the active rows before the update in slot order
+ *            (may be NULL).
+ *   workspace, ws_bytes  at least xhc_fwd_routed_workspace_bytes() bytes
+ *            (required).
+ * Other arguments as in xhc_sublayer_fwd.  bf16 with C a multiple of 64
+ * (XHC_ERR_DTYPE otherwise); not combined with gram_schmidt (XHC_ERR_ARG);
+ * bad `fixed` lists give XHC_ERR_INDEX.  The router's projection is a second
+ * pass over X.
+ */
+size_t xhc_fwd_routed_workspace_bytes(const xhc_shape_t* sh);
+int xhc_sublayer_fwd_routed(const xhc_shape_t* sh, const void* X_in,
+                            void* X_out, const void* out, const float* w4,
+                            const float* w8, const float* w12, const float* W,
+                            const float* W_r, const int32_t* fixed,
+                            int n_fixed, void* x_in, float* saved,
+                            void* saved_active, int32_t* tok_idx,
+                            float* scores, void* workspace, size_t ws_bytes,
+                            xhc_stream_t stream);
+
 /* Workspace the backward needs (bytes). */
 size_t xhc_bwd_workspace_bytes(const xhc_shape_t* sh);
 

@@ -124,6 +124,25 @@ def xhc_sublayer_bwd(sh, X_state, saved_active, out, conv, W, idx, saved, dXp, d
                                                     ws_bytes, _s(stream)))
 
 
+def xhc_fwd_routed_workspace_bytes(sh) -> int:
+    return LIB.xhc_fwd_routed_workspace_bytes(ctypes.byref(sh))
+
+
+def xhc_sublayer_fwd_routed(sh, X_in, X_out, out, conv, W, W_r, fixed, tok_idx, scores, workspace, x_in=None,
+                            saved=None, saved_active=None, stream=None):
+    """The update with per-token active sets from the router (see the C
+    header): ``fixed`` is the host list of always-active streams; ``tok_idx``
+    [B,S,k] int32 and ``scores`` [B,S,N] fp32 are written."""
+    w4, w8, w12 = _conv(conv)
+    fixed = [int(a) for a in fixed]
+    fx = (ctypes.c_int32 * max(len(fixed), 1))(*fixed) if fixed else None
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check("xhc_sublayer_fwd_routed",
+           LIB.xhc_sublayer_fwd_routed(ctypes.byref(sh), _p(X_in), _p(X_out), _p(out), w4, w8, w12, _p(W),
+                                       _p(W_r), fx, len(fixed), _p(x_in), _p(saved), _p(saved_active),
+                                       _p(tok_idx), _p(scores), _p(workspace), ws_bytes, _s(stream)))
+
+
 def xhc_hres_active_weights(sh, W_pp, W_ra, idx, W, stream=None):
     """Full projection W [P, N*C] for H^res logits from the k active rows
     only: W_pp [N+4k, N*C] and W_ra [k*k, k*C] (see the C header)."""

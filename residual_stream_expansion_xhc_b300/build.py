@@ -8,7 +8,7 @@ import sys
 PKG = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG, "csrc")
 LIB = os.path.join(PKG, "libxhc.so")
-SOURCES = ["xhc_api.cu", "xhc_simt.cu", "xhc_bwd.cu", "xhc_tc.cu", "xhc_stream.cu", "xhc_gs.cu", "xhc_noalloc.cu"]
+SOURCES = ["xhc_api.cu", "xhc_simt.cu", "xhc_bwd.cu", "xhc_tc.cu", "xhc_stream.cu", "xhc_gs.cu", "xhc_router.cu", "xhc_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

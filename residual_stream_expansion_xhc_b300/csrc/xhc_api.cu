@@ -11,6 +11,7 @@
 #include "xhc_tc.cuh"
 #include "xhc_stream.cuh"
 #include "xhc_gs.cuh"
+#include "xhc_router.cuh"
 
 using namespace xhc;
 
@@ -365,6 +366,72 @@ int xhc_sublayer_fwd(const xhc_shape_t* sh, const void* X_in, void* X_out, const
   UpdArgs<float> a{(const float*)X_in, (float*)X_out, (const float*)out, {w4, w8, w12}, nullptr, nullptr, nullptr,
                    z, nullptr, (float*)saved_active, X_out != X_in};
   return cuda_status(launch_update_simt<float>(p, a, has_conv, st));
+}
+
+namespace {
+// Router forward workspace: the plain forward's, then W' [P, N*C] fp32, the
+// router pass's logits [T, P+1] and the row sums of W_r.
+size_t routed_extra_bytes(const xhc_shape_t* sh) {
+  const size_t NC = (size_t)sh->N * sh->C;
+  const size_t P = (size_t)(sh->N + 4 * sh->k + sh->k * sh->k);
+  return round_up(P * NC * sizeof(float)) + round_up(tokens(sh) * (P + 1) * sizeof(float)) +
+         round_up((size_t)sh->N * sizeof(float));
+}
+
+int check_fixed(const xhc_shape_t* sh, const int32_t* fixed, int nf) {
+  if (nf < 0 || nf > sh->k || (nf > 0 && !fixed)) return XHC_ERR_INDEX;
+  for (int i = 0; i < nf; ++i) {
+    if (fixed[i] < 0 || fixed[i] >= sh->N) return XHC_ERR_INDEX;
+    for (int j = 0; j < i; ++j)
+      if (fixed[j] == fixed[i]) return XHC_ERR_INDEX;
+  }
+  return XHC_OK;
+}
+}  // namespace
+
+size_t xhc_fwd_routed_workspace_bytes(const xhc_shape_t* sh) {
+  if (check_shape(sh)) return 0;
+  return xhc_fwd_workspace_bytes(sh) + routed_extra_bytes(sh);
+}
+
+int xhc_sublayer_fwd_routed(const xhc_shape_t* sh, const void* X_in, void* X_out, const void* out, const float* w4,
+                            const float* w8, const float* w12, const float* W, const float* W_r,
+                            const int32_t* fixed, int n_fixed, void* x_in, float* saved, void* saved_active,
+                            int32_t* tok_idx, float* scores, void* workspace, size_t ws_bytes,
+                            xhc_stream_t stream) {
+  int s = check_shape(sh);
+  if (s) return s;
+  if (sh->gram_schmidt) return XHC_ERR_ARG;           // not combined with the router
+  if ((s = check_fixed(sh, fixed, n_fixed))) return s;
+  bool has_conv = false;
+  if ((s = check_conv(w4, w8, w12, &has_conv))) return s;
+  if (tokens(sh) == 0) return XHC_OK;
+  if ((s = check_ptrs({X_in, X_out, out, W, W_r, tok_idx, scores, workspace},
+                      {w4, w8, w12, x_in, saved, saved_active})))
+    return s;
+  const Params p = make_params(sh, nullptr);
+  if (!fwd_uses_coef(sh, p)) return XHC_ERR_DTYPE;     // bf16 tensor-core path only
+  if (ws_bytes < xhc_fwd_routed_workspace_bytes(sh)) return XHC_ERR_WORKSPACE;
+  char* ws = (char*)workspace;
+  float* coef = (float*)ws;
+  void* wsplit = ws + fwd_coef_bytes(sh);
+  float* zw = (float*)(ws + fwd_coef_bytes(sh) + fwd_wsplit_bytes(sh));
+  float* z = saved ? saved : zw;
+  char* rbase = ws + xhc_fwd_workspace_bytes(sh);
+  const size_t NC = (size_t)p.N * p.C;
+  float* Wp = (float*)rbase;
+  float* zr = (float*)(rbase + round_up((size_t)p.P * NC * sizeof(float)));
+  float* rs = (float*)((char*)zr + round_up(tokens(sh) * (size_t)(p.P + 1) * sizeof(float)));
+  cudaStream_t st = (cudaStream_t)stream;
+  using T = __nv_bfloat16;
+  // coefficients, then the router's projection pass with W' and the routing
+  if ((s = cuda_status(launch_coeffs_tc(p, X_in, W, wsplit, nullptr, nullptr, nullptr, z, coef, st)))) return s;
+  if ((s = cuda_status(launch_router_weights(p, W_r, Wp, rs, st)))) return s;
+  if ((s = cuda_status(launch_coeffs_tc(p, X_in, Wp, wsplit, nullptr, nullptr, nullptr, zr, nullptr, st)))) return s;
+  if ((s = cuda_status(launch_route(p, zr, rs, fixed, n_fixed, tok_idx, scores, coef, st)))) return s;
+  UpdArgs<T> a{(const T*)X_in, (T*)X_out, (const T*)out, {w4, w8, w12}, nullptr, nullptr, nullptr, z,
+               (T*)x_in, (T*)saved_active, X_out != X_in, tok_idx};
+  return cuda_status(launch_fwd_update(p, a, coef, has_conv, num_sms(), st));
 }
 
 namespace {

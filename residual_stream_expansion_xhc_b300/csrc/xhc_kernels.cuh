@@ -23,6 +23,7 @@ struct UpdArgs {
   T* x_in;               // nullptr: no dense read
   T* saved_active;       // [T, k, C] or nullptr
   int copy_inactive;     // X_out != X_in
+  const int32_t* tok_idx = nullptr;   // [T, k] per-token active streams (router), or nullptr: Params::idx
 };
 
 template <typename T>

@@ -1,0 +1,139 @@
+// Router with per-token active sets, bf16 state (sm_103a):
+//   router_weights_kernel  W' = [W_r; 1; 0] for a second projection pass
+//   rowsum_kernel          row sums of W_r (the LayerNorm mean term)
+//   route_kernel           per token: LayerNorm scores, fixed + top-k slots,
+//                          routed write-back scaled into H^post
+//
+// Method: "xHC: Expanded Hyper-Connections" (qingkeai.online), section "Dense
+// read, sparse write": the router reads the LayerNorm-ed whole state and
+// scores every stream with a sigmoid; fixed streams are always active, the
+// others are chosen per token by top-k; a routed stream's score multiplies
+// its new write-back.
+//
+// The projection pass (coeffs_tc_kernel with W') gives, per token, rstd and
+// rstd * (W_r v, sum v).  With mean m = sum v / (N C), mean square
+// q = 1 / rstd^2 - eps and sd = sqrt(q - m^2 + eps), the scores are
+// sigmoid((W_r v - m rs) / sd), rs the row sums of W_r.
+#include <algorithm>
+
+#include "xhc_router.cuh"
+
+namespace xhc {
+
+__global__ void __launch_bounds__(256) router_weights_kernel(Params p, const float* __restrict__ W_r,
+                                                             float* __restrict__ Wp) {
+  const size_t NC = (size_t)p.N * p.C;
+  const size_t n4 = (size_t)p.P * NC / 4;
+  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x) {
+    const size_t r = (4 * i) / NC, col = (4 * i) % NC;
+    float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    if ((int)r < p.N) v = *reinterpret_cast<const float4*>(W_r + r * NC + col);
+    else if ((int)r == p.N) v = make_float4(1.0f, 1.0f, 1.0f, 1.0f);
+    *reinterpret_cast<float4*>(Wp + r * NC + col) = v;
+  }
+}
+
+// one block per row; fixed-order tree sum
+__global__ void __launch_bounds__(256) rowsum_kernel(const float* __restrict__ W_r, size_t NC, float* __restrict__ rs) {
+  __shared__ float part[256];
+  const float* row = W_r + (size_t)blockIdx.x * NC;
+  float s = 0.0f;
+  for (size_t c = threadIdx.x; c < NC; c += 256) s += row[c];
+  part[threadIdx.x] = s;
+  __syncthreads();
+  for (int o = 128; o > 0; o >>= 1) {
+    if ((int)threadIdx.x < o) part[threadIdx.x] += part[threadIdx.x + o];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) rs[blockIdx.x] = part[0];
+}
+
+struct Fixed {
+  int n;
+  int s[KMAX];
+};
+
+__global__ void __launch_bounds__(64) route_kernel(Params p, const float* __restrict__ zr, const float* __restrict__ rs,
+                                                   Fixed fx, int32_t* __restrict__ tok_idx,
+                                                   float* __restrict__ scores, float* __restrict__ coef,
+                                                   size_t T_all) {
+  const size_t t = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= T_all) return;
+  const int N = p.N, k = p.k, P = p.P;
+  const float* z = zr + t * (P + 1);
+  const float inv = 1.0f / z[P];                               // 1 / rstd
+  const float mean = z[N] * inv / (float)((size_t)N * p.C);
+  const float msq = inv * inv - p.eps;
+  const float sd = sqrtf(fmaxf(msq - mean * mean, 0.0f) + p.eps);
+  float s[NMAX];
+#pragma unroll
+  for (int n = 0; n < NMAX; ++n) s[n] = n < N ? sigmoidf_((z[n] * inv - mean * rs[n]) / sd) : 0.0f;
+  unsigned chosen = 0;
+  int slot[KMAX];
+#pragma unroll
+  for (int i = 0; i < KMAX; ++i) {
+    slot[i] = 0;
+    if (i < fx.n) {
+      slot[i] = fx.s[i];
+      chosen |= 1u << fx.s[i];
+    }
+  }
+  // routed slots: the highest remaining score, the lower index on a tie
+#pragma unroll
+  for (int i = 0; i < KMAX; ++i) {
+    if (i >= fx.n && i < k) {
+      int best = -1;
+      float bs = 0.0f;
+#pragma unroll
+      for (int n = 0; n < NMAX; ++n)
+        if (n < N && !((chosen >> n) & 1u) && (best < 0 || s[n] > bs)) {
+          best = n;
+          bs = s[n];
+        }
+      slot[i] = best;
+      chosen |= 1u << best;
+    }
+  }
+#pragma unroll
+  for (int n = 0; n < NMAX; ++n)
+    if (n < N) scores[t * N + n] = s[n];
+  float* hp = coef + t * COEF_STRIDE + COEF_POST;
+#pragma unroll
+  for (int i = 0; i < KMAX; ++i) {
+    if (i < k) {
+      tok_idx[t * k + i] = slot[i];
+      if (i >= fx.n) {
+        float w = 0.0f;
+#pragma unroll
+        for (int n = 0; n < NMAX; ++n)
+          if (n == slot[i]) w = s[n];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) hp[4 * i + c] *= w;
+      }
+    }
+  }
+}
+
+cudaError_t launch_router_weights(const Params& p, const float* W_r, float* Wp, float* rs, cudaStream_t st) {
+  const size_t NC = (size_t)p.N * p.C;
+  const size_t n4 = (size_t)p.P * NC / 4;
+  timing_begin("router_weights", st);
+  router_weights_kernel<<<(unsigned)std::min<size_t>((n4 + 255) / 256, 148 * 16), 256, 0, st>>>(p, W_r, Wp);
+  rowsum_kernel<<<p.N, 256, 0, st>>>(W_r, NC, rs);
+  timing_end(st);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_route(const Params& p, const float* zr, const float* rs, const int32_t* fixed, int nf,
+                         int32_t* tok_idx, float* scores, float* coef, cudaStream_t st) {
+  const size_t T_all = (size_t)p.B * p.S;
+  Fixed fx{};
+  fx.n = nf;
+  for (int i = 0; i < nf && i < KMAX; ++i) fx.s[i] = fixed[i];
+  timing_begin("route", st);
+  route_kernel<<<(unsigned)((T_all + 63) / 64), 64, 0, st>>>(p, zr, rs, fx, tok_idx, scores, coef, T_all);
+  timing_end(st);
+  return cudaGetLastError();
+}
+
+}  // namespace xhc

@@ -197,7 +197,8 @@ __device__ __forceinline__ void tfa_chunk_s(const uint16_t (*ring)[CB], U (*u_s)
   }
 }
 
-// NI > 0: exactly NI inactive streams, all loaded in one wave; NI = 0: any count.
+// NI > 0: exactly NI inactive streams, all loaded in one wave; NI = 0: any
+// count; NI < 0: per-token active sets (a.tok_idx), the inactive rows by mask.
 template <bool HAS_CONV, int NI>
 __global__ void __launch_bounds__(THREADS, 2) fwd_update_kernel(Params p, UpdArgs<__nv_bfloat16> a,
                                                                 const float* __restrict__ coef, Walk wk) {
@@ -249,10 +250,19 @@ __global__ void __launch_bounds__(THREADS, 2) fwd_update_kernel(Params p, UpdArg
         const float* cf = coef + tok * COEF_STRIDE;
         const __nv_bfloat16* xrow = a.X_in + tok * (size_t)N * C + c_lane;
         __nv_bfloat16* yrow = a.X_out + tok * (size_t)N * C + c_lane;
+        // active streams of this token: the layer's list, or the router's
+        // per-token list (NI < 0)
+        int ai[KMAX];
+        unsigned amask = 0;
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j) {
+          ai[j] = (NI < 0) ? (j < k ? a.tok_idx[tok * k + j] : 0) : p.idx[j];
+          if (NI < 0 && j < k) amask |= 1u << ai[j];
+        }
         uint4 xa[KMAX];
 #pragma unroll
         for (int j = 0; j < KMAX; ++j)
-          if (j < k) xa[j] = ld_stream(xrow + (size_t)p.idx[j] * C);
+          if (j < k) xa[j] = ld_stream(xrow + (size_t)ai[j] * C);
         // x_in partial sums in fp32x2: even and odd inactive rows apart (two
         // independent chains), the active rows into the first
         float2 acc[2][4];
@@ -261,7 +271,29 @@ __global__ void __launch_bounds__(THREADS, 2) fwd_update_kernel(Params p, UpdArg
           acc[0][x] = make_float2(0.0f, 0.0f);
           acc[1][x] = acc[0][x];
         }
-        if (need_all) {
+        if (NI < 0 && need_all) {
+          // per-token active sets: every stream not in the mask, 8 per wave
+#pragma unroll 1
+          for (int q0 = 0; q0 < N; q0 += 8) {
+            uint4 xr[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              if (q0 + q < N && !((amask >> (q0 + q)) & 1u)) xr[q] = ld_stream(xrow + (size_t)(q0 + q) * C);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              const int n = q0 + q;
+              if (n < N && !((amask >> n) & 1u)) {
+                if (a.x_in) {
+                  const float2 h = fx2(cf[n]);
+                  const uint32_t w[4] = {xr[q].x, xr[q].y, xr[q].z, xr[q].w};
+#pragma unroll
+                  for (int x = 0; x < 4; ++x) acc[q & 1][x] = __ffma2_rn(h, bfx2(w[x]), acc[q & 1][x]);
+                }
+                if (a.copy_inactive) st_stream(yrow + (size_t)n * C, xr[q]);
+              }
+            }
+          }
+        } else if (NI >= 0 && need_all) {
           // the inactive streams, NI (or at most 8) rows per wave of loads
           constexpr int WAVE = NI > 0 ? NI : 8;
           const int ni = NI > 0 ? NI : p.n_inactive;
@@ -290,7 +322,7 @@ __global__ void __launch_bounds__(THREADS, 2) fwd_update_kernel(Params p, UpdArg
 #pragma unroll
           for (int j = 0; j < KMAX; ++j) {
             if (j < k) {
-              const float2 h = fx2(cf[p.idx[j]]);
+              const float2 h = fx2(cf[ai[j]]);
               const uint32_t w[4] = {xa[j].x, xa[j].y, xa[j].z, xa[j].w};
 #pragma unroll
               for (int x = 0; x < 4; ++x) acc[0][x] = __ffma2_rn(h, bfx2(w[x]), acc[0][x]);
@@ -357,7 +389,7 @@ __global__ void __launch_bounds__(THREADS, 2) fwd_update_kernel(Params p, UpdArg
               o[2 * x] = y[x].x;
               o[2 * x + 1] = y[x].y;
             }
-            st_stream(yrow + (size_t)p.idx[i] * C, pack8(o));
+            st_stream(yrow + (size_t)ai[i] * C, pack8(o));
           }
         }
       }
@@ -1131,7 +1163,12 @@ cudaError_t launch_fwd_update(const Params& p, const UpdArgs<__nv_bfloat16>& a, 
   const int smem = (int)sizeof(FwdSmem);
   timing_begin("fwd_update", st);
   const bool twelve = p.n_inactive == 12;      // N = 16, k = 4
-  if (has_conv && twelve) {
+  if (a.tok_idx && has_conv) {
+    cudaFuncSetAttribute(fwd_update_kernel<true, -1>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    fwd_update_kernel<true, -1><<<grid, THREADS, smem, st>>>(p, a, coef, wk);
+  } else if (a.tok_idx) {
+    fwd_update_kernel<false, -1><<<grid, THREADS, 0, st>>>(p, a, coef, wk);
+  } else if (has_conv && twelve) {
     cudaFuncSetAttribute(fwd_update_kernel<true, 12>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     fwd_update_kernel<true, 12><<<grid, THREADS, smem, st>>>(p, a, coef, wk);
   } else if (has_conv) {

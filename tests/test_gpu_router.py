@@ -1,0 +1,92 @@
+"""GPU-vs-oracle parity of the sublayer update with per-token active sets
+chosen by the router (xhc_sublayer_fwd_routed), through the C ABI.
+
+Method: "xHC: Expanded Hyper-Connections" (qingkeai.online), section "Dense
+read, sparse write".  The GPU's scores are compared with the oracle's; the
+selection is exact except where two candidate scores tie to within float
+rounding (then either choice is correct and the token is left out of the
+write-back comparison).  Write-back and dense read: the bf16 bound 2e-2 of
+max_i |g_i - r_i| / max(|r_i|, rms(r)); rows outside each token's active set
+bit for bit.
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import xhc_oracle as xo
+from residual_stream_expansion_xhc_b300 import inputs as xin
+from tests.xhc_testlib import TOL, dev_act, dev_f32, host_f64, oracle_inputs, tdtype
+
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    from residual_stream_expansion_xhc_b300 import api
+
+CASES = {
+    "router_ragged": (xin.Workload("router_ragged", 51, B=2, S=77, N=16, C=512, k=4, dtype="bf16", conv_std=0.3),
+                      2),
+    "router_c2048": (xin.Workload("router_c2048", 52, B=1, S=130, N=16, C=2048, k=4, dtype="bf16"), 2),
+    "router_s5_nofixed": (xin.Workload("router_s5", 53, B=3, S=5, N=16, C=256, k=4, dtype="bf16"), 0),
+    "router_k2": (xin.Workload("router_k2", 54, B=2, S=40, N=6, C=256, k=2, dtype="bf16"), 1),
+}
+
+
+def _router_weights(wl):
+    # logits W_r . LN(v) with a standard deviation of about 1
+    std = 1.0 / np.sqrt(wl.N * wl.C)
+    return (np.random.default_rng(1000 * wl.wid + 77).standard_normal((wl.N, wl.N * wl.C)) * std).astype(np.float32)
+
+
+def _run(wl, t, W_r, fixed):
+    sh = api.make_shape(wl.B, wl.S, wl.N, wl.C, wl.k, tdtype(wl), wl.iters, wl.eps)
+    X = dev_act(wl, t.X)
+    X0 = X.clone()
+    out = dev_act(wl, t.out)
+    conv = None if t.conv is None else tuple(dev_f32(w) for w in t.conv)
+    x_in = torch.empty(wl.B, wl.S, wl.C, dtype=tdtype(wl), device="cuda")
+    saved = torch.empty(wl.B, wl.S, wl.P + 1, device="cuda")
+    act = torch.empty(wl.B, wl.S, wl.k, wl.C, dtype=tdtype(wl), device="cuda")
+    tok_idx = torch.empty(wl.B, wl.S, wl.k, dtype=torch.int32, device="cuda")
+    scores = torch.empty(wl.B, wl.S, wl.N, device="cuda")
+    ws = api.workspace(api.xhc_fwd_routed_workspace_bytes(sh))
+    api.xhc_sublayer_fwd_routed(sh, X, X, out, conv, dev_f32(t.W), dev_f32(W_r), fixed, tok_idx, scores, ws,
+                                x_in=x_in, saved=saved, saved_active=act)
+    torch.cuda.synchronize()
+    api.xhc_device_status()
+    return dict(X0=X0, Xp=X, x_in=x_in, idx=tok_idx.cpu().numpy(), scores=scores.cpu().numpy().astype(np.float64),
+                act=act)
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_routed_forward_parity(name):
+    wl, nf = CASES[name]
+    t = xin.make(wl)
+    W_r = _router_weights(wl)
+    fixed = [int(a) for a in t.idx[:nf]]
+    g = _run(wl, t, W_r, fixed)
+    X, out, conv, W, _ = oracle_inputs(wl, t)
+    ref = xo.forward_routed(X, out, conv, W, W_r.astype(np.float64), fixed, wl.k, iters=wl.iters, eps=wl.eps)
+    assert np.abs(g["scores"] - ref["s"]).max() < 1e-4
+    # the selection: equal, or a tie in the oracle's scores
+    same = (g["idx"] == ref["idx"]).all(axis=-1)
+    for b, s_ in zip(*np.nonzero(~same)):
+        gi, ri = set(g["idx"][b, s_]), set(ref["idx"][b, s_])
+        sc = ref["s"][b, s_]
+        assert abs(max(sc[list(gi - ri)]) - max(sc[list(ri - gi)])) < 1e-4 if gi != ri else True
+    assert same.mean() > 0.98
+    tol = TOL[wl.dtype]
+    Xp, X0 = host_f64(g["Xp"]), host_f64(g["X0"])
+    for b, s_ in zip(*np.nonzero(same)):
+        a = list(ref["idx"][b, s_])
+        inactive = [n for n in range(wl.N) if n not in a]
+        assert np.array_equal(Xp[b, s_, inactive], X0[b, s_, inactive])
+    m = same[:, :, None, None]
+    err = xo.max_rel_err(np.where(m, Xp, 0.0), np.where(m, ref["Xp"], 0.0))
+    assert err <= tol, f"X' err {err}"
+    e = xo.max_rel_err(host_f64(g["x_in"]), ref["x_in"])
+    assert e <= tol, f"x_in err {e}"
+    # saved active rows: the slots' rows before the update, bit for bit
+    act = g["act"].view(torch.int16).cpu().numpy()
+    x0 = g["X0"].view(torch.int16).cpu().numpy()
+    gidx = g["idx"].astype(np.int64)
+    assert np.array_equal(act, np.take_along_axis(x0, gidx[..., None], axis=2))
