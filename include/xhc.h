@@ -237,7 +237,9 @@ int xhc_sublayer_fwd_noalloc(const xhc_shape_t* sh, const void* X_in,
  *           sum_c H^post[i][c] u_c multiplied by its stream's score.
  *   W_r      [N, N*C] fp32, read.
  *   tok_idx  [B,S,k] int32 device, written: the slots.
- *   scores   [B,S,N] fp32 device, written.
+ *   rrec     [B,S,2N+2] fp32 device, written: per token the scores s (N),
+ *            the logits W_r . LN(vec X) (N), the LayerNorm mean and its
+ *            standard deviation sqrt(var + eps) (the backward reads them).
  *   saved_active  [B,S,k,C], the active rows before the update in slot order
  *            (may be NULL).
  *   workspace, ws_bytes  at least xhc_fwd_routed_workspace_bytes() bytes
@@ -254,8 +256,31 @@ int xhc_sublayer_fwd_routed(const xhc_shape_t* sh, const void* X_in,
                             const float* W_r, const int32_t* fixed,
                             int n_fixed, void* x_in, float* saved,
                             void* saved_active, int32_t* tok_idx,
-                            float* scores, void* workspace, size_t ws_bytes,
+                            float* rrec, void* workspace, size_t ws_bytes,
                             xhc_stream_t stream);
+
+/*
+ * xhc_sublayer_bwd_routed -- exact reverse mode of xhc_sublayer_fwd_routed
+ * (the active sets are the forward's, a constant; unchosen scores get no
+ * gradient).
+ *   X_pre    [B,S,N,C] dtype: the state BEFORE the update.
+ *   saved, tok_idx, rrec  the forward's outputs (required).
+ *   dW_r     [N, N*C] fp32, written.
+ * Other arguments as in xhc_sublayer_bwd.  bf16 with C a multiple of 128 and
+ * P + N <= 64 (XHC_ERR_DTYPE otherwise); workspace at least
+ * xhc_bwd_routed_workspace_bytes() bytes.
+ */
+size_t xhc_bwd_routed_workspace_bytes(const xhc_shape_t* sh);
+int xhc_sublayer_bwd_routed(const xhc_shape_t* sh, const void* X_pre,
+                            const void* out, const float* w4, const float* w8,
+                            const float* w12, const float* W,
+                            const float* W_r, const int32_t* fixed,
+                            int n_fixed, const float* saved,
+                            const int32_t* tok_idx, const float* rrec,
+                            const void* dXp, const void* dx_in, void* dX,
+                            void* dout, float* dw4, float* dw8, float* dw12,
+                            float* dW, float* dW_r, void* workspace,
+                            size_t ws_bytes, xhc_stream_t stream);
 
 /* Workspace the backward needs (bytes). */
 size_t xhc_bwd_workspace_bytes(const xhc_shape_t* sh);

@@ -434,10 +434,12 @@ def forward_routed(X, out, conv, W, W_r, fixed, k, iters=20, eps=1e-6):
     return res
 
 
-def backward_routed(X, out, conv, W, W_r, fixed, k, dXp, dx_in=None, iters=20, eps=1e-6):
+def backward_routed(X, out, conv, W, W_r, fixed, k, dXp, dx_in=None, iters=20, eps=1e-6, idx=None):
     """Exact reverse mode of ``forward_routed`` (the active sets are the
-    forward's, a constant; unchosen scores get no gradient).  Returns dX, dout,
-    dconv, dW, dW_r."""
+    forward's, a constant; unchosen scores get no gradient).  ``idx``
+    [B, S, k] optionally gives the active sets (where two scores tie either
+    choice is a valid forward); by default ``route`` chooses them.  Returns
+    dX, dout, dconv, dW, dW_r."""
     B, S, N, C = X.shape
     nf = len(fixed)
     dX = np.zeros_like(X)
@@ -449,11 +451,11 @@ def backward_routed(X, out, conv, W, W_r, fixed, k, dXp, dx_in=None, iters=20, e
         Xs = X[b]
         cf = _coeffs_seq(Xs, W, N, C, k, iters, eps)
         s, r, y, sd = router_scores(Xs, W_r, eps)
-        idx = route(s, fixed, k)
-        w = _routed_weights(s, idx, nf)
+        ib = route(s, fixed, k) if idx is None else np.asarray(idx[b], dtype=np.int64)
+        w = _routed_weights(s, ib, nf)
         u = tfa_components(out[b], conv)
-        G = np.take_along_axis(dXp[b], idx[:, :, None], axis=1)             # [S, k, C]
-        Xa = np.take_along_axis(Xs, idx[:, :, None], axis=1)
+        G = np.take_along_axis(dXp[b], ib[:, :, None], axis=1)              # [S, k, C]
+        Xa = np.take_along_axis(Xs, ib[:, :, None], axis=1)
         hpre, hpost = cf["hpre"], cf["hpost"]
         D = np.einsum("sic,xsc->six", G, u)                                  # <G_i, u_c>
         d_hres = np.einsum("sic,sjc->sij", G, Xa)
@@ -473,7 +475,7 @@ def backward_routed(X, out, conv, W, W_r, fixed, k, dXp, dx_in=None, iters=20, e
         ds = np.zeros((S, N))
         rows = np.arange(S)
         for i in range(nf, k):
-            ds[rows, idx[:, i]] += d_w[:, i]
+            ds[rows, ib[:, i]] += d_w[:, i]
         dr = ds * s * (1.0 - s)
         dW_r += dr.T @ y
         dy = dr @ W_r
@@ -483,11 +485,11 @@ def backward_routed(X, out, conv, W, W_r, fixed, k, dXp, dx_in=None, iters=20, e
             dXs += hpre[:, :, None] * dx_in[b][:, None, :]
         # per-token sparse write: a stream passes dX' through unless active
         active = np.zeros((S, N), dtype=bool)
-        np.put_along_axis(active, idx, True, axis=1)
+        np.put_along_axis(active, ib, True, axis=1)
         dXs += np.where(active[:, :, None], 0.0, dXp[b])
         back = np.einsum("sij,sic->sjc", cf["hres"], G)                      # to X[a_j]
         for j in range(k):
-            dXs[rows, idx[:, j]] += back[:, j]
+            dXs[rows, ib[:, j]] += back[:, j]
         dX[b] = dXs
         du = np.einsum("six,sic->xsc", hpost * w[:, :, None], G)
         dout_b = du[0].copy()

@@ -18,7 +18,8 @@ STATUS = {0: "XHC_OK", 1: "XHC_ERR_SHAPE", 2: "XHC_ERR_INDEX", 3: "XHC_ERR_ALIGN
 
 EXPORTS = ("xhc_status_string", "xhc_last_cuda_error", "xhc_device_status", "xhc_num_logits", "xhc_coeffs", "xhc_tfa",
            "xhc_sparse_update", "xhc_fwd_workspace_bytes", "xhc_fwd_workspace_need", "xhc_sublayer_fwd", "xhc_sublayer_fwd_noalloc", "xhc_bwd_workspace_bytes",
-           "xhc_sublayer_bwd", "xhc_fwd_routed_workspace_bytes", "xhc_sublayer_fwd_routed", "xhc_hres_active_weights", "xhc_hres_active_grad", "xhc_copy", "xhc_timing_enable",
+           "xhc_sublayer_bwd", "xhc_fwd_routed_workspace_bytes", "xhc_sublayer_fwd_routed",
+           "xhc_bwd_routed_workspace_bytes", "xhc_sublayer_bwd_routed", "xhc_hres_active_weights", "xhc_hres_active_grad", "xhc_copy", "xhc_timing_enable",
            "xhc_timing_collect")
 
 
@@ -75,6 +76,11 @@ def _load() -> ctypes.CDLL:
     lib.xhc_fwd_routed_workspace_bytes.argtypes = [sh]
     lib.xhc_sublayer_fwd_routed.restype = I
     lib.xhc_sublayer_fwd_routed.argtypes = [sh, P, P, P, P, P, P, P, P, P, I, P, P, P, P, P, P, Z, P]
+    lib.xhc_bwd_routed_workspace_bytes.restype = Z
+    lib.xhc_bwd_routed_workspace_bytes.argtypes = [sh]
+    lib.xhc_sublayer_bwd_routed.restype = I
+    lib.xhc_sublayer_bwd_routed.argtypes = [sh, P, P, P, P, P, P, P, P, I, P, P, P, P, P, P, P, P, P, P, P, P, P, Z,
+                                            P]
     lib.xhc_hres_active_weights.restype = I
     lib.xhc_hres_active_weights.argtypes = [sh, P, P, P, P, P]
     lib.xhc_hres_active_grad.restype = I

@@ -128,11 +128,12 @@ def xhc_fwd_routed_workspace_bytes(sh) -> int:
     return LIB.xhc_fwd_routed_workspace_bytes(ctypes.byref(sh))
 
 
-def xhc_sublayer_fwd_routed(sh, X_in, X_out, out, conv, W, W_r, fixed, tok_idx, scores, workspace, x_in=None,
+def xhc_sublayer_fwd_routed(sh, X_in, X_out, out, conv, W, W_r, fixed, tok_idx, rrec, workspace, x_in=None,
                             saved=None, saved_active=None, stream=None):
     """The update with per-token active sets from the router (see the C
     header): ``fixed`` is the host list of always-active streams; ``tok_idx``
-    [B,S,k] int32 and ``scores`` [B,S,N] fp32 are written."""
+    [B,S,k] int32 and the router record ``rrec`` [B,S,2N+2] fp32 (scores,
+    logits, LayerNorm mean and sd) are written."""
     w4, w8, w12 = _conv(conv)
     fixed = [int(a) for a in fixed]
     fx = (ctypes.c_int32 * max(len(fixed), 1))(*fixed) if fixed else None
@@ -140,7 +141,27 @@ def xhc_sublayer_fwd_routed(sh, X_in, X_out, out, conv, W, W_r, fixed, tok_idx, 
     _check("xhc_sublayer_fwd_routed",
            LIB.xhc_sublayer_fwd_routed(ctypes.byref(sh), _p(X_in), _p(X_out), _p(out), w4, w8, w12, _p(W),
                                        _p(W_r), fx, len(fixed), _p(x_in), _p(saved), _p(saved_active),
-                                       _p(tok_idx), _p(scores), _p(workspace), ws_bytes, _s(stream)))
+                                       _p(tok_idx), _p(rrec), _p(workspace), ws_bytes, _s(stream)))
+
+
+def xhc_bwd_routed_workspace_bytes(sh) -> int:
+    return LIB.xhc_bwd_routed_workspace_bytes(ctypes.byref(sh))
+
+
+def xhc_sublayer_bwd_routed(sh, X_pre, out, conv, W, W_r, fixed, saved, tok_idx, rrec, dXp, dx_in, dX, dout, dconv,
+                            dW, dW_r, workspace, stream=None):
+    """Reverse of xhc_sublayer_fwd_routed (see the C header); X_pre is the
+    state before the update."""
+    w4, w8, w12 = _conv(conv)
+    d4, d8, d12 = _conv(dconv)
+    fixed = [int(a) for a in fixed]
+    fx = (ctypes.c_int32 * max(len(fixed), 1))(*fixed) if fixed else None
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check("xhc_sublayer_bwd_routed",
+           LIB.xhc_sublayer_bwd_routed(ctypes.byref(sh), _p(X_pre), _p(out), w4, w8, w12, _p(W), _p(W_r), fx,
+                                       len(fixed), _p(saved), _p(tok_idx), _p(rrec), _p(dXp), _p(dx_in), _p(dX),
+                                       _p(dout), d4, d8, d12, _p(dW), _p(dW_r), _p(workspace), ws_bytes,
+                                       _s(stream)))
 
 
 def xhc_hres_active_weights(sh, W_pp, W_ra, idx, W, stream=None):

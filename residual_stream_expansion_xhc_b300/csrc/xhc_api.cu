@@ -397,7 +397,7 @@ size_t xhc_fwd_routed_workspace_bytes(const xhc_shape_t* sh) {
 int xhc_sublayer_fwd_routed(const xhc_shape_t* sh, const void* X_in, void* X_out, const void* out, const float* w4,
                             const float* w8, const float* w12, const float* W, const float* W_r,
                             const int32_t* fixed, int n_fixed, void* x_in, float* saved, void* saved_active,
-                            int32_t* tok_idx, float* scores, void* workspace, size_t ws_bytes,
+                            int32_t* tok_idx, float* rrec, void* workspace, size_t ws_bytes,
                             xhc_stream_t stream) {
   int s = check_shape(sh);
   if (s) return s;
@@ -406,7 +406,7 @@ int xhc_sublayer_fwd_routed(const xhc_shape_t* sh, const void* X_in, void* X_out
   bool has_conv = false;
   if ((s = check_conv(w4, w8, w12, &has_conv))) return s;
   if (tokens(sh) == 0) return XHC_OK;
-  if ((s = check_ptrs({X_in, X_out, out, W, W_r, tok_idx, scores, workspace},
+  if ((s = check_ptrs({X_in, X_out, out, W, W_r, tok_idx, rrec, workspace},
                       {w4, w8, w12, x_in, saved, saved_active})))
     return s;
   const Params p = make_params(sh, nullptr);
@@ -428,7 +428,7 @@ int xhc_sublayer_fwd_routed(const xhc_shape_t* sh, const void* X_in, void* X_out
   if ((s = cuda_status(launch_coeffs_tc(p, X_in, W, wsplit, nullptr, nullptr, nullptr, z, coef, st)))) return s;
   if ((s = cuda_status(launch_router_weights(p, W_r, Wp, rs, st)))) return s;
   if ((s = cuda_status(launch_coeffs_tc(p, X_in, Wp, wsplit, nullptr, nullptr, nullptr, zr, nullptr, st)))) return s;
-  if ((s = cuda_status(launch_route(p, zr, rs, fixed, n_fixed, tok_idx, scores, coef, st)))) return s;
+  if ((s = cuda_status(launch_route(p, zr, rs, fixed, n_fixed, tok_idx, rrec, coef, st)))) return s;
   UpdArgs<T> a{(const T*)X_in, (T*)X_out, (const T*)out, {w4, w8, w12}, nullptr, nullptr, nullptr, z,
                (T*)x_in, (T*)saved_active, X_out != X_in, tok_idx};
   return cuda_status(launch_fwd_update(p, a, coef, has_conv, num_sms(), st));
@@ -551,7 +551,7 @@ int xhc_sublayer_bwd(const xhc_shape_t* sh, const void* X_state, const void* sav
       const float* const w[3] = {w4, w8, w12};
       if (have_coef) {
         if ((s = cuda_status(launch_wt_prep(p, W, Wt, st)))) return s;
-      } else if ((s = cuda_status(launch_bwd_prep(p, W, Wt, z, coef, st)))) {
+      } else if ((s = cuda_status(launch_bwd_prep(p, W, nullptr, Wt, z, coef, st)))) {
         return s;
       }
       if (gs) {
@@ -561,7 +561,7 @@ int xhc_sublayer_bwd(const xhc_shape_t* sh, const void* X_state, const void* sav
       }
       if ((s = cuda_status(launch_bwd_col(p, a, coef, has_conv, pdot, cpart, sms, st)))) return s;
       if (gs && (s = cuda_status(launch_gs_rev(p, z, pdot, gsrec, gsdh, sgram, st)))) return s;
-      if ((s = cuda_status(launch_bwd_dz(p, z, pdot, dx_in != nullptr, dP, rec, gsdh, st)))) return s;
+      if ((s = cuda_status(launch_bwd_dz(p, z, pdot, dx_in != nullptr, dP, rec, gsdh, RouterBwd{}, st)))) return s;
       if (gs && (s = cuda_status(launch_gs_bwd(p, (const T*)out, w, sgram, (T*)dout,
                                                cpart + (size_t)L.col_rows * NTAPS * p.C, st))))
         return s;
@@ -593,6 +593,97 @@ int xhc_hres_active_grad(const xhc_shape_t* sh, const float* dW, const int32_t* 
   if (sh->C % 4) return XHC_ERR_ALIGN;
   if ((s = check_ptrs({dW, dW_ra}, {}))) return s;
   return cuda_status(launch_hres_active_grad(make_params(sh, idx), dW, dW_ra, (cudaStream_t)stream));
+}
+
+namespace {
+// Router backward workspace: the plain backward's layout with P + N rows per
+// dW partial, then cm [T, N], c_r [N] and rs [N].
+struct RoutedBwdLayout {
+  BwdLayout L;
+  size_t wpart, cm, cr, rs, total;
+};
+RoutedBwdLayout routed_bwd_layout(const xhc_shape_t* sh) {
+  RoutedBwdLayout R{};
+  R.L = bwd_layout(sh);
+  const Params p = make_params(sh, nullptr);
+  const size_t NC = (size_t)p.N * p.C;
+  R.wpart = R.L.total;
+  R.cm = R.wpart + round_up((size_t)R.L.ranges * (p.P + p.N) * NC * sizeof(float));
+  R.cr = R.cm + round_up(tokens(sh) * p.N * sizeof(float));
+  R.rs = R.cr + round_up((size_t)p.N * sizeof(float));
+  R.total = R.rs + round_up((size_t)p.N * sizeof(float));
+  return R;
+}
+}  // namespace
+
+size_t xhc_bwd_routed_workspace_bytes(const xhc_shape_t* sh) {
+  if (check_shape(sh)) return 0;
+  return routed_bwd_layout(sh).total;
+}
+
+int xhc_sublayer_bwd_routed(const xhc_shape_t* sh, const void* X_pre, const void* out, const float* w4,
+                            const float* w8, const float* w12, const float* W, const float* W_r,
+                            const int32_t* fixed, int n_fixed, const float* saved, const int32_t* tok_idx,
+                            const float* rrec, const void* dXp, const void* dx_in, void* dX, void* dout,
+                            float* dw4, float* dw8, float* dw12, float* dW, float* dW_r, void* workspace,
+                            size_t ws_bytes, xhc_stream_t stream) {
+  int s = check_shape(sh);
+  if (s) return s;
+  if (sh->gram_schmidt) return XHC_ERR_ARG;
+  if ((s = check_fixed(sh, fixed, n_fixed))) return s;
+  bool has_conv = false, has_dconv = false;
+  if ((s = check_conv(w4, w8, w12, &has_conv))) return s;
+  if ((s = check_conv(dw4, dw8, dw12, &has_dconv))) return s;
+  if (has_conv != has_dconv) return XHC_ERR_ARG;
+  if (dX == dXp) return XHC_ERR_ARG;
+  if ((s = check_ptrs({X_pre, out, W, W_r, saved, tok_idx, rrec, dXp, dX, dout, dW, dW_r, workspace},
+                      {w4, w8, w12, dx_in, dw4, dw8, dw12})))
+    return s;
+  const Params p = make_params(sh, nullptr);
+  if (!(sh->dtype == XHC_BF16 && tc_bwd_supported(p)) || p.P + p.N > 64) return XHC_ERR_DTYPE;
+  cudaStream_t st = (cudaStream_t)stream;
+  const size_t NC = (size_t)p.N * p.C;
+  if (tokens(sh) == 0) {
+    cudaError_t e = cudaMemsetAsync(dW, 0, (size_t)p.P * NC * sizeof(float), st);
+    if (e == cudaSuccess) e = cudaMemsetAsync(dW_r, 0, (size_t)p.N * NC * sizeof(float), st);
+    if (has_conv && e == cudaSuccess) e = cudaMemsetAsync(dw4, 0, (size_t)p.C * 4 * sizeof(float), st);
+    if (has_conv && e == cudaSuccess) e = cudaMemsetAsync(dw8, 0, (size_t)p.C * 8 * sizeof(float), st);
+    if (has_conv && e == cudaSuccess) e = cudaMemsetAsync(dw12, 0, (size_t)p.C * 12 * sizeof(float), st);
+    return cuda_status(e);
+  }
+  const RoutedBwdLayout R = routed_bwd_layout(sh);
+  if (ws_bytes < R.total) return XHC_ERR_WORKSPACE;
+  char* ws = (char*)workspace;
+  const BwdLayout& L = R.L;
+  using T = __nv_bfloat16;
+  float* coef = (float*)(ws + L.coef);
+  T* dP = (T*)(ws + L.dP);
+  T* Wt = (T*)(ws + L.Wt);
+  float* pdot = (float*)(ws + L.pdot);
+  float* cpart = (float*)(ws + L.cpart);
+  float* wpart = (float*)(ws + R.wpart);
+  float* cm = (float*)(ws + R.cm);
+  float* cr = (float*)(ws + R.cr);
+  float* rs = (float*)(ws + R.rs);
+  BwdArgs<T> a{(const T*)X_pre, nullptr, (const T*)out, {w4, w8, w12}, W, saved, (const T*)dXp, (const T*)dx_in,
+               (T*)dX, (T*)dout, {dw4, dw8, dw12}, dW, (float*)(ws + L.rec)};
+  a.tok_idx = tok_idx;
+  a.rrec = rrec;
+  a.n_fixed = n_fixed;
+  RouterBwd rb;
+  rb.tok_idx = tok_idx;
+  rb.rrec = rrec;
+  rb.n_fixed = n_fixed;
+  rb.rs = rs;
+  rb.cm = cm;
+  const int sms = num_sms();
+  if ((s = cuda_status(launch_bwd_prep(p, W, W_r, Wt, saved, coef, st)))) return s;
+  if ((s = cuda_status(launch_route_scale(p, tok_idx, rrec, n_fixed, coef, st)))) return s;
+  if ((s = cuda_status(launch_router_rowsums(p, W_r, rs, st)))) return s;
+  if ((s = cuda_status(launch_bwd_col(p, a, coef, has_conv, pdot, cpart, sms, st)))) return s;
+  if ((s = cuda_status(launch_bwd_dz(p, saved, pdot, dx_in != nullptr, dP, a.rec, nullptr, rb, st)))) return s;
+  if ((s = cuda_status(launch_bwd_stream_tc(p, a, Wt, dP, L.ranges, wpart, st)))) return s;
+  return cuda_status(launch_bwd_reduce(p, a, has_conv, cpart, L.cpart_rows, L.ranges, wpart, st, dW_r, cm, cr));
 }
 
 int xhc_copy(const void* src, void* dst, size_t bytes, xhc_stream_t stream) {

@@ -20,13 +20,19 @@ namespace xhc {
 // operand of dV = dP . W in the stream pass, as a hi part and a lo part
 // (Wt + NC * 64 holds bf16(W - hi)), so that hi + lo keeps about 16 bits of W.
 
-__device__ __forceinline__ void wt_prep_block(const float* __restrict__ W, __nv_bfloat16* __restrict__ Wt, int P,
-                                              size_t NC, size_t blk) {
+// With a router, entries P .. P + R - 1 carry W_r^T (R = N router rows).
+__device__ __forceinline__ void wt_prep_block(const float* __restrict__ W, const float* __restrict__ W_r, int R,
+                                              __nv_bfloat16* __restrict__ Wt, int P, size_t NC, size_t blk) {
   __shared__ float tile[64][65];
   const size_t col0 = blk * 64;
   for (int i = threadIdx.x; i < 64 * 64; i += blockDim.x) {
     const int q = i / 64, c = i % 64;
-    tile[q][c] = (q < P && col0 + c < NC) ? W[(size_t)q * NC + col0 + c] : 0.0f;
+    float v = 0.0f;
+    if (col0 + c < NC) {
+      if (q < P) v = W[(size_t)q * NC + col0 + c];
+      else if (W_r && q < P + R) v = W_r[(size_t)(q - P) * NC + col0 + c];
+    }
+    tile[q][c] = v;
   }
   __syncthreads();
   __nv_bfloat16* Wt_lo = Wt + NC * 64;
@@ -43,16 +49,17 @@ __device__ __forceinline__ void wt_prep_block(const float* __restrict__ W, __nv_
 
 __global__ void __launch_bounds__(256) wt_prep_kernel(const float* __restrict__ W, __nv_bfloat16* __restrict__ Wt,
                                                       int P, size_t NC) {
-  wt_prep_block(W, Wt, P, NC, blockIdx.x);
+  wt_prep_block(W, nullptr, 0, Wt, P, NC, blockIdx.x);
 }
 
 // The two independent preparations of the backward in one launch: blocks
 // [0, nwt) build W^T, the others the coefficient block from the saved logits.
 __global__ void __launch_bounds__(256) bwd_prep_kernel(Params p, const float* __restrict__ W,
+                                                       const float* __restrict__ W_r,
                                                        __nv_bfloat16* __restrict__ Wt, unsigned nwt,
                                                        const float* __restrict__ saved, float* __restrict__ coef,
                                                        size_t T_all) {
-  if (blockIdx.x < nwt) wt_prep_block(W, Wt, p.P, (size_t)p.N * p.C, blockIdx.x);
+  if (blockIdx.x < nwt) wt_prep_block(W, W_r, p.N, Wt, p.P, (size_t)p.N * p.C, blockIdx.x);
   else coef_block(p, saved, coef, T_all, blockIdx.x - nwt);
 }
 
@@ -60,9 +67,13 @@ __global__ void __launch_bounds__(256) bwd_prep_kernel(Params p, const float* __
 // [ranges][P][N C].  The first `cblocks` blocks take the conv-weight sums,
 // the others the dW sums, four consecutive entries (one 16-byte vector) per
 // thread and step.
+// With a router each range's partial has the N rows of W_r after W's P rows
+// (PNC covers both, RNC0 = P N C is where they start): they go to dW_r, less
+// the LayerNorm mean term c_r[row] (the same for every column of a row).
 __global__ void bwd_reduce_kernel(int conv_rows, int C, const float* __restrict__ cpart, float* __restrict__ dw4,
                                   float* __restrict__ dw8, float* __restrict__ dw12, int cblocks, int w_ranges,
-                                  size_t PNC, const float* __restrict__ wpart, float* __restrict__ dW) {
+                                  size_t PNC, const float* __restrict__ wpart, float* __restrict__ dW,
+                                  size_t RNC0, size_t NC, float* __restrict__ dW_r, const float* __restrict__ c_r) {
   if ((int)blockIdx.x < cblocks) {
     const size_t stride = (size_t)cblocks * blockDim.x;
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < (size_t)NTAPS * C; i += stride) {
@@ -97,8 +108,29 @@ __global__ void bwd_reduce_kernel(int conv_rows, int C, const float* __restrict_
       s.z += v.z;
       s.w += v.w;
     }
-    reinterpret_cast<float4*>(dW)[i] = s;
+    if (4 * i < RNC0) {
+      reinterpret_cast<float4*>(dW)[i] = s;
+    } else {
+      const size_t j = 4 * i - RNC0;
+      const float c = c_r[j / NC];
+      reinterpret_cast<float4*>(dW_r)[j / 4] = make_float4(s.x - c, s.y - c, s.z - c, s.w - c);
+    }
   }
+}
+
+// c_r[n] = sum over tokens of cm[t][n]: one block per n, fixed-order sums.
+__global__ void __launch_bounds__(256) column_sum_kernel(const float* __restrict__ cm, size_t T_all, int N,
+                                                         float* __restrict__ out) {
+  __shared__ float part[256];
+  float s = 0.0f;
+  for (size_t t = threadIdx.x; t < T_all; t += 256) s += cm[t * N + blockIdx.x];
+  part[threadIdx.x] = s;
+  __syncthreads();
+  for (int o = 128; o > 0; o >>= 1) {
+    if ((int)threadIdx.x < o) part[threadIdx.x] += part[threadIdx.x + o];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) out[blockIdx.x] = part[0];
 }
 
 // ============================================================== H^res from the active rows
@@ -164,27 +196,32 @@ cudaError_t launch_wt_prep(const Params& p, const float* W, __nv_bfloat16* Wt, c
   return cudaGetLastError();
 }
 
-cudaError_t launch_bwd_prep(const Params& p, const float* W, __nv_bfloat16* Wt, const float* saved, float* coef,
-                            cudaStream_t st) {
+cudaError_t launch_bwd_prep(const Params& p, const float* W, const float* W_r, __nv_bfloat16* Wt,
+                            const float* saved, float* coef, cudaStream_t st) {
   const size_t NC = (size_t)p.N * p.C;
   const size_t T_all = (size_t)p.B * p.S;
   const unsigned nwt = (unsigned)((NC + 63) / 64);
   const unsigned ncoef = (unsigned)((T_all * 16 + 255) / 256);
   timing_begin("bwd_prep", st);
-  bwd_prep_kernel<<<nwt + ncoef, 256, 0, st>>>(p, W, Wt, nwt, saved, coef, T_all);
+  bwd_prep_kernel<<<nwt + ncoef, 256, 0, st>>>(p, W, W_r, Wt, nwt, saved, coef, T_all);
   timing_end(st);
   return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_reduce(const Params& p, const BwdArgs<__nv_bfloat16>& a, bool has_conv, const float* cpart,
-                              int conv_rows, int w_ranges, const float* wpart, cudaStream_t st) {
-  const size_t PNC = (size_t)p.P * p.N * p.C;
+                              int conv_rows, int w_ranges, const float* wpart, cudaStream_t st, float* dW_r,
+                              const float* cm, float* c_r) {
+  const size_t NC = (size_t)p.N * p.C;
+  const size_t RNC0 = (size_t)p.P * NC;
+  const size_t PNC = RNC0 + (dW_r ? (size_t)p.N * NC : 0);
   timing_begin("bwd_reduce", st);
+  if (dW_r) column_sum_kernel<<<p.N, 256, 0, st>>>(cm, (size_t)p.B * p.S, p.N, c_r);
   // conv sums: one thread per output (24 C of them); dW: about two float4 per thread
   const int cblocks = has_conv ? (int)((NTAPS * (size_t)p.C + 255) / 256) : 0;
   const int wblocks = (int)std::min<size_t>(2 * 148 * 8, (PNC / 4 + 511) / 512);
   bwd_reduce_kernel<<<cblocks + std::max(wblocks, 1), 256, 0, st>>>(conv_rows, p.C, cpart, a.dw[0], a.dw[1], a.dw[2],
-                                                                   cblocks, w_ranges, PNC, wpart, a.dW);
+                                                                   cblocks, w_ranges, PNC, wpart, a.dW, RNC0, NC,
+                                                                   dW_r, c_r);
   timing_end(st);
   return cudaGetLastError();
 }

@@ -6,14 +6,17 @@
 namespace xhc {
 
 cudaError_t launch_wt_prep(const Params& p, const float* W, __nv_bfloat16* Wt, cudaStream_t st);
-// W^T (as launch_wt_prep) and the coefficient block from saved logits (as
-// launch_coef) in one launch.
-cudaError_t launch_bwd_prep(const Params& p, const float* W, __nv_bfloat16* Wt, const float* saved, float* coef,
-                            cudaStream_t st);
+// W^T (as launch_wt_prep; with W_r non-NULL its N rows follow W's P rows) and
+// the coefficient block from saved logits (as launch_coef) in one launch.
+cudaError_t launch_bwd_prep(const Params& p, const float* W, const float* W_r, __nv_bfloat16* Wt,
+                            const float* saved, float* coef, cudaStream_t st);
 // Fixed-order sums of the conv-weight partials [conv_rows][24][C] and the dW
 // partials [w_ranges][P][N C].
+// With a router (dW_r non-NULL) the dW partials have P + N rows; the W_r rows
+// go to dW_r less c_r = sum_t cm[t] (computed here into c_r [N]).
 cudaError_t launch_bwd_reduce(const Params& p, const BwdArgs<__nv_bfloat16>& a, bool has_conv, const float* cpart,
-                              int conv_rows, int w_ranges, const float* wpart, cudaStream_t st);
+                              int conv_rows, int w_ranges, const float* wpart, cudaStream_t st,
+                              float* dW_r = nullptr, const float* cm = nullptr, float* c_r = nullptr);
 
 // Token ranges the tensor-core stream pass splits the batch into (each range
 // writes one dW partial).

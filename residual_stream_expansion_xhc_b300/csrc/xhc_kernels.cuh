@@ -26,6 +26,15 @@ struct UpdArgs {
   const int32_t* tok_idx = nullptr;   // [T, k] per-token active streams (router), or nullptr: Params::idx
 };
 
+// Router side of the per-token reverse (all NULL without a router).
+struct RouterBwd {
+  const int32_t* tok_idx = nullptr;   // [T, k]
+  const float* rrec = nullptr;        // [T, 2N+2]: scores, logits, LN mean, LN sd
+  int n_fixed = 0;
+  const float* rs = nullptr;          // [N] row sums of W_r
+  float* cm = nullptr;                // [T, N] dp_r * LN mean (the dW_r mean term)
+};
+
 template <typename T>
 struct BwdArgs {
   const T* X;             // state before the update, or after it when saved_active != nullptr
@@ -41,6 +50,9 @@ struct BwdArgs {
   float* dw[3];
   float* dW;
   float* rec;             // per-token records (workspace)
+  const int32_t* tok_idx = nullptr;   // [T, k] per-token active streams (router), or nullptr: Params::idx
+  const float* rrec = nullptr;        // [T, 2N+2] router record (scores, logits, LN mean, LN sd)
+  int n_fixed = 0;                    // router: slots [0, n_fixed) are fixed streams
 };
 
 // Active row i of dX' for token t: G_i = dX'[a_i].

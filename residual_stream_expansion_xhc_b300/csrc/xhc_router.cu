@@ -55,7 +55,7 @@ struct Fixed {
 
 __global__ void __launch_bounds__(64) route_kernel(Params p, const float* __restrict__ zr, const float* __restrict__ rs,
                                                    Fixed fx, int32_t* __restrict__ tok_idx,
-                                                   float* __restrict__ scores, float* __restrict__ coef,
+                                                   float* __restrict__ rrec, float* __restrict__ coef,
                                                    size_t T_all) {
   const size_t t = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (t >= T_all) return;
@@ -65,9 +65,12 @@ __global__ void __launch_bounds__(64) route_kernel(Params p, const float* __rest
   const float mean = z[N] * inv / (float)((size_t)N * p.C);
   const float msq = inv * inv - p.eps;
   const float sd = sqrtf(fmaxf(msq - mean * mean, 0.0f) + p.eps);
-  float s[NMAX];
+  float s[NMAX], r[NMAX];
 #pragma unroll
-  for (int n = 0; n < NMAX; ++n) s[n] = n < N ? sigmoidf_((z[n] * inv - mean * rs[n]) / sd) : 0.0f;
+  for (int n = 0; n < NMAX; ++n) {
+    r[n] = n < N ? (z[n] * inv - mean * rs[n]) / sd : 0.0f;
+    s[n] = n < N ? sigmoidf_(r[n]) : 0.0f;
+  }
   unsigned chosen = 0;
   int slot[KMAX];
 #pragma unroll
@@ -94,9 +97,15 @@ __global__ void __launch_bounds__(64) route_kernel(Params p, const float* __rest
       chosen |= 1u << best;
     }
   }
+  float* rr = rrec + t * (2 * N + 2);
 #pragma unroll
   for (int n = 0; n < NMAX; ++n)
-    if (n < N) scores[t * N + n] = s[n];
+    if (n < N) {
+      rr[n] = s[n];
+      rr[N + n] = r[n];
+    }
+  rr[2 * N] = mean;
+  rr[2 * N + 1] = sd;
   float* hp = coef + t * COEF_STRIDE + COEF_POST;
 #pragma unroll
   for (int i = 0; i < KMAX; ++i) {
@@ -114,6 +123,34 @@ __global__ void __launch_bounds__(64) route_kernel(Params p, const float* __rest
   }
 }
 
+// Backward: the routed slots' H^post rows scaled by their scores again (the
+// coefficient block is rebuilt from the saved logits).
+__global__ void __launch_bounds__(64) route_scale_kernel(Params p, const int32_t* __restrict__ tok_idx,
+                                                         const float* __restrict__ rrec, int nf,
+                                                         float* __restrict__ coef, size_t T_all) {
+  const size_t t = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= T_all) return;
+  const int k = p.k;
+  float* hp = coef + t * COEF_STRIDE + COEF_POST;
+  for (int i = nf; i < k; ++i) {
+    const float w = rrec[t * (2 * p.N + 2) + tok_idx[t * k + i]];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) hp[4 * i + c] *= w;
+  }
+}
+
+cudaError_t launch_route_scale(const Params& p, const int32_t* tok_idx, const float* rrec, int nf, float* coef,
+                               cudaStream_t st) {
+  const size_t T_all = (size_t)p.B * p.S;
+  route_scale_kernel<<<(unsigned)((T_all + 63) / 64), 64, 0, st>>>(p, tok_idx, rrec, nf, coef, T_all);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_router_rowsums(const Params& p, const float* W_r, float* rs, cudaStream_t st) {
+  rowsum_kernel<<<p.N, 256, 0, st>>>(W_r, (size_t)p.N * p.C, rs);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_router_weights(const Params& p, const float* W_r, float* Wp, float* rs, cudaStream_t st) {
   const size_t NC = (size_t)p.N * p.C;
   const size_t n4 = (size_t)p.P * NC / 4;
@@ -125,13 +162,13 @@ cudaError_t launch_router_weights(const Params& p, const float* W_r, float* Wp, 
 }
 
 cudaError_t launch_route(const Params& p, const float* zr, const float* rs, const int32_t* fixed, int nf,
-                         int32_t* tok_idx, float* scores, float* coef, cudaStream_t st) {
+                         int32_t* tok_idx, float* rrec, float* coef, cudaStream_t st) {
   const size_t T_all = (size_t)p.B * p.S;
   Fixed fx{};
   fx.n = nf;
   for (int i = 0; i < nf && i < KMAX; ++i) fx.s[i] = fixed[i];
   timing_begin("route", st);
-  route_kernel<<<(unsigned)((T_all + 63) / 64), 64, 0, st>>>(p, zr, rs, fx, tok_idx, scores, coef, T_all);
+  route_kernel<<<(unsigned)((T_all + 63) / 64), 64, 0, st>>>(p, zr, rs, fx, tok_idx, rrec, coef, T_all);
   timing_end(st);
   return cudaGetLastError();
 }

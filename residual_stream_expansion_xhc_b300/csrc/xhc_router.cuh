@@ -11,11 +11,18 @@ namespace xhc {
 cudaError_t launch_router_weights(const Params& p, const float* W_r, float* Wp, float* rs, cudaStream_t st);
 
 // Per token from the router pass's logits zr [T, P+1] (rstd-scaled W' v, then
-// rstd): LayerNorm scores s = sigmoid(W_r LN(v)), the active slots (the nf
-// fixed streams, then the top k - nf others by score), the scores into
-// `scores` [T, N] and the slots into `tok_idx` [T, k]; the coefficient block's
-// H^post rows of the routed slots are scaled by their scores.
+// rstd): LayerNorm scores s = sigmoid(r), r = W_r LN(v), the active slots (the
+// nf fixed streams, then the top k - nf others by score) into `tok_idx`
+// [T, k], and the router record rrec [T, 2N+2] = (s, r, LN mean, LN sd); the
+// coefficient block's H^post rows of the routed slots are scaled by their
+// scores.
 cudaError_t launch_route(const Params& p, const float* zr, const float* rs, const int32_t* fixed, int nf,
-                         int32_t* tok_idx, float* scores, float* coef, cudaStream_t st);
+                         int32_t* tok_idx, float* rrec, float* coef, cudaStream_t st);
+
+// Backward helpers: the routed slots' H^post rows scaled by their scores
+// (from tok_idx and the router record), and the row sums of W_r.
+cudaError_t launch_route_scale(const Params& p, const int32_t* tok_idx, const float* rrec, int nf, float* coef,
+                               cudaStream_t st);
+cudaError_t launch_router_rowsums(const Params& p, const float* W_r, float* rs, cudaStream_t st);
 
 }  // namespace xhc

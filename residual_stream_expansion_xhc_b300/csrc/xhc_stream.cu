@@ -532,7 +532,8 @@ __device__ __forceinline__ float half_transpose_sum16(float (&v)[16], int l16) {
   return v[0];
 }
 
-template <bool HAS_CONV>
+// ROUTED: per-token active streams a.tok_idx (state before the update in a.X).
+template <bool HAS_CONV, bool ROUTED>
 __global__ void __launch_bounds__(col::THREADS, 3) bwd_col_kernel(Params p, BwdArgs<__nv_bfloat16> a,
                                                                   const float* __restrict__ coef,
                                                                   float* __restrict__ pdot, float* __restrict__ cpart,
@@ -598,7 +599,8 @@ __global__ void __launch_bounds__(col::THREADS, 3) bwd_col_kernel(Params p, BwdA
     for (int i = 0; i < KMAX; ++i) {
       if (i < k) {
         float2 g[4];
-        unpack8x2(ld_na(a.dXp + tok * NC + (size_t)p.idx[i] * C + c_lane), g);
+        const int ai = ROUTED ? a.tok_idx[tok * k + i] : p.idx[i];
+        unpack8x2(ld_na(a.dXp + tok * NC + (size_t)ai * C + c_lane), g);
         const float4 hp = *reinterpret_cast<const float4*>(cf + COEF_POST + 4 * i);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -718,6 +720,9 @@ __global__ void __launch_bounds__(col::THREADS, 3) bwd_col_kernel(Params p, BwdA
     const bool tok_ok = t < s_end;             // per half-warp
     const size_t tok = seq_base + (tok_ok ? t : t0);
     const float* cf = coef + tok * COEF_STRIDE;
+    int ai[KMAX];                             // this token's active streams
+#pragma unroll
+    for (int i = 0; i < KMAX; ++i) ai[i] = ROUTED ? (i < k ? a.tok_idx[tok * k + i] : 0) : p.idx[i];
     float2 G[KMAX][4];
     uint4 gr[KMAX], xr[KMAX];                 // raw bf16 rows; zero where absent
 #pragma unroll
@@ -731,9 +736,9 @@ __global__ void __launch_bounds__(col::THREADS, 3) bwd_col_kernel(Params p, BwdA
 #pragma unroll
       for (int i = 0; i < KMAX; ++i) {
         if (i < k) {
-          gr[i] = ld_na(a.dXp + tok * NC + (size_t)p.idx[i] * C + c_lane);
+          gr[i] = ld_na(a.dXp + tok * NC + (size_t)ai[i] * C + c_lane);
           xr[i] = a.saved_active ? ld_na(a.saved_active + (tok * k + i) * C + c_lane)
-                                 : ld_na(a.X + tok * NC + (size_t)p.idx[i] * C + c_lane);
+                                 : ld_na(a.X + tok * NC + (size_t)ai[i] * C + c_lane);
         }
       }
 #pragma unroll
@@ -757,7 +762,7 @@ __global__ void __launch_bounds__(col::THREADS, 3) bwd_col_kernel(Params p, BwdA
             if (i < k)
 #pragma unroll
               for (int q = 0; q < 4; ++q) mx[q] = __ffma2_rn(f2(hres[i][j]), G[i][q], mx[q]);
-          st_stream(a.dX + tok * NC + (size_t)p.idx[j] * C + c_lane, pack8x2(mx));
+          st_stream(a.dX + tok * NC + (size_t)ai[j] * C + c_lane, pack8x2(mx));
         }
       }
       // du_c = sum_i hpost[i][c] G_i
@@ -969,7 +974,7 @@ template <bool GS>
 __global__ void __launch_bounds__(256) bwd_dz_kernel(Params p, const float* __restrict__ saved,
                                                      const float* __restrict__ pdot, int ncb, int has_dxin,
                                                      __nv_bfloat16* __restrict__ dP, float* __restrict__ rec,
-                                                     const float* __restrict__ gsdh, size_t T_all) {
+                                                     const float* __restrict__ gsdh, RouterBwd rb, size_t T_all) {
   extern __shared__ float trace_s[];           // [16 tokens][iters][32]
   const int lane = threadIdx.x & 31, e = lane & 15;
   const int slot = (threadIdx.x >> 5) * 2 + (lane >> 4);
@@ -1018,9 +1023,48 @@ __global__ void __launch_bounds__(256) bwd_dz_kernel(Params p, const float* __re
   const float dz_res = valid ? g * M0 : 0.0f;
   float dz_post = 0.0f, dz_pre = 0.0f, hpre = 0.0f;
   const float h = e < 4 * k ? sigmoidf_(zt[N + e]) : 0.0f;
+  float dpr = 0.0f, alpha_r = 0.0f, beta_r = 0.0f;   // router: dp of logit e, LayerNorm terms
   if (GS) {
     // dL/dH^post through the Gram-Schmidt fold, from gs_rev_kernel
     if (e < 4 * k) dz_post = gsdh[tc * 16 + e] * h * (1.0f - h);
+  } else if (rb.rrec) {
+    // Router: a routed slot i >= n_fixed wrote w_i H^post[i] u with w_i its
+    // stream's score s; dpost holds D[i][c] = <G_i, u_c> at lane 4 i + c.
+    //   dL/dH^post[i][c] = w_i D[i][c];  dL/dw_i = sum_c H^post[i][c] D[i][c]
+    //   dL/dr_n = s_n (1 - s_n) dL/dw_i for the routed slot i of stream n
+    // r = W_r y, y = (v - m) / sd: the LayerNorm reverse adds, per token,
+    //   alpha_r v + beta_r to dL/dv, alpha_r = -(dr . r) / (N C sd^2),
+    //   beta_r = -(dr . rs) / (N C sd) - m alpha_r,
+    // and dp_r = dr / sd enters the W_r rows of the contractions.
+    const int nf = rb.n_fixed;
+    const int32_t* ti = rb.tok_idx + tc * k;
+    const float* rr = rb.rrec + tc * (2 * N + 2);
+    const int si = e >> 2;
+    const float w = (e < 4 * k && si >= nf) ? rr[ti[si]] : 1.0f;
+    if (e < 4 * k) dz_post = w * dpost * h * (1.0f - h);
+    float hd = e < 4 * k ? h * dpost : 0.0f;
+    hd += __shfl_xor_sync(FULL, hd, 1);
+    hd += __shfl_xor_sync(FULL, hd, 2);            // dL/dw of slot e >> 2
+    float dr = 0.0f;
+#pragma unroll
+    for (int q = 0; q < KMAX; ++q) {
+      const float dw_q = __shfl_sync(FULL, hd, (lane & 16) + 4 * q);
+      if (q >= nf && q < k && e < N && ti[q] == e) dr += dw_q;
+    }
+    const float sn = e < N ? rr[e] : 0.0f, rn = e < N ? rr[N + e] : 0.0f;
+    const float mean = rr[2 * N], sd = rr[2 * N + 1];
+    dr *= sn * (1.0f - sn);
+    dpr = dr / sd;
+    float a1 = dr * rn, a2 = e < N ? dr * rb.rs[e] : 0.0f;
+#pragma unroll
+    for (int o = 1; o < 16; o <<= 1) {
+      a1 += __shfl_xor_sync(FULL, a1, o);
+      a2 += __shfl_xor_sync(FULL, a2, o);
+    }
+    const float ncf = (float)((size_t)N * p.C);
+    alpha_r = -a1 / (ncf * sd * sd);
+    beta_r = -a2 / (ncf * sd) - mean * alpha_r;
+    if (live && e < N) rb.cm[t * N + e] = dpr * mean;
   } else if (e < 4 * k) {
     dz_post = dpost * h * (1.0f - h);
   }
@@ -1049,10 +1093,12 @@ __global__ void __launch_bounds__(256) bwd_dz_kernel(Params p, const float* __re
   if (e < N) put(e, rstd * dz_pre);
   if (e < 4 * k) put(N + e, rstd * dz_post);
   if (valid) put(N + 4 * k + k * i + j, rstd * dz_res);
-  for (int q = P + e; q < 64; q += 16) put(q, 0.0f);
+  // entries P .. P + N - 1: the router logits' dp (zero without a router)
+  for (int q = P + e; q < 64; q += 16) put(q, (rb.rrec && q == P + e && e < N) ? dpr : 0.0f);
   const int rl = 1 + N + 4 * k;
   float* rc = rec + t * rl;
-  if (e == 0) rc[0] = -part * rstd * rstd / (float)((size_t)N * p.C);
+  if (e == 0) rc[0] = -part * rstd * rstd / (float)((size_t)N * p.C) + alpha_r;
+  if (e == 0 && rb.rrec) rc[1 + N] = beta_r;      // first unused record entry
   if (e < N) rc[1 + e] = hpre;
 }
 
@@ -1197,19 +1243,25 @@ cudaError_t launch_bwd_col(const Params& p, const BwdArgs<__nv_bfloat16>& a, con
   dim3 grid(wk.R, wk.ncb);
   const int smem = (int)sizeof(ColSmem);
   timing_begin("bwd_col", st);
-  if (has_conv) {
-    cudaFuncSetAttribute(bwd_col_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    bwd_col_kernel<true><<<grid, col::THREADS, smem, st>>>(p, a, coef, pdot, cpart, wk);
+  if (has_conv && a.tok_idx) {
+    cudaFuncSetAttribute(bwd_col_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    bwd_col_kernel<true, true><<<grid, col::THREADS, smem, st>>>(p, a, coef, pdot, cpart, wk);
+  } else if (a.tok_idx) {
+    cudaFuncSetAttribute(bwd_col_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    bwd_col_kernel<false, true><<<grid, col::THREADS, smem, st>>>(p, a, coef, pdot, cpart, wk);
+  } else if (has_conv) {
+    cudaFuncSetAttribute(bwd_col_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    bwd_col_kernel<true, false><<<grid, col::THREADS, smem, st>>>(p, a, coef, pdot, cpart, wk);
   } else {
-    cudaFuncSetAttribute(bwd_col_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    bwd_col_kernel<false><<<grid, col::THREADS, smem, st>>>(p, a, coef, pdot, cpart, wk);
+    cudaFuncSetAttribute(bwd_col_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    bwd_col_kernel<false, false><<<grid, col::THREADS, smem, st>>>(p, a, coef, pdot, cpart, wk);
   }
   timing_end(st);
   return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_dz(const Params& p, const float* saved, const float* pdot, bool has_dxin,
-                          __nv_bfloat16* dP, float* rec, const float* gsdh, cudaStream_t st) {
+                          __nv_bfloat16* dP, float* rec, const float* gsdh, const RouterBwd& rb, cudaStream_t st) {
   const size_t T_all = (size_t)p.B * p.S;
   const int ncb = (p.C + col::CB - 1) / col::CB;
   const size_t smem = (size_t)16 * std::max(p.iters, 1) * 32 * sizeof(float);
@@ -1217,10 +1269,11 @@ cudaError_t launch_bwd_dz(const Params& p, const float* saved, const float* pdot
   timing_begin("bwd_dz", st);
   if (gsdh) {
     cudaFuncSetAttribute(bwd_dz_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    bwd_dz_kernel<true><<<grid, 256, smem, st>>>(p, saved, pdot, ncb, has_dxin ? 1 : 0, dP, rec, gsdh, T_all);
+    bwd_dz_kernel<true><<<grid, 256, smem, st>>>(p, saved, pdot, ncb, has_dxin ? 1 : 0, dP, rec, gsdh, rb, T_all);
   } else {
     cudaFuncSetAttribute(bwd_dz_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    bwd_dz_kernel<false><<<grid, 256, smem, st>>>(p, saved, pdot, ncb, has_dxin ? 1 : 0, dP, rec, nullptr, T_all);
+    bwd_dz_kernel<false><<<grid, 256, smem, st>>>(p, saved, pdot, ncb, has_dxin ? 1 : 0, dP, rec, nullptr, rb,
+                                                  T_all);
   }
   timing_end(st);
   return cudaGetLastError();

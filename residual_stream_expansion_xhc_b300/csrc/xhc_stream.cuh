@@ -25,7 +25,7 @@ cudaError_t launch_bwd_col(const Params& p, const BwdArgs<__nv_bfloat16>& a, con
 // [alpha | hpre (N) | unused (4k)].  With Gram-Schmidt, gsdh [T, 16] holds
 // dL/dH^post (from launch_gs_rev) in place of the column pass's dots.
 cudaError_t launch_bwd_dz(const Params& p, const float* saved, const float* pdot, bool has_dxin,
-                          __nv_bfloat16* dP, float* rec, const float* gsdh, cudaStream_t st);
+                          __nv_bfloat16* dP, float* rec, const float* gsdh, const RouterBwd& rb, cudaStream_t st);
 
 // Gram-Schmidt reverse per token: dL/dH^post [T, 16] into gsdh and the Gram
 // term S = dM + dM^T [T, 16] into sgram, from the column pass's dots, the

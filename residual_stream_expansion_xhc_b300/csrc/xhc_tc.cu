@@ -566,6 +566,10 @@ __global__ void __launch_bounds__(bwdtc::THREADS, 1)
   const int cblocks = C / CB;
   const int nblocks = N * cblocks;
   const int nitems = nblocks * ranges;
+  // router: per-token active sets; dp carries N more entries (the W_r rows of
+  // W^T), so the contractions run K = 64 (dV) and N = 64 (dW)
+  const bool routed = a.tok_idx != nullptr;
+  const int wrows = routed ? P + N : P;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -639,7 +643,8 @@ __global__ void __launch_bounds__(bwdtc::THREADS, 1)
     // ------------------------------------------------ MMA issuer
     if (lane == 0) {
       const uint32_t idesc_v = idesc_bf16(TT, CB, 0, 0);
-      const uint32_t idesc_w = idesc_bf16(CB, 48, 1, 1);
+      const uint32_t idesc_w = idesc_bf16(CB, routed ? 64 : 48, 1, 1);
+      const int ksteps = routed ? 4 : 3;
       const uint32_t wt_addr = smem_u32(wt_s);
       int it = 0, tl = 0, ii = 0;
       for (int item = blockIdx.x; item < nitems; item += gridDim.x, ++ii) {
@@ -654,10 +659,10 @@ __global__ void __launch_bounds__(bwdtc::THREADS, 1)
           if (tl >= 2 && !mbar_wait(&tempty[buf], ((tl >> 1) & 1) ^ 1, err, 26)) { ok = false; break; }
           tc_fence_after();
           const uint32_t st = smem_u32(smem + s * STAGE_BYTES);
-          // dV = dP . Wt^T  (K = 48: three K16 steps inside the 128-byte rows);
-          // hi.hi + hi.lo + lo.hi
-#pragma unroll
-          for (int ks = 0; ks < 3; ++ks) {
+          // dV = dP . Wt^T  (K = 48: three K16 steps inside the 128-byte rows,
+          // four with the router rows); hi.hi + hi.lo + lo.hi
+#pragma unroll 4
+          for (int ks = 0; ks < ksteps; ++ks) {
             const uint64_t ph = sdesc_sw128(st + OFF_P + ks * 32, 16, 1024);
             const uint64_t pl = sdesc_sw128(st + OFF_PL + ks * 32, 16, 1024);
             const uint64_t wh = sdesc_sw128(wt_addr + ks * 32, 16, 1024);
@@ -736,10 +741,15 @@ __global__ void __launch_bounds__(bwdtc::THREADS, 1)
         const uint32_t ph = (it / STAGES) & 1;
         const size_t t = t0 + row;
         const bool live = t < T_all;
-        float alpha = 0.0f, hp = 0.0f;           // loaded before the waits
+        float alpha = 0.0f, hp = 0.0f, beta = 0.0f;   // loaded before the waits
+        bool act_row = false;                   // router: stream n active for this token
         if (live) {
           alpha = a.rec[t * rl];
           if (a.dx_in) hp = a.rec[t * rl + 1 + n];
+          if (routed) {
+            beta = a.rec[t * rl + 1 + N];
+            for (int i = 0; i < k; ++i) act_row |= a.tok_idx[t * k + i] == n;
+          }
         }
         if (!mbar_wait(&full[s], ph, err, 27)) { ok = false; break; }
         if (!mbar_wait(&tfull[buf], (tl >> 1) & 1, err, 28)) { ok = false; break; }
@@ -757,8 +767,14 @@ __global__ void __launch_bounds__(bwdtc::THREADS, 1)
           const uint8_t* br = st + OFF_B + h * HALF;
           const uint4 x0 = *reinterpret_cast<const uint4*>(xr + o0);
           const uint4 x1 = *reinterpret_cast<const uint4*>(xr + o1);
-          const uint4 b0 = *reinterpret_cast<const uint4*>(br + o0);
-          const uint4 b1 = *reinterpret_cast<const uint4*>(br + o1);
+          uint4 b0 = *reinterpret_cast<const uint4*>(br + o0);
+          uint4 b1 = *reinterpret_cast<const uint4*>(br + o1);
+          if (act_row) {
+            // an active row's base is the mix the column pass wrote to dX
+            const uint4* src = reinterpret_cast<const uint4*>(a.dX + (t * N + n) * (size_t)C + c0 + cc * 16);
+            b0 = src[0];
+            b1 = src[1];
+          }
           const uint32_t xw[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
           const uint32_t bw[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
           float g[16];
@@ -783,8 +799,8 @@ __global__ void __launch_bounds__(bwdtc::THREADS, 1)
             float yb = __uint_as_float(d[2 * e + 1]) + bf_hi(bw[e]);
             ya = fmaf(alpha, bf_lo(xw[e]), ya);
             yb = fmaf(alpha, bf_hi(xw[e]), yb);
-            ya = fmaf(hp, g[2 * e], ya);
-            yb = fmaf(hp, g[2 * e + 1], yb);
+            ya = fmaf(hp, g[2 * e], ya) + beta;
+            yb = fmaf(hp, g[2 * e + 1], yb) + beta;
             o[e] = pack_bf2(ya, yb);
           }
           uint8_t* orow = st + OFF_P + h * HALF;        // dX box h, same swizzle as the loads
@@ -804,15 +820,15 @@ __global__ void __launch_bounds__(bwdtc::THREADS, 1)
       // dW partial of this item: TMEM lane = column of the block, 48 columns = q
       if (!mbar_wait(&d2full, ii & 1, err, 29)) break;
       tc_fence_after();
-      float* dst = wpart + (size_t)r * P * NC + (size_t)n * C + c0 + row;
-#pragma unroll
-      for (int qc = 16 * part; qc < 48; qc += 16 * SPLIT) {
+      float* dst = wpart + (size_t)r * wrows * NC + (size_t)n * C + c0 + row;
+#pragma unroll 1
+      for (int qc = 16 * part; qc < wrows; qc += 16 * SPLIT) {
         uint32_t d[16];
         tmem_ld16(tmem + lane_base + D2_COL + qc, d);
         tmem_wait_ld();
 #pragma unroll
         for (int e = 0; e < 16; ++e)
-          if (qc + e < P) dst[(size_t)(qc + e) * NC] = __uint_as_float(d[e]);
+          if (qc + e < wrows) dst[(size_t)(qc + e) * NC] = __uint_as_float(d[e]);
       }
       tc_fence_before();
       __syncwarp();

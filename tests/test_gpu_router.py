@@ -47,14 +47,15 @@ def _run(wl, t, W_r, fixed):
     saved = torch.empty(wl.B, wl.S, wl.P + 1, device="cuda")
     act = torch.empty(wl.B, wl.S, wl.k, wl.C, dtype=tdtype(wl), device="cuda")
     tok_idx = torch.empty(wl.B, wl.S, wl.k, dtype=torch.int32, device="cuda")
-    scores = torch.empty(wl.B, wl.S, wl.N, device="cuda")
+    rrec = torch.empty(wl.B, wl.S, 2 * wl.N + 2, device="cuda")
     ws = api.workspace(api.xhc_fwd_routed_workspace_bytes(sh))
-    api.xhc_sublayer_fwd_routed(sh, X, X, out, conv, dev_f32(t.W), dev_f32(W_r), fixed, tok_idx, scores, ws,
+    api.xhc_sublayer_fwd_routed(sh, X, X, out, conv, dev_f32(t.W), dev_f32(W_r), fixed, tok_idx, rrec, ws,
                                 x_in=x_in, saved=saved, saved_active=act)
     torch.cuda.synchronize()
     api.xhc_device_status()
-    return dict(X0=X0, Xp=X, x_in=x_in, idx=tok_idx.cpu().numpy(), scores=scores.cpu().numpy().astype(np.float64),
-                act=act)
+    rr = rrec.cpu().numpy().astype(np.float64)
+    return dict(X0=X0, Xp=X, x_in=x_in, idx=tok_idx.cpu().numpy(), scores=rr[..., : wl.N], rrec=rr, act=act,
+                tok_idx=tok_idx, rrec_dev=rrec, saved=saved)
 
 
 @pytest.mark.parametrize("name", list(CASES))
@@ -67,6 +68,13 @@ def test_routed_forward_parity(name):
     X, out, conv, W, _ = oracle_inputs(wl, t)
     ref = xo.forward_routed(X, out, conv, W, W_r.astype(np.float64), fixed, wl.k, iters=wl.iters, eps=wl.eps)
     assert np.abs(g["scores"] - ref["s"]).max() < 1e-4
+    # the record's logits, LayerNorm mean and sd
+    for b in range(wl.B):
+        _, r, y, sd = xo.router_scores(X[b], W_r.astype(np.float64), wl.eps)
+        assert np.abs(g["rrec"][b, :, wl.N:2 * wl.N] - r).max() < 1e-3
+        assert np.abs(g["rrec"][b, :, 2 * wl.N + 1] - sd).max() < 1e-4 * sd.max()
+        mean = X[b].reshape(wl.S, -1).mean(axis=1)
+        assert np.abs(g["rrec"][b, :, 2 * wl.N] - mean).max() < 1e-4
     # the selection: equal, or a tie in the oracle's scores
     same = (g["idx"] == ref["idx"]).all(axis=-1)
     for b, s_ in zip(*np.nonzero(~same)):
@@ -90,3 +98,40 @@ def test_routed_forward_parity(name):
     x0 = g["X0"].view(torch.int16).cpu().numpy()
     gidx = g["idx"].astype(np.int64)
     assert np.array_equal(act, np.take_along_axis(x0, gidx[..., None], axis=2))
+
+
+@pytest.mark.parametrize("name", list(CASES))
+@pytest.mark.parametrize("with_dxin", [False, True])
+def test_routed_backward_parity(name, with_dxin):
+    wl, nf = CASES[name]
+    t = xin.make(wl, grads=True, dx_in=with_dxin)
+    W_r = _router_weights(wl)
+    fixed = [int(a) for a in t.idx[:nf]]
+    g = _run(wl, t, W_r, fixed)
+    sh = api.make_shape(wl.B, wl.S, wl.N, wl.C, wl.k, tdtype(wl), wl.iters, wl.eps)
+    out = dev_act(wl, t.out)
+    conv = None if t.conv is None else tuple(dev_f32(w) for w in t.conv)
+    W, Wr = dev_f32(t.W), dev_f32(W_r)
+    dXp = dev_act(wl, t.dXp)
+    dxi = dev_act(wl, t.dx_in) if with_dxin else None
+    dX = torch.empty_like(dXp)
+    dout = torch.empty_like(out)
+    dconv = None if conv is None else tuple(torch.empty_like(w) for w in conv)
+    dW, dW_r = torch.empty_like(W), torch.empty_like(Wr)
+    ws = api.workspace(api.xhc_bwd_routed_workspace_bytes(sh))
+    api.xhc_sublayer_bwd_routed(sh, g["X0"], out, conv, W, Wr, fixed, g["saved"], g["tok_idx"], g["rrec_dev"], dXp,
+                                dxi, dX, dout, dconv, dW, dW_r, ws)
+    torch.cuda.synchronize()
+    api.xhc_device_status()
+    X, out64, conv64, W64, _ = oracle_inputs(wl, t)
+    ref = xo.backward_routed(X, out64, conv64, W64, W_r.astype(np.float64), fixed, wl.k, xin.to_f64(wl, t.dXp),
+                             xin.to_f64(wl, t.dx_in) if with_dxin else None, iters=wl.iters, eps=wl.eps,
+                             idx=g["idx"])
+    tol = TOL[wl.dtype]
+    for key, got in (("dX", dX), ("dout", dout), ("dW", dW), ("dW_r", dW_r)):
+        e = xo.max_rel_err(host_f64(got), ref[key])
+        assert e <= tol, f"{key} err {e}"
+    if conv is not None:
+        for j in range(3):
+            e = xo.max_rel_err(host_f64(dconv[j]), ref["dconv"][j])
+            assert e <= tol, f"dw{(4, 8, 12)[j]} err {e}"
