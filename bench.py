@@ -147,6 +147,9 @@ def oracle_sample(wl, tensors, ntok: int):
     out = xin.to_f64(wl, tensors.out[:1, :ntok])
     dXp = xin.to_f64(wl, tensors.dXp[:1, :ntok])
     conv = None if tensors.conv is None else tuple(np.asarray(w, np.float64) for w in tensors.conv)
+    if wl.router_fixed >= 0:
+        W_r = np.asarray(tensors.extra["W_r"], np.float64)
+        return X, out, conv, np.asarray(tensors.W, np.float64), (W_r, list(tensors.idx[: wl.router_fixed])), dXp
     return X, out, conv, np.asarray(tensors.W, np.float64), tensors.idx, dXp
 
 
@@ -154,8 +157,13 @@ def time_oracle(sample, wl):
     from oracle import xhc_oracle as xo
     X, out, conv, W, idx, dXp = sample
     t0 = time.perf_counter()
-    xo.forward(X, out, conv, W, idx, iters=wl.iters, eps=wl.eps, gs=wl.gram_schmidt)
-    xo.backward(X, out, conv, W, idx, dXp, None, iters=wl.iters, eps=wl.eps, gs=wl.gram_schmidt)
+    if wl.router_fixed >= 0:
+        W_r, fixed = idx
+        xo.forward_routed(X, out, conv, W, W_r, fixed, wl.k, iters=wl.iters, eps=wl.eps)
+        xo.backward_routed(X, out, conv, W, W_r, fixed, wl.k, dXp, None, iters=wl.iters, eps=wl.eps)
+    else:
+        xo.forward(X, out, conv, W, idx, iters=wl.iters, eps=wl.eps, gs=wl.gram_schmidt)
+        xo.backward(X, out, conv, W, idx, dXp, None, iters=wl.iters, eps=wl.eps, gs=wl.gram_schmidt)
     return time.perf_counter() - t0
 
 
@@ -199,9 +207,13 @@ def run_reference(args, wl):
 
 
 def wl_desc(wl):
+    head = f"{wl.name}: B={wl.B} S={wl.S} N={wl.N} C={wl.C} k={wl.k} {wl.dtype}; "
+    if wl.router_fixed >= 0:
+        return head + (f"router: {wl.router_fixed} fixed + {wl.k - wl.router_fixed} routed slots per token; forward "
+                       f"(out of place, x_in, saved logits, router record) + backward (dX', no dx_in)")
     gs = "; Gram-Schmidt of the TFA components" if wl.gram_schmidt else ""
-    return (f"{wl.name}: B={wl.B} S={wl.S} N={wl.N} C={wl.C} k={wl.k} {wl.dtype}; forward (training mode: in "
-            f"place, x_in, saved logits, saved active rows) + backward (dX', no dx_in){gs}")
+    return head + (f"forward (training mode: in place, x_in, saved logits, saved active rows) + backward (dX', "
+                   f"no dx_in){gs}")
 
 
 # ----------------------------------------------------------------------------- GPU arm
@@ -249,6 +261,33 @@ class Step:
     def __call__(self):
         self.fwd()
         self.bwd()
+
+
+class RoutedStep(Step):
+    """The router's forward (out of place: the backward takes the state before
+    the update) and backward on the same buffers."""
+
+    def __init__(self, wl, tensors, dev):
+        super().__init__(wl, tensors, dev)
+        torch = self.torch
+        B, S, N, k = wl.B, wl.S, wl.N, wl.k
+        self.W_r = torch.from_numpy(tensors.extra["W_r"]).to(dev)
+        self.fixed = self.idx[: wl.router_fixed]
+        self.Xo = torch.empty_like(self.X)
+        self.tok_idx = torch.empty(B, S, k, dtype=torch.int32, device=dev)
+        self.rrec = torch.empty(B, S, 2 * N + 2, dtype=torch.float32, device=dev)
+        self.dW_r = torch.empty_like(self.W_r)
+        self.fws = self.api.workspace(self.api.xhc_fwd_routed_workspace_bytes(self.sh), dev)
+        self.ws = self.api.workspace(self.api.xhc_bwd_routed_workspace_bytes(self.sh), dev)
+
+    def fwd(self):
+        self.api.xhc_sublayer_fwd_routed(self.sh, self.X, self.Xo, self.out, self.conv, self.W, self.W_r, self.fixed,
+                                         self.tok_idx, self.rrec, self.fws, x_in=self.x_in, saved=self.saved)
+
+    def bwd(self):
+        self.api.xhc_sublayer_bwd_routed(self.sh, self.X, self.out, self.conv, self.W, self.W_r, self.fixed,
+                                         self.saved, self.tok_idx, self.rrec, self.dXp, None, self.dX, self.dout,
+                                         self.dconv, self.dW, self.dW_r, self.ws)
 
 
 def timed(fn, steps):
@@ -299,7 +338,7 @@ def e2e_run(step, tensors, steps):
 
     hX, hout, hdXp = pinned(tensors.X), pinned(tensors.out), pinned(tensors.dXp)
     as_raw = (lambda t: t) if wl.dtype == "f32" else (lambda t: t.view(torch.int16))
-    sets = [step, Step(wl, tensors, dev)]
+    sets = [step, type(step)(wl, tensors, dev)]
     res = []
     for _ in sets:
         rdc = None if step.dconv is None else [torch.empty(w.shape, dtype=torch.float32).pin_memory()
@@ -367,7 +406,7 @@ def run_gpu(args, wl):
     from residual_stream_expansion_xhc_b300 import api
 
     tensors = xin.make(wl, grads=True)
-    step = Step(wl, tensors, dev)
+    step = RoutedStep(wl, tensors, dev) if wl.router_fixed >= 0 else Step(wl, tensors, dev)
     same_run_copy = copy_peak(dev)
     esz = wl.esize
     cunit = wl.C * esz

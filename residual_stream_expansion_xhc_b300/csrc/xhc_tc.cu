@@ -545,6 +545,8 @@ struct StreamMaps {
   CUtensorMap X, Xa, dXp, dX, dP, dPl, Wt, Wtl;
 };
 
+// ROUTED: per-token active sets (a.tok_idx) and the router rows of dp / W^T.
+template <bool ROUTED>
 __global__ void __launch_bounds__(bwdtc::THREADS, 1)
     bwd_stream_tc_kernel(const __grid_constant__ StreamMaps m, Params p, BwdArgs<__nv_bfloat16> a, int ranges,
                          int range_len, float* __restrict__ wpart) {
@@ -568,7 +570,7 @@ __global__ void __launch_bounds__(bwdtc::THREADS, 1)
   const int nitems = nblocks * ranges;
   // router: per-token active sets; dp carries N more entries (the W_r rows of
   // W^T), so the contractions run K = 64 (dV) and N = 64 (dW)
-  const bool routed = a.tok_idx != nullptr;
+  constexpr bool routed = ROUTED;
   const int wrows = routed ? P + N : P;
 
   if (threadIdx.x == 0) {
@@ -746,7 +748,7 @@ __global__ void __launch_bounds__(bwdtc::THREADS, 1)
         if (live) {
           alpha = a.rec[t * rl];
           if (a.dx_in) hp = a.rec[t * rl + 1 + n];
-          if (routed) {
+          if (ROUTED) {
             beta = a.rec[t * rl + 1 + N];
             for (int i = 0; i < k; ++i) act_row |= a.tok_idx[t * k + i] == n;
           }
@@ -769,7 +771,7 @@ __global__ void __launch_bounds__(bwdtc::THREADS, 1)
           const uint4 x1 = *reinterpret_cast<const uint4*>(xr + o1);
           uint4 b0 = *reinterpret_cast<const uint4*>(br + o0);
           uint4 b1 = *reinterpret_cast<const uint4*>(br + o1);
-          if (act_row) {
+          if (ROUTED && act_row) {
             // an active row's base is the mix the column pass wrote to dX
             const uint4* src = reinterpret_cast<const uint4*>(a.dX + (t * N + n) * (size_t)C + c0 + cc * 16);
             b0 = src[0];
@@ -799,8 +801,12 @@ __global__ void __launch_bounds__(bwdtc::THREADS, 1)
             float yb = __uint_as_float(d[2 * e + 1]) + bf_hi(bw[e]);
             ya = fmaf(alpha, bf_lo(xw[e]), ya);
             yb = fmaf(alpha, bf_hi(xw[e]), yb);
-            ya = fmaf(hp, g[2 * e], ya) + beta;
-            yb = fmaf(hp, g[2 * e + 1], yb) + beta;
+            ya = fmaf(hp, g[2 * e], ya);
+            yb = fmaf(hp, g[2 * e + 1], yb);
+            if (ROUTED) {
+              ya += beta;
+              yb += beta;
+            }
             o[e] = pack_bf2(ya, yb);
           }
           uint8_t* orow = st + OFF_P + h * HALF;        // dX box h, same swizzle as the loads
@@ -902,9 +908,14 @@ cudaError_t launch_bwd_stream_tc(const Params& p, const BwdArgs<__nv_bfloat16>& 
   const int range_len = (int)(((tiles + ranges - 1) / ranges) * TT);
   const int nitems = p.N * (p.C / CB) * ranges;
   const int grid = std::min(nitems, sm_count());
-  cudaFuncSetAttribute(bwd_stream_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
   timing_begin("bwd_stream_tc", st);
-  bwd_stream_tc_kernel<<<grid, THREADS, SMEM, st>>>(m, p, a, ranges, range_len, wpart);
+  if (a.tok_idx) {
+    cudaFuncSetAttribute(bwd_stream_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+    bwd_stream_tc_kernel<true><<<grid, THREADS, SMEM, st>>>(m, p, a, ranges, range_len, wpart);
+  } else {
+    cudaFuncSetAttribute(bwd_stream_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+    bwd_stream_tc_kernel<false><<<grid, THREADS, SMEM, st>>>(m, p, a, ranges, range_len, wpart);
+  }
   timing_end(st);
   return cudaGetLastError();
 }

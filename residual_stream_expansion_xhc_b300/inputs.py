@@ -16,7 +16,7 @@ from typing import Optional
 
 import numpy as np
 
-T_X, T_OUT, T_W4, T_W8, T_W12, T_W, T_IDX, T_DXP, T_DXIN = range(9)
+T_X, T_OUT, T_W4, T_W8, T_W12, T_W, T_IDX, T_DXP, T_DXIN, T_WR = range(10)
 CONV_KS = (4, 8, 12)
 
 
@@ -40,6 +40,7 @@ class Workload:
     iters: int = 20
     eps: float = 1e-6
     gram_schmidt: bool = False    # orthogonalise the TFA components
+    router_fixed: int = -1        # >= 0: router with this many fixed streams (W_r ~ N(0, 1/(N C)))
 
     @property
     def P(self) -> int:
@@ -69,6 +70,10 @@ WORKLOADS = {
     # the sublayer without TFA (u_0 = out only) at N = 16, k = 4
     "noconv_bf16": Workload("noconv_bf16", 8, B=4, S=4096, N=16, C=2048, k=4, dtype="bf16", conv="none",
                             backward=True),
+    # per-token active sets from the router: the first two slots of the
+    # layer's index list are fixed, two more are chosen per token
+    "router_bf16": Workload("router_bf16", 9, B=4, S=4096, N=16, C=2048, k=4, dtype="bf16", backward=True,
+                            router_fixed=2),
     "gs_bf16": Workload("gs_bf16", 7, B=4, S=4096, N=16, C=2048, k=4, dtype="bf16", backward=True,
                         conv_std=0.3, gram_schmidt=True),
 }
@@ -157,6 +162,9 @@ def make(wl: Workload, layer: int = 0, *, state: bool = True, grads: bool = Fals
         t.dXp = _act(wl, seed_of(wl.wid, layer, T_DXP), (B, S, N, C))
     if dx_in:
         t.dx_in = _act(wl, seed_of(wl.wid, layer, T_DXIN), (B, S, C))
+    if wl.router_fixed >= 0:
+        # router logits W_r . LN(vec X) with a standard deviation of about 1
+        t.extra["W_r"] = _normal(seed_of(wl.wid, layer, T_WR), (N, N * C), 1.0 / float(np.sqrt(N * C)))
     return t
 
 
