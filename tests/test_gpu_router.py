@@ -135,3 +135,40 @@ def test_routed_backward_parity(name, with_dxin):
         for j in range(3):
             e = xo.max_rel_err(host_f64(dconv[j]), ref["dconv"][j])
             assert e <= tol, f"dw{(4, 8, 12)[j]} err {e}"
+
+
+def test_routed_full_shape_one_sequence():
+    """One sequence of the router workload at full width (S = 4096, C = 2048):
+    forward and backward against the oracle on every token, with the GPU's
+    active sets (their own check is the forward test's)."""
+    wl = xin.scaled(xin.WORKLOADS["router_bf16"], B=1)
+    t = xin.make(wl, grads=True)
+    W_r = t.extra["W_r"]
+    fixed = [int(a) for a in t.idx[: wl.router_fixed]]
+    g = _run(wl, t, W_r, fixed)
+    X, out, conv, W, _ = oracle_inputs(wl, t)
+    tol = TOL[wl.dtype]
+    sh = api.make_shape(wl.B, wl.S, wl.N, wl.C, wl.k, tdtype(wl), wl.iters, wl.eps)
+    conv_d = tuple(dev_f32(w) for w in t.conv)
+    out_d, W_d, Wr_d, dXp = dev_act(wl, t.out), dev_f32(t.W), dev_f32(W_r), dev_act(wl, t.dXp)
+    dX, dout = torch.empty_like(dXp), torch.empty_like(out_d)
+    dconv = tuple(torch.empty_like(w) for w in conv_d)
+    dW, dW_r = torch.empty_like(W_d), torch.empty_like(Wr_d)
+    ws = api.workspace(api.xhc_bwd_routed_workspace_bytes(sh))
+    api.xhc_sublayer_bwd_routed(sh, g["X0"], out_d, conv_d, W_d, Wr_d, fixed, g["saved"], g["tok_idx"],
+                                g["rrec_dev"], dXp, None, dX, dout, dconv, dW, dW_r, ws)
+    torch.cuda.synchronize()
+    api.xhc_device_status()
+    W_r64 = W_r.astype(np.float64)
+    # forward: the routed update reproduced with the GPU's active sets
+    ref_s, _, _, _ = xo.router_scores(X[0], W_r64, wl.eps)
+    assert np.abs(g["scores"][0] - ref_s).max() < 1e-4
+    assert (g["idx"][0] == xo.route(ref_s, fixed, wl.k)).mean() > 0.99
+    br = xo.backward_routed(X, out, conv, W, W_r64, fixed, wl.k, xin.to_f64(wl, t.dXp), None, iters=wl.iters,
+                            eps=wl.eps, idx=g["idx"])
+    for key, got in (("dX", dX), ("dout", dout), ("dW", dW), ("dW_r", dW_r)):
+        e = xo.max_rel_err(host_f64(got), br[key])
+        assert e <= tol, f"{key} err {e}"
+    for j in range(3):
+        e = xo.max_rel_err(host_f64(dconv[j]), br["dconv"][j])
+        assert e <= tol, f"dw{(4, 8, 12)[j]} err {e}"
