@@ -178,3 +178,33 @@ def test_gram_schmidt_rejections(lib):
     assert L.xhc_tfa(ctypes.byref(sh), FAKE, FAKE, FAKE, FAKE, FAKE, None) == 8
     assert L.xhc_sparse_update(ctypes.byref(sh), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
                                idx(0, 1, 2, 3), None) == 8
+
+
+# ---------------------------------------------------------------- router entry points
+
+def test_router_rejections(lib):
+    L = lib.LIB
+    sh = shape(lib)
+    need = L.xhc_fwd_routed_workspace_bytes(ctypes.byref(sh))
+    assert need > L.xhc_fwd_workspace_bytes(ctypes.byref(sh))
+
+    def fwd_r(sh, fixed, nf, ws=FAKE, wsb=None):
+        fx = (ctypes.c_int32 * 4)(*fixed) if fixed is not None else None
+        return L.xhc_sublayer_fwd_routed(ctypes.byref(sh), FAKE, FAKE, FAKE, None, None, None, FAKE, FAKE, fx, nf,
+                                         None, None, None, FAKE, FAKE, ws, need if wsb is None else wsb, None)
+    assert fwd_r(sh, (0, 1, 0, 0), 2, wsb=need - 1) == 5
+    assert fwd_r(sh, (0, 0, 0, 0), 2) == 2            # repeated fixed stream
+    assert fwd_r(sh, (0, 16, 0, 0), 2) == 2           # outside [0, N)
+    assert fwd_r(sh, (0, 1, 2, 3), 5) == 2            # more fixed streams than slots
+    assert fwd_r(shape(lib, dtype=0), (0, 1, 0, 0), 2) == 4
+    gs = shape(lib)
+    gs.gram_schmidt = 1
+    assert fwd_r(gs, (0, 1, 0, 0), 2) == 8
+    bneed = L.xhc_bwd_routed_workspace_bytes(ctypes.byref(sh))
+    assert bneed > L.xhc_bwd_workspace_bytes(ctypes.byref(sh))
+    fx = (ctypes.c_int32 * 2)(0, 1)
+    # P + N > 64 has no room for the router rows in the backward (N = 16, k = 4 fits; N = 8, k = 4 fits;
+    # N = 12, k = 4: P = 44, 44 + 12 = 56 fits) -- fp32 is refused
+    assert L.xhc_sublayer_bwd_routed(ctypes.byref(shape(lib, dtype=0)), FAKE, FAKE, None, None, None, FAKE, FAKE,
+                                     fx, 2, FAKE, FAKE, FAKE, ctypes.c_void_p(1 << 22), None, FAKE, FAKE, None, None,
+                                     None, FAKE, FAKE, FAKE, bneed, None) == 4

@@ -28,6 +28,8 @@ CASES = {
     "router_c2048": (xin.Workload("router_c2048", 52, B=1, S=130, N=16, C=2048, k=4, dtype="bf16"), 2),
     "router_s5_nofixed": (xin.Workload("router_s5", 53, B=3, S=5, N=16, C=256, k=4, dtype="bf16"), 0),
     "router_k2": (xin.Workload("router_k2", 54, B=2, S=40, N=6, C=256, k=2, dtype="bf16"), 1),
+    "router_noconv": (xin.Workload("router_noconv", 55, B=2, S=40, N=16, C=256, k=4, dtype="bf16", conv="none"), 2),
+    "router_all_fixed": (xin.Workload("router_all_fixed", 56, B=1, S=33, N=16, C=256, k=4, dtype="bf16"), 4),
 }
 
 
