@@ -252,6 +252,47 @@ def forward(X, out, conv, W, idx, iters=20, eps=1e-6, gs=False):
     return res
 
 
+def round_bf16(x):
+    """Nearest bf16 value of each entry (round half to even), as float64.
+
+    A bf16 number keeps 8 significant bits: x = m 2^e with 1/2 <= |m| < 1 is
+    replaced by round(m 2^8) 2^(e - 8).  Magnitudes stay far inside bf16's
+    exponent range here, so neither overflow nor subnormals arise.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    m, e = np.frexp(x)
+    return np.ldexp(np.round(np.ldexp(m, 8)), e - 8)
+
+
+def forward_stack(X, outs, convs, Ws, idxs, iters=20, eps=1e-6, gs=False, store=None):
+    """A stack of L sublayers applied in order to one state (in place in
+    memory): sublayer l reads the state S_l that sublayer l - 1 wrote, with its
+    own out_l, conv_l, W_l and index list a_l, and writes S_{l+1}.
+
+    [xHC] "Dense read, sparse write" (the state of the next sublayer is the
+    scatter-updated state of this one; the next input is a dense read of it)
+    and "Beyond N=16" (xHC-Flash: a stack whose per-sublayer memory traffic a
+    reordered schedule lowers, with an exact dense-read correction).  ``store="bf16"``: the state is rounded to bf16 after
+    every sublayer, as a bf16 state in memory holds it between sublayers; the
+    first state is taken as given.
+
+    Returns dict(states=[S_0 .. S_L], x_in=[per sublayer], z=[per sublayer],
+    rstd=[per sublayer]).
+    """
+    L = len(outs)
+    assert len(convs) == len(Ws) == len(idxs) == L
+    states, x_ins, zs, rstds = [X], [], [], []
+    S = X
+    for l in range(L):
+        r = forward(S, outs[l], convs[l], Ws[l], idxs[l], iters=iters, eps=eps, gs=gs)
+        S = round_bf16(r["Xp"]) if store == "bf16" else r["Xp"]
+        states.append(S)
+        x_ins.append(r["x_in"])
+        zs.append(r["z"])
+        rstds.append(r["rstd"])
+    return dict(states=states, x_in=x_ins, z=zs, rstd=rstds)
+
+
 def backward(X, out, conv, W, idx, dXp, dx_in=None, iters=20, eps=1e-6, keep=False, gs=False):
     """Exact reverse mode of ``forward``.
 
