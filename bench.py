@@ -37,13 +37,18 @@ METRIC = "tokens/s per xHC sublayer (fwd, fwd+bwd) and achieved HBM GB/s vs peak
 #   backward, token:  4 (dX' active) + 4 (old active rows) + 1 (out) = 9
 #   backward, stream: 16 (X) + 16 (dX') + 1 (out) + 16 (dX) + 1 (dout) = 50
 ALG_C = {  # algorithmic bytes per token in C-units (one row of C state elements)
-    "coeffs_tc": 16, "fwd_update": 26, "bwd_col": 14, "bwd_stream_tc": 48,
+    "coeffs_tc": 16, "fwd_update": 26, "bwd_col": 14, "bwd_stream_tc": 48, "flash_tc": 22,
     "coeffs_simt": 17, "update_simt": 26,
     "bwd_token_simt": 9, "bwd_dx_simt": 48, "bwd_dw_simt": 16, "bwd_tfa_simt": 6,
 }
 ALG_SIDE = {  # fp32 bytes per token
-    "coeffs_tc": 196, "coeffs_simt": 196,
+    "coeffs_tc": 196, "coeffs_simt": 196, "flash_tc": 192 + 196,
 }
+# The fused stack step (flash_tc) of sublayer l: 16 (read X) + 1 (read out) +
+# 4 (write the active rows in place) + 1 (write x_in) = 22 C, plus sublayer
+# l's coefficient block read (192 B) and sublayer l+1's logits and block
+# written (196 B).  The closing update of a stack writes no saved rows: 22 C.
+ALG_C_STACK = {"fwd_update": 22}
 
 
 def load_peaks():
@@ -153,6 +158,22 @@ def oracle_sample(wl, tensors, ntok: int):
     return X, out, conv, np.asarray(tensors.W, np.float64), tensors.idx, dXp
 
 
+def stack_sample(wl, layers, ntok: int):
+    """The first ``ntok`` tokens of sequence 0 through every sublayer of a stack."""
+    X = xin.to_f64(wl, layers[0].X[:1, :ntok])
+    outs = [xin.to_f64(wl, t.out[:1, :ntok]) for t in layers]
+    convs = [None if t.conv is None else tuple(np.asarray(w, np.float64) for w in t.conv) for t in layers]
+    return X, outs, convs, [np.asarray(t.W, np.float64) for t in layers], [list(t.idx) for t in layers]
+
+
+def time_oracle_stack(sample, wl):
+    from oracle import xhc_oracle as xo
+    X, outs, convs, Ws, idxs = sample
+    t0 = time.perf_counter()
+    xo.forward_stack(X, outs, convs, Ws, idxs, iters=wl.iters, eps=wl.eps, gs=wl.gram_schmidt, store="bf16")
+    return time.perf_counter() - t0
+
+
 def time_oracle(sample, wl):
     from oracle import xhc_oracle as xo
     X, out, conv, W, idx, dXp = sample
@@ -176,6 +197,14 @@ def blas_threads() -> int:
         return os.cpu_count() or 1
 
 
+def cpu_baseline_stack(wl, layers, ntok=256):
+    sample = stack_sample(wl, layers, ntok)
+    dt = time_oracle_stack(sample, wl)
+    return {"value": ntok * wl.layers / dt, "unit": "sublayer-tokens/s", "cores": blas_threads(), "kind": "oracle",
+            "sample": f"fp64 numpy oracle, the {wl.layers}-sublayer stack forward of the first {ntok} tokens of "
+                      f"sequence 0 ({dt:.1f} s)"}
+
+
 def cpu_baseline(wl, tensors, ntok=1024):
     sample = oracle_sample(wl, tensors, ntok)
     dt = time_oracle(sample, wl)
@@ -188,8 +217,26 @@ def run_reference(args, wl):
     world, rank, _ = dist_setup()
     if rank != 0:
         return
-    tensors = xin.make(wl, grads=True)
     ntok = args.ref_tokens
+    if wl.layers > 1:
+        layers = [xin.make(wl, l, state=(l == 0)) for l in range(wl.layers)]
+        sample = stack_sample(wl, layers, ntok)
+        for _ in range(args.warmup):
+            time_oracle_stack(sample, wl)
+        t = sum(time_oracle_stack(sample, wl) for _ in range(args.steps))
+        value = ntok * wl.layers * args.steps / t
+        desc = f"fp64 numpy oracle, the {wl.layers}-sublayer stack forward of the first {ntok} tokens of sequence 0"
+        line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "sublayer-tokens/s",
+                "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / args.steps,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "config": {"workload": wl_desc(wl), "sample_tokens_per_step": ntok},
+                "cpu_baseline": {"value": value, "unit": "sublayer-tokens/s", "cores": blas_threads(),
+                                 "kind": "oracle", "sample": desc + " per step"},
+                "e2e": {"value": value, "unit": "sublayer-tokens/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
+    tensors = xin.make(wl, grads=True)
     sample = oracle_sample(wl, tensors, ntok)
     for _ in range(args.warmup):
         time_oracle(sample, wl)
@@ -208,6 +255,9 @@ def run_reference(args, wl):
 
 def wl_desc(wl):
     head = f"{wl.name}: B={wl.B} S={wl.S} N={wl.N} C={wl.C} k={wl.k} {wl.dtype}; "
+    if wl.layers > 1:
+        return head + (f"stack of {wl.layers} sublayers, forward in place (inference: x_in of every sublayer, no "
+                       f"saved rows), each update fused with the next sublayer's coefficient projection")
     if wl.router_fixed >= 0:
         return head + (f"router: {wl.router_fixed} fixed + {wl.k - wl.router_fixed} routed slots per token; forward "
                        f"(out of place, x_in, saved logits, router record) + backward (dX', no dx_in)")
@@ -288,6 +338,61 @@ class RoutedStep(Step):
         self.api.xhc_sublayer_bwd_routed(self.sh, self.X, self.out, self.conv, self.W, self.W_r, self.fixed,
                                          self.saved, self.tok_idx, self.rrec, self.dXp, None, self.dX, self.dout,
                                          self.dconv, self.dW, self.dW_r, self.ws)
+
+
+class StackStep:
+    """Device buffers of a stack of sublayers and the fused stack forward."""
+
+    def __init__(self, wl, layers, dev):
+        import torch
+        from residual_stream_expansion_xhc_b300 import api
+        self.api, self.wl, self.torch = api, wl, torch
+
+        def act(a):
+            return torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+
+        self.sh = api.make_shape(wl.B, wl.S, wl.N, wl.C, wl.k, torch.bfloat16, wl.iters, wl.eps, wl.gram_schmidt)
+        self.X = act(layers[0].X)
+        self.outs = [act(t.out) for t in layers]
+        self.convs = None if layers[0].conv is None else [tuple(torch.from_numpy(w).to(dev) for w in t.conv)
+                                                          for t in layers]
+        self.Ws = [torch.from_numpy(t.W).to(dev) for t in layers]
+        self.idxs = [[int(i) for i in t.idx] for t in layers]
+        self.x_ins = [torch.empty(wl.B, wl.S, wl.C, dtype=torch.bfloat16, device=dev) for _ in layers]
+        self.ws = api.workspace(api.xhc_stack_fwd_workspace_bytes(self.sh), dev)
+
+    def fwd(self):
+        self.api.xhc_stack_fwd(self.sh, self.X, self.outs, self.convs, self.Ws, self.idxs, self.ws, x_ins=self.x_ins)
+
+    def __call__(self):
+        self.fwd()
+
+
+def stack_e2e_run(step, layers, steps):
+    """Host buffers through the public API: every step copies the state and
+    every sublayer's `out` from pinned host memory, runs the stack and reads
+    the final state and every sublayer's x_in back (one stream, in order)."""
+    torch = step.torch
+    hX = torch.from_numpy(layers[0].X.view(np.int16)).pin_memory()
+    houts = [torch.from_numpy(t.out.view(np.int16)).pin_memory() for t in layers]
+    rX = torch.empty_like(hX).pin_memory()
+    rxin = [torch.empty(o.shape, dtype=torch.int16).pin_memory() for o in houts]
+
+    def one():
+        step.X.view(torch.int16).copy_(hX, non_blocking=True)
+        for d, h in zip(step.outs, houts):
+            d.view(torch.int16).copy_(h, non_blocking=True)
+        step()
+        rX.copy_(step.X.view(torch.int16), non_blocking=True)
+        for h, d in zip(rxin, step.x_ins):
+            h.copy_(d.view(torch.int16), non_blocking=True)
+
+    one()
+    ms = timed(one, steps)
+    h2d = hX.numel() * 2 + sum(h.numel() * 2 for h in houts)
+    d2h = rX.numel() * 2 + sum(h.numel() * 2 for h in rxin)
+    return {"value": step.wl.tokens * step.wl.layers * steps / (ms * 1e-3), "unit": "sublayer-tokens/s",
+            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": ms / steps}
 
 
 def timed(fn, steps):
@@ -405,6 +510,8 @@ def run_gpu(args, wl):
     torch.cuda.set_device(dev)
     from residual_stream_expansion_xhc_b300 import api
 
+    if wl.layers > 1:
+        return run_gpu_stack(args, wl, world, rank, local, dev)
     tensors = xin.make(wl, grads=True)
     step = RoutedStep(wl, tensors, dev) if wl.router_fixed >= 0 else Step(wl, tensors, dev)
     same_run_copy = copy_peak(dev)
@@ -470,6 +577,73 @@ def run_gpu(args, wl):
                 "alg_GBps": fwd_alg / (fwd_ms * 1e-3) / 1e9, "alg_bytes": fwd_alg},
         "bwd": {"tokens_per_s": wl.tokens / (bwd_ms * 1e-3), "ms": bwd_ms,
                 "alg_GBps": bwd_alg / (bwd_ms * 1e-3) / 1e9, "alg_bytes": bwd_alg},
+        "kernels": {k: {"launches": c, "avg_ms": t / c, "share": t / sum(v[1] for v in kern.values())}
+                    for k, (c, t) in kern.items()},
+        "gpu_launches": int(sum(c for c, _ in kern.values())),
+        "same_run_copy_GBps": same_run_copy,
+        "clocks": clocks,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_gpu_stack(args, wl, world, rank, local, dev):
+    """The fused stack forward: a step is the whole stack of wl.layers
+    sublayers over one batch; the metric counts tokens x sublayers."""
+    import torch
+    from residual_stream_expansion_xhc_b300 import api
+    layers = [xin.make(wl, l, state=(l == 0)) for l in range(wl.layers)]
+    step = StackStep(wl, layers, dev)
+    same_run_copy = copy_peak(dev)
+    cunit = wl.C * wl.esize
+    for _ in range(args.warmup):
+        step()
+    api.xhc_timing_collect()
+    torch.cuda.synchronize()
+    barrier(world)
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    api.xhc_timing_enable(True)
+    ms = timed(step, args.steps)
+    api.xhc_timing_enable(False)
+    torch.cuda.synchronize()
+    barrier(world)
+    clocks = sampler.stop() if sampler else None
+    kern = api.xhc_timing_collect()
+    ms = max_over_ranks(ms, world)
+    units = wl.tokens * wl.layers * world
+    value = units * args.steps / (ms * 1e-3)
+    peak, peak_kind = load_peaks()
+    dname, (dcount, dtotal) = max(kern.items(), key=lambda kv: kv[1][1])
+    per_launch_ms = dtotal / dcount
+    c_units = ALG_C_STACK.get(dname, ALG_C.get(dname, 0))
+    alg = (c_units * cunit + ALG_SIDE.get(dname, 0)) * wl.tokens
+    achieved = alg / (per_launch_ms * 1e-3) / 1e9
+    e2e = None
+    if not args.no_e2e:
+        e2e = stack_e2e_run(step, layers, max(1, args.e2e_steps // 2))
+        e2e["value"] *= world
+    cpu = cpu_baseline_stack(wl, layers, min(args.cpu_tokens, 512)) if rank == 0 and not args.no_cpu else None
+    if rank != 0:
+        return
+    # bytes per sublayer of the stack as the fused schedule moves them
+    stack_alg = ((wl.layers - 1) * 22 + 22 + 16) * cunit * wl.tokens
+    line = {
+        "metric": METRIC, "value": value, "unit": "sublayer-tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
+        "config": {"workload": wl_desc(wl), "tokens_per_step_per_gpu": wl.tokens, "sublayers": wl.layers,
+                   "l2": "inputs larger than L2 (state X is %.2f GB per GPU)" % (wl.tokens * wl.N * cunit / 1e9),
+                   "parallelism": f"replicas x{world} (independent batches, no collective)"},
+        "roofline": {"kernel": dname, "bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": load_traffic(dname, wl.tokens),
+                     "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_kind})",
+                     "alg_bytes_per_launch": alg, "launch_ms": per_launch_ms},
+        "stack": {"C_units_per_sublayer": stack_alg / (cunit * wl.tokens * wl.layers),
+                  "alg_GBps": stack_alg / (ms / args.steps * 1e-3) / 1e9, "alg_bytes": stack_alg},
         "kernels": {k: {"launches": c, "avg_ms": t / c, "share": t / sum(v[1] for v in kern.values())}
                     for k, (c, t) in kern.items()},
         "gpu_launches": int(sum(c for c, _ in kern.values())),

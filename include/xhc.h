@@ -260,6 +260,42 @@ int xhc_sublayer_fwd_routed(const xhc_shape_t* sh, const void* X_in,
                             xhc_stream_t stream);
 
 /*
+ * xhc_stack_fwd -- forward of a stack of L sublayers on one state, in place,
+ * with each sublayer's update fused with the next sublayer's coefficient
+ * projection (section "Beyond N=16": xHC-Flash reorders the reads and writes
+ * of consecutive sublayers to lower the traffic per sublayer).  Sublayer l
+ * reads the state that sublayer l - 1 wrote and applies the update of
+ * xhc_sublayer_fwd with its own out[l], conv weights, W[l] and index list.
+ * One pass over the state per sublayer: it forms sublayer l's dense read and
+ * sparse write and, from the updated tile still on chip, sublayer l+1's
+ * coefficients.  A first pass computes sublayer 0's coefficients.
+ *   X        [B,S,N,C] bf16 device, read and written (the final state).
+ *   out      host array of L device pointers, out[l] [B,S,C] bf16.
+ *   w4, w8, w12  NULL, or host arrays of L device pointers ([C,4], [C,8],
+ *            [C,12] fp32); per sublayer all three or none (no TFA).
+ *   W        host array of L device pointers, W[l] [P, N*C] fp32.
+ *   idx      host int32 [L*k]: sublayer l's slots at idx + l*k.
+ *   x_in     NULL, or host array of L device pointers (entries may be NULL):
+ *            sublayer l's dense read [B,S,C] bf16, written.
+ *   saved    NULL, or host array of L device pointers (entries may be NULL):
+ *            sublayer l's logits and rstd [B,S,P+1] fp32, written.
+ *   workspace, ws_bytes  at least xhc_stack_fwd_workspace_bytes() bytes.
+ * bf16 only (XHC_ERR_DTYPE), C a multiple of 64 and P <= 48
+ * (XHC_ERR_SHAPE); L >= 1 (XHC_ERR_ARG).  With sh->gram_schmidt each
+ * sublayer's components are orthogonalised as in xhc_sublayer_fwd.  The
+ * state between sublayers is the bf16 state in memory.  Inference form: the
+ * old active rows are not saved (training uses xhc_sublayer_fwd per
+ * sublayer).  On error nothing is launched.
+ */
+size_t xhc_stack_fwd_workspace_bytes(const xhc_shape_t* sh);
+int xhc_stack_fwd(const xhc_shape_t* sh, int L, void* X,
+                  const void* const* out, const float* const* w4,
+                  const float* const* w8, const float* const* w12,
+                  const float* const* W, const int32_t* idx,
+                  void* const* x_in, float* const* saved, void* workspace,
+                  size_t ws_bytes, xhc_stream_t stream);
+
+/*
  * xhc_sublayer_bwd_routed -- exact reverse mode of xhc_sublayer_fwd_routed
  * (the active sets are the forward's, a constant; unchosen scores get no
  * gradient).

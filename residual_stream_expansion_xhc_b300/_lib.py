@@ -20,7 +20,7 @@ EXPORTS = ("xhc_status_string", "xhc_last_cuda_error", "xhc_device_status", "xhc
            "xhc_sparse_update", "xhc_fwd_workspace_bytes", "xhc_fwd_workspace_need", "xhc_sublayer_fwd", "xhc_sublayer_fwd_noalloc", "xhc_bwd_workspace_bytes",
            "xhc_sublayer_bwd", "xhc_fwd_routed_workspace_bytes", "xhc_sublayer_fwd_routed",
            "xhc_bwd_routed_workspace_bytes", "xhc_sublayer_bwd_routed", "xhc_hres_active_weights", "xhc_hres_active_grad", "xhc_copy", "xhc_timing_enable",
-           "xhc_timing_collect")
+           "xhc_timing_collect", "xhc_stack_fwd_workspace_bytes", "xhc_stack_fwd")
 
 
 class XhcShape(ctypes.Structure):
@@ -85,6 +85,10 @@ def _load() -> ctypes.CDLL:
     lib.xhc_hres_active_weights.argtypes = [sh, P, P, P, P, P]
     lib.xhc_hres_active_grad.restype = I
     lib.xhc_hres_active_grad.argtypes = [sh, P, P, P, P]
+    lib.xhc_stack_fwd_workspace_bytes.restype = Z
+    lib.xhc_stack_fwd_workspace_bytes.argtypes = [sh]
+    lib.xhc_stack_fwd.restype = I
+    lib.xhc_stack_fwd.argtypes = [sh, I, P, P, P, P, P, P, P, P, P, P, Z, P]
     lib.xhc_copy.restype = I
     lib.xhc_copy.argtypes = [P, P, Z, P]
     lib.xhc_timing_enable.restype = I

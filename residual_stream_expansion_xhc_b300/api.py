@@ -124,6 +124,35 @@ def xhc_sublayer_bwd(sh, X_state, saved_active, out, conv, W, idx, saved, dXp, d
                                                     ws_bytes, _s(stream)))
 
 
+def xhc_stack_fwd_workspace_bytes(sh) -> int:
+    return LIB.xhc_stack_fwd_workspace_bytes(ctypes.byref(sh))
+
+
+def _ptr_array(ts):
+    """Host array of device pointers (None entries -> NULL), or NULL for None."""
+    if ts is None:
+        return None
+    return (ctypes.c_void_p * len(ts))(*[None if t is None else t.data_ptr() for t in ts])
+
+
+def xhc_stack_fwd(sh, X, outs, convs, Ws, idxs, workspace, x_ins=None, saveds=None, stream=None):
+    """Forward of a stack of L = len(outs) sublayers on X in place, each
+    sublayer's update fused with the next one's coefficient projection (see
+    the C header).  ``convs``: None, or a list of L (w4, w8, w12) tuples or
+    Nones (all sublayers with conv weights, or none); ``idxs``: L index
+    lists; ``x_ins`` / ``saveds``: None or lists of L tensors (or Nones)."""
+    L = len(outs)
+    flat = [int(a) for ix in idxs for a in ix]
+    if convs is None or all(c is None for c in convs):
+        w4 = w8 = w12 = None
+    else:
+        w4, w8, w12 = (_ptr_array([None if c is None else c[j] for c in convs]) for j in range(3))
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check("xhc_stack_fwd", LIB.xhc_stack_fwd(ctypes.byref(sh), L, _p(X), _ptr_array(outs), w4, w8, w12,
+                                              _ptr_array(Ws), _idx(flat), _ptr_array(x_ins), _ptr_array(saveds),
+                                              _p(workspace), ws_bytes, _s(stream)))
+
+
 def xhc_fwd_routed_workspace_bytes(sh) -> int:
     return LIB.xhc_fwd_routed_workspace_bytes(ctypes.byref(sh))
 

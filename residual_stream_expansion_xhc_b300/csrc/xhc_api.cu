@@ -479,6 +479,98 @@ BwdLayout bwd_layout(const xhc_shape_t* sh) {
 }
 }  // namespace
 
+// ---------------------------------------------------------------- fused stack forward
+
+namespace {
+// Stack workspace: two coefficient blocks (sublayer l read, l+1 written), the
+// bf16 split of the next W, the tap-major conv weights, Gram partials.
+size_t stack_taps_bytes(const xhc_shape_t* sh) {
+  return round_up((size_t)NTAPS * (size_t)sh->C * sizeof(float));
+}
+size_t stack_wsplit_bytes(const xhc_shape_t* sh) {
+  return round_up(coeffs_wsplit_bytes(make_params(sh, nullptr)));
+}
+}  // namespace
+
+size_t xhc_stack_fwd_workspace_bytes(const xhc_shape_t* sh) {
+  if (check_shape(sh)) return 0;
+  return 2 * fwd_coef_bytes(sh) + stack_wsplit_bytes(sh) + stack_taps_bytes(sh) + gs_gpart_bytes(sh);
+}
+
+int xhc_stack_fwd(const xhc_shape_t* sh, int L, void* X, const void* const* out, const float* const* w4,
+                  const float* const* w8, const float* const* w12, const float* const* W, const int32_t* idx,
+                  void* const* x_in, float* const* saved, void* workspace, size_t ws_bytes, xhc_stream_t stream) {
+  int s = check_shape(sh);
+  if (s) return s;
+  if (L < 1 || !out || !W || !idx) return XHC_ERR_ARG;
+  if (sh->dtype != XHC_BF16) return XHC_ERR_DTYPE;
+  const Params p0 = make_params(sh, nullptr);
+  if (!flash_supported(p0) || !tc_coeffs_supported(p0) || !stream_update_supported(p0)) return XHC_ERR_SHAPE;
+  const int nconv = (w4 != nullptr) + (w8 != nullptr) + (w12 != nullptr);
+  if (nconv != 0 && nconv != 3) return XHC_ERR_ARG;
+  std::vector<bool> conv(L, false);
+  for (int l = 0; l < L; ++l) {
+    if ((s = check_idx(sh, idx + (size_t)l * sh->k))) return s;
+    bool has = false;
+    if (nconv && (s = check_conv(w4[l], w8[l], w12[l], &has))) return s;
+    conv[l] = has;
+    if ((s = check_ptrs({out[l], W[l]}, {nconv ? w4[l] : nullptr, nconv ? w8[l] : nullptr,
+                                         nconv ? w12[l] : nullptr, x_in ? x_in[l] : nullptr,
+                                         saved ? saved[l] : nullptr})))
+      return s;
+  }
+  if ((s = check_ptrs({X}, {workspace}))) return s;
+  if (tokens(sh) == 0) return XHC_OK;
+  const size_t need = xhc_stack_fwd_workspace_bytes(sh);
+  if (!workspace || ws_bytes < need) return XHC_ERR_WORKSPACE;
+  char* ws = (char*)workspace;
+  float* coef[2] = {(float*)ws, (float*)(ws + fwd_coef_bytes(sh))};
+  void* wsplit = ws + 2 * fwd_coef_bytes(sh);
+  float* taps = (float*)(ws + 2 * fwd_coef_bytes(sh) + stack_wsplit_bytes(sh));
+  float* gpart = (float*)(ws + 2 * fwd_coef_bytes(sh) + stack_wsplit_bytes(sh) + stack_taps_bytes(sh));
+  cudaStream_t st = (cudaStream_t)stream;
+  using T = __nv_bfloat16;
+  auto weights = [&](int l, const float* (&w)[3]) {
+    w[0] = conv[l] ? w4[l] : nullptr;
+    w[1] = conv[l] ? w8[l] : nullptr;
+    w[2] = conv[l] ? w12[l] : nullptr;
+  };
+  // Gram-Schmidt of sublayer l's components folded into its coefficient block
+  auto fold = [&](const Params& p, int l, float* cf) -> int {
+    if (!sh->gram_schmidt || !conv[l]) return XHC_OK;
+    const float* w[3];
+    weights(l, w);
+    const float* const wc[3] = {w[0], w[1], w[2]};
+    int r = cuda_status(launch_gs_gram(p, (const T*)out[l], wc, gpart, st));
+    return r ? r : cuda_status(launch_gs_fold(p, gpart, cf, nullptr, st));
+  };
+  Params p = make_params(sh, idx);
+  if ((s = cuda_status(launch_coeffs_tc(p, X, W[0], wsplit, nullptr, nullptr, nullptr, saved ? saved[0] : nullptr,
+                                        coef[0], st))))
+    return s;
+  if ((s = fold(p, 0, coef[0]))) return s;
+  for (int l = 0; l < L; ++l) {
+    p = make_params(sh, idx + (size_t)l * sh->k);
+    const float* w[3];
+    weights(l, w);
+    float* cur = coef[l & 1];
+    float* nxt = coef[(l + 1) & 1];
+    if (l + 1 < L) {
+      if ((s = cuda_status(launch_w_split(p, W[l + 1], wsplit, st)))) return s;
+      const float* const wc[3] = {w[0], w[1], w[2]};
+      if ((s = cuda_status(launch_flash_step(p, X, out[l], wc, taps, cur, wsplit, x_in ? x_in[l] : nullptr, nxt,
+                                             saved ? saved[l + 1] : nullptr, st))))
+        return s;
+      if ((s = fold(make_params(sh, idx + (size_t)(l + 1) * sh->k), l + 1, nxt))) return s;
+    } else {
+      UpdArgs<T> a{(const T*)X, (T*)X, (const T*)out[l], {w[0], w[1], w[2]}, nullptr, nullptr, nullptr, nullptr,
+                   x_in ? (T*)x_in[l] : nullptr, nullptr, 0};
+      if ((s = cuda_status(launch_fwd_update(p, a, cur, conv[l], num_sms(), st)))) return s;
+    }
+  }
+  return XHC_OK;
+}
+
 size_t xhc_bwd_workspace_bytes(const xhc_shape_t* sh) {
   if (check_shape(sh)) return 0;
   return bwd_layout(sh).total;

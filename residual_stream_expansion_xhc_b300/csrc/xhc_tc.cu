@@ -137,6 +137,65 @@ struct CoeffsOut {
   const uint8_t* wsplit;   // stage images of the bf16 hi/lo split of W, or nullptr
 };
 
+// Coefficients of token t from its unscaled logits pz (vec X . W^T) and the
+// sum of squares of its state: rstd, logits, sigmoid, Sinkhorn, stores.
+__device__ __forceinline__ void coeffs_epilogue(const Params& p, const float (&pz)[coeffs::W_ROWS], float ss,
+                                                size_t t, const CoeffsOut& o) {
+  const int N = p.N, k = p.k, P = p.P;
+  const float rstd = 1.0f / sqrtf(ss / (float)(N * p.C) + p.eps);
+  if (o.saved) {
+    float* sv = o.saved + t * (P + 1);
+#pragma unroll
+    for (int q = 0; q < coeffs::W_ROWS; ++q)
+      if (q < P) sv[q] = rstd * pz[q];
+    sv[P] = rstd;
+  }
+  float zl[PMAX];
+#pragma unroll
+  for (int q = 0; q < coeffs::W_ROWS; ++q) zl[q] = rstd * pz[q];
+  if (o.hpre) {
+#pragma unroll
+    for (int q = 0; q < NMAX; ++q)
+      if (q < N) o.hpre[t * N + q] = sigmoidf_(zl[q]);
+  }
+  if (o.hpost) {
+#pragma unroll
+    for (int q = 0; q < 4 * KMAX; ++q)
+      if (q < 4 * k) o.hpost[t * 4 * k + q] = sigmoidf_(zl[N + q]);
+  }
+  if (o.hres || o.coef) {
+    // Sinkhorn of this token's k x k logits in registers (one thread)
+    float M[KMAX][KMAX];
+    sinkhorn_thread(zl + N + 4 * k, k, p.iters, M);
+    if (o.hres) {
+#pragma unroll
+      for (int i = 0; i < KMAX; ++i)
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j)
+          if (i < k && j < k) o.hres[t * k * k + k * i + j] = M[i][j];
+    }
+    if (o.coef) {
+      float4* cf = reinterpret_cast<float4*>(o.coef + t * COEF_STRIDE);
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        float h[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) h[e] = (4 * v + e < N) ? sigmoidf_(zl[4 * v + e]) : 0.0f;
+        cf[v] = make_float4(h[0], h[1], h[2], h[3]);
+      }
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        float h[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) h[e] = (4 * v + e < 4 * k) ? sigmoidf_(zl[N + 4 * v + e]) : 0.0f;
+        cf[4 + v] = make_float4(h[0], h[1], h[2], h[3]);
+      }
+#pragma unroll
+      for (int i = 0; i < KMAX; ++i) cf[8 + i] = make_float4(M[i][0], M[i][1], M[i][2], M[i][3]);
+    }
+  }
+}
+
 template <bool PRESPLIT>
 __global__ void __launch_bounds__(coeffs::THREADS, 1)
     coeffs_tc_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__ CUtensorMap mapW,
@@ -330,60 +389,384 @@ __global__ void __launch_bounds__(coeffs::THREADS, 1)
 
       const size_t t = (size_t)tile * rows + row;
       if (row >= rows || t >= (size_t)p.B * p.S) continue;
-      const int N = p.N, k = p.k, P = p.P;
-      const float rstd = 1.0f / sqrtf(ss / (float)(N * p.C) + p.eps);
-      if (o.saved) {
-        float* sv = o.saved + t * (P + 1);
-#pragma unroll
-        for (int q = 0; q < W_ROWS; ++q)
-          if (q < P) sv[q] = rstd * pz[q];
-        sv[P] = rstd;
-      }
-      float zl[PMAX];
-#pragma unroll
-      for (int q = 0; q < W_ROWS; ++q) zl[q] = rstd * pz[q];
-      if (o.hpre) {
-#pragma unroll
-        for (int q = 0; q < NMAX; ++q)
-          if (q < N) o.hpre[t * N + q] = sigmoidf_(zl[q]);
-      }
-      if (o.hpost) {
-#pragma unroll
-        for (int q = 0; q < 4 * KMAX; ++q)
-          if (q < 4 * k) o.hpost[t * 4 * k + q] = sigmoidf_(zl[N + q]);
-      }
-      if (o.hres || o.coef) {
-        // Sinkhorn of this token's k x k logits in registers (one thread)
-        float M[KMAX][KMAX];
-        sinkhorn_thread(zl + N + 4 * k, k, p.iters, M);
-        if (o.hres) {
-#pragma unroll
-          for (int i = 0; i < KMAX; ++i)
-#pragma unroll
-            for (int j = 0; j < KMAX; ++j)
-              if (i < k && j < k) o.hres[t * k * k + k * i + j] = M[i][j];
-        }
-        if (o.coef) {
-          float4* cf = reinterpret_cast<float4*>(o.coef + t * COEF_STRIDE);
-#pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            float h[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) h[e] = (4 * v + e < N) ? sigmoidf_(zl[4 * v + e]) : 0.0f;
-            cf[v] = make_float4(h[0], h[1], h[2], h[3]);
+      coeffs_epilogue(p, pz, ss, t, o);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tmem, TMEM_COLS);
+}
+
+// ---------------------------------------------------------------- fused stack step
+//
+// One pass over the state per sublayer of a stack (section "Beyond N=16":
+// xHC-Flash lowers a sublayer's traffic by reordering reads and writes across
+// sublayers).  For sublayer l the pass
+//   - reads every stream of S_l once (TMA tiles [128 tokens x 64 channels]),
+//   - forms the dense read x_in_l = sum_n hpre_l[n] S_l[n] (section "Dense
+//     read, sparse write"),
+//   - rewrites the k active rows of each tile in shared memory with the
+//     update of sublayer l (H^res mix + H^post of the TFA components) and
+//     stores them back in place (TMA stores),
+//   - and projects the tile, as it now holds S_{l+1}, onto W_{l+1} on the
+//     tensor cores (bf16 hi + lo parts of W, fp32 TMEM accumulators), with the
+//     sum of squares taken on the same values,
+// so that the epilogue writes sublayer l+1's coefficient block: the separate
+// coefficient pass over S_{l+1} (16 C of reads per token) disappears, and a
+// sublayer of the stack costs the update pass's 22 C.
+//
+// Stage order within a 64-channel chunk: the k active streams of sublayer l
+// first (slot order), then the others.  Warp roles as in the coefficient
+// pass: warp 0 TMA producer (state tiles, W_{l+1} image, the chunk's `out`
+// tile with 16 rows of history and its tap-major conv weights), warp 1 MMA
+// issuer, warps 2..9 math (two threads per token row, 32 channels each):
+// dense read, update, sum of squares, then the epilogue.
+namespace flash {
+constexpr int TILE_T = 128;
+constexpr int KC = 64;
+constexpr int X_BYTES = TILE_T * KC * 2;                 // 16 KB
+constexpr int W_BYTES = coeffs::W_BYTES;                 // 6 KB per bf16 part
+constexpr int STAGE_BYTES = X_BYTES + 2 * W_BYTES;       // 28 KB
+constexpr int STAGES = 7;
+constexpr int HALO_R = 16;               // out rows above the tile (11 used; 16 keeps the swizzle phase of row r)
+constexpr int OUT_BYTES = (TILE_T + HALO_R) * 128;       // 18 KB
+constexpr int TAP_BYTES = NTAPS * KC * 4;                // [24 taps][64 channels] fp32
+constexpr int OFF_OUT = STAGES * STAGE_BYTES;
+constexpr int OFF_TAP = OFF_OUT + OUT_BYTES;
+constexpr int SMEM = OFF_TAP + TAP_BYTES + 1024;
+constexpr int MATH_WARPS = 8;
+constexpr int THREADS = 64 + 32 * MATH_WARPS;
+constexpr int TMEM_COLS = 128;
+}  // namespace flash
+
+struct FlashArgs {
+  const float* coef;       // [T, COEF_STRIDE] coefficients of sublayer l
+  const float* taps;       // tap-major conv weights of sublayer l ([C/64][24][64]) or nullptr
+  const uint8_t* wsplit;   // stage images of the hi/lo split of W_{l+1}
+  __nv_bfloat16* x_in;     // [T, C] or nullptr
+  CoeffsOut next;          // sublayer l+1: coef block and saved logits
+};
+
+template <bool HAS_CONV>
+__global__ void __launch_bounds__(flash::THREADS, 1)
+    flash_tc_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__ CUtensorMap mapOut, Params p,
+                    FlashArgs f, int ntiles, int rows) {
+  using namespace flash;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  __shared__ uint64_t full[STAGES], bready[STAGES], empty[STAGES], ofull, oempty, updated, tfull[2], tempty[2],
+      ssfull[2], ssempty[2];
+  __shared__ uint32_t tmem_slot;
+  __shared__ int ord[NMAX];
+  __shared__ float ss_half[2][TILE_T];
+  int* err = &g_device_error;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int N = p.N, k = p.k, C = p.C;
+  const int cchunks = C / KC;
+  const size_t T_all = (size_t)p.B * p.S;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&bready[s], MATH_WARPS);       // stage seen (inactive) or rewritten (active) by every math warp
+      mbar_init(&empty[s], 1 + MATH_WARPS);    // MMA commit + the math warps
+    }
+    mbar_init(&ofull, 1);
+    mbar_init(&oempty, MATH_WARPS);
+    mbar_init(&updated, MATH_WARPS);           // the chunk's active rows rewritten by every math warp
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 4);
+      mbar_init(&ssfull[b], 4);
+      mbar_init(&ssempty[b], 4);
+    }
+    for (int i = 0; i < k; ++i) ord[i] = p.idx[i];
+    for (int j = 0; j < N - k; ++j) ord[k + j] = p.inactive[j];
+    fence_mbar_init();
+    tma_prefetch_desc(&mapX);
+    tma_prefetch_desc(&mapOut);
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_slot, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const uint64_t pol_x = policy_evict_first(), pol_w = policy_evict_last();
+      int it = 0, oc = 0;
+      for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+        for (int cc = 0; cc < cchunks; ++cc, ++oc) {
+          if (oc > 0 && !mbar_wait(&oempty, (oc - 1) & 1, err, 21)) goto done_prod;
+          mbar_expect_tx(&ofull, (rows + HALO_R) * 128 + (HAS_CONV ? TAP_BYTES : 0));
+          tma_load_2d(smem + OFF_OUT, &mapOut, &ofull, cc * KC, tile * rows - HALO_R, pol_x);
+          if (HAS_CONV) bulk_load(smem + OFF_TAP, f.taps + (size_t)cc * NTAPS * KC, TAP_BYTES, &ofull, pol_w);
+          for (int j = 0; j < N; ++j, ++it) {
+            const int s = it % STAGES;
+            if (it >= STAGES && !mbar_wait(&empty[s], ((it / STAGES) & 1) ^ 1, err, 22)) goto done_prod;
+            uint8_t* st = smem + s * STAGE_BYTES;
+            const int n = ord[j];
+            mbar_expect_tx(&full[s], rows * KC * 2 + 2 * W_BYTES);
+            tma_load_3d(st, &mapX, &full[s], cc * KC, n, tile * rows, pol_x);
+            bulk_load(st + X_BYTES, f.wsplit + (size_t)(n * cchunks + cc) * 2 * W_BYTES, 2 * W_BYTES, &full[s],
+                      pol_w);
           }
-#pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            float h[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) h[e] = (4 * v + e < 4 * k) ? sigmoidf_(zl[N + 4 * v + e]) : 0.0f;
-            cf[4 + v] = make_float4(h[0], h[1], h[2], h[3]);
-          }
-#pragma unroll
-          for (int i = 0; i < KMAX; ++i) cf[8 + i] = make_float4(M[i][0], M[i][1], M[i][2], M[i][3]);
         }
+      }
+    done_prod:;
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16(TILE_T, coeffs::W_ROWS, 0, 0);
+      int it = 0, tl = 0;
+      for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++tl) {
+        const int buf = tl & 1;
+        if (tl >= 2 && !mbar_wait(&tempty[buf], ((tl >> 1) & 1) ^ 1, err, 23)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + buf * 64;
+        bool ok = true;
+        for (int kc = 0; kc < cchunks * N; ++kc, ++it) {
+          const int s = it % STAGES;
+          if (!mbar_wait(&bready[s], (it / STAGES) & 1, err, 24)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t xs = smem_u32(smem + s * STAGE_BYTES);
+#pragma unroll
+          for (int ks = 0; ks < KC / 16; ++ks) {
+            const uint64_t a = sdesc_sw128(xs + ks * 32, 16, 1024);
+            const uint64_t bh = sdesc_sw128(xs + X_BYTES + ks * 32, 16, 1024);
+            const uint64_t bl = sdesc_sw128(xs + X_BYTES + W_BYTES + ks * 32, 16, 1024);
+            umma_bf16(d, a, bh, idesc, (kc | ks) != 0);
+            umma_bf16(d, a, bl, idesc, 1);
+          }
+          umma_commit(&empty[s]);
+        }
+        if (!ok) break;
+        umma_commit(&tfull[buf]);
       }
     }
+  } else {
+    // ------------------------------------------------ math: dense read, update, sum of squares, epilogue
+    const int row = 32 * (warp & 3) + lane;             // token row == TMEM lane
+    const int half = (warp - 2) >> 2;                   // channels 32 half .. 32 half + 31 of each chunk
+    const int mt = threadIdx.x - 64;
+    const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
+    int it = 0, tl = 0, oc = 0;
+    for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++tl) {
+      const size_t t = (size_t)tile * rows + row;
+      const bool live = row < rows && t < T_all;
+      const float* cf = f.coef + (live ? t : 0) * COEF_STRIDE;
+      float hpost[KMAX][4], hres[KMAX][KMAX], hact[KMAX];
+#pragma unroll
+      for (int i = 0; i < KMAX; ++i) {
+        const float4 a = *reinterpret_cast<const float4*>(cf + COEF_POST + 4 * i);
+        const float4 b = *reinterpret_cast<const float4*>(cf + COEF_RES + 4 * i);
+        hpost[i][0] = a.x; hpost[i][1] = a.y; hpost[i][2] = a.z; hpost[i][3] = a.w;
+        hres[i][0] = b.x; hres[i][1] = b.y; hres[i][2] = b.z; hres[i][3] = b.w;
+        hact[i] = i < k ? cf[ord[i]] : 0.0f;
+      }
+      const int spos = live ? (int)(t % (size_t)p.S) : 0;
+      float ss = 0.0f;
+      bool ok = true;
+      for (int cc = 0; cc < cchunks; ++cc, ++oc) {
+        float xacc[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) xacc[e] = 0.0f;
+        if (!mbar_wait(&ofull, oc & 1, err, 25)) { ok = false; break; }
+        // ---- the k active rows of this chunk: read, update, write back
+#pragma unroll
+        for (int i = 0; i < KMAX; ++i)
+          if (i < k && !mbar_wait(&full[(it + i) % STAGES], ((it + i) / STAGES) & 1, err, 26)) ok = false;
+        if (!ok) break;
+        const uint8_t* os = smem + OFF_OUT;
+        const float* tp = reinterpret_cast<const float*>(smem + OFF_TAP);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int gl = half * 4 + q;                    // 16-byte group of the row (8 channels)
+          const uint32_t off = row * 128 + ((gl ^ (row & 7)) << 4);
+          float o[KMAX][8];
+#pragma unroll
+          for (int i = 0; i < KMAX; ++i) {
+            uint4 v = make_uint4(0, 0, 0, 0);
+            if (i < k) v = *reinterpret_cast<const uint4*>(smem + ((it + i) % STAGES) * STAGE_BYTES + off);
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              o[i][2 * e] = bf_lo(w[e]);
+              o[i][2 * e + 1] = bf_hi(w[e]);
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) xacc[8 * q + e] = fmaf(hact[i], o[i][e], xacc[8 * q + e]);
+          }
+          // TFA components of this token's 8 channels; row r of the tile is
+          // row r + HALO_R of the out tile, tap tau reads row r + HALO_R - tau
+          float u[4][8];
+          {
+            const uint4 v = *reinterpret_cast<const uint4*>(os + (row + HALO_R) * 128 + ((gl ^ (row & 7)) << 4));
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              u[0][2 * e] = bf_lo(w[e]);
+              u[0][2 * e + 1] = bf_hi(w[e]);
+            }
+          }
+#pragma unroll
+          for (int c = 1; c < 4; ++c)
+#pragma unroll
+            for (int e = 0; e < 8; ++e) u[c][e] = 0.0f;
+          if (HAS_CONV) {
+#pragma unroll
+            for (int tau = 0; tau < 12; ++tau) {
+              const int r = row + HALO_R - tau;
+              uint4 v = *reinterpret_cast<const uint4*>(os + r * 128 + ((gl ^ (r & 7)) << 4));
+              if (tau > spos) v = make_uint4(0, 0, 0, 0);   // before the start of the sequence
+              const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+              float x[8];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                x[2 * e] = bf_lo(w[e]);
+                x[2 * e + 1] = bf_hi(w[e]);
+              }
+              // tap rows: w4 taps at rows 0..3, w8 at 4..11, w12 at 12..23
+#pragma unroll
+              for (int c = 1; c < 4; ++c) {
+                const int K = 4 * c, r0 = (c == 1) ? 0 : (c == 2 ? 4 : 12);
+                if (tau < K) {
+                  const float4 a = *reinterpret_cast<const float4*>(tp + (r0 + tau) * KC + gl * 8);
+                  const float4 b = *reinterpret_cast<const float4*>(tp + (r0 + tau) * KC + gl * 8 + 4);
+                  const float wv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+                  for (int e = 0; e < 8; ++e) u[c][e] = fmaf(wv[e], x[e], u[c][e]);
+                }
+              }
+            }
+          }
+          // the new active rows: X'[a_i] = sum_j Hres[i][j] X[a_j] + sum_c Hpost[i][c] u_c
+#pragma unroll
+          for (int i = 0; i < KMAX; ++i) {
+            if (i < k) {
+              float y[8];
+#pragma unroll
+              for (int e = 0; e < 8; ++e) {
+                float acc = 0.0f;
+#pragma unroll
+                for (int j = 0; j < KMAX; ++j) acc = fmaf(hres[i][j], o[j][e], acc);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) acc = fmaf(hpost[i][c], u[c][e], acc);
+                y[e] = acc;
+              }
+              uint4 v;
+              v.x = pack_bf2(y[0], y[1]);
+              v.y = pack_bf2(y[2], y[3]);
+              v.z = pack_bf2(y[4], y[5]);
+              v.w = pack_bf2(y[6], y[7]);
+              const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float a = bf_lo(w[e]), b = bf_hi(w[e]);
+                ss = fmaf(a, a, ss);
+                ss = fmaf(b, b, ss);
+              }
+              if (live) *reinterpret_cast<uint4*>(smem + ((it + i) % STAGES) * STAGE_BYTES + off) = v;
+            }
+          }
+        }
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          for (int i = 0; i < k; ++i) mbar_arrive(&bready[(it + i) % STAGES]);
+          mbar_arrive(&oempty);
+          mbar_arrive(&updated);
+        }
+        // once every math warp has written its rows, one thread stores the new
+        // rows in place; its warp releases the stages after the store has read them
+        if (mt == 0) {
+          if (mbar_wait(&updated, oc & 1, err, 31)) {
+            for (int i = 0; i < k; ++i)
+              tma_store_3d(&mapX, smem + ((it + i) % STAGES) * STAGE_BYTES, cc * KC, ord[i], tile * rows);
+            tma_store_commit();
+            tma_store_wait_read0();
+          } else {
+            ok = false;
+          }
+        }
+        ok = __shfl_sync(FULL, ok, 0);
+        if (!ok) break;
+        if (lane == 0)
+          for (int i = 0; i < k; ++i) mbar_arrive(&empty[(it + i) % STAGES]);
+        it += k;
+        // ---- the other streams: dense read and sum of squares
+        for (int j = k; j < N; ++j, ++it) {
+          const int s = it % STAGES;
+          if (!mbar_wait(&full[s], (it / STAGES) & 1, err, 27)) { ok = false; break; }
+          if (lane == 0) mbar_arrive(&bready[s]);
+          const float h = cf[ord[j]];
+          const uint8_t* xs = smem + s * STAGE_BYTES + row * 128;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int gl = half * 4 + q;
+            const uint4 v = *reinterpret_cast<const uint4*>(xs + ((gl ^ (row & 7)) << 4));
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float a = bf_lo(w[e]), b = bf_hi(w[e]);
+              ss = fmaf(a, a, ss);
+              ss = fmaf(b, b, ss);
+              xacc[8 * q + 2 * e] = fmaf(h, a, xacc[8 * q + 2 * e]);
+              xacc[8 * q + 2 * e + 1] = fmaf(h, b, xacc[8 * q + 2 * e + 1]);
+            }
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&empty[s]);
+        }
+        if (!ok) break;
+        if (f.x_in && live) {
+          uint4* dst = reinterpret_cast<uint4*>(f.x_in + t * C + cc * KC + half * 32);
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            dst[q] = make_uint4(pack_bf2(xacc[8 * q], xacc[8 * q + 1]), pack_bf2(xacc[8 * q + 2], xacc[8 * q + 3]),
+                                pack_bf2(xacc[8 * q + 4], xacc[8 * q + 5]),
+                                pack_bf2(xacc[8 * q + 6], xacc[8 * q + 7]));
+        }
+      }
+      if (!ok) break;
+      // ---- epilogue: sublayer l+1's coefficients from the projection of S_{l+1}
+      const int sb = tl & 1;
+      if (half == 1) {
+        if (tl >= 2 && !mbar_wait(&ssempty[sb], ((tl >> 1) & 1) ^ 1, err, 28)) break;
+        ss_half[sb][row] = ss;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ssfull[sb]);
+        continue;
+      }
+      if (!mbar_wait(&ssfull[sb], (tl >> 1) & 1, err, 29)) break;
+      ss += ss_half[sb][row];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ssempty[sb]);
+      const int buf = tl & 1;
+      if (!mbar_wait(&tfull[buf], (tl >> 1) & 1, err, 30)) break;
+      tc_fence_after();
+      float pz[coeffs::W_ROWS];
+#pragma unroll
+      for (int c = 0; c < coeffs::W_ROWS; c += 16) {
+        uint32_t r[16];
+        tmem_ld16(tmem + lane_base + buf * 64 + c, r);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) pz[c + j] = __uint_as_float(r[j]);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[buf]);
+      if (live) coeffs_epilogue(p, pz, ss, t, f.next);
+    }
+    if (mt == 0) tma_store_wait0();
   }
   tc_fence_before();
   __syncthreads();
@@ -474,6 +857,77 @@ cudaError_t launch_coeffs_tc(const Params& p, const void* X, const float* W, voi
     cudaFuncSetAttribute(coeffs_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<false>());
     timing_begin("coeffs_tc", st);
     coeffs_tc_kernel<false><<<grid, THREADS, smem_bytes<false>(), st>>>(mx, mw, mwl, p, o, ntiles, rows);
+  }
+  timing_end(st);
+  return cudaGetLastError();
+}
+
+// Conv weights w4 [C, 4], w8 [C, 8], w12 [C, 12] -> tap-major per 64-channel
+// chunk: taps[cc][r][c'] with rows r = 0..3 the taps of w4, 4..11 those of
+// w8, 12..23 those of w12, for channel cc * 64 + c'.
+__global__ void taps_major_kernel(const float* __restrict__ w4, const float* __restrict__ w8,
+                                  const float* __restrict__ w12, float* __restrict__ taps, int C) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= C * NTAPS) return;
+  const int c = i % C, r = i / C;
+  const float v = r < 4 ? w4[c * 4 + r] : (r < 12 ? w8[c * 8 + (r - 4)] : w12[c * 12 + (r - 12)]);
+  taps[((size_t)(c / flash::KC) * NTAPS + r) * flash::KC + (c % flash::KC)] = v;
+}
+
+bool flash_supported(const Params& p) { return p.C % flash::KC == 0 && p.P <= coeffs::W_ROWS && p.k <= KMAX; }
+size_t flash_taps_bytes(const Params& p) { return (size_t)NTAPS * p.C * sizeof(float); }
+
+cudaError_t launch_w_split(const Params& p, const float* W, void* Wsplit, cudaStream_t st) {
+  const size_t NC = (size_t)p.N * p.C;
+  const size_t threads = (size_t)coeffs::W_ROWS * (NC / 8);
+  timing_begin("w_split", st);
+  w_split_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, st>>>(W, (uint8_t*)Wsplit, p.P, NC);
+  timing_end(st);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_flash_step(const Params& p, void* X, const void* out, const float* const (&w)[3], float* taps,
+                              const float* coef, const void* Wsplit_next, void* x_in, float* coef_next,
+                              float* saved_next, cudaStream_t st) {
+  using namespace flash;
+  const size_t T_all = (size_t)p.B * p.S;
+  const bool has_conv = w[0] != nullptr;
+  if (has_conv) {
+    const int n = p.C * NTAPS;
+    timing_begin("taps_major", st);
+    taps_major_kernel<<<(n + 255) / 256, 256, 0, st>>>(w[0], w[1], w[2], taps, p.C);
+    timing_end(st);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  // tokens per tile as in the coefficient pass: one wave over the SMs where
+  // that keeps at least 64 tokens per tile
+  const size_t per_sm = (T_all + sm_count() - 1) / sm_count();
+  const int rows = (int)std::min<size_t>(TILE_T, std::max<size_t>(64, (per_sm + 7) / 8 * 8));
+  CUtensorMap mx, mo;
+  {
+    const uint64_t dims[3] = {(uint64_t)p.C, (uint64_t)p.N, T_all};
+    const uint64_t strides[2] = {(uint64_t)p.C * 2, (uint64_t)p.N * p.C * 2};
+    const uint32_t box[3] = {KC, 1, (uint32_t)rows};
+    if (!make_map(&mx, X, 3, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  {
+    const uint64_t dims[2] = {(uint64_t)p.C, T_all};
+    const uint64_t strides[1] = {(uint64_t)p.C * 2};
+    const uint32_t box[2] = {KC, (uint32_t)(rows + HALO_R)};
+    if (!make_map(&mo, out, 2, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  const int ntiles = (int)((T_all + rows - 1) / rows);
+  const int grid = std::min(ntiles, sm_count());
+  FlashArgs f{coef, has_conv ? taps : nullptr, (const uint8_t*)Wsplit_next, (__nv_bfloat16*)x_in,
+              CoeffsOut{nullptr, nullptr, nullptr, saved_next, coef_next, nullptr}};
+  timing_begin("flash_tc", st);
+  if (has_conv) {
+    cudaFuncSetAttribute(flash_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+    flash_tc_kernel<true><<<grid, THREADS, SMEM, st>>>(mx, mo, p, f, ntiles, rows);
+  } else {
+    cudaFuncSetAttribute(flash_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM);
+    flash_tc_kernel<false><<<grid, THREADS, SMEM, st>>>(mx, mo, p, f, ntiles, rows);
   }
   timing_end(st);
   return cudaGetLastError();

@@ -14,6 +14,18 @@ bool tc_coeffs_supported(const Params& p);
 size_t coeffs_wsplit_bytes(const Params& p);
 cudaError_t launch_coeffs_tc(const Params& p, const void* X, const float* W, void* Wsplit, float* hpre,
                              float* hpost, float* hres, float* saved, float* coef, cudaStream_t st);
+// Fused stack step (bf16, C % 64 == 0): sublayer l's dense read (x_in,
+// nullable), TFA and sparse write of X in place, and the projection of the
+// updated state onto W_{l+1} (split by launch_w_split into Wsplit_next) giving
+// sublayer l+1's coefficient block and, if saved_next is set, its logits.
+// `coef` is sublayer l's block; w = {w4, w8, w12} or all nullptr; `taps`
+// (flash_taps_bytes) receives the tap-major copy of the conv weights.
+bool flash_supported(const Params& p);
+size_t flash_taps_bytes(const Params& p);
+cudaError_t launch_w_split(const Params& p, const float* W, void* Wsplit, cudaStream_t st);
+cudaError_t launch_flash_step(const Params& p, void* X, const void* out, const float* const (&w)[3], float* taps,
+                              const float* coef, const void* Wsplit_next, void* x_in, float* coef_next,
+                              float* saved_next, cudaStream_t st);
 // Status recorded by bounded device-side waits (0: none); synchronises `st`
 // and clears the record.
 int read_device_error(cudaStream_t st);

@@ -208,3 +208,39 @@ def test_router_rejections(lib):
     assert L.xhc_sublayer_bwd_routed(ctypes.byref(shape(lib, dtype=0)), FAKE, FAKE, None, None, None, FAKE, FAKE,
                                      fx, 2, FAKE, FAKE, FAKE, ctypes.c_void_p(1 << 22), None, FAKE, FAKE, None, None,
                                      None, FAKE, FAKE, FAKE, bneed, None) == 4
+
+
+# ---------------------------------------------------------------- fused stack forward
+
+def test_stack_rejections(lib):
+    L = lib.LIB
+    sh = shape(lib)
+    need = L.xhc_stack_fwd_workspace_bytes(ctypes.byref(sh))
+    # two coefficient blocks, the bf16 split of one W, the tap-major conv weights
+    assert need >= 2 * 16 * 48 * 4 + 2 * 48 * 16 * 256 * 2 + 24 * 256 * 4
+
+    def arr(n, v=FAKE):
+        return (ctypes.c_void_p * n)(*([v.value] * n))
+
+    def stack(sh, nl, ix, conv=True, wsb=None, outs=None, Ws=None, x=FAKE):
+        c = (arr(nl), arr(nl), arr(nl)) if conv else (None, None, None)
+        return L.xhc_stack_fwd(ctypes.byref(sh), nl, x, arr(nl) if outs is None else outs, *c,
+                               arr(nl) if Ws is None else Ws, ix, None, None, FAKE,
+                               need if wsb is None else wsb, None)
+    good = idx(0, 1, 2, 3, 4, 5, 6, 7)
+    assert stack(sh, 2, good, wsb=need - 1) == 5                         # workspace too small
+    assert stack(sh, 0, good) == 8                                       # no sublayer
+    assert stack(sh, 2, idx(0, 1, 2, 3, 4, 4, 6, 7)) == 2                # repeated stream in sublayer 1
+    assert stack(sh, 2, idx(0, 1, 2, 3, 4, 5, 6, 16)) == 2               # outside [0, N)
+    assert stack(shape(lib, dtype=0), 2, good) == 4                      # fp32 state
+    assert stack(shape(lib, C=96), 2, good) == 1                         # C not a multiple of 64
+    assert stack(sh, 2, good, x=MIS) == 3                                # misaligned state
+    assert stack(sh, 2, good, outs=(ctypes.c_void_p * 2)(FAKE.value, None)) == 8   # missing out
+    assert stack(sh, 2, good, Ws=(ctypes.c_void_p * 2)(FAKE.value, MIS.value)) == 3
+    part = (ctypes.c_void_p * 2)(FAKE.value, None)
+    assert L.xhc_stack_fwd(ctypes.byref(sh), 2, FAKE, arr(2), arr(2), arr(2), part, arr(2), good, None, None, FAKE,
+                           need, None) == 8                               # sublayer 1: two of three conv weights
+    assert L.xhc_stack_fwd(ctypes.byref(sh), 2, FAKE, arr(2), arr(2), None, None, arr(2), good, None, None, FAKE,
+                           need, None) == 8                               # conv arrays: all three or none
+    empty = shape(lib, B=0)
+    assert stack(empty, 2, good, wsb=0) == 0                             # nothing to do
