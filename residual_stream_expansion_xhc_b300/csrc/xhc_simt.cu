@@ -633,7 +633,6 @@ template <typename T, bool HAS_CONV>
 __global__ void __launch_bounds__(256) bwd_tfa_simt_kernel(Params p, BwdArgs<T> a, float* __restrict__ partial) {
   extern __shared__ float smem[];
   const int N = p.N, k = p.k, C = p.C, S = p.S, P = p.P, R = 2 * P + 1;
-  const size_t NC = (size_t)N * C;
   const int b = blockIdx.z, s0 = blockIdx.y * TFA_TT, c0 = blockIdx.x * TFA_CC;
   const int ntok = min(TFA_TT, S - s0);
   const int nrows = min(TFA_TT + HALO, S - s0);          // du rows needed (forward halo)
