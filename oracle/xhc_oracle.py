@@ -449,10 +449,12 @@ def _routed_weights(s, idx, nfixed):
     return w
 
 
-def forward_routed(X, out, conv, W, W_r, fixed, k, iters=20, eps=1e-6):
+def forward_routed(X, out, conv, W, W_r, fixed, k, iters=20, eps=1e-6, idx=None):
     """The sublayer update with per-token active sets chosen by the router.
     X [B,S,N,C], out [B,S,C], conv as in ``forward``, W [P, N*C] (P for k
     slots), W_r [N, N*C], fixed: the always-active streams (ordered).
+    ``idx`` [B, S, k] optionally gives the active sets (where two scores tie
+    either choice is a valid forward); by default ``route`` chooses them.
     Returns Xp, x_in, idx [B,S,k], s [B,S,N]."""
     B, S, N, C = X.shape
     res = dict(Xp=X.copy(), x_in=np.zeros((B, S, C)), idx=np.zeros((B, S, k), dtype=np.int64),
@@ -460,17 +462,17 @@ def forward_routed(X, out, conv, W, W_r, fixed, k, iters=20, eps=1e-6):
     for b in range(B):
         cf = _coeffs_seq(X[b], W, N, C, k, iters, eps)
         s, _, _, _ = router_scores(X[b], W_r, eps)
-        idx = route(s, fixed, k)
-        w = _routed_weights(s, idx, len(fixed))
+        ib = route(s, fixed, k) if idx is None else np.asarray(idx[b], dtype=np.int64)
+        w = _routed_weights(s, ib, len(fixed))
         u = tfa_components(out[b], conv)
-        Xa = np.take_along_axis(X[b], idx[:, :, None], axis=1)              # [S, k, C]
+        Xa = np.take_along_axis(X[b], ib[:, :, None], axis=1)               # [S, k, C]
         mix = np.einsum("sij,sjc->sic", cf["hres"], Xa)
         write = np.einsum("sic,csx->six", cf["hpost"], u) * w[:, :, None]
         Xp = X[b].copy()
-        np.put_along_axis(Xp, idx[:, :, None], mix + write, axis=1)
+        np.put_along_axis(Xp, ib[:, :, None], mix + write, axis=1)
         res["Xp"][b] = Xp
         res["x_in"][b] = np.einsum("sn,snc->sc", cf["hpre"], X[b])
-        res["idx"][b] = idx
+        res["idx"][b] = ib
         res["s"][b] = s
     return res
 

@@ -81,7 +81,10 @@ __global__ void __launch_bounds__(64) route_kernel(Params p, const float* __rest
       chosen |= 1u << fx.s[i];
     }
   }
-  // routed slots: the highest remaining score, the lower index on a tie
+  // routed slots: the highest remaining score, the lower index on a tie.
+  // The ranking compares the logits r[n]: the sigmoid is monotone, so the
+  // order is the scores' order, without the ties that fp32 sigmoid rounding
+  // makes of distinct large logits (sigmoid rounds to 1 above about 17).
 #pragma unroll
   for (int i = 0; i < KMAX; ++i) {
     if (i >= fx.n && i < k) {
@@ -89,9 +92,9 @@ __global__ void __launch_bounds__(64) route_kernel(Params p, const float* __rest
       float bs = 0.0f;
 #pragma unroll
       for (int n = 0; n < NMAX; ++n)
-        if (n < N && !((chosen >> n) & 1u) && (best < 0 || s[n] > bs)) {
+        if (n < N && !((chosen >> n) & 1u) && (best < 0 || r[n] > bs)) {
           best = n;
-          bs = s[n];
+          bs = r[n];
         }
       slot[i] = best;
       chosen |= 1u << best;
