@@ -212,7 +212,13 @@ int xhc_sublayer_fwd(const xhc_shape_t* sh, const void* X_in, void* X_out,
  *          without: at C = 2048 about 141,000 and 70,000 tokens.  Larger
  *          calls return XHC_ERR_WORKSPACE before touching the GPU.
  *   The first call on each device looks up the scratch address on that
- *   device (no allocation); make that first call before any stream capture.
+ *   device; make that first call before any stream capture.  The lookup
+ *   makes the driver load the library's device code on that device, which
+ *   reserves the 32 MiB there (the driver's doing, not an allocation call by
+ *   this library): when the device's memory is already taken, for example
+ *   by a caching pool, that first call can fail with XHC_ERR_CUDA
+ *   (out of memory).  The address is cached per device and context; after a
+ *   cudaDeviceReset the next call looks it up again in the new context.
  *   Every call shares the one scratch area: calls whose work overlaps on the
  *   GPU (different streams, or different threads) race and must be ordered
  *   by the caller.  The area keeps the last call's contents; nothing in it

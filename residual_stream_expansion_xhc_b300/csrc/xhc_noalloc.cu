@@ -11,6 +11,8 @@
 // For them this file reserves a fixed scratch area in the library itself, a
 // file-scope __device__ array that every GPU which loads the library holds
 // until the process exits.  Nothing here calls cudaMalloc or cudaFree.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "../../include/xhc.h"
@@ -27,22 +29,45 @@ static __device__ __align__(256) unsigned char g_fwd_scratch[kScratchBytes];
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mutex;
-void* g_scratch_ptr[kMaxDevices] = {};
+struct ScratchAddr {
+  CUcontext ctx;     // the context the address belongs to
+  void* ptr;
+};
+ScratchAddr g_scratch[kMaxDevices] = {};
 
 // Device address of the scratch array on the current device.  The host-side
 // name g_fwd_scratch is only a stand-in for the symbol, never a device
-// address, so the address is looked up once per device, with that device
-// current, and cached.
+// address, so the address is looked up with that device current and cached
+// per device, together with the context it was found in: a new context on
+// the device (after cudaDeviceReset) holds its own copy of the array, which
+// is looked up again.  The first lookup in a context makes the driver load
+// this module there, which reserves the 32 MiB; it can fail with
+// out-of-memory when the device is full.  A failed lookup leaves no error
+// behind in the runtime's last-error slot.
 int scratch_on_current_device(void** out) {
   int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return XHC_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(g_mutex);
-  if (!g_scratch_ptr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_fwd_scratch) != cudaSuccess || p == nullptr) return XHC_ERR_CUDA;
-    g_scratch_ptr[dev] = p;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cudaGetLastError();
+    return XHC_ERR_CUDA;
   }
-  *out = g_scratch_ptr[dev];
+  CUcontext ctx = nullptr;
+  if (cuCtxGetCurrent(&ctx) != CUDA_SUCCESS) ctx = nullptr;
+  std::lock_guard<std::mutex> lock(g_mutex);
+  ScratchAddr& c = g_scratch[dev];
+  if (!c.ptr || ctx == nullptr || c.ctx != ctx) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_fwd_scratch) != cudaSuccess || p == nullptr) {
+      cudaGetLastError();
+      c.ptr = nullptr;
+      return XHC_ERR_CUDA;
+    }
+    // the runtime makes the primary context current on its first call, so
+    // ask again after the lookup
+    if (ctx == nullptr && cuCtxGetCurrent(&ctx) != CUDA_SUCCESS) ctx = nullptr;
+    c.ctx = ctx;
+    c.ptr = p;
+  }
+  *out = c.ptr;
   return XHC_OK;
 }
 

@@ -28,12 +28,16 @@ if torch.cuda.is_available():
     from residual_stream_expansion_xhc_b300 import _lib, api
 
 CASES = [
-    xin.Workload("noalloc_bf16", 40, B=2, S=96, N=16, C=512, k=4, dtype="bf16"),
-    xin.Workload("noalloc_f32", 41, B=1, S=70, N=8, C=96, k=3, dtype="f32"),
+    # (workload, keep the logits in `saved`)
+    (xin.Workload("noalloc_bf16", 40, B=2, S=96, N=16, C=512, k=4, dtype="bf16"), False),
+    (xin.Workload("noalloc_bf16_saved", 43, B=1, S=150, N=16, C=256, k=4, dtype="bf16"), True),
+    (xin.Workload("noalloc_f32", 41, B=1, S=70, N=8, C=96, k=3, dtype="f32"), False),
+    # fp32 with `saved` needs no scratch at all: the call goes straight through
+    (xin.Workload("noalloc_f32_saved", 44, B=2, S=33, N=8, C=64, k=2, dtype="f32"), True),
 ]
 
 
-def _run(wl, t, use_noalloc):
+def _run(wl, t, use_noalloc, keep_saved):
     sh = api.make_shape(wl.B, wl.S, wl.N, wl.C, wl.k, tdtype(wl), wl.iters, wl.eps)
     X = dev_act(wl, t.X)
     out = dev_act(wl, t.out)
@@ -41,26 +45,34 @@ def _run(wl, t, use_noalloc):
     W = dev_f32(t.W)
     x_in = torch.empty(wl.B, wl.S, wl.C, dtype=tdtype(wl), device="cuda")
     act = torch.empty(wl.B, wl.S, wl.k, wl.C, dtype=tdtype(wl), device="cuda")
+    saved = torch.empty(wl.B, wl.S, wl.P + 1, device="cuda") if keep_saved else None
     if use_noalloc:
-        api.xhc_sublayer_fwd_noalloc(sh, X, X, out, conv, W, t.idx, x_in=x_in, saved=None, saved_active=act)
+        api.xhc_sublayer_fwd_noalloc(sh, X, X, out, conv, W, t.idx, x_in=x_in, saved=saved, saved_active=act)
     else:
-        ws = api.workspace(api.xhc_fwd_workspace_need(sh, False))
-        api.xhc_sublayer_fwd(sh, X, X, out, conv, W, t.idx, x_in=x_in, saved=None, saved_active=act, workspace=ws)
+        ws = api.workspace(api.xhc_fwd_workspace_need(sh, keep_saved))
+        api.xhc_sublayer_fwd(sh, X, X, out, conv, W, t.idx, x_in=x_in, saved=saved, saved_active=act, workspace=ws)
     torch.cuda.synchronize()
     api.xhc_device_status()
-    return X, x_in, act
+    res = {"X'": X, "x_in": x_in, "saved_active": act}
+    if keep_saved:
+        res["saved"] = saved
+    return res
 
 
-@pytest.mark.parametrize("wl", CASES, ids=[w.name for w in CASES])
-def test_noalloc_matches_workspace_path_twice(wl):
+@pytest.mark.parametrize("wl,keep_saved", CASES, ids=[w.name for w, _ in CASES])
+def test_noalloc_matches_workspace_path_twice(wl, keep_saved):
+    if wl.dtype == "f32" and keep_saved:
+        sh = api.make_shape(wl.B, wl.S, wl.N, wl.C, wl.k, tdtype(wl), wl.iters, wl.eps)
+        assert api.xhc_fwd_workspace_need(sh, True) == 0
     for call in range(2):
         # a different seeded draw for each call
         t = xin.make(xin.scaled(wl, wid=wl.wid + 100 * call))
-        ref = _run(wl, t, use_noalloc=False)
-        got = _run(wl, t, use_noalloc=True)
-        for r, g in zip(ref, got):
-            e = xo.max_rel_err(host_f64(g), host_f64(r))
-            assert e <= TOL[wl.dtype], f"call {call}: err {e}"
+        ref = _run(wl, t, use_noalloc=False, keep_saved=keep_saved)
+        got = _run(wl, t, use_noalloc=True, keep_saved=keep_saved)
+        assert set(ref) == set(got)
+        for key in ref:
+            e = xo.max_rel_err(host_f64(got[key]), host_f64(ref[key]))
+            assert e <= TOL[wl.dtype], f"call {call}, {key}: err {e}"
 
 
 def test_noalloc_refuses_calls_beyond_its_scratch():
@@ -74,12 +86,3 @@ def test_noalloc_refuses_calls_beyond_its_scratch():
     st = _lib.LIB.xhc_sublayer_fwd_noalloc(ctypes.byref(sh), fake, fake, fake, None, None, None, fake, idx, None,
                                            None, None, None)
     assert st == 5                     # XHC_ERR_WORKSPACE
-    # a call that keeps its logits runs
-    wl = xin.Workload("noalloc_saved", 42, B=1, S=40, N=16, C=256, k=4, dtype="bf16")
-    t = xin.make(wl)
-    shp = api.make_shape(wl.B, wl.S, wl.N, wl.C, wl.k, torch.bfloat16)
-    X = dev_act(wl, t.X)
-    saved = torch.empty(wl.B, wl.S, wl.P + 1, device="cuda")
-    api.xhc_sublayer_fwd_noalloc(shp, X, X, dev_act(wl, t.out), None, dev_f32(t.W), t.idx, saved=saved)
-    torch.cuda.synchronize()
-    assert torch.isfinite(saved).all()
