@@ -48,7 +48,40 @@ ALG_SIDE = {  # fp32 bytes per token
 # 4 (write the active rows in place) + 1 (write x_in) = 22 C, plus sublayer
 # l's coefficient block read (192 B) and sublayer l+1's logits and block
 # written (196 B).  The closing update of a stack writes no saved rows: 22 C.
-ALG_C_STACK = {"fwd_update": 22}
+
+
+def pass_c_units(N: int, k: int, mode: str) -> int:
+    """Algorithmic bytes per token of one pass, in C-units (the minimum a pass
+    must move; N streams, k active):
+      forward, inference: N (read X) + 1 (read out) + k (write the active rows)
+                          + 1 (write x_in)                      = 22 at N=16, k=4
+      forward, training:  adds the k saved active rows          = 26
+      backward:           2k + 1 (per-token quantities: dX' and the old rows
+                          of the active streams, out) + 3N + 2 (stream pass:
+                          X, dX', dX, out, dout)                = 59"""
+    fwd = N + 1 + k + 1
+    if mode == "fwd_inference":
+        return fwd
+    if mode == "fwd_training":
+        return fwd + k
+    if mode == "bwd":
+        return (2 * k + 1) + (3 * N + 2)
+    raise ValueError(mode)
+
+
+def kernel_c_units(name: str, N: int, k: int, saved_active: bool = True) -> int:
+    """Algorithmic bytes per token of one launch of a kernel, in C-units: what
+    its own job must read and write at least."""
+    table = {
+        "coeffs_tc": N,                                   # read X
+        "fwd_update": N + 1 + k + 1 + (k if saved_active else 0),
+        "flash_tc": N + 1 + k + 1,                        # dense read + sparse write of sublayer l
+        "bwd_col": 3 * k + 2,                             # read dX'[a], old rows, out; write mix, dout
+        "bwd_stream_tc": 3 * N,                           # read X, dX'; write dX
+    }
+    if name in table:
+        return table[name]
+    return ALG_C.get(name, 0)
 
 
 def load_peaks():
@@ -205,12 +238,37 @@ def cpu_baseline_stack(wl, layers, ntok=256):
                       f"sequence 0 ({dt:.1f} s)"}
 
 
-def cpu_baseline(wl, tensors, ntok=1024):
+def cpu_baseline(wl, tensors, ntok=1024, ntok1=1024):
+    """The oracle on all host cores (its BLAS calls threaded), and beside it
+    the same oracle on one thread (BLAS limited to one thread)."""
     sample = oracle_sample(wl, tensors, ntok)
     dt = time_oracle(sample, wl)
-    return {"value": ntok / dt, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
-            "sample": f"fp64 numpy oracle, forward+backward of the first {ntok} tokens of sequence 0 "
-                      f"({dt:.1f} s)"}
+    res = {"value": ntok / dt, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
+           "sample": f"fp64 numpy oracle, forward+backward of the first {ntok} tokens of sequence 0 "
+                     f"({dt:.1f} s)", "host_cpus": os.cpu_count()}
+    # one thread: a child process whose BLAS pools are started with one
+    # thread (the thread counts are read when the BLAS library loads)
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    try:
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-once", str(ntok1),
+                            "--workload", wl.name], env=env, capture_output=True, text=True, timeout=600)
+        dt1 = float(json.loads(r.stdout.strip().splitlines()[-1])["seconds"])
+    except (subprocess.SubprocessError, ValueError, IndexError, KeyError, OSError):
+        return res
+    res["single_thread"] = {"value": ntok1 / dt1, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                            "sample": f"fp64 numpy oracle on one thread (1 of {os.cpu_count()} host CPUs), "
+                                      f"forward+backward of one sequence of {ntok1} tokens drawn with the "
+                                      f"workload's widths and distributions ({dt1:.1f} s)"}
+    return res
+
+
+def oracle_once(wl, ntok):
+    """Child-process leg of the one-thread oracle timing: draw the workload,
+    time the oracle on the first ``ntok`` tokens, print the seconds."""
+    tensors = xin.make(xin.scaled(wl, B=1, S=max(ntok, 1)), grads=True)
+    dt = time_oracle(oracle_sample(wl, tensors, ntok), wl)
+    print(json.dumps({"seconds": dt, "tokens": ntok, "blas_threads": blas_threads()}), flush=True)
 
 
 def run_reference(args, wl):
@@ -262,6 +320,8 @@ def wl_desc(wl):
         return head + (f"router: {wl.router_fixed} fixed + {wl.k - wl.router_fixed} routed slots per token; forward "
                        f"(out of place, x_in, saved logits, router record) + backward (dX', no dx_in)")
     gs = "; Gram-Schmidt of the TFA components" if wl.gram_schmidt else ""
+    if not wl.backward:
+        return head + f"forward (inference: in place, x_in written, no saved logits or rows){gs}"
     return head + (f"forward (training mode: in place, x_in, saved logits, saved active rows) + backward (dX', "
                    f"no dx_in){gs}")
 
@@ -366,6 +426,106 @@ class StackStep:
 
     def __call__(self):
         self.fwd()
+
+
+class InfStep:
+    """The inference forward of one sublayer: in place, x_in written, no saved
+    logits and no saved rows (the logits go to the workspace)."""
+
+    def __init__(self, wl, tensors, dev):
+        import torch
+        from residual_stream_expansion_xhc_b300 import api
+        self.api, self.wl, self.torch = api, wl, torch
+
+        def act(a):
+            return torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+
+        self.sh = api.make_shape(wl.B, wl.S, wl.N, wl.C, wl.k, torch.bfloat16, wl.iters, wl.eps, wl.gram_schmidt)
+        self.X = act(tensors.X)
+        self.out = act(tensors.out)
+        self.conv = None if tensors.conv is None else tuple(torch.from_numpy(w).to(dev) for w in tensors.conv)
+        self.W = torch.from_numpy(tensors.W).to(dev)
+        self.idx = [int(i) for i in tensors.idx]
+        self.x_in = torch.empty(wl.B, wl.S, wl.C, dtype=torch.bfloat16, device=dev)
+        self.fws = api.workspace(api.xhc_fwd_workspace_need(self.sh, False), dev)
+
+    def __call__(self):
+        self.api.xhc_sublayer_fwd(self.sh, self.X, self.X, self.out, self.conv, self.W, self.idx, x_in=self.x_in,
+                                  saved=None, saved_active=None, workspace=self.fws)
+
+
+def measure_leg(step, wl, steps, warmup, alg_c_per_unit, units_per_step, unit, peak, saved_active=True):
+    """Time one workload leg: ``steps`` steps after ``warmup`` (CUDA events on
+    the launching stream), then the same steps again with the library's
+    per-kernel events for the kernel table.  Bytes: ``alg_c_per_unit`` C-units
+    (the pass model) per unit of work; moved = what the launched kernels must
+    move by their own jobs (kernel_c_units) per step."""
+    import torch
+    from residual_stream_expansion_xhc_b300 import api
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    ms = timed(step, steps) / steps
+    api.xhc_timing_collect()
+    api.xhc_timing_enable(True)
+    timed(step, steps)
+    api.xhc_timing_enable(False)
+    torch.cuda.synchronize()
+    kern = api.xhc_timing_collect()
+    cunit = wl.C * wl.esize
+    alg = alg_c_per_unit * cunit * units_per_step
+    moved_c = sum((c / steps) * kernel_c_units(n, wl.N, wl.k, saved_active) for n, (c, _) in kern.items())
+    moved = moved_c * cunit * wl.tokens
+    total = sum(t for _, t in kern.values())
+    dname, (dcount, dtotal) = max(kern.items(), key=lambda kv: kv[1][1])
+    d_ms = dtotal / dcount
+    d_alg = (kernel_c_units(dname, wl.N, wl.k, saved_active) * cunit + ALG_SIDE.get(dname, 0)) * wl.tokens
+    return {
+        "workload": wl_desc(wl), "ms_per_step": ms, "value": units_per_step / (ms * 1e-3), "unit": unit,
+        "alg_C_per_unit": alg_c_per_unit, "alg_bytes_per_step": alg,
+        "alg_GBps": alg / (ms * 1e-3) / 1e9, "alg_frac": alg / (ms * 1e-3) / 1e9 / peak,
+        "moved_C_per_token": moved_c, "moved_GBps": moved / (ms * 1e-3) / 1e9,
+        "moved_frac": moved / (ms * 1e-3) / 1e9 / peak,
+        "dominant": {"kernel": dname, "avg_ms": d_ms, "alg_bytes_per_launch": d_alg,
+                     "GBps": d_alg / (d_ms * 1e-3) / 1e9, "frac": d_alg / (d_ms * 1e-3) / 1e9 / peak},
+        "kernels": {n: {"launches_per_step": c / steps, "avg_ms": t / c, "share": t / total}
+                    for n, (c, t) in kern.items()},
+    }
+
+
+def extra_legs(args, dev, peak):
+    """The other bf16 workloads of the benchmark suite, one line each, on the
+    same GPU after the main leg: the inference forward (B4 S4096 C2048), the
+    eight-sublayer stack (B2 S8192 C4096, fused stack forward) and the
+    mHC-shaped forward + backward (N = k = 4, no TFA)."""
+    import torch
+    out = {}
+    steps = max(3, args.steps)
+    wl = xin.WORKLOADS["fwd_bf16"]
+    st = InfStep(wl, xin.make(wl), dev)
+    out["fwd_inference"] = measure_leg(st, wl, steps, args.warmup, pass_c_units(wl.N, wl.k, "fwd_inference"),
+                                       wl.tokens, "tokens/s", peak, saved_active=False)
+    del st
+    torch.cuda.empty_cache()
+    wl = xin.WORKLOADS["mhc_bf16"]
+    st = Step(wl, xin.make(wl, grads=True), dev)
+    out["mhc"] = measure_leg(st, wl, steps, args.warmup,
+                             pass_c_units(wl.N, wl.k, "fwd_training") + pass_c_units(wl.N, wl.k, "bwd"),
+                             wl.tokens, "tokens/s", peak)
+    out["mhc"]["forward_ms"] = timed(st.fwd, steps) / steps
+    out["mhc"]["backward_ms"] = timed(st.bwd, steps) / steps
+    del st
+    torch.cuda.empty_cache()
+    wl = xin.WORKLOADS["stack8_bf16"]
+    layers = [xin.make(wl, l, state=(l == 0)) for l in range(wl.layers)]
+    st = StackStep(wl, layers, dev)
+    del layers
+    out["stack8"] = measure_leg(st, wl, max(3, steps // 4), args.warmup, pass_c_units(wl.N, wl.k, "fwd_inference"),
+                                wl.tokens * wl.layers, "sublayer-tokens/s", peak, saved_active=False)
+    out["stack8"]["moved_C_per_sublayer"] = out["stack8"].pop("moved_C_per_token") / wl.layers
+    del st
+    torch.cuda.empty_cache()
+    return out
 
 
 def stack_e2e_run(step, layers, steps):
@@ -548,7 +708,7 @@ def run_gpu(args, wl):
     dom = max(kern.items(), key=lambda kv: kv[1][1])
     dname, (dcount, dtotal) = dom
     per_launch_ms = dtotal / dcount
-    alg = (ALG_C.get(dname, 0) * cunit + ALG_SIDE.get(dname, 0)) * wl.tokens
+    alg = (kernel_c_units(dname, wl.N, wl.k) * cunit + ALG_SIDE.get(dname, 0)) * wl.tokens
     achieved = alg / (per_launch_ms * 1e-3) / 1e9
     traffic = load_traffic(dname, wl.tokens)
     e2e = None
@@ -558,10 +718,22 @@ def run_gpu(args, wl):
     cpu = None
     if rank == 0 and not args.no_cpu:
         cpu = cpu_baseline(wl, tensors, args.cpu_tokens)
+    extras = None
+    if not args.no_extra and wl.name == "fwdbwd_bf16":
+        del step, tensors
+        torch.cuda.empty_cache()
+        sampler2 = ClockSampler(local) if rank == 0 else None
+        if sampler2:
+            sampler2.start()
+            time.sleep(0.3)
+        extras = extra_legs(args, dev, peak)
+        clocks2 = sampler2.stop() if sampler2 else None
+        for v in extras.values():
+            v["clocks"] = clocks2
     if rank != 0:
         return
-    fwd_alg = 26 * cunit * wl.tokens
-    bwd_alg = 59 * cunit * wl.tokens
+    fwd_alg = pass_c_units(wl.N, wl.k, "fwd_training") * cunit * wl.tokens
+    bwd_alg = pass_c_units(wl.N, wl.k, "bwd") * cunit * wl.tokens
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
@@ -573,10 +745,15 @@ def run_gpu(args, wl):
                      "frac": achieved / peak, "traffic": traffic,
                      "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_kind})",
                      "alg_bytes_per_launch": alg, "launch_ms": per_launch_ms},
+        "step": {"alg_C_per_token": (fwd_alg + bwd_alg) / (cunit * wl.tokens),
+                 "alg_GBps": (fwd_alg + bwd_alg) / (ms_step * 1e-3) / 1e9,
+                 "alg_frac": (fwd_alg + bwd_alg) / (ms_step * 1e-3) / 1e9 / peak},
         "fwd": {"tokens_per_s": wl.tokens / (fwd_ms * 1e-3), "ms": fwd_ms,
-                "alg_GBps": fwd_alg / (fwd_ms * 1e-3) / 1e9, "alg_bytes": fwd_alg},
+                "alg_GBps": fwd_alg / (fwd_ms * 1e-3) / 1e9, "alg_bytes": fwd_alg,
+                "alg_frac": fwd_alg / (fwd_ms * 1e-3) / 1e9 / peak},
         "bwd": {"tokens_per_s": wl.tokens / (bwd_ms * 1e-3), "ms": bwd_ms,
-                "alg_GBps": bwd_alg / (bwd_ms * 1e-3) / 1e9, "alg_bytes": bwd_alg},
+                "alg_GBps": bwd_alg / (bwd_ms * 1e-3) / 1e9, "alg_bytes": bwd_alg,
+                "alg_frac": bwd_alg / (bwd_ms * 1e-3) / 1e9 / peak},
         "kernels": {k: {"launches": c, "avg_ms": t / c, "share": t / sum(v[1] for v in kern.values())}
                     for k, (c, t) in kern.items()},
         "gpu_launches": int(sum(c for c, _ in kern.values())),
@@ -585,6 +762,8 @@ def run_gpu(args, wl):
         "e2e": e2e,
         "cpu_baseline": cpu,
     }
+    if extras:
+        line.update(extras)
     print(json.dumps(line), flush=True)
 
 
@@ -619,7 +798,7 @@ def run_gpu_stack(args, wl, world, rank, local, dev):
     peak, peak_kind = load_peaks()
     dname, (dcount, dtotal) = max(kern.items(), key=lambda kv: kv[1][1])
     per_launch_ms = dtotal / dcount
-    c_units = ALG_C_STACK.get(dname, ALG_C.get(dname, 0))
+    c_units = kernel_c_units(dname, wl.N, wl.k, saved_active=False)
     alg = (c_units * cunit + ALG_SIDE.get(dname, 0)) * wl.tokens
     achieved = alg / (per_launch_ms * 1e-3) / 1e9
     e2e = None
@@ -681,11 +860,17 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=8)
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the inference-forward, stack and mHC-shape lines of the default run")
     ap.add_argument("--cpu-tokens", type=int, default=8192)
     ap.add_argument("--ref-tokens", type=int, default=256)
+    ap.add_argument("--oracle-once", type=int, default=0, help=argparse.SUPPRESS)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     wl = xin.WORKLOADS[args.workload]
+    if args.oracle_once:
+        oracle_once(wl, args.oracle_once)
+        return
     if args.impl == "reference":
         run_reference(args, wl)
     else:
