@@ -44,14 +44,32 @@ ScratchAddr g_scratch[kMaxDevices] = {};
 // this module there, which reserves the 32 MiB; it can fail with
 // out-of-memory when the device is full.  A failed lookup leaves no error
 // behind in the runtime's last-error slot.
+// The driver's cuCtxGetCurrent, fetched through the runtime so that the
+// library does not link the driver library directly.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+CUcontext current_context() {
+  static CtxGetCurrentFn fn = [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess) {
+      cudaGetLastError();
+      p = nullptr;
+    }
+    return reinterpret_cast<CtxGetCurrentFn>(p);
+  }();
+  CUcontext ctx = nullptr;
+  if (!fn || fn(&ctx) != CUDA_SUCCESS) return nullptr;
+  return ctx;
+}
+
 int scratch_on_current_device(void** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
     cudaGetLastError();
     return XHC_ERR_CUDA;
   }
-  CUcontext ctx = nullptr;
-  if (cuCtxGetCurrent(&ctx) != CUDA_SUCCESS) ctx = nullptr;
+  CUcontext ctx = current_context();
   std::lock_guard<std::mutex> lock(g_mutex);
   ScratchAddr& c = g_scratch[dev];
   if (!c.ptr || ctx == nullptr || c.ctx != ctx) {
@@ -63,7 +81,7 @@ int scratch_on_current_device(void** out) {
     }
     // the runtime makes the primary context current on its first call, so
     // ask again after the lookup
-    if (ctx == nullptr && cuCtxGetCurrent(&ctx) != CUDA_SUCCESS) ctx = nullptr;
+    if (ctx == nullptr) ctx = current_context();
     c.ctx = ctx;
     c.ptr = p;
   }
