@@ -103,6 +103,31 @@ int xhc_last_cuda_error(void);
  */
 int xhc_device_status(xhc_stream_t stream);
 
+/*
+ * Limit of the library's bounded device-side waits (mbarrier waits of the
+ * tensor-core kernels), in nanoseconds, for kernels launched after the call;
+ * 0 restores the default of 2 s.  A wait that runs out records
+ * XHC_ERR_TIMEOUT for xhc_device_status, and every wait of the kernels in
+ * flight then gives up at once; before a kernel ends, each of its roles waits
+ * (again within the limit) for the asynchronous copies and tensor-core
+ * operations it issued, so nothing is left writing its shared memory or
+ * tensor memory.  Synchronises the device (call it between steps).  The
+ * pages have no counterpart: failure detection of this library.
+ * Returns XHC_OK, or XHC_ERR_CUDA.
+ */
+int xhc_set_wait_limit_ns(unsigned long long ns);
+
+/*
+ * Failure-detection test hook (the pages have no counterpart): the next
+ * coefficient projection this process launches (the first kernel of
+ * xhc_coeffs, xhc_sublayer_fwd and the other forward entry points) issues
+ * none of its loads, so the waits of its tensor-core and math roles run out
+ * after the wait limit with nothing in flight.  That call's outputs are
+ * undefined; xhc_device_status then returns XHC_ERR_TIMEOUT and clears the
+ * record, and later calls run normally.  Returns XHC_OK.
+ */
+int xhc_debug_starve_next_projection(void);
+
 /* Number of projection rows P = N + 4k + k^2 for a shape. */
 int xhc_num_logits(const xhc_shape_t* sh);
 

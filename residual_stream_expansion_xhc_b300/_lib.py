@@ -16,7 +16,8 @@ XHC_F32, XHC_BF16 = 0, 1
 STATUS = {0: "XHC_OK", 1: "XHC_ERR_SHAPE", 2: "XHC_ERR_INDEX", 3: "XHC_ERR_ALIGN", 4: "XHC_ERR_DTYPE",
           5: "XHC_ERR_WORKSPACE", 6: "XHC_ERR_CUDA", 7: "XHC_ERR_TIMEOUT", 8: "XHC_ERR_ARG"}
 
-EXPORTS = ("xhc_status_string", "xhc_last_cuda_error", "xhc_device_status", "xhc_num_logits", "xhc_coeffs", "xhc_tfa",
+EXPORTS = ("xhc_status_string", "xhc_last_cuda_error", "xhc_device_status", "xhc_set_wait_limit_ns",
+           "xhc_debug_starve_next_projection", "xhc_num_logits", "xhc_coeffs", "xhc_tfa",
            "xhc_sparse_update", "xhc_fwd_workspace_bytes", "xhc_fwd_workspace_need", "xhc_sublayer_fwd", "xhc_sublayer_fwd_noalloc", "xhc_bwd_workspace_bytes",
            "xhc_sublayer_bwd", "xhc_fwd_routed_workspace_bytes", "xhc_sublayer_fwd_routed",
            "xhc_bwd_routed_workspace_bytes", "xhc_sublayer_bwd_routed", "xhc_hres_active_weights", "xhc_hres_active_grad", "xhc_copy", "xhc_timing_enable",
@@ -52,6 +53,10 @@ def _load() -> ctypes.CDLL:
     lib.xhc_last_cuda_error.argtypes = []
     lib.xhc_device_status.restype = I
     lib.xhc_device_status.argtypes = [P]
+    lib.xhc_set_wait_limit_ns.restype = I
+    lib.xhc_set_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
+    lib.xhc_debug_starve_next_projection.restype = I
+    lib.xhc_debug_starve_next_projection.argtypes = []
     lib.xhc_num_logits.restype = I
     lib.xhc_num_logits.argtypes = [sh]
     lib.xhc_coeffs.restype = I

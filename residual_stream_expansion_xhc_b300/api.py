@@ -81,6 +81,16 @@ def xhc_device_status(stream=None):
     _check("xhc_device_status", LIB.xhc_device_status(_s(stream)))
 
 
+def xhc_set_wait_limit_ns(ns: int):
+    """Limit of the bounded device-side waits for later launches (0: 2 s)."""
+    _check("xhc_set_wait_limit_ns", LIB.xhc_set_wait_limit_ns(ctypes.c_ulonglong(int(ns))))
+
+
+def xhc_debug_starve_next_projection():
+    """Test hook: the next coefficient projection issues no loads."""
+    _check("xhc_debug_starve_next_projection", LIB.xhc_debug_starve_next_projection())
+
+
 def xhc_fwd_workspace_bytes(sh) -> int:
     return int(LIB.xhc_fwd_workspace_bytes(ctypes.byref(sh)))
 

@@ -229,6 +229,16 @@ int xhc_device_status(xhc_stream_t stream) {
   return v ? XHC_ERR_TIMEOUT : XHC_OK;
 }
 
+int xhc_set_wait_limit_ns(unsigned long long ns) {
+  if (set_wait_limit_ns(ns) != 0) return cuda_status(cudaGetLastError());
+  return XHC_OK;
+}
+
+int xhc_debug_starve_next_projection(void) {
+  starve_next_projection();
+  return XHC_OK;
+}
+
 int xhc_num_logits(const xhc_shape_t* sh) {
   if (!sh) return 0;
   return sh->N + 4 * sh->k + sh->k * sh->k;

@@ -50,20 +50,39 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait for the phase with the given parity; gives up after `limit_ns` and
-// records `code` in *err (first error wins).  Returns false on timeout.
-constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
+// Limit of every bounded wait, in ns: 2 s unless the host sets another.
+// One translation unit (the tensor-core kernels and their launchers)
+// includes this header, so there is one copy of the variable.
+static __device__ unsigned long long g_wait_limit_ns = 2000000000ull;
+
+// Wait for the phase with the given parity; gives up after g_wait_limit_ns
+// and records `code` in *err (first error wins), or as soon as another thread
+// has recorded one.  Returns false when it gives up.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* err, int code) {
   if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t limit = *(volatile unsigned long long*)&g_wait_limit_ns;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*(volatile int*)err) return false;           // another thread already gave up
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+    if (globaltimer_ns() - t0 > limit) {
       atomicCAS(err, 0, code);
       return false;
     }
   }
+}
+
+// Bounded wait used when a role drains its own asynchronous copies or MMAs
+// before the CTA ends: it does not give up early on another thread's error
+// (those copies still write this CTA's shared memory or TMEM), only after
+// g_wait_limit_ns.
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t limit = *(volatile unsigned long long*)&g_wait_limit_ns;
+  const uint64_t t0 = globaltimer_ns();
+  while (globaltimer_ns() - t0 <= limit)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
 }
 
 // ---------------------------------------------------------------- TMA

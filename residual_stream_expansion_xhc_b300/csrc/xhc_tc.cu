@@ -8,6 +8,7 @@
 // contraction of the forward: z = rstd * (vec X . W^T), [tokens x N*C] x
 // [N*C x P], P = N + 4k + k^2.
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 
 #include "xhc_sm100.cuh"
@@ -19,6 +20,20 @@ namespace xhc {
 using namespace sm100;
 
 __device__ int g_device_error = 0;
+
+namespace {
+// Failure-detection test hook: when set, the next coefficient projection
+// issues no loads (consumed by that launch).
+std::atomic<int> g_starve_next_projection{0};
+}  // namespace
+
+int set_wait_limit_ns(unsigned long long ns) {
+  const unsigned long long v = ns ? ns : 2000000000ull;
+  if (cudaDeviceSynchronize() != cudaSuccess) return -1;
+  return cudaMemcpyToSymbol(sm100::g_wait_limit_ns, &v, sizeof(v)) == cudaSuccess ? 0 : -1;
+}
+
+void starve_next_projection() { g_starve_next_projection.store(1); }
 
 // ---------------------------------------------------------------- host: tensor maps
 
@@ -199,14 +214,16 @@ __device__ __forceinline__ void coeffs_epilogue(const Params& p, const float (&p
 template <bool PRESPLIT>
 __global__ void __launch_bounds__(coeffs::THREADS, 1)
     coeffs_tc_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__ CUtensorMap mapW,
-                     const __grid_constant__ CUtensorMap mapWlo, Params p, CoeffsOut o, int ntiles, int rows) {
+                     const __grid_constant__ CUtensorMap mapWlo, Params p, CoeffsOut o, int ntiles, int rows,
+                     int starve) {
   using namespace coeffs;
   using L = Layout<PRESPLIT>;
   constexpr int STAGES = L::STAGES, STAGE_BYTES = L::STAGE_BYTES, BOXES = L::BOXES;
   constexpr int OFF_WRAW = L::OFF_WRAW, OFF_WHI = L::OFF_WHI, OFF_WLO = L::OFF_WLO;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
-  __shared__ uint64_t full[STAGES], bready[STAGES], empty[STAGES], tfull[2], tempty[2], ssfull[2], ssempty[2];
+  __shared__ uint64_t full[STAGES], bready[STAGES], empty[STAGES], tfull[2], tempty[2], ssfull[2], ssempty[2],
+      mdrain;
   __shared__ uint32_t tmem_slot;
   __shared__ float ss_half[2][TILE_T];          // second halves of the row sums of squares
   int* err = &g_device_error;
@@ -227,6 +244,7 @@ __global__ void __launch_bounds__(coeffs::THREADS, 1)
       mbar_init(&ssfull[b], 4);                 // warps 6..9 wrote their halves
       mbar_init(&ssempty[b], 4);                // warps 2..5 read them
     }
+    mbar_init(&mdrain, 1);                      // every MMA of the CTA complete
     fence_mbar_init();
     tma_prefetch_desc(&mapX);
     if (!PRESPLIT) tma_prefetch_desc(&mapW);
@@ -245,6 +263,7 @@ __global__ void __launch_bounds__(coeffs::THREADS, 1)
     if (lane == 0) {
       const uint64_t pol_x = policy_evict_first(), pol_w = policy_evict_last();
       int it = 0;
+      if (starve) goto done_prod;               // test hook: no loads, so every consumer's wait runs out
       for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
         for (int kc = 0; kc < nk; ++kc, ++it) {
           const int s = it % STAGES;
@@ -262,7 +281,10 @@ __global__ void __launch_bounds__(coeffs::THREADS, 1)
           }
         }
       }
-    done_prod:;
+    done_prod:
+      // the loads issued land before the CTA may end (on every path: after
+      // a normal run these waits return at once)
+      for (int d = it > STAGES ? it - STAGES : 0; d < it; ++d) mbar_wait_drain(&full[d % STAGES], (d / STAGES) & 1);
     }
   } else if (warp == 1) {
     // ------------------------------------------------ MMA issuer
@@ -296,6 +318,9 @@ __global__ void __launch_bounds__(coeffs::THREADS, 1)
         if (!ok) break;
         umma_commit(&tfull[buf]);
       }
+      // every MMA issued completes before the CTA may end
+      umma_commit(&mdrain);
+      mbar_wait_drain(&mdrain, 0);
     }
   } else {
     // ------------------------------------------------ sum of squares + epilogue
@@ -455,7 +480,7 @@ __global__ void __launch_bounds__(flash::THREADS, 1)
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   __shared__ uint64_t full[STAGES], bready[STAGES], empty[STAGES], ofull, oempty, updated, tfull[2], tempty[2],
-      ssfull[2], ssempty[2];
+      ssfull[2], ssempty[2], mdrain;
   __shared__ uint32_t tmem_slot;
   __shared__ int ord[NMAX];
   __shared__ float ss_half[2][TILE_T];
@@ -481,6 +506,7 @@ __global__ void __launch_bounds__(flash::THREADS, 1)
       mbar_init(&ssfull[b], 4);
       mbar_init(&ssempty[b], 4);
     }
+    mbar_init(&mdrain, 1);
     for (int i = 0; i < k; ++i) ord[i] = p.idx[i];
     for (int j = 0; j < N - k; ++j) ord[k + j] = p.inactive[j];
     fence_mbar_init();
@@ -500,10 +526,11 @@ __global__ void __launch_bounds__(flash::THREADS, 1)
     // ------------------------------------------------ TMA producer
     if (lane == 0) {
       const uint64_t pol_x = policy_evict_first(), pol_w = policy_evict_last();
-      int it = 0, oc = 0;
+      int it = 0, oc = 0, nout = 0;
       for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
         for (int cc = 0; cc < cchunks; ++cc, ++oc) {
           if (oc > 0 && !mbar_wait(&oempty, (oc - 1) & 1, err, 21)) goto done_prod;
+          ++nout;
           mbar_expect_tx(&ofull, (rows + HALO_R) * 128 + (HAS_CONV ? TAP_BYTES : 0));
           tma_load_2d(smem + OFF_OUT, &mapOut, &ofull, cc * KC, tile * rows - HALO_R, pol_x);
           if (HAS_CONV) bulk_load(smem + OFF_TAP, f.taps + (size_t)cc * NTAPS * KC, TAP_BYTES, &ofull, pol_w);
@@ -519,7 +546,10 @@ __global__ void __launch_bounds__(flash::THREADS, 1)
           }
         }
       }
-    done_prod:;
+    done_prod:
+      // the loads issued land before the CTA may end
+      for (int d = it > STAGES ? it - STAGES : 0; d < it; ++d) mbar_wait_drain(&full[d % STAGES], (d / STAGES) & 1);
+      if (nout > 0) mbar_wait_drain(&ofull, (nout - 1) & 1);
     }
   } else if (warp == 1) {
     // ------------------------------------------------ MMA issuer
@@ -550,6 +580,8 @@ __global__ void __launch_bounds__(flash::THREADS, 1)
         if (!ok) break;
         umma_commit(&tfull[buf]);
       }
+      umma_commit(&mdrain);
+      mbar_wait_drain(&mdrain, 0);
     }
   } else {
     // ------------------------------------------------ math: dense read, update, sum of squares, epilogue
@@ -843,6 +875,7 @@ cudaError_t launch_coeffs_tc(const Params& p, const void* X, const float* W, voi
   const int ntiles = (int)((T_all + rows - 1) / rows);
   const int grid = std::min(ntiles, sm_count());
   CoeffsOut o{hpre, hpost, hres, saved, coef, (const uint8_t*)Wsplit};
+  const int starve = g_starve_next_projection.exchange(0);
   if (presplit) {
     const size_t threads = (size_t)W_ROWS * (NC / 8);
     timing_begin("w_split", st);
@@ -852,11 +885,11 @@ cudaError_t launch_coeffs_tc(const Params& p, const void* X, const float* W, voi
     if (e != cudaSuccess) return e;
     cudaFuncSetAttribute(coeffs_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<true>());
     timing_begin("coeffs_tc", st);
-    coeffs_tc_kernel<true><<<grid, THREADS, smem_bytes<true>(), st>>>(mx, mw, mwl, p, o, ntiles, rows);
+    coeffs_tc_kernel<true><<<grid, THREADS, smem_bytes<true>(), st>>>(mx, mw, mwl, p, o, ntiles, rows, starve);
   } else {
     cudaFuncSetAttribute(coeffs_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<false>());
     timing_begin("coeffs_tc", st);
-    coeffs_tc_kernel<false><<<grid, THREADS, smem_bytes<false>(), st>>>(mx, mw, mwl, p, o, ntiles, rows);
+    coeffs_tc_kernel<false><<<grid, THREADS, smem_bytes<false>(), st>>>(mx, mw, mwl, p, o, ntiles, rows, starve);
   }
   timing_end(st);
   return cudaGetLastError();
@@ -1012,7 +1045,7 @@ __global__ void __launch_bounds__(bwdtc::THREADS, 1)
   // contractions done with the stage; out_ready: dX tile written to the Pt
   // region; p_free: the store has read it
   __shared__ uint64_t full[STAGES], xb_free[STAGES], mma_done[STAGES], out_ready[STAGES], p_free[STAGES];
-  __shared__ uint64_t tfull[2], tempty[2], wt_full, wt_empty, d2full, d2empty;
+  __shared__ uint64_t tfull[2], tempty[2], wt_full, wt_empty, d2full, d2empty, mdrain;
   __shared__ uint32_t tmem_slot;
   int* err = &g_device_error;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1043,6 +1076,7 @@ __global__ void __launch_bounds__(bwdtc::THREADS, 1)
     mbar_init(&wt_empty, 1);
     mbar_init(&d2full, 1);
     mbar_init(&d2empty, EPI_WARPS);
+    mbar_init(&mdrain, 1);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -1058,7 +1092,7 @@ __global__ void __launch_bounds__(bwdtc::THREADS, 1)
     // ------------------------------------------------ TMA producer
     if (lane == 0) {
       const uint64_t pol_stream = policy_evict_first(), pol_keep = policy_evict_last();
-      int it = 0, ii = 0;
+      int it = 0, ii = 0, issued = 0, nwt = 0;
       for (int item = blockIdx.x; item < nitems; item += gridDim.x, ++ii) {
         const int blk = item / ranges, r = item % ranges;
         const int n = blk / cblocks, c0 = (blk % cblocks) * CB;
@@ -1081,6 +1115,7 @@ __global__ void __launch_bounds__(bwdtc::THREADS, 1)
             if (slot) tma_load_3d(st + OFF_B + h * HALF, &m.dX, &full[s], c0 + 64 * h, n, tt, pol_stream);
             else tma_load_3d(st + OFF_B + h * HALF, &m.dXp, &full[s], c0 + 64 * h, n, tt, pol_stream);
           }
+          issued = it + 1;
           if (it >= STAGES && !mbar_wait(&p_free[s], ph, err, 31)) { ok = false; break; }
           tma_load_2d(st + OFF_P, &m.dP, &full[s], 0, tt, pol_keep);
           tma_load_2d(st + OFF_PL, &m.dPl, &full[s], 0, tt, pol_keep);
@@ -1090,10 +1125,17 @@ __global__ void __launch_bounds__(bwdtc::THREADS, 1)
             mbar_expect_tx(&wt_full, 2 * WT_BYTES);
             tma_load_2d(wt_s, &m.Wt, &wt_full, 0, (int)((size_t)n * C + c0), pol_keep);
             tma_load_2d(wt_s + WT_BYTES, &m.Wtl, &wt_full, 0, (int)((size_t)n * C + c0), pol_keep);
+            ++nwt;
           }
         }
         if (!ok) break;
       }
+      // the loads issued land before the CTA may end (a stage whose dp loads
+      // were not issued never completes: its wait gives up after the limit,
+      // long after its state loads have landed)
+      for (int d = issued > STAGES ? issued - STAGES : 0; d < issued; ++d)
+        mbar_wait_drain(&full[d % STAGES], (d / STAGES) & 1);
+      if (nwt > 0) mbar_wait_drain(&wt_full, (nwt - 1) & 1);
     }
   } else if (warp == 1) {
     // ------------------------------------------------ MMA issuer
@@ -1150,6 +1192,8 @@ __global__ void __launch_bounds__(bwdtc::THREADS, 1)
         umma_commit(&d2full);
         umma_commit(&wt_empty);
       }
+      umma_commit(&mdrain);
+      mbar_wait_drain(&mdrain, 0);
     }
   } else if (warp == STORE_WARP) {
     // ------------------------------------------------ dX tile stores

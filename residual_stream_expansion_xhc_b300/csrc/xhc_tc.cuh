@@ -29,6 +29,11 @@ cudaError_t launch_flash_step(const Params& p, void* X, const void* out, const f
 // Status recorded by bounded device-side waits (0: none); synchronises `st`
 // and clears the record.
 int read_device_error(cudaStream_t st);
+// Limit of the bounded device waits for later launches (0: the default 2 s);
+// synchronises the device.  0 on success.
+int set_wait_limit_ns(unsigned long long ns);
+// The next coefficient projection issues no loads (failure-detection test hook).
+void starve_next_projection();
 
 // The bf16 backward built from the token pass, the TFA pass, the tensor-core
 // stream pass and the reduction (see xhc_bwd.cuh) serves these shapes.
