@@ -128,6 +128,30 @@ int xhc_set_wait_limit_ns(unsigned long long ns);
  */
 int xhc_debug_starve_next_projection(void);
 
+/*
+ * Debug build record (the pages have no counterpart; a stand-in for a
+ * memory checker).  libxhc_debug.so, built with -DXHC_DEBUG, checks every
+ * global load and store of the forward update and the backward column pass
+ * against the extents of the buffers of that launch (as the shape gives
+ * them); an access outside all of them is skipped and the first one is
+ * recorded.  This call synchronises the device and returns 1 with the
+ * source line of the access in *line and its address in *address (then
+ * clears the record), 0 when nothing was recorded, -1 in a release build
+ * (which checks nothing), -2 on a CUDA error.  line and address may be NULL.
+ */
+int xhc_debug_record(unsigned long long* line, unsigned long long* address);
+
+/*
+ * Self-test of the debug build's checker: one checked 4-byte load from
+ * byte 128 of `buf` with only the first 64 bytes of `buf` registered, result
+ * to out[0].  `buf` must hold at least 256 bytes (so that even an unchecked
+ * load stays inside it) and be 16-byte aligned; `out` at least 4 bytes.  A
+ * debug build skips the load (out[0] = 0) and records it; a release build
+ * performs it.  Asynchronous on `stream`.  XHC_OK, XHC_ERR_ALIGN or
+ * XHC_ERR_CUDA.
+ */
+int xhc_debug_selftest(const float* buf, float* out, xhc_stream_t stream);
+
 /* Number of projection rows P = N + 4k + k^2 for a shape. */
 int xhc_num_logits(const xhc_shape_t* sh);
 

@@ -10,14 +10,16 @@ import ctypes
 import os
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libxhc.so")
+# XHC_DEBUG=1 loads the debug build (bounds-checked streaming kernels)
+DEBUG = os.environ.get("XHC_DEBUG") == "1"
+LIB_PATH = os.path.join(_HERE, "libxhc_debug.so" if DEBUG else "libxhc.so")
 
 XHC_F32, XHC_BF16 = 0, 1
 STATUS = {0: "XHC_OK", 1: "XHC_ERR_SHAPE", 2: "XHC_ERR_INDEX", 3: "XHC_ERR_ALIGN", 4: "XHC_ERR_DTYPE",
           5: "XHC_ERR_WORKSPACE", 6: "XHC_ERR_CUDA", 7: "XHC_ERR_TIMEOUT", 8: "XHC_ERR_ARG"}
 
 EXPORTS = ("xhc_status_string", "xhc_last_cuda_error", "xhc_device_status", "xhc_set_wait_limit_ns",
-           "xhc_debug_starve_next_projection", "xhc_num_logits", "xhc_coeffs", "xhc_tfa",
+           "xhc_debug_starve_next_projection", "xhc_debug_record", "xhc_debug_selftest", "xhc_num_logits", "xhc_coeffs", "xhc_tfa",
            "xhc_sparse_update", "xhc_fwd_workspace_bytes", "xhc_fwd_workspace_need", "xhc_sublayer_fwd", "xhc_sublayer_fwd_noalloc", "xhc_bwd_workspace_bytes",
            "xhc_sublayer_bwd", "xhc_fwd_routed_workspace_bytes", "xhc_sublayer_fwd_routed",
            "xhc_bwd_routed_workspace_bytes", "xhc_sublayer_bwd_routed", "xhc_hres_active_weights", "xhc_hres_active_grad", "xhc_copy", "xhc_timing_enable",
@@ -42,7 +44,7 @@ class XhcError(RuntimeError):
 
 def _load() -> ctypes.CDLL:
     if not os.path.exists(LIB_PATH):
-        raise ImportError(f"libxhc.so not built at {LIB_PATH}; run "
+        raise ImportError(f"{os.path.basename(LIB_PATH)} not built at {LIB_PATH}; run "
                           "`python -m residual_stream_expansion_xhc_b300.build`")
     lib = ctypes.CDLL(LIB_PATH)
     P, I, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
@@ -57,6 +59,10 @@ def _load() -> ctypes.CDLL:
     lib.xhc_set_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
     lib.xhc_debug_starve_next_projection.restype = I
     lib.xhc_debug_starve_next_projection.argtypes = []
+    lib.xhc_debug_record.restype = I
+    lib.xhc_debug_record.argtypes = [ctypes.POINTER(ctypes.c_ulonglong), ctypes.POINTER(ctypes.c_ulonglong)]
+    lib.xhc_debug_selftest.restype = I
+    lib.xhc_debug_selftest.argtypes = [P, P, P]
     lib.xhc_num_logits.restype = I
     lib.xhc_num_logits.argtypes = [sh]
     lib.xhc_coeffs.restype = I

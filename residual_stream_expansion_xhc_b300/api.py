@@ -91,6 +91,21 @@ def xhc_debug_starve_next_projection():
     _check("xhc_debug_starve_next_projection", LIB.xhc_debug_starve_next_projection())
 
 
+def xhc_debug_record():
+    """(status, source line, address) of the debug build's first recorded
+    out-of-extent access; status 1 = recorded (then cleared), 0 = none, -1 =
+    release build."""
+    line, addr = ctypes.c_ulonglong(0), ctypes.c_ulonglong(0)
+    st = LIB.xhc_debug_record(ctypes.byref(line), ctypes.byref(addr))
+    if st < -1:
+        raise XhcError("xhc_debug_record", 6, LIB)
+    return st, line.value, addr.value
+
+
+def xhc_debug_selftest(buf, out, stream=None):
+    _check("xhc_debug_selftest", LIB.xhc_debug_selftest(_p(buf), _p(out), _s(stream)))
+
+
 def xhc_fwd_workspace_bytes(sh) -> int:
     return int(LIB.xhc_fwd_workspace_bytes(ctypes.byref(sh)))
 

@@ -8,6 +8,7 @@ import sys
 PKG = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG, "csrc")
 LIB = os.path.join(PKG, "libxhc.so")
+LIB_DEBUG = os.path.join(PKG, "libxhc_debug.so")   # -DXHC_DEBUG: bounds-checked streaming kernels
 SOURCES = ["xhc_api.cu", "xhc_simt.cu", "xhc_bwd.cu", "xhc_tc.cu", "xhc_stream.cu", "xhc_gs.cu", "xhc_router.cu", "xhc_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -19,30 +20,33 @@ def _nvcc() -> str:
     return "nvcc"
 
 
-def _stale() -> bool:
-    if not os.path.exists(LIB):
+def _stale(lib: str) -> bool:
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     deps = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
     deps.append(os.path.join(os.path.dirname(PKG), "include", "xhc.h"))
     return any(os.path.getmtime(d) > t for d in deps if os.path.exists(d))
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile every CUDA source of the library into one shared object."""
-    if not force and not _stale():
-        return LIB
+def build(force: bool = False, verbose: bool = False, debug: bool = False) -> str:
+    """Compile every CUDA source of the library into one shared object
+    (debug: the bounds-checked build, libxhc_debug.so)."""
+    lib = LIB_DEBUG if debug else LIB
+    if not force and not _stale(lib):
+        return lib
     cmd = [_nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-shared",
-           "-diag-suppress", "128", "-o", LIB + ".tmp"]
+           "-diag-suppress", "128", "-o", lib + ".tmp"]
+    if debug:
+        cmd += ["-DXHC_DEBUG"]
     cmd += [os.path.join(CSRC, s) for s in SOURCES]
     cmd += ["-lcuda"]
     if verbose:
         print(" ".join(cmd), file=sys.stderr)
     subprocess.run(cmd, check=True)
-    os.replace(LIB + ".tmp", LIB)
-    return LIB
+    os.replace(lib + ".tmp", lib)
+    return lib
 
 
 if __name__ == "__main__":
-    build(force="--force" in sys.argv, verbose=True)
-    print(LIB)
+    print(build(force="--force" in sys.argv, verbose=True, debug="--debug" in sys.argv))

@@ -239,6 +239,16 @@ int xhc_debug_starve_next_projection(void) {
   return XHC_OK;
 }
 
+int xhc_debug_record(unsigned long long* line, unsigned long long* address) {
+  return debug_record(line, address);
+}
+
+int xhc_debug_selftest(const float* buf, float* out, xhc_stream_t stream) {
+  if (!buf || !out || (reinterpret_cast<uintptr_t>(buf) & 15)) return XHC_ERR_ALIGN;
+  const int r = debug_selftest(buf, out, (cudaStream_t)stream);
+  return r == 0 ? XHC_OK : cuda_status(cudaGetLastError());
+}
+
 int xhc_num_logits(const xhc_shape_t* sh) {
   if (!sh) return 0;
   return sh->N + 4 * sh->k + sh->k * sh->k;

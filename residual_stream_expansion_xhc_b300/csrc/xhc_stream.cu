@@ -23,6 +23,7 @@
 // in shared memory, so every row of `out` is read from HBM once per walk.
 #include <algorithm>
 
+#include "xhc_debug.cuh"
 #include "xhc_gs.cuh"
 #include "xhc_stream.cuh"
 
@@ -47,11 +48,33 @@ __device__ __forceinline__ void unpack8(const uint4& a, float (&v)[8]) {
 __device__ __forceinline__ uint4 pack8(const float (&v)[8]) {
   return make_uint4(pack_bf2(v[0], v[1]), pack_bf2(v[2], v[3]), pack_bf2(v[4], v[5]), pack_bf2(v[6], v[7]));
 }
-__device__ __forceinline__ uint4 ld_stream(const __nv_bfloat16* p) {
+// Global accesses of the big buffers.  In debug builds each is checked
+// against the launch's buffer extents (dbg::ok; the caller's source line is
+// recorded on a miss) and skipped when it lies outside them.
+__device__ __forceinline__ uint4 ld_stream(const __nv_bfloat16* p, int line = __builtin_LINE()) {
+  if (!dbg::ok(p, 16, line)) return make_uint4(0, 0, 0, 0);
   return __ldcs(reinterpret_cast<const uint4*>(p));
 }
-__device__ __forceinline__ void st_stream(__nv_bfloat16* p, const uint4& v) {
+__device__ __forceinline__ void st_stream(__nv_bfloat16* p, const uint4& v, int line = __builtin_LINE()) {
+  if (!dbg::ok(p, 16, line)) return;
   __stcs(reinterpret_cast<uint4*>(p), v);
+}
+__device__ __forceinline__ float4 ld_f4(const float* p, int line = __builtin_LINE()) {
+  if (!dbg::ok(p, 16, line)) return make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  return *reinterpret_cast<const float4*>(p);
+}
+__device__ __forceinline__ float ld_f(const float* p, int line = __builtin_LINE()) {
+  if (!dbg::ok(p, 4, line)) return 0.0f;
+  return *p;
+}
+__device__ __forceinline__ int ld_i(const int32_t* p, int line = __builtin_LINE()) {
+  if (!dbg::ok(p, 4, line)) return 0;
+  return *p;
+}
+template <typename V>
+__device__ __forceinline__ void st_v(V* p, const V& v, int line = __builtin_LINE()) {
+  if (!dbg::ok(p, sizeof(V), line)) return;
+  *p = v;
 }
 __device__ __forceinline__ float bf16_bits(uint16_t h) { return __uint_as_float((uint32_t)h << 16); }
 
@@ -80,7 +103,8 @@ __device__ __forceinline__ void load_taps(const float* const (&w)[3], int c, int
 __device__ __forceinline__ uint4 fetch_out_row(const __nv_bfloat16* __restrict__ out, size_t seq_base, int S, int C,
                                                int c_lane, int r) {
   uint4 v = make_uint4(0, 0, 0, 0);
-  if (r >= 0 && r < S && c_lane < C) v = *reinterpret_cast<const uint4*>(out + (seq_base + r) * C + c_lane);
+  const __nv_bfloat16* q = out + (seq_base + r) * C + c_lane;
+  if (r >= 0 && r < S && c_lane < C && dbg::ok(q, 16, __LINE__)) v = *reinterpret_cast<const uint4*>(q);
   return v;
 }
 __device__ __forceinline__ void commit_out_row(uint16_t (*ring)[CB], int r, int lane, const uint4& v) {
@@ -256,7 +280,7 @@ __global__ void __launch_bounds__(THREADS, 2) fwd_update_kernel(Params p, UpdArg
         unsigned amask = 0;
 #pragma unroll
         for (int j = 0; j < KMAX; ++j) {
-          ai[j] = (NI < 0) ? (j < k ? a.tok_idx[tok * k + j] : 0) : p.idx[j];
+          ai[j] = (NI < 0) ? (j < k ? ld_i(a.tok_idx + tok * k + j) : 0) : p.idx[j];
           if (NI < 0 && j < k) amask |= 1u << ai[j];
         }
         uint4 xa[KMAX];
@@ -284,7 +308,7 @@ __global__ void __launch_bounds__(THREADS, 2) fwd_update_kernel(Params p, UpdArg
               const int n = q0 + q;
               if (n < N && !((amask >> n) & 1u)) {
                 if (a.x_in) {
-                  const float2 h = fx2(cf[n]);
+                  const float2 h = fx2(ld_f(cf + n));
                   const uint32_t w[4] = {xr[q].x, xr[q].y, xr[q].z, xr[q].w};
 #pragma unroll
                   for (int x = 0; x < 4; ++x) acc[q & 1][x] = __ffma2_rn(h, bfx2(w[x]), acc[q & 1][x]);
@@ -322,7 +346,7 @@ __global__ void __launch_bounds__(THREADS, 2) fwd_update_kernel(Params p, UpdArg
 #pragma unroll
           for (int j = 0; j < KMAX; ++j) {
             if (j < k) {
-              const float2 h = fx2(cf[ai[j]]);
+              const float2 h = fx2(ld_f(cf + ai[j]));
               const uint32_t w[4] = {xa[j].x, xa[j].y, xa[j].z, xa[j].w};
 #pragma unroll
               for (int x = 0; x < 4; ++x) acc[0][x] = __ffma2_rn(h, bfx2(w[x]), acc[0][x]);
@@ -362,8 +386,8 @@ __global__ void __launch_bounds__(THREADS, 2) fwd_update_kernel(Params p, UpdArg
 #pragma unroll
         for (int i = 0; i < KMAX; ++i) {
           if (i < k) {
-            const float4 hp = *reinterpret_cast<const float4*>(cf + COEF_POST + 4 * i);
-            const float4 hr = *reinterpret_cast<const float4*>(cf + COEF_RES + 4 * i);
+            const float4 hp = ld_f4(cf + COEF_POST + 4 * i);
+            const float4 hr = ld_f4(cf + COEF_RES + 4 * i);
             const float hrv[4] = {hr.x, hr.y, hr.z, hr.w};
             float2 y[4];
 #pragma unroll
@@ -500,8 +524,9 @@ __device__ __forceinline__ uint4 pack8x2(const float2 (&v)[4]) {
                     pack_bf2(v[3].x, v[3].y));
 }
 // Streaming read that does not allocate in L1.
-__device__ __forceinline__ uint4 ld_na(const __nv_bfloat16* p) {
-  uint4 v;
+__device__ __forceinline__ uint4 ld_na(const __nv_bfloat16* p, int line = __builtin_LINE()) {
+  uint4 v = make_uint4(0, 0, 0, 0);
+  if (!dbg::ok(p, 16, line)) return v;
   asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
                : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                : "l"(p));
@@ -599,9 +624,9 @@ __global__ void __launch_bounds__(col::THREADS, 3) bwd_col_kernel(Params p, BwdA
     for (int i = 0; i < KMAX; ++i) {
       if (i < k) {
         float2 g[4];
-        const int ai = ROUTED ? a.tok_idx[tok * k + i] : p.idx[i];
+        const int ai = ROUTED ? ld_i(a.tok_idx + tok * k + i) : p.idx[i];
         unpack8x2(ld_na(a.dXp + tok * NC + (size_t)ai * C + c_lane), g);
-        const float4 hp = *reinterpret_cast<const float4*>(cf + COEF_POST + 4 * i);
+        const float4 hp = ld_f4(cf + COEF_POST + 4 * i);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           du[0][q] = __ffma2_rn(f2(hp.y), g[q], du[0][q]);
@@ -722,7 +747,7 @@ __global__ void __launch_bounds__(col::THREADS, 3) bwd_col_kernel(Params p, BwdA
     const float* cf = coef + tok * COEF_STRIDE;
     int ai[KMAX];                             // this token's active streams
 #pragma unroll
-    for (int i = 0; i < KMAX; ++i) ai[i] = ROUTED ? (i < k ? a.tok_idx[tok * k + i] : 0) : p.idx[i];
+    for (int i = 0; i < KMAX; ++i) ai[i] = ROUTED ? (i < k ? ld_i(a.tok_idx + tok * k + i) : 0) : p.idx[i];
     float2 G[KMAX][4];
     uint4 gr[KMAX], xr[KMAX];                 // raw bf16 rows; zero where absent
 #pragma unroll
@@ -748,7 +773,7 @@ __global__ void __launch_bounds__(col::THREADS, 3) bwd_col_kernel(Params p, BwdA
       float hres[KMAX][KMAX];
 #pragma unroll
       for (int i = 0; i < KMAX; ++i) {
-        const float4 h = *reinterpret_cast<const float4*>(cf + COEF_RES + 4 * i);
+        const float4 h = ld_f4(cf + COEF_RES + 4 * i);
         hres[i][0] = h.x; hres[i][1] = h.y; hres[i][2] = h.z; hres[i][3] = h.w;
       }
 #pragma unroll
@@ -774,7 +799,7 @@ __global__ void __launch_bounds__(col::THREADS, 3) bwd_col_kernel(Params p, BwdA
 #pragma unroll
       for (int i = 0; i < KMAX; ++i) {
         if (i < k) {
-          const float4 hp = *reinterpret_cast<const float4*>(cf + COEF_POST + 4 * i);
+          const float4 hp = ld_f4(cf + COEF_POST + 4 * i);
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             du[0][q] = __ffma2_rn(f2(hp.x), G[i][q], du[0][q]);
@@ -856,7 +881,7 @@ __global__ void __launch_bounds__(col::THREADS, 3) bwd_col_kernel(Params p, BwdA
       const float2 r = lane < 16 ? make_float2(dA[0], dA[1]) : make_float2(dB[0], dB[1]);
       const int gi = (lane >> 2) & 3, n0 = 2 * (lane & 3);
       const int at = n0 < 4 ? 4 * gi + n0 : 16 + 4 * gi + (n0 - 4);
-      if (tok_ok) *reinterpret_cast<float2*>(pdot + (tok * ncb + cb) * PDOT + at) = r;
+      if (tok_ok) st_v(reinterpret_cast<float2*>(pdot + (tok * ncb + cb) * PDOT + at), r);
     }
     if (a.dx_in) {
       // <dx_in, X_n> for every stream n
@@ -880,7 +905,7 @@ __global__ void __launch_bounds__(col::THREADS, 3) bwd_col_kernel(Params p, BwdA
         }
       }
       const float r = half_transpose_sum16(w2, l16);
-      if (tok_ok) pdot[(tok * ncb + cb) * PDOT + 32 + l16] = r;
+      if (tok_ok) st_v(pdot + (tok * ncb + cb) * PDOT + 32 + l16, r);
     }
     if (refill) *reinterpret_cast<uint4*>(&sm.ring[(t0 - TTc - HALO + hw) & (ORc - 1)][8 * l16]) = next_row;
     if (!HAS_CONV) continue;
@@ -954,8 +979,8 @@ __global__ void __launch_bounds__(col::THREADS, 3) bwd_col_kernel(Params p, BwdA
 #pragma unroll
     for (int q = 0; q < 12; ++q) {
       float* row = dst + (size_t)(12 * grp + q) * C;
-      row[0] = dw[q].x;
-      row[1] = dw[q].y;
+      st_v(row, dw[q].x);
+      st_v(row + 1, dw[q].y);
     }
   }
 }
@@ -1205,6 +1230,14 @@ bool stream_update_supported(const Params& p) { return p.C % 8 == 0; }
 cudaError_t launch_fwd_update(const Params& p, const UpdArgs<__nv_bfloat16>& a, const float* coef, bool has_conv,
                               int sms, cudaStream_t st) {
   const Walk wk = make_walk(p, sms);
+  {
+    const size_t T = (size_t)p.B * p.S, row = (size_t)p.C * 2;
+    dbg::ExtentList l;
+    l.add(a.X_in, T * p.N * row).add(a.X_out, T * p.N * row).add(a.out, T * row).add(a.x_in, T * row);
+    l.add(a.saved_active, T * p.k * row).add(coef, T * COEF_STRIDE * 4).add(a.tok_idx, T * p.k * 4);
+    for (int j = 0; j < 3; ++j) l.add(a.w[j], (size_t)p.C * 4 * (j + 1) * 4);
+    if (cudaError_t e = dbg::set_extents(l, st)) return e;
+  }
   dim3 grid(wk.R, wk.ncb);
   const int smem = (int)sizeof(FwdSmem);
   timing_begin("fwd_update", st);
@@ -1240,6 +1273,15 @@ int bwd_col_cpart_rows(const Params& p, int sms) { return make_walk_col(p, sms).
 cudaError_t launch_bwd_col(const Params& p, const BwdArgs<__nv_bfloat16>& a, const float* coef, bool has_conv,
                            float* pdot, float* cpart, int sms, cudaStream_t st) {
   const Walk wk = make_walk_col(p, sms);
+  {
+    const size_t T = (size_t)p.B * p.S, row = (size_t)p.C * 2;
+    dbg::ExtentList l;
+    l.add(a.X, T * p.N * row).add(a.saved_active, T * p.k * row).add(a.out, T * row).add(a.dXp, T * p.N * row);
+    l.add(a.dx_in, T * row).add(a.dX, T * p.N * row).add(a.dout, T * row).add(coef, T * COEF_STRIDE * 4);
+    l.add(a.tok_idx, T * p.k * 4).add(pdot, bwd_col_pdot_floats(p) * 4).add(cpart, bwd_col_cpart_floats(p, sms) * 4);
+    for (int j = 0; j < 3; ++j) l.add(a.w[j], (size_t)p.C * 4 * (j + 1) * 4);
+    if (cudaError_t e = dbg::set_extents(l, st)) return e;
+  }
   dim3 grid(wk.R, wk.ncb);
   const int smem = (int)sizeof(ColSmem);
   timing_begin("bwd_col", st);
@@ -1277,6 +1319,42 @@ cudaError_t launch_bwd_dz(const Params& p, const float* saved, const float* pdot
   }
   timing_end(st);
   return cudaGetLastError();
+}
+
+// Reads and clears the first out-of-extent access recorded by a debug build
+// (0: none; -1: release build, which records nothing).
+int debug_record(unsigned long long* line, unsigned long long* addr) {
+#ifdef XHC_DEBUG
+  unsigned long long r[2] = {0, 0};
+  if (cudaDeviceSynchronize() != cudaSuccess) return -2;
+  if (cudaMemcpyFromSymbol(r, dbg::g_record, sizeof(r)) != cudaSuccess) return -2;
+  if (line) *line = r[0];
+  if (addr) *addr = r[1];
+  if (!r[0]) return 0;
+  const unsigned long long z[2] = {0, 0};
+  cudaMemcpyToSymbol(dbg::g_record, z, sizeof(z));
+  return 1;
+#else
+  if (line) *line = 0;
+  if (addr) *addr = 0;
+  return -1;
+#endif
+}
+
+// Debug builds: one checked load outside the registered extent of `buf`
+// (`bytes` >= 256 long): the extent covers its first 64 bytes, the load
+// targets byte 128, inside the allocation, so even an unchecked load would
+// stay in bounds.  The check must skip it and record it.
+__global__ void debug_selftest_kernel(const float* buf, float* out) {
+  out[0] = ld_f(buf + 32);
+}
+
+int debug_selftest(const float* buf, float* out, cudaStream_t st) {
+  dbg::ExtentList l;
+  l.add(buf, 64).add(out, 4);
+  if (dbg::set_extents(l, st) != cudaSuccess) return -2;
+  debug_selftest_kernel<<<1, 1, 0, st>>>(buf, out);
+  return cudaGetLastError() == cudaSuccess ? 0 : -2;
 }
 
 }  // namespace xhc

@@ -33,4 +33,10 @@ cudaError_t launch_bwd_dz(const Params& p, const float* saved, const float* pdot
 cudaError_t launch_gs_rev(const Params& p, const float* saved, const float* pdot, const float* gsrec, float* gsdh,
                           float* sgram, cudaStream_t st);
 
+// Debug builds (XHC_DEBUG): read and clear the first out-of-extent access of
+// the streaming kernels (1 and its source line and address; 0: none; -1:
+// release build; -2: CUDA error), and run the checker's self-test.
+int debug_record(unsigned long long* line, unsigned long long* addr);
+int debug_selftest(const float* buf, float* out, cudaStream_t st);
+
 }  // namespace xhc

@@ -16,3 +16,14 @@ def pytest_configure(config):
 @pytest.fixture(scope="session")
 def root():
     return ROOT
+
+
+@pytest.fixture(autouse=True)
+def _debug_build_record(request):
+    """Under the debug build (XHC_DEBUG=1) every GPU test must leave no
+    out-of-extent access recorded by the streaming kernels' bounds checks."""
+    yield
+    if os.environ.get("XHC_DEBUG") == "1" and request.node.get_closest_marker("gpu"):
+        from residual_stream_expansion_xhc_b300 import api
+        st, line, addr = api.xhc_debug_record()
+        assert st == 0, f"out-of-extent access recorded at source line {line}, address {addr:#x}"

@@ -244,3 +244,17 @@ def test_stack_rejections(lib):
                            need, None) == 8                               # conv arrays: all three or none
     empty = shape(lib, B=0)
     assert stack(empty, 2, good, wsb=0) == 0                             # nothing to do
+
+
+def test_debug_library_exports_the_same_symbols():
+    """The bounds-checked build (libxhc_debug.so) loads on a machine without a
+    GPU and exports every entry point the header declares."""
+    import os
+    from residual_stream_expansion_xhc_b300 import build
+    if not os.path.exists(build.LIB_DEBUG):
+        pytest.skip("debug build not built")
+    names = declared_functions()
+    out = subprocess.run(["nm", "-D", "--defined-only", build.LIB_DEBUG], capture_output=True, text=True).stdout
+    for n in names:
+        assert re.search(rf"\bT {n}$", out, flags=re.M), n
+    ctypes.CDLL(build.LIB_DEBUG)
