@@ -781,9 +781,9 @@ __global__ void __launch_bounds__(col::THREADS, 3) bwd_col_kernel(Params p, BwdA
         if (j < k) {
           float2 mx[4];
 #pragma unroll
-          for (int q = 0; q < 4; ++q) mx[q] = make_float2(0.0f, 0.0f);
+          for (int q = 0; q < 4; ++q) mx[q] = __fmul2_rn(f2(hres[0][j]), G[0][q]);   // k >= 1
 #pragma unroll
-          for (int i = 0; i < KMAX; ++i)
+          for (int i = 1; i < KMAX; ++i)
             if (i < k)
 #pragma unroll
               for (int q = 0; q < 4; ++q) mx[q] = __ffma2_rn(f2(hres[i][j]), G[i][q], mx[q]);
@@ -926,9 +926,9 @@ __global__ void __launch_bounds__(col::THREADS, 3) bwd_col_kernel(Params p, BwdA
           d2[i] = *reinterpret_cast<const float2*>(&sm.du2[(t0 + i) & (col::D2 - 1)][2 * pr]);
         }
 #pragma unroll
-        for (int tt = 0; tt < TTc; ++tt) part[tt] = make_float2(0.0f, 0.0f);
+        for (int tt = 0; tt < TTc; ++tt) part[tt] = __fmul2_rn(tp[0], d1[tt]);
 #pragma unroll
-        for (int tau = 0; tau < 4; ++tau)
+        for (int tau = 1; tau < 4; ++tau)
 #pragma unroll
           for (int tt = 0; tt < TTc; ++tt) part[tt] = __ffma2_rn(tp[tau], d1[tt + tau], part[tt]);
 #pragma unroll
@@ -953,9 +953,9 @@ __global__ void __launch_bounds__(col::THREADS, 3) bwd_col_kernel(Params p, BwdA
         for (int i = 0; i < TTc + 11; ++i)
           d3[i] = *reinterpret_cast<const float2*>(&sm.du3[(t0 + i) & (col::D3 - 1)][2 * pr]);
 #pragma unroll
-        for (int tt = 0; tt < TTc; ++tt) part[tt] = make_float2(0.0f, 0.0f);
+        for (int tt = 0; tt < TTc; ++tt) part[tt] = __fmul2_rn(tp[0], d3[tt]);
 #pragma unroll
-        for (int tau = 0; tau < 12; ++tau)
+        for (int tau = 1; tau < 12; ++tau)
 #pragma unroll
           for (int tt = 0; tt < TTc; ++tt) part[tt] = __ffma2_rn(tp[tau], d3[tt + tau], part[tt]);
         float2 ow[TTc + HALO];

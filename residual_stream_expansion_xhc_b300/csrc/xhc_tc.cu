@@ -152,6 +152,88 @@ struct CoeffsOut {
   const uint8_t* wsplit;   // stage images of the bf16 hi/lo split of W, or nullptr
 };
 
+// Sinkhorn of a k x k = 4 x 4 logit block held in registers: the operations
+// of sinkhorn_thread in the same order, with every index fixed at compile
+// time (so nothing goes through local memory).
+__device__ __forceinline__ void sinkhorn4(const float (&z)[16], int iters, float (&M)[4][4]) {
+  float zmax = -INFINITY;
+#pragma unroll
+  for (int e = 0; e < 16; ++e) zmax = fmaxf(zmax, z[e]);
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) M[i][j] = expf(z[4 * i + j] - zmax);
+  for (int it = 0; it < iters; ++it) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float r = __frcp_rn((M[i][0] + M[i][1]) + (M[i][2] + M[i][3]));
+#pragma unroll
+      for (int j = 0; j < 4; ++j) M[i][j] *= r;
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float r = __frcp_rn((M[0][j] + M[1][j]) + (M[2][j] + M[3][j]));
+#pragma unroll
+      for (int i = 0; i < 4; ++i) M[i][j] *= r;
+    }
+  }
+}
+
+// The epilogue of the N = 16, k = 4 shape split over the two math halves of
+// a token row: part 0 the Sinkhorn of H^res (coefficient block entries
+// 32..47, and `hres`), part 1 rstd and the logits (`saved`), the sigmoids of
+// H^pre and H^post (entries 0..31, `hpre`, `hpost`).  Same values as
+// coeffs_epilogue.  The projection's rows are ordered as the coefficient
+// block at this shape (P = 48): H^pre 0..15, H^post 16..31, H^res 32..47.
+__device__ __forceinline__ void coeffs_epilogue_16x4(const Params& p, const float (&pz)[coeffs::W_ROWS], float ss,
+                                                     size_t t, const CoeffsOut& o, int part) {
+  const float rstd = 1.0f / sqrtf(ss / (float)(16 * p.C) + p.eps);
+  if (part == 0) {
+    if (!o.hres && !o.coef) return;
+    float z[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) z[e] = rstd * pz[32 + e];
+    float M[4][4];
+    sinkhorn4(z, p.iters, M);
+    if (o.hres) {
+      float4* hr = reinterpret_cast<float4*>(o.hres + t * 16);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) hr[i] = make_float4(M[i][0], M[i][1], M[i][2], M[i][3]);
+    }
+    if (o.coef) {
+      float4* cf = reinterpret_cast<float4*>(o.coef + t * COEF_STRIDE);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) cf[8 + i] = make_float4(M[i][0], M[i][1], M[i][2], M[i][3]);
+    }
+    return;
+  }
+  if (o.saved) {
+    float* sv = o.saved + t * 49;
+#pragma unroll
+    for (int q = 0; q < 48; ++q) sv[q] = rstd * pz[q];
+    sv[48] = rstd;
+  }
+  if (!o.hpre && !o.hpost && !o.coef) return;
+  float h[32];
+#pragma unroll
+  for (int q = 0; q < 32; ++q) h[q] = sigmoidf_(rstd * pz[q]);
+  if (o.hpre) {
+    float4* d = reinterpret_cast<float4*>(o.hpre + t * 16);
+#pragma unroll
+    for (int v = 0; v < 4; ++v) d[v] = make_float4(h[4 * v], h[4 * v + 1], h[4 * v + 2], h[4 * v + 3]);
+  }
+  if (o.hpost) {
+    float4* d = reinterpret_cast<float4*>(o.hpost + t * 16);
+#pragma unroll
+    for (int v = 0; v < 4; ++v) d[v] = make_float4(h[16 + 4 * v], h[17 + 4 * v], h[18 + 4 * v], h[19 + 4 * v]);
+  }
+  if (o.coef) {
+    float4* cf = reinterpret_cast<float4*>(o.coef + t * COEF_STRIDE);
+#pragma unroll
+    for (int v = 0; v < 8; ++v) cf[v] = make_float4(h[4 * v], h[4 * v + 1], h[4 * v + 2], h[4 * v + 3]);
+  }
+}
+
 // Coefficients of token t from its unscaled logits pz (vec X . W^T) and the
 // sum of squares of its state: rstd, logits, sigmoid, Sinkhorn, stores.
 __device__ __forceinline__ void coeffs_epilogue(const Params& p, const float (&pz)[coeffs::W_ROWS], float ss,
@@ -225,7 +307,7 @@ __global__ void __launch_bounds__(coeffs::THREADS, 1)
   __shared__ uint64_t full[STAGES], bready[STAGES], empty[STAGES], tfull[2], tempty[2], ssfull[2], ssempty[2],
       mdrain;
   __shared__ uint32_t tmem_slot;
-  __shared__ float ss_half[2][TILE_T];          // second halves of the row sums of squares
+  __shared__ float ss_half[2][TILE_T];          // the two halves' row sums of squares
   int* err = &g_device_error;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -240,9 +322,9 @@ __global__ void __launch_bounds__(coeffs::THREADS, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], 4);
-      mbar_init(&ssfull[b], 4);                 // warps 6..9 wrote their halves
-      mbar_init(&ssempty[b], 4);                // warps 2..5 read them
+      mbar_init(&tempty[b], MATH_WARPS);        // every math warp (those that do not read it arrive at once)
+      mbar_init(&ssfull[b], MATH_WARPS);        // both halves wrote their row sums (index 0 used)
+      mbar_init(&ssempty[b], MATH_WARPS);       // and read them
     }
     mbar_init(&mdrain, 1);                      // every MMA of the CTA complete
     fence_mbar_init();
@@ -383,20 +465,23 @@ __global__ void __launch_bounds__(coeffs::THREADS, 1)
         if (lane == 0) mbar_arrive(&empty[s]);
       }
       if (!ok) break;
-      const int sb = tl & 1;
-      if (half == 1) {
-        // hand the second half of the row sums to warps 2..5 (double-buffered)
-        if (tl >= 2 && !mbar_wait(&ssempty[sb], ((tl >> 1) & 1) ^ 1, err, 16)) break;
-        ss_half[sb][row] = ss;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&ssfull[sb]);
+      // the row's total sum of squares from both halves (the same sum, in
+      // the same order, in both)
+      if (tl >= 1 && !mbar_wait(&ssempty[0], (tl - 1) & 1, err, 16)) break;
+      ss_half[half][row] = ss;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ssfull[0]);
+      if (!mbar_wait(&ssfull[0], tl & 1, err, 17)) break;
+      ss = ss_half[0][row] + ss_half[1][row];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ssempty[0]);
+      // at N = 16, k = 4 both halves share the epilogue; otherwise half 0 alone
+      const bool split = p.N == 16 && p.k == 4;
+      const int buf = tl & 1;
+      if (!split && half == 1) {
+        if (lane == 0) mbar_arrive(&tempty[buf]);
         continue;
       }
-      if (!mbar_wait(&ssfull[sb], (tl >> 1) & 1, err, 17)) break;
-      ss += ss_half[sb][row];
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&ssempty[sb]);
-      const int buf = tl & 1;
       if (!mbar_wait(&tfull[buf], (tl >> 1) & 1, err, 15)) break;
       tc_fence_after();
       float pz[W_ROWS];
@@ -414,7 +499,8 @@ __global__ void __launch_bounds__(coeffs::THREADS, 1)
 
       const size_t t = (size_t)tile * rows + row;
       if (row >= rows || t >= (size_t)p.B * p.S) continue;
-      coeffs_epilogue(p, pz, ss, t, o);
+      if (split) coeffs_epilogue_16x4(p, pz, ss, t, o, half);
+      else coeffs_epilogue(p, pz, ss, t, o);
     }
   }
   tc_fence_before();
@@ -502,9 +588,9 @@ __global__ void __launch_bounds__(flash::THREADS, 1)
     mbar_init(&updated, MATH_WARPS);           // the chunk's active rows rewritten by every math warp
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], 4);
-      mbar_init(&ssfull[b], 4);
-      mbar_init(&ssempty[b], 4);
+      mbar_init(&tempty[b], MATH_WARPS);
+      mbar_init(&ssfull[b], MATH_WARPS);
+      mbar_init(&ssempty[b], MATH_WARPS);
     }
     mbar_init(&mdrain, 1);
     for (int i = 0; i < k; ++i) ord[i] = p.idx[i];
@@ -769,19 +855,21 @@ __global__ void __launch_bounds__(flash::THREADS, 1)
       }
       if (!ok) break;
       // ---- epilogue: sublayer l+1's coefficients from the projection of S_{l+1}
-      const int sb = tl & 1;
+      if (tl >= 1 && !mbar_wait(&ssempty[0], (tl - 1) & 1, err, 28)) break;
+      ss_half[half][row] = ss;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ssfull[0]);
+      if (!mbar_wait(&ssfull[0], tl & 1, err, 29)) break;
+      ss = ss_half[0][row] + ss_half[1][row];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ssempty[0]);
+      // half 0 runs the epilogue (the split one of the projection would cost
+      // this kernel spills: it holds more registers through the chunk loop)
+      const int buf = tl & 1;
       if (half == 1) {
-        if (tl >= 2 && !mbar_wait(&ssempty[sb], ((tl >> 1) & 1) ^ 1, err, 28)) break;
-        ss_half[sb][row] = ss;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&ssfull[sb]);
+        if (lane == 0) mbar_arrive(&tempty[buf]);
         continue;
       }
-      if (!mbar_wait(&ssfull[sb], (tl >> 1) & 1, err, 29)) break;
-      ss += ss_half[sb][row];
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&ssempty[sb]);
-      const int buf = tl & 1;
       if (!mbar_wait(&tfull[buf], (tl >> 1) & 1, err, 30)) break;
       tc_fence_after();
       float pz[coeffs::W_ROWS];
