@@ -389,12 +389,13 @@ int xhc_sublayer_fwd(const xhc_shape_t* sh, const void* X_in, void* X_out, const
 }
 
 namespace {
-// Router forward workspace: the plain forward's, then W' [P, N*C] fp32, the
-// router pass's logits [T, P+1] and the row sums of W_r.
+// Router forward workspace: the plain forward's, then the 64-row split of
+// [W; W_r] (stage images of the projection that carries the router rows), the
+// router's record inputs [T, P+1] and the row sums of W_r.
 size_t routed_extra_bytes(const xhc_shape_t* sh) {
   const size_t NC = (size_t)sh->N * sh->C;
   const size_t P = (size_t)(sh->N + 4 * sh->k + sh->k * sh->k);
-  return round_up(P * NC * sizeof(float)) + round_up(tokens(sh) * (P + 1) * sizeof(float)) +
+  return round_up((size_t)2 * 64 * NC * sizeof(uint16_t)) + round_up(tokens(sh) * (P + 1) * sizeof(float)) +
          round_up((size_t)sh->N * sizeof(float));
 }
 
@@ -437,17 +438,18 @@ int xhc_sublayer_fwd_routed(const xhc_shape_t* sh, const void* X_in, void* X_out
   void* wsplit = ws + fwd_coef_bytes(sh);
   float* zw = (float*)(ws + fwd_coef_bytes(sh) + fwd_wsplit_bytes(sh));
   float* z = saved ? saved : zw;
+  (void)wsplit;                                        // the router's projection uses its own 64-row split
   char* rbase = ws + xhc_fwd_workspace_bytes(sh);
   const size_t NC = (size_t)p.N * p.C;
-  float* Wp = (float*)rbase;
-  float* zr = (float*)(rbase + round_up((size_t)p.P * NC * sizeof(float)));
+  void* wsplit_r = rbase;
+  float* zr = (float*)(rbase + round_up((size_t)2 * 64 * NC * sizeof(uint16_t)));
   float* rs = (float*)((char*)zr + round_up(tokens(sh) * (size_t)(p.P + 1) * sizeof(float)));
   cudaStream_t st = (cudaStream_t)stream;
   using T = __nv_bfloat16;
-  // coefficients, then the router's projection pass with W' and the routing
-  if ((s = cuda_status(launch_coeffs_tc(p, X_in, W, wsplit, nullptr, nullptr, nullptr, z, coef, st)))) return s;
-  if ((s = cuda_status(launch_router_weights(p, W_r, Wp, rs, st)))) return s;
-  if ((s = cuda_status(launch_coeffs_tc(p, X_in, Wp, wsplit, nullptr, nullptr, nullptr, zr, nullptr, st)))) return s;
+  // one projection pass gives the coefficients and the router's logits
+  // (W_r rides along as 16 more MMA rows); then the routing
+  if ((s = cuda_status(launch_router_rowsums(p, W_r, rs, st)))) return s;
+  if ((s = cuda_status(launch_coeffs_tc_router(p, X_in, W, W_r, wsplit_r, z, coef, zr, st)))) return s;
   if ((s = cuda_status(launch_route(p, zr, rs, fixed, n_fixed, tok_idx, rrec, coef, st)))) return s;
   UpdArgs<T> a{(const T*)X_in, (T*)X_out, (const T*)out, {w4, w8, w12}, nullptr, nullptr, nullptr, z,
                (T*)x_in, (T*)saved_active, X_out != X_in, tok_idx};

@@ -1,5 +1,4 @@
 // Router with per-token active sets, bf16 state (sm_103a):
-//   router_weights_kernel  W' = [W_r; 1; 0] for a second projection pass
 //   rowsum_kernel          row sums of W_r (the LayerNorm mean term)
 //   route_kernel           per token: LayerNorm scores, fixed + top-k slots,
 //                          routed write-back scaled into H^post
@@ -10,7 +9,8 @@
 // others are chosen per token by top-k; a routed stream's score multiplies
 // its new write-back.
 //
-// The projection pass (coeffs_tc_kernel with W') gives, per token, rstd and
+// The coefficient projection carries W_r as 16 more MMA rows and sums the
+// state beside its sum of squares, so it gives, per token, rstd and
 // rstd * (W_r v, sum v).  With mean m = sum v / (N C), mean square
 // q = 1 / rstd^2 - eps and sd = sqrt(q - m^2 + eps), the scores are
 // sigmoid((W_r v - m rs) / sd), rs the row sums of W_r.
@@ -19,19 +19,6 @@
 #include "xhc_router.cuh"
 
 namespace xhc {
-
-__global__ void __launch_bounds__(256) router_weights_kernel(Params p, const float* __restrict__ W_r,
-                                                             float* __restrict__ Wp) {
-  const size_t NC = (size_t)p.N * p.C;
-  const size_t n4 = (size_t)p.P * NC / 4;
-  for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x) {
-    const size_t r = (4 * i) / NC, col = (4 * i) % NC;
-    float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-    if ((int)r < p.N) v = *reinterpret_cast<const float4*>(W_r + r * NC + col);
-    else if ((int)r == p.N) v = make_float4(1.0f, 1.0f, 1.0f, 1.0f);
-    *reinterpret_cast<float4*>(Wp + r * NC + col) = v;
-  }
-}
 
 // one block per row; fixed-order tree sum
 __global__ void __launch_bounds__(256) rowsum_kernel(const float* __restrict__ W_r, size_t NC, float* __restrict__ rs) {
@@ -151,16 +138,6 @@ cudaError_t launch_route_scale(const Params& p, const int32_t* tok_idx, const fl
 
 cudaError_t launch_router_rowsums(const Params& p, const float* W_r, float* rs, cudaStream_t st) {
   rowsum_kernel<<<p.N, 256, 0, st>>>(W_r, (size_t)p.N * p.C, rs);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_router_weights(const Params& p, const float* W_r, float* Wp, float* rs, cudaStream_t st) {
-  const size_t NC = (size_t)p.N * p.C;
-  const size_t n4 = (size_t)p.P * NC / 4;
-  timing_begin("router_weights", st);
-  router_weights_kernel<<<(unsigned)std::min<size_t>((n4 + 255) / 256, 148 * 16), 256, 0, st>>>(p, W_r, Wp);
-  rowsum_kernel<<<p.N, 256, 0, st>>>(W_r, NC, rs);
-  timing_end(st);
   return cudaGetLastError();
 }
 

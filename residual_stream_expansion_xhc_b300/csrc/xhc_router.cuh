@@ -5,13 +5,8 @@
 
 namespace xhc {
 
-// W' [P, N*C] for the router's projection pass: rows 0 .. N-1 = W_r, row N = 1
-// (the projection then gives the sum of the state), the other rows 0; and the
-// row sums rs [N] of W_r (fixed order).
-cudaError_t launch_router_weights(const Params& p, const float* W_r, float* Wp, float* rs, cudaStream_t st);
-
-// Per token from the router pass's logits zr [T, P+1] (rstd-scaled W' v, then
-// rstd): LayerNorm scores s = sigmoid(r), r = W_r LN(v), the active slots (the
+// Per token from the router's record inputs zr [T, P+1] (rstd W_r v at
+// 0..N-1, rstd sum(v) at N, rstd at P; launch_coeffs_tc_router): LayerNorm scores s = sigmoid(r), r = W_r LN(v), the active slots (the
 // nf fixed streams, then the top k - nf others by score) into `tok_idx`
 // [T, k], and the router record rrec [T, 2N+2] = (s, r, LN mean, LN sd); the
 // coefficient block's H^post rows of the routed slots are scaled by their

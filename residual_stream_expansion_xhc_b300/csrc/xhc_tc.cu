@@ -120,17 +120,23 @@ constexpr int TMEM_COLS = 128;                    // 2 buffers x 64 columns
 // call (w_split_kernel, which stores each stage's 12 KB as one contiguous,
 // already swizzled image), so a stage is X + hi + lo.  Otherwise the fp32 W
 // tile arrives and the math warps split it into hi and lo in the stage.
-template <bool PRESPLIT> struct Layout;
-template <> struct Layout<true> {
+// ROUTER: the projection also carries the N router rows W_r (MMA rows 48 ..
+// 48 + N - 1, N = 64 columns of the accumulator), for the router's scores.
+template <bool PRESPLIT, bool ROUTER = false> struct Layout;
+template <> struct Layout<true, false> {
+  static constexpr int WR = W_ROWS;                 // rows of W in the MMA
+  static constexpr int WPART = W_BYTES;             // bytes of one bf16 part of a 64-column chunk
   static constexpr int BOXES = 2;                   // 64-entry chunks per stage: 256 contiguous bytes per row
   static constexpr int STAGES = 4;
-  static constexpr int OFF_WHI = BOXES * X_BYTES;   // chunk b: hi at OFF_WHI + b WBOX, lo W_BYTES later
-  static constexpr int OFF_WLO = OFF_WHI + W_BYTES;
-  static constexpr int WBOX = 2 * W_BYTES;
+  static constexpr int OFF_WHI = BOXES * X_BYTES;   // chunk b: hi at OFF_WHI + b WBOX, lo WPART later
+  static constexpr int OFF_WLO = OFF_WHI + WPART;
+  static constexpr int WBOX = 2 * WPART;
   static constexpr int OFF_WRAW = 0;                // unused
   static constexpr int STAGE_BYTES = OFF_WHI + BOXES * WBOX;   // 56 KB
 };
-template <> struct Layout<false> {
+template <> struct Layout<false, false> {
+  static constexpr int WR = W_ROWS;
+  static constexpr int WPART = W_BYTES;
   static constexpr int BOXES = 1;
   static constexpr int WBOX = 0;
   static constexpr int STAGES = 5;
@@ -139,8 +145,21 @@ template <> struct Layout<false> {
   static constexpr int OFF_WLO = OFF_WHI + W_BYTES;
   static constexpr int STAGE_BYTES = OFF_WLO + W_BYTES;   // 40 KB
 };
-template <bool PRESPLIT>
-constexpr int smem_bytes() { return Layout<PRESPLIT>::STAGES * Layout<PRESPLIT>::STAGE_BYTES + 1024; }
+template <> struct Layout<true, true> {
+  static constexpr int WR = 64;
+  static constexpr int WPART = WR * KC * 2;         // 8 KB
+  static constexpr int BOXES = 2;
+  static constexpr int STAGES = 3;
+  static constexpr int OFF_WHI = BOXES * X_BYTES;
+  static constexpr int OFF_WLO = OFF_WHI + WPART;
+  static constexpr int WBOX = 2 * WPART;
+  static constexpr int OFF_WRAW = 0;
+  static constexpr int STAGE_BYTES = OFF_WHI + BOXES * WBOX;   // 64 KB
+};
+template <bool PRESPLIT, bool ROUTER = false>
+constexpr int smem_bytes() {
+  return Layout<PRESPLIT, ROUTER>::STAGES * Layout<PRESPLIT, ROUTER>::STAGE_BYTES + 1024;
+}
 }  // namespace coeffs
 
 struct CoeffsOut {
@@ -150,6 +169,7 @@ struct CoeffsOut {
   float* saved;
   float* coef;    // [T, COEF_STRIDE] coefficient block, or nullptr
   const uint8_t* wsplit;   // stage images of the bf16 hi/lo split of W, or nullptr
+  float* router = nullptr; // ROUTER: [T, P + 1] rstd (W_r v) at 0..N-1, rstd sum(v) at N, rstd at P
 };
 
 // Sinkhorn of a k x k = 4 x 4 logit block held in registers: the operations
@@ -293,13 +313,13 @@ __device__ __forceinline__ void coeffs_epilogue(const Params& p, const float (&p
   }
 }
 
-template <bool PRESPLIT>
+template <bool PRESPLIT, bool ROUTER>
 __global__ void __launch_bounds__(coeffs::THREADS, 1)
     coeffs_tc_kernel(const __grid_constant__ CUtensorMap mapX, const __grid_constant__ CUtensorMap mapW,
                      const __grid_constant__ CUtensorMap mapWlo, Params p, CoeffsOut o, int ntiles, int rows,
                      int starve) {
   using namespace coeffs;
-  using L = Layout<PRESPLIT>;
+  using L = Layout<PRESPLIT, ROUTER>;
   constexpr int STAGES = L::STAGES, STAGE_BYTES = L::STAGE_BYTES, BOXES = L::BOXES;
   constexpr int OFF_WRAW = L::OFF_WRAW, OFF_WHI = L::OFF_WHI, OFF_WLO = L::OFF_WLO;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -308,6 +328,7 @@ __global__ void __launch_bounds__(coeffs::THREADS, 1)
       mdrain;
   __shared__ uint32_t tmem_slot;
   __shared__ float ss_half[2][TILE_T];          // the two halves' row sums of squares
+  __shared__ float s1_half[ROUTER ? 2 : 1][ROUTER ? TILE_T : 1];   // ROUTER: and their row sums
   int* err = &g_device_error;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -352,12 +373,13 @@ __global__ void __launch_bounds__(coeffs::THREADS, 1)
           const uint32_t ph = (it / STAGES) & 1;
           if (it >= STAGES && !mbar_wait(&empty[s], ph ^ 1, err, 11)) goto done_prod;
           uint8_t* st = smem + s * STAGE_BYTES;
-          mbar_expect_tx(&full[s], BOXES * rows * KC * 2 + (PRESPLIT ? BOXES * 2 * W_BYTES : p.P * KC * 4));
+          mbar_expect_tx(&full[s], BOXES * rows * KC * 2 + (PRESPLIT ? BOXES * 2 * L::WPART : p.P * KC * 4));
           const int n = kc / cchunks, c0 = (kc % cchunks) * KC * BOXES;
 #pragma unroll
           for (int b = 0; b < BOXES; ++b) tma_load_3d(st + b * X_BYTES, &mapX, &full[s], c0 + b * KC, n, tile * rows, pol_x);
           if (PRESPLIT) {
-            bulk_load(st + OFF_WHI, o.wsplit + (size_t)kc * BOXES * 2 * W_BYTES, BOXES * 2 * W_BYTES, &full[s], pol_w);
+            bulk_load(st + OFF_WHI, o.wsplit + (size_t)kc * BOXES * 2 * L::WPART, BOXES * 2 * L::WPART, &full[s],
+                      pol_w);
           } else {
             tma_load_2d_f32(st + OFF_WRAW, &mapW, &full[s], kc * KC, 0, pol_w);
           }
@@ -371,7 +393,7 @@ __global__ void __launch_bounds__(coeffs::THREADS, 1)
   } else if (warp == 1) {
     // ------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t idesc = idesc_bf16(TILE_T, W_ROWS, 0, 0);
+      const uint32_t idesc = idesc_bf16(TILE_T, L::WR, 0, 0);
       int it = 0, tl = 0;
       for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++tl) {
         const int buf = tl & 1;
@@ -412,7 +434,7 @@ __global__ void __launch_bounds__(coeffs::THREADS, 1)
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
     int it = 0, tl = 0;
     for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++tl) {
-      float ss = 0.0f;
+      float ss = 0.0f, s1 = 0.0f;
       bool ok = true;
       for (int kc = 0; kc < nk; ++kc, ++it) {
         const int s = it % STAGES;
@@ -459,6 +481,7 @@ __global__ void __launch_bounds__(coeffs::THREADS, 1)
             const float a = bf_lo(w[h]), b = bf_hi(w[h]);
             ss = fmaf(a, a, ss);
             ss = fmaf(b, b, ss);
+            if (ROUTER) s1 += a + b;
           }
         }
         __syncwarp();
@@ -469,10 +492,12 @@ __global__ void __launch_bounds__(coeffs::THREADS, 1)
       // the same order, in both)
       if (tl >= 1 && !mbar_wait(&ssempty[0], (tl - 1) & 1, err, 16)) break;
       ss_half[half][row] = ss;
+      if (ROUTER) s1_half[half][row] = s1;
       __syncwarp();
       if (lane == 0) mbar_arrive(&ssfull[0]);
       if (!mbar_wait(&ssfull[0], tl & 1, err, 17)) break;
       ss = ss_half[0][row] + ss_half[1][row];
+      if (ROUTER) s1 = s1_half[0][row] + s1_half[1][row];
       __syncwarp();
       if (lane == 0) mbar_arrive(&ssempty[0]);
       // at N = 16, k = 4 both halves share the epilogue; otherwise half 0 alone
@@ -484,9 +509,9 @@ __global__ void __launch_bounds__(coeffs::THREADS, 1)
       }
       if (!mbar_wait(&tfull[buf], (tl >> 1) & 1, err, 15)) break;
       tc_fence_after();
-      float pz[W_ROWS];
+      float pz[L::WR];
 #pragma unroll
-      for (int c = 0; c < W_ROWS; c += 16) {
+      for (int c = 0; c < L::WR; c += 16) {
         uint32_t r[16];
         tmem_ld16(tmem + lane_base + buf * 64 + c, r);
         tmem_wait_ld();
@@ -499,8 +524,19 @@ __global__ void __launch_bounds__(coeffs::THREADS, 1)
 
       const size_t t = (size_t)tile * rows + row;
       if (row >= rows || t >= (size_t)p.B * p.S) continue;
-      if (split) coeffs_epilogue_16x4(p, pz, ss, t, o, half);
-      else coeffs_epilogue(p, pz, ss, t, o);
+      const float (&pzc)[W_ROWS] = *reinterpret_cast<const float(*)[W_ROWS]>(&pz[0]);
+      if (split) coeffs_epilogue_16x4(p, pzc, ss, t, o, half);
+      else coeffs_epilogue(p, pzc, ss, t, o);
+      if (ROUTER && half == 0) {
+        // the router's logits and the LayerNorm's sum, scaled by rstd
+        const float rstd = 1.0f / sqrtf(ss / (float)(p.N * p.C) + p.eps);
+        float* zr = o.router + t * (p.P + 1);
+#pragma unroll
+        for (int n = 0; n < NMAX; ++n)
+          if (n < p.N) zr[n] = rstd * pz[W_ROWS + n];
+        zr[p.N] = rstd * s1;
+        zr[p.P] = rstd;
+      }
     }
   }
   tc_fence_before();
@@ -903,16 +939,22 @@ bool tc_coeffs_supported(const Params& p) { return p.C % coeffs::KC == 0 && p.P 
 // row's eight 16-byte groups placed by the 128-byte swizzle (group g of row q
 // at (g ^ (q mod 8)) * 16).  One bulk copy then brings a stage's 12 KB.  One
 // thread per 8 consecutive columns of one row.
-__global__ void w_split_kernel(const float* __restrict__ W, uint8_t* __restrict__ Ws, int P, size_t NC) {
+// With Wr (the router): `rows` = 64, rows 48 .. 48 + NR - 1 of the image are
+// the rows of Wr.
+__global__ void w_split_kernel(const float* __restrict__ W, uint8_t* __restrict__ Ws, int P, size_t NC,
+                               const float* __restrict__ Wr = nullptr, int NR = 0, int rows = coeffs::W_ROWS) {
   const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
   const size_t groups = NC / 8;
-  if (i >= (size_t)coeffs::W_ROWS * groups) return;
+  if (i >= (size_t)rows * groups) return;
   const int q = (int)(i / groups);
   const size_t c = (i % groups) * 8;
   float w[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-  if (q < P) {
-    const float4 a = *reinterpret_cast<const float4*>(W + (size_t)q * NC + c);
-    const float4 b = *reinterpret_cast<const float4*>(W + (size_t)q * NC + c + 4);
+  const float* src = q < P ? W + (size_t)q * NC
+                           : (Wr && q >= coeffs::W_ROWS && q < coeffs::W_ROWS + NR ? Wr + (size_t)(q - coeffs::W_ROWS) * NC
+                                                                                    : nullptr);
+  if (src) {
+    const float4 a = *reinterpret_cast<const float4*>(src + c);
+    const float4 b = *reinterpret_cast<const float4*>(src + c + 4);
     w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w; w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
   }
   uint32_t h[4], l[4];
@@ -923,10 +965,11 @@ __global__ void w_split_kernel(const float* __restrict__ W, uint8_t* __restrict_
   }
   const size_t kk = c / coeffs::KC;
   const int g = (int)((c % coeffs::KC) / 8);
-  uint8_t* tile = Ws + kk * 2 * coeffs::W_BYTES;
+  const size_t part = (size_t)rows * coeffs::KC * 2;
+  uint8_t* tile = Ws + kk * 2 * part;
   const uint32_t off = sw128_offset(q, g * 16);
   *reinterpret_cast<uint4*>(tile + off) = make_uint4(h[0], h[1], h[2], h[3]);
-  *reinterpret_cast<uint4*>(tile + coeffs::W_BYTES + off) = make_uint4(l[0], l[1], l[2], l[3]);
+  *reinterpret_cast<uint4*>(tile + part + off) = make_uint4(l[0], l[1], l[2], l[3]);
 }
 
 size_t coeffs_wsplit_bytes(const Params& p) { return (size_t)2 * coeffs::W_ROWS * p.N * p.C * sizeof(uint16_t); }
@@ -971,14 +1014,60 @@ cudaError_t launch_coeffs_tc(const Params& p, const void* X, const float* W, voi
     timing_end(st);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    cudaFuncSetAttribute(coeffs_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<true>());
+    cudaFuncSetAttribute(coeffs_tc_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         smem_bytes<true>());
     timing_begin("coeffs_tc", st);
-    coeffs_tc_kernel<true><<<grid, THREADS, smem_bytes<true>(), st>>>(mx, mw, mwl, p, o, ntiles, rows, starve);
+    coeffs_tc_kernel<true, false><<<grid, THREADS, smem_bytes<true>(), st>>>(mx, mw, mwl, p, o, ntiles, rows, starve);
   } else {
-    cudaFuncSetAttribute(coeffs_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes<false>());
+    cudaFuncSetAttribute(coeffs_tc_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         smem_bytes<false>());
     timing_begin("coeffs_tc", st);
-    coeffs_tc_kernel<false><<<grid, THREADS, smem_bytes<false>(), st>>>(mx, mw, mwl, p, o, ntiles, rows, starve);
+    coeffs_tc_kernel<false, false><<<grid, THREADS, smem_bytes<false>(), st>>>(mx, mw, mwl, p, o, ntiles, rows,
+                                                                              starve);
   }
+  timing_end(st);
+  return cudaGetLastError();
+}
+
+size_t coeffs_router_wsplit_bytes(const Params& p) {
+  return (size_t)2 * coeffs::Layout<true, true>::WR * p.N * p.C * sizeof(uint16_t);
+}
+
+// The projection with the router rows: W [P, N*C] and W_r [N, N*C] split
+// into 64-row stage images (rows 48 .. 48 + N - 1 = W_r), then one pass that
+// gives the coefficients (as launch_coeffs_tc) and the router's record
+// inputs `zr` [T, P + 1] (rstd W_r v, rstd sum(v), rstd).
+cudaError_t launch_coeffs_tc_router(const Params& p, const void* X, const float* W, const float* W_r, void* Wsplit,
+                                    float* saved, float* coef, float* zr, cudaStream_t st) {
+  using namespace coeffs;
+  using L = Layout<true, true>;
+  const size_t T_all = (size_t)p.B * p.S;
+  const size_t NC = (size_t)p.N * p.C;
+  if (p.C % (KC * L::BOXES) != 0 || p.N > L::WR - W_ROWS) return cudaErrorInvalidValue;
+  const size_t per_sm = (T_all + sm_count() - 1) / sm_count();
+  const int rows = (int)std::min<size_t>(TILE_T, std::max<size_t>(64, (per_sm + 7) / 8 * 8));
+  CUtensorMap mx;
+  {
+    const uint64_t dims[3] = {(uint64_t)p.C, (uint64_t)p.N, T_all};
+    const uint64_t strides[2] = {(uint64_t)p.C * 2, NC * 2};
+    const uint32_t box[3] = {KC, 1, (uint32_t)rows};
+    if (!make_map(&mx, X, 3, dims, strides, box)) return cudaErrorInvalidValue;
+  }
+  const int ntiles = (int)((T_all + rows - 1) / rows);
+  const int grid = std::min(ntiles, sm_count());
+  CoeffsOut o{nullptr, nullptr, nullptr, saved, coef, (const uint8_t*)Wsplit, zr};
+  const int starve = g_starve_next_projection.exchange(0);
+  const size_t threads = (size_t)L::WR * (NC / 8);
+  timing_begin("w_split", st);
+  w_split_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, st>>>(W, (uint8_t*)Wsplit, p.P, NC, W_r, p.N, L::WR);
+  timing_end(st);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  cudaFuncSetAttribute(coeffs_tc_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                       smem_bytes<true, true>());
+  timing_begin("coeffs_tc_router", st);
+  coeffs_tc_kernel<true, true><<<grid, THREADS, smem_bytes<true, true>(), st>>>(mx, mx, mx, p, o, ntiles, rows,
+                                                                                starve);
   timing_end(st);
   return cudaGetLastError();
 }

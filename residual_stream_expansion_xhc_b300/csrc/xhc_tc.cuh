@@ -28,6 +28,13 @@ cudaError_t launch_flash_step(const Params& p, void* X, const void* out, const f
                               float* saved_next, cudaStream_t st);
 // Status recorded by bounded device-side waits (0: none); synchronises `st`
 // and clears the record.
+// The coefficient projection with the router rows W_r carried along (64 MMA
+// rows): coefficients as launch_coeffs_tc (saved logits, coefficient block),
+// and zr [T, P+1] = (rstd W_r v, rstd sum(v), ..., rstd) for the router.
+// Wsplit: coeffs_router_wsplit_bytes() of scratch.
+size_t coeffs_router_wsplit_bytes(const Params& p);
+cudaError_t launch_coeffs_tc_router(const Params& p, const void* X, const float* W, const float* W_r, void* Wsplit,
+                                    float* saved, float* coef, float* zr, cudaStream_t st);
 int read_device_error(cudaStream_t st);
 // Limit of the bounded device waits for later launches (0: the default 2 s);
 // synchronises the device.  0 on success.
