@@ -38,6 +38,7 @@ METRIC = "tokens/s per xHC sublayer (fwd, fwd+bwd) and achieved HBM GB/s vs peak
 #   backward, stream: 16 (X) + 16 (dX') + 1 (out) + 16 (dX) + 1 (dout) = 50
 ALG_C = {  # algorithmic bytes per token in C-units (one row of C state elements)
     "coeffs_tc": 16, "fwd_update": 26, "bwd_col": 14, "bwd_stream_tc": 48, "flash_tc": 22,
+    "restore_active": 8,  # read the k saved rows, write them back into the state
     "coeffs_simt": 17, "update_simt": 26,
     "bwd_token_simt": 9, "bwd_dx_simt": 48, "bwd_dw_simt": 16, "bwd_tfa_simt": 6,
 }
@@ -78,6 +79,7 @@ def kernel_c_units(name: str, N: int, k: int, saved_active: bool = True) -> int:
         "flash_tc": N + 1 + k + 1,                        # dense read + sparse write of sublayer l
         "bwd_col": 3 * k + 2,                             # read dX'[a], old rows, out; write mix, dout
         "bwd_stream_tc": 3 * N,                           # read X, dX'; write dX
+        "restore_active": 2 * k,                          # read the saved rows, write them into the state
     }
     if name in table:
         return table[name]
@@ -318,7 +320,8 @@ def wl_desc(wl):
                        f"saved rows), each update fused with the next sublayer's coefficient projection")
     if wl.router_fixed >= 0:
         return head + (f"router: {wl.router_fixed} fixed + {wl.k - wl.router_fixed} routed slots per token; forward "
-                       f"(out of place, x_in, saved logits, router record) + backward (dX', no dx_in)")
+                       f"(in place, x_in, saved logits, saved active rows, router record) + backward (the saved rows "
+                       f"written back first; dX', no dx_in)")
     gs = "; Gram-Schmidt of the TFA components" if wl.gram_schmidt else ""
     if not wl.backward:
         return head + f"forward (inference: in place, x_in written, no saved logits or rows){gs}"
@@ -374,8 +377,9 @@ class Step:
 
 
 class RoutedStep(Step):
-    """The router's forward (out of place: the backward takes the state before
-    the update) and backward on the same buffers."""
+    """The router's forward, in place with the old active rows saved, and its
+    backward, which writes those rows back (the state before the update) before
+    it reads the state."""
 
     def __init__(self, wl, tensors, dev):
         super().__init__(wl, tensors, dev)
@@ -383,7 +387,6 @@ class RoutedStep(Step):
         B, S, N, k = wl.B, wl.S, wl.N, wl.k
         self.W_r = torch.from_numpy(tensors.extra["W_r"]).to(dev)
         self.fixed = self.idx[: wl.router_fixed]
-        self.Xo = torch.empty_like(self.X)
         self.tok_idx = torch.empty(B, S, k, dtype=torch.int32, device=dev)
         self.rrec = torch.empty(B, S, 2 * N + 2, dtype=torch.float32, device=dev)
         self.dW_r = torch.empty_like(self.W_r)
@@ -391,13 +394,14 @@ class RoutedStep(Step):
         self.ws = self.api.workspace(self.api.xhc_bwd_routed_workspace_bytes(self.sh), dev)
 
     def fwd(self):
-        self.api.xhc_sublayer_fwd_routed(self.sh, self.X, self.Xo, self.out, self.conv, self.W, self.W_r, self.fixed,
-                                         self.tok_idx, self.rrec, self.fws, x_in=self.x_in, saved=self.saved)
+        self.api.xhc_sublayer_fwd_routed(self.sh, self.X, self.X, self.out, self.conv, self.W, self.W_r, self.fixed,
+                                         self.tok_idx, self.rrec, self.fws, x_in=self.x_in, saved=self.saved,
+                                         saved_active=self.act)
 
     def bwd(self):
         self.api.xhc_sublayer_bwd_routed(self.sh, self.X, self.out, self.conv, self.W, self.W_r, self.fixed,
                                          self.saved, self.tok_idx, self.rrec, self.dXp, None, self.dX, self.dout,
-                                         self.dconv, self.dW, self.dW_r, self.ws)
+                                         self.dconv, self.dW, self.dW_r, self.ws, saved_active=self.act)
 
 
 class StackStep:

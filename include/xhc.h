@@ -301,8 +301,8 @@ int xhc_sublayer_fwd_noalloc(const xhc_shape_t* sh, const void* X_in,
  *            (required).
  * Other arguments as in xhc_sublayer_fwd.  bf16 with C a multiple of 64
  * (XHC_ERR_DTYPE otherwise); not combined with gram_schmidt (XHC_ERR_ARG);
- * bad `fixed` lists give XHC_ERR_INDEX.  The router's projection is a second
- * pass over X.
+ * bad `fixed` lists give XHC_ERR_INDEX.  The router's logits come from the
+ * same projection pass as the coefficients (W_r adds N rows to it).
  */
 size_t xhc_fwd_routed_workspace_bytes(const xhc_shape_t* sh);
 int xhc_sublayer_fwd_routed(const xhc_shape_t* sh, const void* X_in,
@@ -354,7 +354,14 @@ int xhc_stack_fwd(const xhc_shape_t* sh, int L, void* X,
  * xhc_sublayer_bwd_routed -- exact reverse mode of xhc_sublayer_fwd_routed
  * (the active sets are the forward's, a constant; unchosen scores get no
  * gradient).
- *   X_pre    [B,S,N,C] dtype: the state BEFORE the update.
+ *   X_state  [B,S,N,C] dtype.  If saved_active is NULL it is the state BEFORE
+ *            the update and is only read.  Otherwise it is the state AFTER an
+ *            in-place forward (X_out == X_in): the call first writes the
+ *            saved old active rows back at each token's slots, so that on
+ *            return X_state holds the state before the update (what the
+ *            backward of the sublayer below reads).  Slot entries of tok_idx
+ *            outside [0, N) are skipped by that write.
+ *   saved_active  [B,S,k,C] dtype from the in-place forward, or NULL.
  *   saved, tok_idx, rrec  the forward's outputs (required).
  *   dW_r     [N, N*C] fp32, written.
  * Other arguments as in xhc_sublayer_bwd.  bf16 with C a multiple of 128 and
@@ -362,8 +369,8 @@ int xhc_stack_fwd(const xhc_shape_t* sh, int L, void* X,
  * xhc_bwd_routed_workspace_bytes() bytes.
  */
 size_t xhc_bwd_routed_workspace_bytes(const xhc_shape_t* sh);
-int xhc_sublayer_bwd_routed(const xhc_shape_t* sh, const void* X_pre,
-                            const void* out, const float* w4, const float* w8,
+int xhc_sublayer_bwd_routed(const xhc_shape_t* sh, void* X_state,
+                            const void* saved_active, const void* out, const float* w4, const float* w8,
                             const float* w12, const float* W,
                             const float* W_r, const int32_t* fixed,
                             int n_fixed, const float* saved,

@@ -90,7 +90,7 @@ def _load() -> ctypes.CDLL:
     lib.xhc_bwd_routed_workspace_bytes.restype = Z
     lib.xhc_bwd_routed_workspace_bytes.argtypes = [sh]
     lib.xhc_sublayer_bwd_routed.restype = I
-    lib.xhc_sublayer_bwd_routed.argtypes = [sh, P, P, P, P, P, P, P, P, I, P, P, P, P, P, P, P, P, P, P, P, P, P, Z,
+    lib.xhc_sublayer_bwd_routed.argtypes = [sh, P, P, P, P, P, P, P, P, P, I, P, P, P, P, P, P, P, P, P, P, P, P, P, Z,
                                             P]
     lib.xhc_hres_active_weights.restype = I
     lib.xhc_hres_active_weights.argtypes = [sh, P, P, P, P, P]

@@ -202,17 +202,19 @@ def xhc_bwd_routed_workspace_bytes(sh) -> int:
     return LIB.xhc_bwd_routed_workspace_bytes(ctypes.byref(sh))
 
 
-def xhc_sublayer_bwd_routed(sh, X_pre, out, conv, W, W_r, fixed, saved, tok_idx, rrec, dXp, dx_in, dX, dout, dconv,
-                            dW, dW_r, workspace, stream=None):
-    """Reverse of xhc_sublayer_fwd_routed (see the C header); X_pre is the
-    state before the update."""
+def xhc_sublayer_bwd_routed(sh, X_state, out, conv, W, W_r, fixed, saved, tok_idx, rrec, dXp, dx_in, dX, dout, dconv,
+                            dW, dW_r, workspace, saved_active=None, stream=None):
+    """Reverse of xhc_sublayer_fwd_routed (see the C header).  Without
+    ``saved_active`` X_state is the state before the update; with it, the
+    state after an in-place forward, which the call turns back into the state
+    before the update."""
     w4, w8, w12 = _conv(conv)
     d4, d8, d12 = _conv(dconv)
     fixed = [int(a) for a in fixed]
     fx = (ctypes.c_int32 * max(len(fixed), 1))(*fixed) if fixed else None
     ws_bytes = workspace.numel() * workspace.element_size()
     _check("xhc_sublayer_bwd_routed",
-           LIB.xhc_sublayer_bwd_routed(ctypes.byref(sh), _p(X_pre), _p(out), w4, w8, w12, _p(W), _p(W_r), fx,
+           LIB.xhc_sublayer_bwd_routed(ctypes.byref(sh), _p(X_state), _p(saved_active), _p(out), w4, w8, w12, _p(W), _p(W_r), fx,
                                        len(fixed), _p(saved), _p(tok_idx), _p(rrec), _p(dXp), _p(dx_in), _p(dX),
                                        _p(dout), d4, d8, d12, _p(dW), _p(dW_r), _p(workspace), ws_bytes,
                                        _s(stream)))

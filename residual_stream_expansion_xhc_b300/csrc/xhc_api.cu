@@ -735,7 +735,7 @@ size_t xhc_bwd_routed_workspace_bytes(const xhc_shape_t* sh) {
   return routed_bwd_layout(sh).total;
 }
 
-int xhc_sublayer_bwd_routed(const xhc_shape_t* sh, const void* X_pre, const void* out, const float* w4,
+int xhc_sublayer_bwd_routed(const xhc_shape_t* sh, void* X_state, const void* saved_active, const void* out, const float* w4,
                             const float* w8, const float* w12, const float* W, const float* W_r,
                             const int32_t* fixed, int n_fixed, const float* saved, const int32_t* tok_idx,
                             const float* rrec, const void* dXp, const void* dx_in, void* dX, void* dout,
@@ -750,8 +750,8 @@ int xhc_sublayer_bwd_routed(const xhc_shape_t* sh, const void* X_pre, const void
   if ((s = check_conv(dw4, dw8, dw12, &has_dconv))) return s;
   if (has_conv != has_dconv) return XHC_ERR_ARG;
   if (dX == dXp) return XHC_ERR_ARG;
-  if ((s = check_ptrs({X_pre, out, W, W_r, saved, tok_idx, rrec, dXp, dX, dout, dW, dW_r, workspace},
-                      {w4, w8, w12, dx_in, dw4, dw8, dw12})))
+  if ((s = check_ptrs({X_state, out, W, W_r, saved, tok_idx, rrec, dXp, dX, dout, dW, dW_r, workspace},
+                      {w4, w8, w12, dx_in, dw4, dw8, dw12, saved_active})))
     return s;
   const Params p = make_params(sh, nullptr);
   if (!(sh->dtype == XHC_BF16 && tc_bwd_supported(p)) || p.P + p.N > 64) return XHC_ERR_DTYPE;
@@ -779,7 +779,7 @@ int xhc_sublayer_bwd_routed(const xhc_shape_t* sh, const void* X_pre, const void
   float* cm = (float*)(ws + R.cm);
   float* cr = (float*)(ws + R.cr);
   float* rs = (float*)(ws + R.rs);
-  BwdArgs<T> a{(const T*)X_pre, nullptr, (const T*)out, {w4, w8, w12}, W, saved, (const T*)dXp, (const T*)dx_in,
+  BwdArgs<T> a{(const T*)X_state, nullptr, (const T*)out, {w4, w8, w12}, W, saved, (const T*)dXp, (const T*)dx_in,
                (T*)dX, (T*)dout, {dw4, dw8, dw12}, dW, (float*)(ws + L.rec)};
   a.tok_idx = tok_idx;
   a.rrec = rrec;
@@ -791,6 +791,8 @@ int xhc_sublayer_bwd_routed(const xhc_shape_t* sh, const void* X_pre, const void
   rb.rs = rs;
   rb.cm = cm;
   const int sms = num_sms();
+  // after an in-place forward: the state before the update first
+  if (saved_active && (s = cuda_status(launch_restore_active(p, X_state, saved_active, tok_idx, sms, st)))) return s;
   if ((s = cuda_status(launch_bwd_prep(p, W, W_r, Wt, saved, coef, st)))) return s;
   if ((s = cuda_status(launch_route_scale(p, tok_idx, rrec, n_fixed, coef, st)))) return s;
   if ((s = cuda_status(launch_router_rowsums(p, W_r, rs, st)))) return s;

@@ -2,6 +2,9 @@
 //   rowsum_kernel          row sums of W_r (the LayerNorm mean term)
 //   route_kernel           per token: LayerNorm scores, fixed + top-k slots,
 //                          routed write-back scaled into H^post
+//   restore_active_kernel  backward of an in-place routed update: the saved
+//                          old active rows back into the state at each
+//                          token's slots
 //
 // Method: "xHC: Expanded Hyper-Connections" (qingkeai.online), section "Dense
 // read, sparse write": the router reads the LayerNorm-ed whole state and
@@ -133,6 +136,35 @@ cudaError_t launch_route_scale(const Params& p, const int32_t* tok_idx, const fl
                                cudaStream_t st) {
   const size_t T_all = (size_t)p.B * p.S;
   route_scale_kernel<<<(unsigned)((T_all + 63) / 64), 64, 0, st>>>(p, tok_idx, rrec, nf, coef, T_all);
+  return cudaGetLastError();
+}
+
+// One thread per 16-byte piece of a saved row: piece q of row (t, i) goes to
+// X[t, tok_idx[t, i]].  Slot indices outside [0, N) are skipped.
+__global__ void __launch_bounds__(256) restore_active_kernel(uint4* __restrict__ X, const uint4* __restrict__ sa,
+                                                             const int32_t* __restrict__ tok_idx, size_t rows,
+                                                             int N, int k, int vpr) {
+  const size_t n_all = rows * (size_t)vpr;
+  for (size_t e = (size_t)blockIdx.x * blockDim.x + threadIdx.x; e < n_all; e += (size_t)gridDim.x * blockDim.x) {
+    const size_t r = e / (size_t)vpr;                  // row t * k + i of saved_active
+    const int q = (int)(e - r * (size_t)vpr);
+    const int n = __ldg(tok_idx + r);
+    if (n < 0 || n >= N) continue;
+    const size_t t = r / (size_t)k;
+    X[(t * N + n) * vpr + q] = sa[e];
+  }
+}
+
+cudaError_t launch_restore_active(const Params& p, void* X, const void* saved_active, const int32_t* tok_idx, int sms,
+                                  cudaStream_t st) {
+  const size_t rows = (size_t)p.B * p.S * p.k;
+  const int vpr = p.C * 2 / 16;                        // bf16 rows, C a multiple of 8
+  if (rows == 0) return cudaSuccess;
+  const size_t n_all = rows * (size_t)vpr;
+  const unsigned grid = (unsigned)std::min<size_t>((n_all + 255) / 256, (size_t)sms * 8);
+  timing_begin("restore_active", st);
+  restore_active_kernel<<<grid, 256, 0, st>>>((uint4*)X, (const uint4*)saved_active, tok_idx, rows, p.N, p.k, vpr);
+  timing_end(st);
   return cudaGetLastError();
 }
 

@@ -20,4 +20,10 @@ cudaError_t launch_route_scale(const Params& p, const int32_t* tok_idx, const fl
                                cudaStream_t st);
 cudaError_t launch_router_rowsums(const Params& p, const float* W_r, float* rs, cudaStream_t st);
 
+// The state before an in-place routed update from the state after it: the
+// saved old active rows saved_active [T, k, C] (bf16) written back into
+// X [T, N, C] at each token's slots tok_idx [T, k].
+cudaError_t launch_restore_active(const Params& p, void* X, const void* saved_active, const int32_t* tok_idx, int sms,
+                                  cudaStream_t st);
+
 }  // namespace xhc

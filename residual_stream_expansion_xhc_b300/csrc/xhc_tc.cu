@@ -1420,12 +1420,20 @@ __global__ void __launch_bounds__(bwdtc::THREADS, 1)
         const bool live = t < T_all;
         float alpha = 0.0f, hp = 0.0f, beta = 0.0f;   // loaded before the waits
         bool act_row = false;                   // router: stream n active for this token
+        // router: an active row's base is the mix the column pass wrote to
+        // dX; this thread's 64 channels of it, loaded before the waits too
+        uint4 mix[ROUTED ? 2 * CC : 1];
         if (live) {
           alpha = a.rec[t * rl];
           if (a.dx_in) hp = a.rec[t * rl + 1 + n];
           if (ROUTED) {
             beta = a.rec[t * rl + 1 + N];
             for (int i = 0; i < k; ++i) act_row |= a.tok_idx[t * k + i] == n;
+            if (act_row) {
+              const uint4* src = reinterpret_cast<const uint4*>(a.dX + (t * N + n) * (size_t)C + c0 + part * CC * 16);
+#pragma unroll
+              for (int v = 0; v < 2 * CC; ++v) mix[v] = src[v];
+            }
           }
         }
         if (!mbar_wait(&full[s], ph, err, 27)) { ok = false; break; }
@@ -1433,8 +1441,9 @@ __global__ void __launch_bounds__(bwdtc::THREADS, 1)
         if (!mbar_wait(&mma_done[s], ph, err, 32)) { ok = false; break; }
         tc_fence_after();
         uint8_t* st = smem + s * STAGE_BYTES;
-#pragma unroll 1
-        for (int cc = part * CC; cc < (part + 1) * CC; ++cc) {
+#pragma unroll
+        for (int ci = 0; ci < CC; ++ci) {
+          const int cc = part * CC + ci;
           uint32_t d[16];
           tmem_ld16(tmem + lane_base + buf * 128 + cc * 16, d);
           const int h = cc >> 2;                        // which 64-column box
@@ -1447,10 +1456,8 @@ __global__ void __launch_bounds__(bwdtc::THREADS, 1)
           uint4 b0 = *reinterpret_cast<const uint4*>(br + o0);
           uint4 b1 = *reinterpret_cast<const uint4*>(br + o1);
           if (ROUTED && act_row) {
-            // an active row's base is the mix the column pass wrote to dX
-            const uint4* src = reinterpret_cast<const uint4*>(a.dX + (t * N + n) * (size_t)C + c0 + cc * 16);
-            b0 = src[0];
-            b1 = src[1];
+            b0 = mix[2 * ci];
+            b1 = mix[2 * ci + 1];
           }
           const uint32_t xw[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
           const uint32_t bw[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};

@@ -205,8 +205,8 @@ def test_router_rejections(lib):
     fx = (ctypes.c_int32 * 2)(0, 1)
     # P + N > 64 has no room for the router rows in the backward (N = 16, k = 4 fits; N = 8, k = 4 fits;
     # N = 12, k = 4: P = 44, 44 + 12 = 56 fits) -- fp32 is refused
-    assert L.xhc_sublayer_bwd_routed(ctypes.byref(shape(lib, dtype=0)), FAKE, FAKE, None, None, None, FAKE, FAKE,
-                                     fx, 2, FAKE, FAKE, FAKE, ctypes.c_void_p(1 << 22), None, FAKE, FAKE, None, None,
+    assert L.xhc_sublayer_bwd_routed(ctypes.byref(shape(lib, dtype=0)), FAKE, None, FAKE, None, None, None, FAKE,
+                                     FAKE, fx, 2, FAKE, FAKE, FAKE, ctypes.c_void_p(1 << 22), None, FAKE, FAKE, None, None,
                                      None, FAKE, FAKE, FAKE, bneed, None) == 4
 
 

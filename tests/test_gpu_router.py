@@ -113,7 +113,11 @@ def test_routed_forward_parity(name):
 
 @pytest.mark.parametrize("name", list(CASES))
 @pytest.mark.parametrize("with_dxin", [False, True])
-def test_routed_backward_parity(name, with_dxin):
+@pytest.mark.parametrize("in_place", [False, True])
+def test_routed_backward_parity(name, with_dxin, in_place):
+    """in_place: the backward gets the state after the in-place forward and
+    the saved active rows, and must leave the state before the update in it,
+    bit for bit."""
     wl, nf = CASES[name]
     t = xin.make(wl, grads=True, dx_in=with_dxin)
     W_r = _router_weights(wl)
@@ -130,10 +134,13 @@ def test_routed_backward_parity(name, with_dxin):
     dconv = None if conv is None else tuple(torch.empty_like(w) for w in conv)
     dW, dW_r = torch.empty_like(W), torch.empty_like(Wr)
     ws = api.workspace(api.xhc_bwd_routed_workspace_bytes(sh))
-    api.xhc_sublayer_bwd_routed(sh, g["X0"], out, conv, W, Wr, fixed, g["saved"], g["tok_idx"], g["rrec_dev"], dXp,
-                                dxi, dX, dout, dconv, dW, dW_r, ws)
+    state = g["Xp"] if in_place else g["X0"]
+    api.xhc_sublayer_bwd_routed(sh, state, out, conv, W, Wr, fixed, g["saved"], g["tok_idx"], g["rrec_dev"], dXp,
+                                dxi, dX, dout, dconv, dW, dW_r, ws, saved_active=g["act"] if in_place else None)
     torch.cuda.synchronize()
     api.xhc_device_status()
+    if in_place:
+        assert torch.equal(state.view(torch.int16), g["X0"].view(torch.int16))
     X, out64, conv64, W64, _ = oracle_inputs(wl, t)
     ref = xo.backward_routed(X, out64, conv64, W64, W_r.astype(np.float64), fixed, wl.k, xin.to_f64(wl, t.dXp),
                              xin.to_f64(wl, t.dx_in) if with_dxin else None, iters=wl.iters, eps=wl.eps,
@@ -151,7 +158,9 @@ def test_routed_backward_parity(name, with_dxin):
 def test_routed_full_shape_one_sequence():
     """One sequence of the router workload at full width (S = 4096, C = 2048):
     forward and backward against the oracle on every token, with the GPU's
-    active sets (their own check is the forward test's)."""
+    active sets (their own check is the forward test's).  In place, as in
+    training: the backward gets the updated state and the saved active rows
+    and leaves the state before the update."""
     wl = xin.scaled(xin.WORKLOADS["router_bf16"], B=1)
     t = xin.make(wl, grads=True)
     W_r = t.extra["W_r"]
@@ -166,10 +175,12 @@ def test_routed_full_shape_one_sequence():
     dconv = tuple(torch.empty_like(w) for w in conv_d)
     dW, dW_r = torch.empty_like(W_d), torch.empty_like(Wr_d)
     ws = api.workspace(api.xhc_bwd_routed_workspace_bytes(sh))
-    api.xhc_sublayer_bwd_routed(sh, g["X0"], out_d, conv_d, W_d, Wr_d, fixed, g["saved"], g["tok_idx"],
-                                g["rrec_dev"], dXp, None, dX, dout, dconv, dW, dW_r, ws)
+    Xp = host_f64(g["Xp"])
+    api.xhc_sublayer_bwd_routed(sh, g["Xp"], out_d, conv_d, W_d, Wr_d, fixed, g["saved"], g["tok_idx"],
+                                g["rrec_dev"], dXp, None, dX, dout, dconv, dW, dW_r, ws, saved_active=g["act"])
     torch.cuda.synchronize()
     api.xhc_device_status()
+    assert torch.equal(g["Xp"].view(torch.int16), g["X0"].view(torch.int16))
     W_r64 = W_r.astype(np.float64)
     # forward: the routed update reproduced with the GPU's active sets
     ref_s, ref_r, _, _ = xo.router_scores(X[0], W_r64, wl.eps)
@@ -177,7 +188,7 @@ def test_routed_full_shape_one_sequence():
     ltol, _ = _logit_tol(g, ref_r[None], wl.N)
     check_selection(g["idx"], ref_r[None], fixed, wl.k, ltol)
     fr = xo.forward_routed(X, out, conv, W, W_r64, fixed, wl.k, iters=wl.iters, eps=wl.eps, idx=g["idx"])
-    Xp, X0 = host_f64(g["Xp"]), host_f64(g["X0"])
+    X0 = host_f64(g["X0"])
     inactive = np.ones((wl.B, wl.S, wl.N), dtype=bool)
     np.put_along_axis(inactive, g["idx"].astype(np.int64), False, axis=-1)
     assert np.array_equal(Xp[inactive], X0[inactive])
