@@ -567,7 +567,10 @@ __global__ void __launch_bounds__(coeffs::THREADS, 1)
 // pass: warp 0 TMA producer (state tiles, W_{l+1} image, the chunk's `out`
 // tile with 16 rows of history and its tap-major conv weights), warp 1 MMA
 // issuer, warps 2..9 math (two threads per token row, 32 channels each):
-// dense read, update, sum of squares, then the epilogue.
+// dense read, update, sum of squares, then the epilogue; warp 10 stores the
+// rewritten active tiles (TMA) and releases their stages once the stores
+// have read them, on behalf of the math warps, which go straight on to the
+// other streams.
 namespace flash {
 constexpr int TILE_T = 128;
 constexpr int KC = 64;
@@ -582,7 +585,8 @@ constexpr int OFF_OUT = STAGES * STAGE_BYTES;
 constexpr int OFF_TAP = OFF_OUT + OUT_BYTES;
 constexpr int SMEM = OFF_TAP + TAP_BYTES + 1024;
 constexpr int MATH_WARPS = 8;
-constexpr int THREADS = 64 + 32 * MATH_WARPS;
+constexpr int STORE_WARP = 2 + MATH_WARPS;
+constexpr int THREADS = 64 + 32 * MATH_WARPS + 32;
 constexpr int TMEM_COLS = 128;
 }  // namespace flash
 
@@ -705,11 +709,29 @@ __global__ void __launch_bounds__(flash::THREADS, 1)
       umma_commit(&mdrain);
       mbar_wait_drain(&mdrain, 0);
     }
+  } else if (warp == STORE_WARP) {
+    // ------------------------------------------------ active tile stores
+    if (lane == 0) {
+      int it = 0, oc = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x) {
+        for (int cc = 0; cc < cchunks; ++cc, ++oc, it += N) {
+          // every math warp has rewritten its rows of the chunk's k active tiles
+          if (!mbar_wait(&updated, oc & 1, err, 31)) { ok = false; break; }
+          for (int i = 0; i < k; ++i)
+            tma_store_3d(&mapX, smem + ((it + i) % STAGES) * STAGE_BYTES, cc * KC, ord[i], tile * rows);
+          tma_store_commit();
+          tma_store_wait_read0();
+          // the math warps' releases of these stages (the MMA commits its own)
+          for (int i = 0; i < k; ++i) mbar_arrive_cnt(&empty[(it + i) % STAGES], MATH_WARPS);
+        }
+      }
+      tma_store_wait0();
+    }
   } else {
     // ------------------------------------------------ math: dense read, update, sum of squares, epilogue
     const int row = 32 * (warp & 3) + lane;             // token row == TMEM lane
     const int half = (warp - 2) >> 2;                   // channels 32 half .. 32 half + 31 of each chunk
-    const int mt = threadIdx.x - 64;
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;
     int it = 0, tl = 0, oc = 0;
     for (int tile = blockIdx.x; tile < ntiles; tile += gridDim.x, ++tl) {
@@ -744,36 +766,37 @@ __global__ void __launch_bounds__(flash::THREADS, 1)
         for (int q = 0; q < 4; ++q) {
           const int gl = half * 4 + q;                    // 16-byte group of the row (8 channels)
           const uint32_t off = row * 128 + ((gl ^ (row & 7)) << 4);
-          float o[KMAX][8];
+          // channel pairs (2e, 2e + 1) in fp32x2: each lane is the scalar
+          // fmaf of that channel, in the same order
+          float2 o[KMAX][4];
 #pragma unroll
           for (int i = 0; i < KMAX; ++i) {
             uint4 v = make_uint4(0, 0, 0, 0);
             if (i < k) v = *reinterpret_cast<const uint4*>(smem + ((it + i) % STAGES) * STAGE_BYTES + off);
             const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              o[i][2 * e] = bf_lo(w[e]);
-              o[i][2 * e + 1] = bf_hi(w[e]);
-            }
+            for (int e = 0; e < 4; ++e) o[i][e] = make_float2(bf_lo(w[e]), bf_hi(w[e]));
 #pragma unroll
-            for (int e = 0; e < 8; ++e) xacc[8 * q + e] = fmaf(hact[i], o[i][e], xacc[8 * q + e]);
+            for (int e = 0; e < 4; ++e) {
+              float2 xa = make_float2(xacc[8 * q + 2 * e], xacc[8 * q + 2 * e + 1]);
+              xa = __ffma2_rn(make_float2(hact[i], hact[i]), o[i][e], xa);
+              xacc[8 * q + 2 * e] = xa.x;
+              xacc[8 * q + 2 * e + 1] = xa.y;
+            }
           }
           // TFA components of this token's 8 channels; row r of the tile is
           // row r + HALO_R of the out tile, tap tau reads row r + HALO_R - tau
-          float u[4][8];
+          float2 u[4][4];
           {
             const uint4 v = *reinterpret_cast<const uint4*>(os + (row + HALO_R) * 128 + ((gl ^ (row & 7)) << 4));
             const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              u[0][2 * e] = bf_lo(w[e]);
-              u[0][2 * e + 1] = bf_hi(w[e]);
-            }
+            for (int e = 0; e < 4; ++e) u[0][e] = make_float2(bf_lo(w[e]), bf_hi(w[e]));
           }
 #pragma unroll
           for (int c = 1; c < 4; ++c)
 #pragma unroll
-            for (int e = 0; e < 8; ++e) u[c][e] = 0.0f;
+            for (int e = 0; e < 4; ++e) u[c][e] = make_float2(0.0f, 0.0f);
           if (HAS_CONV) {
 #pragma unroll
             for (int tau = 0; tau < 12; ++tau) {
@@ -781,12 +804,9 @@ __global__ void __launch_bounds__(flash::THREADS, 1)
               uint4 v = *reinterpret_cast<const uint4*>(os + r * 128 + ((gl ^ (r & 7)) << 4));
               if (tau > spos) v = make_uint4(0, 0, 0, 0);   // before the start of the sequence
               const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-              float x[8];
+              float2 x[4];
 #pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                x[2 * e] = bf_lo(w[e]);
-                x[2 * e + 1] = bf_hi(w[e]);
-              }
+              for (int e = 0; e < 4; ++e) x[e] = make_float2(bf_lo(w[e]), bf_hi(w[e]));
               // tap rows: w4 taps at rows 0..3, w8 at 4..11, w12 at 12..23
 #pragma unroll
               for (int c = 1; c < 4; ++c) {
@@ -794,9 +814,10 @@ __global__ void __launch_bounds__(flash::THREADS, 1)
                 if (tau < K) {
                   const float4 a = *reinterpret_cast<const float4*>(tp + (r0 + tau) * KC + gl * 8);
                   const float4 b = *reinterpret_cast<const float4*>(tp + (r0 + tau) * KC + gl * 8 + 4);
-                  const float wv[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
-#pragma unroll
-                  for (int e = 0; e < 8; ++e) u[c][e] = fmaf(wv[e], x[e], u[c][e]);
+                  u[c][0] = __ffma2_rn(make_float2(a.x, a.y), x[0], u[c][0]);
+                  u[c][1] = __ffma2_rn(make_float2(a.z, a.w), x[1], u[c][1]);
+                  u[c][2] = __ffma2_rn(make_float2(b.x, b.y), x[2], u[c][2]);
+                  u[c][3] = __ffma2_rn(make_float2(b.z, b.w), x[3], u[c][3]);
                 }
               }
             }
@@ -805,21 +826,21 @@ __global__ void __launch_bounds__(flash::THREADS, 1)
 #pragma unroll
           for (int i = 0; i < KMAX; ++i) {
             if (i < k) {
-              float y[8];
+              float2 y[4];
 #pragma unroll
-              for (int e = 0; e < 8; ++e) {
-                float acc = 0.0f;
+              for (int e = 0; e < 4; ++e) {
+                float2 acc = make_float2(0.0f, 0.0f);
 #pragma unroll
-                for (int j = 0; j < KMAX; ++j) acc = fmaf(hres[i][j], o[j][e], acc);
+                for (int j = 0; j < KMAX; ++j) acc = __ffma2_rn(make_float2(hres[i][j], hres[i][j]), o[j][e], acc);
 #pragma unroll
-                for (int c = 0; c < 4; ++c) acc = fmaf(hpost[i][c], u[c][e], acc);
+                for (int c = 0; c < 4; ++c) acc = __ffma2_rn(make_float2(hpost[i][c], hpost[i][c]), u[c][e], acc);
                 y[e] = acc;
               }
               uint4 v;
-              v.x = pack_bf2(y[0], y[1]);
-              v.y = pack_bf2(y[2], y[3]);
-              v.z = pack_bf2(y[4], y[5]);
-              v.w = pack_bf2(y[6], y[7]);
+              v.x = pack_bf2(y[0].x, y[0].y);
+              v.y = pack_bf2(y[1].x, y[1].y);
+              v.z = pack_bf2(y[2].x, y[2].y);
+              v.w = pack_bf2(y[3].x, y[3].y);
               const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
@@ -836,24 +857,8 @@ __global__ void __launch_bounds__(flash::THREADS, 1)
         if (lane == 0) {
           for (int i = 0; i < k; ++i) mbar_arrive(&bready[(it + i) % STAGES]);
           mbar_arrive(&oempty);
-          mbar_arrive(&updated);
+          mbar_arrive(&updated);          // the store warp stores the rows and releases the stages
         }
-        // once every math warp has written its rows, one thread stores the new
-        // rows in place; its warp releases the stages after the store has read them
-        if (mt == 0) {
-          if (mbar_wait(&updated, oc & 1, err, 31)) {
-            for (int i = 0; i < k; ++i)
-              tma_store_3d(&mapX, smem + ((it + i) % STAGES) * STAGE_BYTES, cc * KC, ord[i], tile * rows);
-            tma_store_commit();
-            tma_store_wait_read0();
-          } else {
-            ok = false;
-          }
-        }
-        ok = __shfl_sync(FULL, ok, 0);
-        if (!ok) break;
-        if (lane == 0)
-          for (int i = 0; i < k; ++i) mbar_arrive(&empty[(it + i) % STAGES]);
         it += k;
         // ---- the other streams: dense read and sum of squares
         for (int j = k; j < N; ++j, ++it) {
@@ -872,8 +877,10 @@ __global__ void __launch_bounds__(flash::THREADS, 1)
               const float a = bf_lo(w[e]), b = bf_hi(w[e]);
               ss = fmaf(a, a, ss);
               ss = fmaf(b, b, ss);
-              xacc[8 * q + 2 * e] = fmaf(h, a, xacc[8 * q + 2 * e]);
-              xacc[8 * q + 2 * e + 1] = fmaf(h, b, xacc[8 * q + 2 * e + 1]);
+              const float2 xa = __ffma2_rn(make_float2(h, h), make_float2(a, b),
+                                           make_float2(xacc[8 * q + 2 * e], xacc[8 * q + 2 * e + 1]));
+              xacc[8 * q + 2 * e] = xa.x;
+              xacc[8 * q + 2 * e + 1] = xa.y;
             }
           }
           __syncwarp();
@@ -922,7 +929,6 @@ __global__ void __launch_bounds__(flash::THREADS, 1)
       if (lane == 0) mbar_arrive(&tempty[buf]);
       if (live) coeffs_epilogue(p, pz, ss, t, f.next);
     }
-    if (mt == 0) tma_store_wait0();
   }
   tc_fence_before();
   __syncthreads();
