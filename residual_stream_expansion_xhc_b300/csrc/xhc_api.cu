@@ -463,7 +463,7 @@ namespace {
 // token), W^T (bf16 hi and lo parts, 64 each per column), the coefficient block, the column pass's coefficient dots and
 // conv partials, dW partials (one per token range).
 struct BwdLayout {
-  size_t rec, saved, dP, Wt, coef, pdot, cpart, wpart, wsplit, gpart, gsrec, sgram, gsdh, total;
+  size_t rec, saved, dP, Wt, coef, pdot, cpart, wpart, wsplit, gpart, gsrec, sgram, gsdh, ctaps, total;
   int ranges, cpart_rows, col_rows;
 };
 BwdLayout bwd_layout(const xhc_shape_t* sh) {
@@ -490,7 +490,8 @@ BwdLayout bwd_layout(const xhc_shape_t* sh) {
     L.gsrec = L.gpart + gs_gpart_bytes(sh);
     L.sgram = L.gsrec + (sh->gram_schmidt ? round_up(T * GS_REC * sizeof(float)) : 0);
     L.gsdh = L.sgram + (sh->gram_schmidt ? round_up(T * 16 * sizeof(float)) : 0);
-    L.total = L.gsdh + (sh->gram_schmidt ? round_up(T * 16 * sizeof(float)) : 0);
+    L.ctaps = L.gsdh + (sh->gram_schmidt ? round_up(T * 16 * sizeof(float)) : 0);
+    L.total = L.ctaps + round_up(bwd_col_taps_floats(p) * sizeof(float));
   } else {
     L.rec = 0;
     L.saved = round_up(T * (size_t)(2 * p.P + 1) * sizeof(float));
@@ -673,7 +674,8 @@ int xhc_sublayer_bwd(const xhc_shape_t* sh, const void* X_state, const void* sav
         if ((s = cuda_status(launch_gs_gram(p, (const T*)out, w, (float*)(ws + L.gpart), st)))) return s;
         if ((s = cuda_status(launch_gs_fold(p, (const float*)(ws + L.gpart), coef, gsrec, st)))) return s;
       }
-      if ((s = cuda_status(launch_bwd_col(p, a, coef, has_conv, pdot, cpart, sms, st)))) return s;
+      if ((s = cuda_status(launch_bwd_col(p, a, coef, has_conv, pdot, cpart, (float*)(ws + L.ctaps), sms, st))))
+        return s;
       if (gs && (s = cuda_status(launch_gs_rev(p, z, pdot, gsrec, gsdh, sgram, st)))) return s;
       if ((s = cuda_status(launch_bwd_dz(p, z, pdot, dx_in != nullptr, dP, rec, gsdh, RouterBwd{}, st)))) return s;
       if (gs && (s = cuda_status(launch_gs_bwd(p, (const T*)out, w, sgram, (T*)dout,
@@ -796,7 +798,8 @@ int xhc_sublayer_bwd_routed(const xhc_shape_t* sh, void* X_state, const void* sa
   if ((s = cuda_status(launch_bwd_prep(p, W, W_r, Wt, saved, coef, st)))) return s;
   if ((s = cuda_status(launch_route_scale(p, tok_idx, rrec, n_fixed, coef, st)))) return s;
   if ((s = cuda_status(launch_router_rowsums(p, W_r, rs, st)))) return s;
-  if ((s = cuda_status(launch_bwd_col(p, a, coef, has_conv, pdot, cpart, sms, st)))) return s;
+  if ((s = cuda_status(launch_bwd_col(p, a, coef, has_conv, pdot, cpart, (float*)(ws + L.ctaps), sms, st))))
+    return s;
   if ((s = cuda_status(launch_bwd_dz(p, saved, pdot, dx_in != nullptr, dP, a.rec, nullptr, rb, st)))) return s;
   if ((s = cuda_status(launch_bwd_stream_tc(p, a, Wt, dP, L.ranges, wpart, st)))) return s;
   return cuda_status(launch_bwd_reduce(p, a, has_conv, cpart, L.cpart_rows, L.ranges, wpart, st, dW_r, cm, cr));

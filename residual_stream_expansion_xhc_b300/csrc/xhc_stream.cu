@@ -472,10 +472,12 @@ struct ColSmem {
   float du1[col::D1][col::CB];
   float du2[col::D2][col::CB];
   float du3[col::D3][col::CB];
-  float dconv[col::TT][2][col::CB];           // per token slot: convolution parts of dout (K4 + K8 | K12);
-                                              // in the token phase, after they are consumed: the slot's G rows
-  uint32_t xa[col::TT][KMAX][col::CB / 2];    // the slot's old active rows Xa_j, rotated
-  float tap[NTAPS][col::CB];
+  float dconv[col::TT][2][col::CB];           // per token slot: convolution parts of dout (K4 + K8 | K12)
+  // staged by cp.async one chunk ahead (each warp stages its own two slots
+  // once its coefficient dots are done): per token slot
+  uint16_t g[col::TT][KMAX][col::CB];         // the G_i rows, rotated (zero where absent)
+  uint32_t xa[col::TT][KMAX][col::CB / 2];    // the old active rows Xa_j, rotated
+  float cf[col::TT][32];                      // hpost (16) and H^res (16) of the token
 };
 
 // ldmatrix of four 8 x 8 bf16 matrices; mma.sync m16n8k16 bf16 -> fp32
@@ -493,6 +495,13 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
                : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
 }
 __device__ __forceinline__ uint32_t rot_chunk(int q, int rot) { return (uint32_t)((q + rot) & 15) << 4; }
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+               "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -562,7 +571,7 @@ template <bool HAS_CONV, bool ROUTED>
 __global__ void __launch_bounds__(col::THREADS, 3) bwd_col_kernel(Params p, BwdArgs<__nv_bfloat16> a,
                                                                   const float* __restrict__ coef,
                                                                   float* __restrict__ pdot, float* __restrict__ cpart,
-                                                                  Walk wk) {
+                                                                  const float* __restrict__ taps, Walk wk) {
   constexpr int CBc = col::CB, TTc = col::TT, ORc = col::ORING;
   extern __shared__ __align__(16) uint8_t smem_raw[];
   ColSmem& sm = *reinterpret_cast<ColSmem*>(smem_raw);
@@ -582,12 +591,6 @@ __global__ void __launch_bounds__(col::THREADS, 3) bwd_col_kernel(Params p, BwdA
   for (int q = threadIdx.x; q < (int)(sizeof(ColSmem) / 16); q += col::THREADS)
     reinterpret_cast<uint4*>(smem_raw)[q] = make_uint4(0, 0, 0, 0);
   __syncthreads();
-  if (HAS_CONV) {
-    float t[NTAPS];
-    load_taps(a.w, cb0 + threadIdx.x, C, t);
-#pragma unroll
-    for (int g = 0; g < NTAPS; ++g) sm.tap[g][threadIdx.x] = t[g];
-  }
   float2 dw[12];                                            // this group's 12 taps, two channels
 #pragma unroll
   for (int q = 0; q < 12; ++q) dw[q] = make_float2(0.0f, 0.0f);
@@ -679,10 +682,54 @@ __global__ void __launch_bounds__(col::THREADS, 3) bwd_col_kernel(Params p, BwdA
     }
   };
 
+  // the group's 12 taps of the thread's two channels, from the tap-major
+  // copy [24][C] (L1-resident after the first chunk)
   auto load_tap_pairs = [&](float2 (&tp)[12]) {
 #pragma unroll
-    for (int q = 0; q < 12; ++q) tp[q] = *reinterpret_cast<const float2*>(&sm.tap[12 * grp + q][2 * pr]);
+    for (int q = 0; q < 12; ++q) {
+      const float* src = taps + (size_t)(12 * grp + q) * C + c2;
+      tp[q] = dbg::ok(src, 8, __LINE__) ? __ldg(reinterpret_cast<const float2*>(src)) : make_float2(0.0f, 0.0f);
+    }
   };
+
+  // Stage a chunk's per-token rows into the slot buffers by cp.async: the
+  // half-warp of slot hw takes token t0s + hw (its lane 8 channels; lanes
+  // 0-7 also the token's 32 coefficients).  Rows of absent tokens, channels
+  // past C and slots i >= k are zero.  Without convolution branches u_0 (the
+  // token's out row) goes to ring row hw.
+  auto stage_rows = [&](size_t seq_base_s, int t0s, int s_end_s, const int (&as)[KMAX]) {
+    const int ts = t0s + hw;
+    const bool ok = ts < s_end_s && lane_ok;
+    const size_t tk = seq_base_s + ts;
+    const int rot_g = 4 * (hw & 1);
+#pragma unroll
+    for (int i = 0; i < KMAX; ++i) {
+      uint8_t* gd = reinterpret_cast<uint8_t*>(&sm.g[hw][i][0]) + rot_chunk(l16, i + rot_g);
+      uint8_t* xd = reinterpret_cast<uint8_t*>(&sm.xa[hw][i][0]) + rot_chunk(l16, i + 1);
+      const __nv_bfloat16* gs = a.dXp + tk * NC + (size_t)as[i] * C + c_lane;
+      const __nv_bfloat16* xs = a.saved_active ? a.saved_active + (tk * k + i) * C + c_lane
+                                               : a.X + tk * NC + (size_t)as[i] * C + c_lane;
+      if (ok && i < k && dbg::ok(gs, 16, __LINE__)) cp_async16(gd, gs);
+      else *reinterpret_cast<uint4*>(gd) = make_uint4(0, 0, 0, 0);
+      if (ok && i < k && dbg::ok(xs, 16, __LINE__)) cp_async16(xd, xs);
+      else *reinterpret_cast<uint4*>(xd) = make_uint4(0, 0, 0, 0);
+    }
+    if (l16 < 8) {
+      const float* cs = coef + tk * COEF_STRIDE + COEF_POST + 4 * l16;
+      if (ts < s_end_s && dbg::ok(cs, 16, __LINE__)) cp_async16(&sm.cf[hw][4 * l16], cs);
+      else *reinterpret_cast<float4*>(&sm.cf[hw][4 * l16]) = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    }
+    if (!HAS_CONV) {
+      const __nv_bfloat16* os = a.out + tk * C + c_lane;
+      if (ok && dbg::ok(os, 16, __LINE__)) cp_async16(&sm.ring[hw][8 * l16], os);
+      else *reinterpret_cast<uint4*>(&sm.ring[hw][8 * l16]) = make_uint4(0, 0, 0, 0);
+    }
+    cp_async_commit();
+  };
+  bool have_pre = false;                                    // this chunk's rows were staged ahead
+  int ai_nx[KMAX];                                          // router: the slots of the next chunk's token
+#pragma unroll
+  for (int i = 0; i < KMAX; ++i) ai_nx[i] = 0;
 
   const long g_beg = (long)blockIdx.x * wk.per;
   const long g_total = (long)p.B * wk.nch;
@@ -744,36 +791,39 @@ __global__ void __launch_bounds__(col::THREADS, 3) bwd_col_kernel(Params p, BwdA
     const int t = t0 + hw;
     const bool tok_ok = t < s_end;             // per half-warp
     const size_t tok = seq_base + (tok_ok ? t : t0);
-    const float* cf = coef + tok * COEF_STRIDE;
     int ai[KMAX];                             // this token's active streams
 #pragma unroll
-    for (int i = 0; i < KMAX; ++i) ai[i] = ROUTED ? (i < k ? ld_i(a.tok_idx + tok * k + i) : 0) : p.idx[i];
-    float2 G[KMAX][4];
-    uint4 gr[KMAX], xr[KMAX];                 // raw bf16 rows; zero where absent
+    for (int i = 0; i < KMAX; ++i)
+      ai[i] = ROUTED ? (have_pre ? ai_nx[i] : (i < k ? ld_i(a.tok_idx + tok * k + i) : 0)) : p.idx[i];
+    // this chunk's rows: staged during the previous chunk, or now
+    if (!have_pre) stage_rows(seq_base, t0, s_end, ai);
+    cp_async_wait_all();
+    __syncwarp();
+    if (ROUTED && has_next) {
+      // the slots of the next chunk's token (a full chunk of this sequence)
+      const size_t tn = seq_base + (t0 - TTc) + hw;
 #pragma unroll
-    for (int i = 0; i < KMAX; ++i) {
-      gr[i] = make_uint4(0, 0, 0, 0);
-      xr[i] = make_uint4(0, 0, 0, 0);
+      for (int i = 0; i < KMAX; ++i) ai_nx[i] = i < k ? ld_i(a.tok_idx + tn * k + i) : 0;
+    }
+    const float* cs = &sm.cf[hw][0];          // hpost [0, 16), H^res [16, 32)
+    float2 G[KMAX][4];
+#pragma unroll
+    for (int i = 0; i < KMAX; ++i)
 #pragma unroll
       for (int q = 0; q < 4; ++q) G[i][q] = make_float2(0.0f, 0.0f);
-    }
     if (tok_ok && lane_ok) {
-#pragma unroll
-      for (int i = 0; i < KMAX; ++i) {
-        if (i < k) {
-          gr[i] = ld_na(a.dXp + tok * NC + (size_t)ai[i] * C + c_lane);
-          xr[i] = a.saved_active ? ld_na(a.saved_active + (tok * k + i) * C + c_lane)
-                                 : ld_na(a.X + tok * NC + (size_t)ai[i] * C + c_lane);
-        }
-      }
+      const int rot_g = 4 * (hw & 1);
 #pragma unroll
       for (int i = 0; i < KMAX; ++i)
-        if (i < k) unpack8x2(gr[i], G[i]);
+        if (i < k)
+          unpack8x2(*reinterpret_cast<const uint4*>(reinterpret_cast<const uint8_t*>(&sm.g[hw][i][0]) +
+                                                    rot_chunk(l16, i + rot_g)),
+                    G[i]);
       // active-stream mix: dX[a_j] = sum_i Hres[i][j] G_i
       float hres[KMAX][KMAX];
 #pragma unroll
       for (int i = 0; i < KMAX; ++i) {
-        const float4 h = ld_f4(cf + COEF_RES + 4 * i);
+        const float4 h = *reinterpret_cast<const float4*>(cs + 16 + 4 * i);
         hres[i][0] = h.x; hres[i][1] = h.y; hres[i][2] = h.z; hres[i][3] = h.w;
       }
 #pragma unroll
@@ -799,7 +849,7 @@ __global__ void __launch_bounds__(col::THREADS, 3) bwd_col_kernel(Params p, BwdA
 #pragma unroll
       for (int i = 0; i < KMAX; ++i) {
         if (i < k) {
-          const float4 hp = ld_f4(cf + COEF_POST + 4 * i);
+          const float4 hp = *reinterpret_cast<const float4*>(cs + 4 * i);
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             du[0][q] = __ffma2_rn(f2(hp.x), G[i][q], du[0][q]);
@@ -832,23 +882,11 @@ __global__ void __launch_bounds__(col::THREADS, 3) bwd_col_kernel(Params p, BwdA
     // Y; the token's own rows of D are kept.  The bf16 products are exact and
     // the sums are fp32, as with the CUDA-core dots they replace.
     {
-      if (!HAS_CONV) {
-        // u_0 = out row of the token (staged in the unused ring); ring[ORING - 1] stays zero
-        const uint4 ov = (tok_ok && lane_ok) ? ld_na(a.out + tok * C + c_lane) : make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4*>(&sm.ring[hw][8 * l16]) = ov;
-      }
-      __syncwarp();                            // finalize() has read this slot's dconv rows
-      uint32_t* gs = reinterpret_cast<uint32_t*>(&sm.dconv[hw][0][0]);
-      const int rot_g = 4 * (hw & 1);
-#pragma unroll
-      for (int i = 0; i < KMAX; ++i) {
-        *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(gs + 64 * i) + rot_chunk(l16, i + rot_g)) = gr[i];
-        *reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(&sm.xa[hw][i][0]) + rot_chunk(l16, i + 1)) = xr[i];
-      }
-      __syncwarp();
+      // the staged rows (without convolution branches u_0 = the token's out
+      // row, staged in the unused ring; ring[ORING - 1] stays zero)
       const int mq = lane >> 3, rr = lane & 7;  // ldmatrix: this lane addresses row rr of matrix mq
       const int sa = 2 * warp + (rr >> 2), ia = rr & 3;
-      const uint32_t a_row = smem_u32(&sm.dconv[sa][0][0]) + 256 * ia;
+      const uint32_t a_row = smem_u32(&sm.g[sa][ia][0]);
       const int a_rot = mq + ia + 4 * (sa & 1);
       uint32_t b_row[2];
       int b_rot;
@@ -882,6 +920,16 @@ __global__ void __launch_bounds__(col::THREADS, 3) bwd_col_kernel(Params p, BwdA
       const int gi = (lane >> 2) & 3, n0 = 2 * (lane & 3);
       const int at = n0 < 4 ? 4 * gi + n0 : 16 + 4 * gi + (n0 - 4);
       if (tok_ok) st_v(reinterpret_cast<float2*>(pdot + (tok * ncb + cb) * PDOT + at), r);
+    }
+    // the warp's slots are read: stage the next chunk of the walk into them,
+    // to land while the channel phase runs
+    __syncwarp();
+    have_pre = has_next;
+    if (has_next) {
+      int an[KMAX];
+#pragma unroll
+      for (int i = 0; i < KMAX; ++i) an[i] = ROUTED ? ai_nx[i] : p.idx[i];
+      stage_rows(seq_base, t0 - TTc, t0, an);
     }
     if (a.dx_in) {
       // <dx_in, X_n> for every stream n
@@ -1270,9 +1318,26 @@ size_t bwd_col_cpart_floats(const Params& p, int sms) {
 }
 int bwd_col_cpart_rows(const Params& p, int sms) { return make_walk_col(p, sms).R; }
 
+// Conv weights w4 [C, 4], w8 [C, 8], w12 [C, 12] -> tap-major [24][C]: row g
+// is tap g of the three branches in the order of load_taps.
+__global__ void col_taps_kernel(const float* __restrict__ w4, const float* __restrict__ w8,
+                                const float* __restrict__ w12, float* __restrict__ taps, int C) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= NTAPS * C) return;
+  const int g = i / C, c = i - g * C;
+  taps[i] = g < 4 ? w4[(size_t)c * 4 + g] : (g < 12 ? w8[(size_t)c * 8 + (g - 4)] : w12[(size_t)c * 12 + (g - 12)]);
+}
+
+size_t bwd_col_taps_floats(const Params& p) { return (size_t)NTAPS * p.C; }
+
 cudaError_t launch_bwd_col(const Params& p, const BwdArgs<__nv_bfloat16>& a, const float* coef, bool has_conv,
-                           float* pdot, float* cpart, int sms, cudaStream_t st) {
+                           float* pdot, float* cpart, float* taps, int sms, cudaStream_t st) {
   const Walk wk = make_walk_col(p, sms);
+  if (has_conv) {
+    const int n = NTAPS * p.C;
+    col_taps_kernel<<<(n + 255) / 256, 256, 0, st>>>(a.w[0], a.w[1], a.w[2], taps, p.C);
+    if (cudaError_t e = cudaGetLastError()) return e;
+  }
   {
     const size_t T = (size_t)p.B * p.S, row = (size_t)p.C * 2;
     dbg::ExtentList l;
@@ -1280,6 +1345,7 @@ cudaError_t launch_bwd_col(const Params& p, const BwdArgs<__nv_bfloat16>& a, con
     l.add(a.dx_in, T * row).add(a.dX, T * p.N * row).add(a.dout, T * row).add(coef, T * COEF_STRIDE * 4);
     l.add(a.tok_idx, T * p.k * 4).add(pdot, bwd_col_pdot_floats(p) * 4).add(cpart, bwd_col_cpart_floats(p, sms) * 4);
     for (int j = 0; j < 3; ++j) l.add(a.w[j], (size_t)p.C * 4 * (j + 1) * 4);
+    if (has_conv) l.add(taps, bwd_col_taps_floats(p) * 4);
     if (cudaError_t e = dbg::set_extents(l, st)) return e;
   }
   dim3 grid(wk.R, wk.ncb);
@@ -1287,16 +1353,16 @@ cudaError_t launch_bwd_col(const Params& p, const BwdArgs<__nv_bfloat16>& a, con
   timing_begin("bwd_col", st);
   if (has_conv && a.tok_idx) {
     cudaFuncSetAttribute(bwd_col_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    bwd_col_kernel<true, true><<<grid, col::THREADS, smem, st>>>(p, a, coef, pdot, cpart, wk);
+    bwd_col_kernel<true, true><<<grid, col::THREADS, smem, st>>>(p, a, coef, pdot, cpart, taps, wk);
   } else if (a.tok_idx) {
     cudaFuncSetAttribute(bwd_col_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    bwd_col_kernel<false, true><<<grid, col::THREADS, smem, st>>>(p, a, coef, pdot, cpart, wk);
+    bwd_col_kernel<false, true><<<grid, col::THREADS, smem, st>>>(p, a, coef, pdot, cpart, taps, wk);
   } else if (has_conv) {
     cudaFuncSetAttribute(bwd_col_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    bwd_col_kernel<true, false><<<grid, col::THREADS, smem, st>>>(p, a, coef, pdot, cpart, wk);
+    bwd_col_kernel<true, false><<<grid, col::THREADS, smem, st>>>(p, a, coef, pdot, cpart, taps, wk);
   } else {
     cudaFuncSetAttribute(bwd_col_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    bwd_col_kernel<false, false><<<grid, col::THREADS, smem, st>>>(p, a, coef, pdot, cpart, wk);
+    bwd_col_kernel<false, false><<<grid, col::THREADS, smem, st>>>(p, a, coef, pdot, cpart, taps, wk);
   }
   timing_end(st);
   return cudaGetLastError();

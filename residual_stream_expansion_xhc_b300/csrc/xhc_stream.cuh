@@ -15,11 +15,14 @@ cudaError_t launch_fwd_update(const Params& p, const UpdArgs<__nv_bfloat16>& a, 
 
 // Backward column pass: active-stream mix into dX, dout, conv-weight partials
 // (rows of [24][C], one per CTA of a channel block) and coefficient dots.
+// `taps` is scratch of bwd_col_taps_floats() floats (the tap-major copy of the
+// conv weights the pass reads; unused without convolution branches).
 size_t bwd_col_pdot_floats(const Params& p);
 size_t bwd_col_cpart_floats(const Params& p, int sms);
+size_t bwd_col_taps_floats(const Params& p);
 int bwd_col_cpart_rows(const Params& p, int sms);
 cudaError_t launch_bwd_col(const Params& p, const BwdArgs<__nv_bfloat16>& a, const float* coef, bool has_conv,
-                           float* pdot, float* cpart, int sms, cudaStream_t st);
+                           float* pdot, float* cpart, float* taps, int sms, cudaStream_t st);
 
 // Backward per-token reverse: dp (bf16, 64 per token) and records
 // [alpha | hpre (N) | unused (4k)].  With Gram-Schmidt, gsdh [T, 16] holds
