@@ -1335,7 +1335,9 @@ cudaError_t launch_bwd_col(const Params& p, const BwdArgs<__nv_bfloat16>& a, con
   const Walk wk = make_walk_col(p, sms);
   if (has_conv) {
     const int n = NTAPS * p.C;
+    timing_begin("col_taps", st);
     col_taps_kernel<<<(n + 255) / 256, 256, 0, st>>>(a.w[0], a.w[1], a.w[2], taps, p.C);
+    timing_end(st);
     if (cudaError_t e = cudaGetLastError()) return e;
   }
   {
