@@ -44,6 +44,7 @@ ALG_C = {  # algorithmic bytes per token in C-units (one row of C state elements
 }
 ALG_SIDE = {  # fp32 bytes per token
     "coeffs_tc": 196, "coeffs_simt": 196, "flash_tc": 192 + 196,
+    "coeffs_tc_router": 196 + 196,  # the logits and the router's inputs
 }
 # The fused stack step (flash_tc) of sublayer l: 16 (read X) + 1 (read out) +
 # 4 (write the active rows in place) + 1 (write x_in) = 22 C, plus sublayer
@@ -75,6 +76,7 @@ def kernel_c_units(name: str, N: int, k: int, saved_active: bool = True) -> int:
     its own job must read and write at least."""
     table = {
         "coeffs_tc": N,                                   # read X
+        "coeffs_tc_router": N,                            # read X (the router rows ride along)
         "fwd_update": N + 1 + k + 1 + (k if saved_active else 0),
         "flash_tc": N + 1 + k + 1,                        # dense read + sparse write of sublayer l
         "bwd_col": 3 * k + 2,                             # read dX'[a], old rows, out; write mix, dout

@@ -76,6 +76,9 @@ WORKLOADS = {
                             router_fixed=2),
     "gs_bf16": Workload("gs_bf16", 7, B=4, S=4096, N=16, C=2048, k=4, dtype="bf16", backward=True,
                         conv_std=0.3, gram_schmidt=True),
+    # a quarter of the router workload (state 268 MB, above L2) for profiler captures
+    "router_quarter_bf16": Workload("router_quarter_bf16", 11, B=1, S=4096, N=16, C=2048, k=4, dtype="bf16",
+                                    backward=True, router_fixed=2),
     # a two-sublayer stack at the eight-sublayer stack's width (state 537 MB,
     # above L2) for profiler captures of the fused stack step
     "stack2_quarter_bf16": Workload("stack2_quarter_bf16", 10, B=1, S=4096, N=16, C=4096, k=4, dtype="bf16",
