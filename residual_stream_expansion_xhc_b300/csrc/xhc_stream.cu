@@ -1048,7 +1048,7 @@ __global__ void __launch_bounds__(256) bwd_dz_kernel(Params p, const float* __re
                                                      const float* __restrict__ pdot, int ncb, int has_dxin,
                                                      __nv_bfloat16* __restrict__ dP, float* __restrict__ rec,
                                                      const float* __restrict__ gsdh, RouterBwd rb, size_t T_all) {
-  extern __shared__ float trace_s[];           // [16 tokens][iters][32]
+  extern __shared__ float trace_s[];           // [16 tokens][iters][16]: each iteration's column-normalisation input
   const int lane = threadIdx.x & 31, e = lane & 15;
   const int slot = (threadIdx.x >> 5) * 2 + (lane >> 4);
   const size_t t = (size_t)blockIdx.x * 16 + slot;
@@ -1084,14 +1084,22 @@ __global__ void __launch_bounds__(256) bwd_dz_kernel(Params p, const float* __re
   const int i = e >> 2, j = e & 3;
   const bool valid = i < k && j < k;
   const float z = valid ? zt[N + 4 * k + k * i + j] : 0.0f;
-  float* tr = trace_s + (size_t)slot * p.iters * 32;
+  float* tr = trace_s + (size_t)slot * p.iters * 16;
   const float M0 = sinkhorn_init(z, valid);
   float M = M0;
-  for (int it = 0; it < p.iters; ++it) M = sinkhorn_step(M, valid, &tr[it * 32 + e], &tr[it * 32 + 16 + e]);
+  for (int it = 0; it < p.iters; ++it) M = sinkhorn_step(M, valid, nullptr, &tr[it * 16 + e]);
   float g = valid ? dres : 0.0f;
   for (int it = p.iters - 1; it >= 0; --it) {
-    g = norm_reverse_col(g, tr[it * 32 + 16 + e], valid);
-    g = norm_reverse_row(g, tr[it * 32 + e], valid);
+    g = norm_reverse_col(g, tr[it * 16 + e], valid);
+    // the row normalisation's input: M0, or the previous iteration's output,
+    // recomputed from its column-normalisation input by the same operations
+    float xr = M0;
+    if (it > 0) {
+      const float pc = tr[(it - 1) * 16 + e];
+      const float s = colsum16(pc);
+      xr = valid ? pc * __frcp_rn(s) : 0.0f;
+    }
+    g = norm_reverse_row(g, xr, valid);
   }
   const float dz_res = valid ? g * M0 : 0.0f;
   float dz_post = 0.0f, dz_pre = 0.0f, hpre = 0.0f;
@@ -1374,7 +1382,7 @@ cudaError_t launch_bwd_dz(const Params& p, const float* saved, const float* pdot
                           __nv_bfloat16* dP, float* rec, const float* gsdh, const RouterBwd& rb, cudaStream_t st) {
   const size_t T_all = (size_t)p.B * p.S;
   const int ncb = (p.C + col::CB - 1) / col::CB;
-  const size_t smem = (size_t)16 * std::max(p.iters, 1) * 32 * sizeof(float);
+  const size_t smem = (size_t)16 * std::max(p.iters, 1) * 16 * sizeof(float);
   const unsigned grid = (unsigned)((T_all + 15) / 16);
   timing_begin("bwd_dz", st);
   if (gsdh) {
