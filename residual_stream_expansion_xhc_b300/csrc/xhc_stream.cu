@@ -433,7 +433,11 @@ __global__ void __launch_bounds__(THREADS, 2) fwd_update_kernel(Params p, UpdArg
 // of 8-token chunks downwards (the anti-causal direction of the transposed
 // convolutions).  Per chunk:
 //   token phase (half-warp = token, lane = 8 channels)
-//     G_i = dX'[a_i], Xa_j (old active rows), u_c of the token
+//     G_i = dX'[a_i], Xa_j (old active rows) and the token's coefficients,
+//           staged in shared memory by cp.async: each warp stages its two
+//           token slots of the next chunk as soon as its dots are done, so
+//           the loads land while the channel phase runs
+//     u_c of the token
 //     mix   dX[a_j] = sum_i Hres[i][j] G_i
 //     du_c  = sum_i hpost[i][c] G_i: du_1..du_3 -> rings, du_0 kept in registers
 //     dots  <G_i, Xa_j>, <G_i, u_c> over the CTA's channels on mma.sync (the
@@ -443,7 +447,8 @@ __global__ void __launch_bounds__(THREADS, 2) fwd_update_kernel(Params p, UpdArg
 //           channel phase left in shared memory
 //     (and the `out` rows the channel phase of this chunk needs next)
 //   channel phase (thread = two adjacent channels; threads 0-63 take the K = 4
-//   and K = 8 convolutions, threads 64-127 the K = 12 one: 12 taps each)
+//   and K = 8 convolutions, threads 64-127 the K = 12 one: 12 taps each, read
+//   from a tap-major copy of the conv weights)
 //     u_1..u_3 of the next (earlier) chunk
 //     convolution parts of dout: sum_tau w_j[tau] du_j[t + tau] (inside the sequence)
 //     dw_j[tau] += du_j[t] out[t - tau], in registers for the whole walk
