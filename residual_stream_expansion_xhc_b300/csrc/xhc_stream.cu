@@ -600,6 +600,8 @@ __global__ void __launch_bounds__(col::THREADS, 3) bwd_col_kernel(Params p, BwdA
 #pragma unroll
   for (int q = 0; q < 12; ++q) dw[q] = make_float2(0.0f, 0.0f);
   float2 du0r[4];                                           // du_0 of the token awaiting its dout
+#pragma unroll
+  for (int q = 0; q < 4; ++q) du0r[q] = make_float2(0.0f, 0.0f);
   bool fin = false;
   size_t fin_tok = 0;
 
